@@ -1,0 +1,164 @@
+/*
+ * sinkattn.h -- C ABI of the sink-bias GQA attention forward pass for B300 (sm_103a).
+ *
+ * The operation is the attention layer of the "MiMo-V2-Flash Technical Report"
+ * (full Chinese translation, garden.houmin.site/digest/mimo-v2-flash):
+ *
+ *   §2.2 eq. (1)  a_ij = q_i . k_j / sqrt(d)          (d = 192, the QK head dim)
+ *   §2.2 eq. (2)  s_ij = exp(a_ij - m_i) / (exp(sink_h - m_i) + sum_j' exp(a_ij' - m_i)),
+ *                 m_i = max(max_j a_ij, sink_h)      (one learnable sink per query head)
+ *   §2.2 eq. (3)  o_i = sum_j s_ij v_j                (the sink carries no value)
+ *
+ * with the shapes of §2.1 Table 1: grouped-query attention (SWA layers 64 query /
+ * 8 KV heads with a 128-token sliding window; GA layers 64 query / 4 KV heads,
+ * global causal), QK head dim 192, V head dim 128, and rotary position
+ * embedding on the first 64 dims of q and k only (RoPE base 10,000 for SWA,
+ * 5,000,000 for GA after the 256K extension, §3.2).
+ *
+ * Conventions shared by every call:
+ *   - All tensor arguments are DEVICE pointers owned by the caller, dense and
+ *     row-major with the head index varying faster than the token index.
+ *     q, k, v, kcache, vcache and out must be 16-byte aligned; lse and sink
+ *     4-byte aligned.  The library keeps no pointer after a call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  No call allocates, frees or synchronises, except
+ *     sinkattn_get_device_status, which synchronises the current device.
+ *   - Window: window = 0 means global causal attention; window = W > 0 means key
+ *     j is visible to query i iff i - W < j <= i (W keys including i itself).
+ *   - Keys are passed UNROTATED; the kernels rotate q and k on chip.  RoPE pairs
+ *     dims (2t, 2t+1) for t < 32 with angle pos * base^(-2t/64) (RoFormer), unless
+ *     a params struct selects pairs (t, t+32).
+ *   - lse is the natural-log log-sum-exp of the row INCLUDING the sink:
+ *     lse_i = ln(exp(sink_h) + sum_{j visible} exp(a_ij)).
+ *   - out is bf16 (round to nearest even of the fp32 result), lse fp32.
+ *   - A row with no visible key gets out = 0 and lse = sink (-inf if the sink
+ *     is -inf).
+ *   - Functions return a status and never throw.  SINKATTN_EINVAL and
+ *     SINKATTN_EUNSUPPORTED are returned before anything is launched;
+ *     SINKATTN_ECUDA reports a CUDA error from a launch; kernels that hit an
+ *     internal wait limit record SINKATTN_ETIMEOUT in a device status word
+ *     that sinkattn_get_device_status reads.  Kernels never trap.
+ *   - Results are deterministic: the same inputs give the same bits.
+ */
+#ifndef SINKATTN_H
+#define SINKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SINKATTN_OK = 0,
+    SINKATTN_EINVAL = 1,       /* bad pointer, size, alignment or combination */
+    SINKATTN_EUNSUPPORTED = 2, /* head dims, group size or device not supported */
+    SINKATTN_EWORKSPACE = 3,   /* decode workspace missing or too small */
+    SINKATTN_ECUDA = 4,        /* a CUDA runtime call failed */
+    SINKATTN_ETIMEOUT = 5      /* a kernel gave up on an internal wait */
+} sinkattn_status;
+
+/* cudaStream_t, passed as an opaque pointer so that this header needs no CUDA include. */
+typedef void *sinkattn_stream_t;
+
+/* Optional knobs of the _ex calls.  Zero-initialise for the defaults. */
+typedef struct {
+    float scale;        /* logit scale; 0 -> 1/sqrt(192) (eq. (1) with d = 192) */
+    int32_t rope_off;   /* 1 -> no rotary embedding at all (positions ignored) */
+    int32_t rope_style; /* 0 -> pairs (2t, 2t+1) (default); 1 -> pairs (t, t+32) */
+    int32_t reserved;
+} sinkattn_params;
+
+/*
+ * Prefill over a varlen batch of self-attention sequences (the forward pass of
+ * one SWA or GA layer, §2.1-§2.2).
+ *
+ *   q          bf16 [total, num_q_heads, 192]
+ *   k          bf16 [total, num_kv_heads, 192], unrotated
+ *   v          bf16 [total, num_kv_heads, 128]
+ *   sink       fp32 [num_q_heads], may hold -inf (no sink for that head)
+ *   cu_seqlens int32 [batch + 1], device: cu_seqlens[0] = 0, non-decreasing,
+ *              cu_seqlens[batch] = total.  Sequence b holds tokens
+ *              cu_seqlens[b] .. cu_seqlens[b+1]-1 at RoPE positions 0, 1, ...
+ *   batch, total, max_seqlen  host copies of the sizes; max_seqlen must be at
+ *              least the longest sequence (it bounds the tile schedule).
+ *   num_q_heads / num_kv_heads  must be a power of two between 1 and 128;
+ *              query head h uses KV head h / (num_q_heads / num_kv_heads).
+ *   window     0 = global causal, W > 0 = sliding window of W keys.
+ *   rope_base  RoPE base (> 0).
+ *   out        bf16 [total, num_q_heads, 128]
+ *   lse        fp32 [total, num_q_heads]
+ */
+sinkattn_status sinkattn_prefill(const void *q, const void *k, const void *v, const float *sink,
+                                 const int32_t *cu_seqlens, int32_t batch, int32_t total,
+                                 int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t window, float rope_base, void *out, float *lse,
+                                 sinkattn_stream_t stream);
+
+sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v, const float *sink,
+                                    const int32_t *cu_seqlens, int32_t batch, int32_t total,
+                                    int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t window, float rope_base, const sinkattn_params *params,
+                                    void *out, float *lse, sinkattn_stream_t stream);
+
+/*
+ * Bytes of device workspace sinkattn_decode needs for these sizes (the split-KV
+ * partials of §2.3.1's multi-token verify: each KV chunk's running max, sum and
+ * unnormalised output).  Returns 0 for arguments sinkattn_decode would reject.
+ */
+size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t max_seqlen, int32_t window);
+
+/*
+ * Multi-token (MTP-verify) decode against a KV cache (§2.3.1: the main model
+ * verifies 1 + K draft tokens in one pass without extra KV-cache I/O).  The T
+ * new tokens of each sequence are already appended to the cache.
+ *
+ *   q        bf16 [batch, T, num_q_heads, 192]; query t of sequence b sits at
+ *            position seqlens[b] - T + t and sees cache positions j <= its own
+ *            position (causal among the drafts) and, with a window, j > pos - W.
+ *   kcache   bf16 [batch, S_cap, num_kv_heads, 192], unrotated keys at positions 0..
+ *   vcache   bf16 [batch, S_cap, num_kv_heads, 128]
+ *   seqlens  int32 [batch], device: cached tokens including the T new ones,
+ *            T <= seqlens[b] <= S_cap (shorter caches give empty rows).
+ *   max_seqlen  host bound on max(seqlens).
+ *   T        1 <= T and T * (num_q_heads / num_kv_heads) <= 128.
+ *   workspace, workspace_bytes  device scratch of at least
+ *            sinkattn_decode_workspace_size(...) bytes, 256-byte aligned.
+ *   out      bf16 [batch, T, num_q_heads, 128];  lse fp32 [batch, T, num_q_heads]
+ */
+sinkattn_status sinkattn_decode(const void *q, const void *kcache, const void *vcache,
+                                const int32_t *seqlens, const float *sink, int32_t window,
+                                float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                void *workspace, size_t workspace_bytes, void *out, float *lse,
+                                sinkattn_stream_t stream);
+
+sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void *vcache,
+                                   const int32_t *seqlens, const float *sink, int32_t window,
+                                   float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                   int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                   const sinkattn_params *params, void *workspace,
+                                   size_t workspace_bytes, void *out, float *lse,
+                                   sinkattn_stream_t stream);
+
+/* A static string naming a status code. */
+const char *sinkattn_status_string(sinkattn_status status);
+
+/*
+ * Synchronises the current device, then reads and clears the library's device
+ * status word.  Returns SINKATTN_OK, SINKATTN_ETIMEOUT (a kernel gave up on a
+ * wait and wrote no trustworthy output) or SINKATTN_ECUDA.  `detail`, if not
+ * NULL, receives the raw word (bit 0: timeout; bits 8..15: the wait site).
+ */
+sinkattn_status sinkattn_get_device_status(uint32_t *detail);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int32_t sinkattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKATTN_H */

@@ -1,0 +1,190 @@
+"""sink-bias GQA attention forward for B300 (sm_103a): a thin Python binding.
+
+The work happens in ``libsinkattn.so`` (hand-written CUDA, C ABI declared in
+``include/sinkattn.h``).  This module only checks tensor dtypes/shapes and
+passes raw device pointers and the current CUDA stream through ctypes.  There
+is no fallback: if the library is missing, every call raises.
+
+    out, lse = prefill(q, k, v, sink, cu_seqlens, max_seqlen=..., window=128, rope_base=1e4)
+    out, lse = decode(q, kcache, vcache, seqlens, sink, max_seqlen=..., window=0, rope_base=5e6)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsinkattn.so")
+
+# status codes of include/sinkattn.h
+OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA, ETIMEOUT = range(6)
+
+EXPORTED = (
+    "sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode_workspace_size",
+    "sinkattn_decode", "sinkattn_decode_ex", "sinkattn_status_string",
+    "sinkattn_get_device_status", "sinkattn_version",
+)
+
+
+class SinkAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+class Params(ctypes.Structure):
+    """sinkattn_params: scale (0 = 1/sqrt(192)), rope_off, rope_style."""
+    _fields_ = [("scale", ctypes.c_float), ("rope_off", ctypes.c_int32),
+                ("rope_style", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsinkattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m sliding_window_sink_bias_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        L.sinkattn_prefill.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P]
+        L.sinkattn_prefill_ex.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
+                                          ctypes.POINTER(Params), P, P, P]
+        L.sinkattn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.sinkattn_decode_workspace_size.restype = ctypes.c_size_t
+        L.sinkattn_decode.argtypes = [P, P, P, P, P, i32, f32, i32, i32, i32, i32, i32, i32,
+                                      P, ctypes.c_size_t, P, P, P]
+        L.sinkattn_decode_ex.argtypes = [P, P, P, P, P, i32, f32, i32, i32, i32, i32, i32, i32,
+                                         ctypes.POINTER(Params), P, ctypes.c_size_t, P, P, P]
+        L.sinkattn_status_string.argtypes = [i32]
+        L.sinkattn_status_string.restype = ctypes.c_char_p
+        L.sinkattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        L.sinkattn_version.restype = i32
+        for name in ("sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode",
+                     "sinkattn_decode_ex", "sinkattn_get_device_status"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise SinkAttnError(fn, status, lib().sinkattn_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _params(scale, rope_style, rope_off):
+    if scale is None and rope_style == 0 and not rope_off:
+        return None
+    return Params(float(scale or 0.0), int(bool(rope_off)), int(rope_style), 0)
+
+
+def _require(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_base: float,
+            out=None, lse=None, scale=None, rope_style: int = 0, rope_off: bool = False,
+            stream=None):
+    """Varlen prefill (one SWA or GA layer).  q [total, Hq, 192], k [total, Hkv, 192],
+    v [total, Hkv, 128] bf16; sink fp32 [Hq]; cu_seqlens int32 [B+1] on the device.
+    Returns (out bf16 [total, Hq, 128], lse fp32 [total, Hq])."""
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k, "k", torch.bfloat16, 3)
+    _require(v, "v", torch.bfloat16, 3)
+    _require(sink, "sink", torch.float32, 1)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    total, hq, dqk = q.shape
+    hkv = k.shape[1]
+    if dqk != 192 or k.shape != (total, hkv, 192) or v.shape != (total, hkv, 128):
+        raise ValueError("expected q [T,Hq,192], k [T,Hkv,192], v [T,Hkv,128]")
+    if sink.shape[0] != hq:
+        raise ValueError("sink must have one entry per query head")
+    if out is None:
+        out = torch.empty(total, hq, 128, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(total, hq, dtype=torch.float32, device=q.device)
+    _require(out, "out", torch.bfloat16, 3)
+    _require(lse, "lse", torch.float32, 2)
+    p = _params(scale, rope_style, rope_off)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(cu_seqlens), cu_seqlens.shape[0] - 1,
+            total, int(max_seqlen), hq, hkv, int(window), float(rope_base))
+    if p is None:
+        st = lib().sinkattn_prefill(*args, _ptr(out), _ptr(lse), _stream(stream))
+    else:
+        st = lib().sinkattn_prefill_ex(*args, ctypes.byref(p), _ptr(out), _ptr(lse),
+                                       _stream(stream))
+    _check("sinkattn_prefill", st)
+    return out, lse
+
+
+def decode_workspace_size(batch: int, t: int, hq: int, hkv: int, max_seqlen: int,
+                          window: int) -> int:
+    return int(lib().sinkattn_decode_workspace_size(batch, t, hq, hkv, max_seqlen, window))
+
+
+def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, rope_base: float,
+           workspace=None, out=None, lse=None, scale=None, rope_style: int = 0,
+           rope_off: bool = False, stream=None):
+    """MTP-verify decode.  q [B, T, Hq, 192]; kcache [B, S_cap, Hkv, 192];
+    vcache [B, S_cap, Hkv, 128] bf16; seqlens int32 [B] (cached tokens including
+    the T new ones); sink fp32 [Hq].  Returns (out [B, T, Hq, 128], lse [B, T, Hq])."""
+    _require(q, "q", torch.bfloat16, 4)
+    _require(kcache, "kcache", torch.bfloat16, 4)
+    _require(vcache, "vcache", torch.bfloat16, 4)
+    _require(seqlens, "seqlens", torch.int32, 1)
+    _require(sink, "sink", torch.float32, 1)
+    b, t, hq, dqk = q.shape
+    s_cap, hkv = kcache.shape[1], kcache.shape[2]
+    if dqk != 192 or kcache.shape != (b, s_cap, hkv, 192) or vcache.shape != (b, s_cap, hkv, 128):
+        raise ValueError("expected q [B,T,Hq,192], kcache [B,S,Hkv,192], vcache [B,S,Hkv,128]")
+    need = decode_workspace_size(b, t, hq, hkv, max_seqlen, window)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(b, t, hq, 128, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(b, t, hq, dtype=torch.float32, device=q.device)
+    p = _params(scale, rope_style, rope_off)
+    args = (_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(sink), int(window),
+            float(rope_base), b, t, s_cap, int(max_seqlen), hq, hkv)
+    tail = (_ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+            _stream(stream))
+    if p is None:
+        st = lib().sinkattn_decode(*args, *tail)
+    else:
+        st = lib().sinkattn_decode_ex(*args, ctypes.byref(p), *tail)
+    _check("sinkattn_decode", st)
+    return out, lse
+
+
+def device_status():
+    """(status, raw word) of the device status word; synchronises the device."""
+    w = ctypes.c_uint32(0)
+    st = lib().sinkattn_get_device_status(ctypes.byref(w))
+    return int(st), int(w.value)
+
+
+def version() -> int:
+    return int(lib().sinkattn_version())

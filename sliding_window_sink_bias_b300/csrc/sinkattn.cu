@@ -1,0 +1,326 @@
+// sinkattn.cu -- host side of the C ABI declared in include/sinkattn.h:
+// argument checks, TMA tensor maps, tile-schedule parameters and launches.
+// All arithmetic of the attention runs in the kernels of attn_kernel.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_kernel.cuh"
+#include "sinkattn.h"
+
+namespace {
+
+using sa::AttnArgs;
+using sa::Layout;
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+constexpr int32_t kBNWide = 144;   // one key block covers a 128-key window + 16-token tile
+constexpr int32_t kBN = 128;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool pow2_upto_128(int32_t x) { return x >= 1 && x <= 128 && (x & (x - 1)) == 0; }
+
+// ----------------------------------------------------------------- driver entry
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A 3-D bf16 tensor map over rows of `heads` x `dim` elements: dims
+// (dim, heads, rows) with a box of (64, box_heads, box_rows), 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t dim, uint64_t heads, uint64_t rows,
+              uint32_t box_heads, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t gdim[3] = {dim, heads, rows};
+  const cuuint64_t gstride[2] = {dim * 2, dim * heads * 2};
+  const cuuint32_t box[3] = {64, box_heads, box_rows};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim,
+                        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+bool device_info(DeviceInfo &d) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return false;
+  if (cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  return true;
+}
+
+// RoPE angles as 64-bit fixed-point turns: theta_t = base^(-2t/64) (RoFormer
+// frequencies over the 64 rotated dims, §2.1), stored as round(theta_t/(2 pi) * 2^64).
+void fill_turns(AttnArgs &a, float rope_base) {
+  for (int t = 0; t < 32; ++t) {
+    const double theta = std::pow(static_cast<double>(rope_base), -2.0 * t / 64.0);
+    const double turns = theta / (2.0 * M_PI);
+    a.rope_turns[t] = static_cast<unsigned long long>(std::ldexp(turns, 64));
+  }
+}
+
+sinkattn_status fill_common(AttnArgs &a, const sinkattn_params *p, float rope_base,
+                            int32_t hq, int32_t hkv, int32_t window) {
+  std::memset(&a, 0, sizeof a);
+  a.Hq = hq;
+  a.Hkv = hkv;
+  a.G = hq / hkv;
+  a.window = window;
+  float scale = 1.0f / std::sqrt(192.0f);
+  a.rope_on = 1;
+  a.rope_style = 0;
+  if (p) {
+    if (p->scale != 0.f) scale = p->scale;
+    a.rope_on = p->rope_off ? 0 : 1;
+    a.rope_style = p->rope_style;
+    if (p->rope_style != 0 && p->rope_style != 1) return SINKATTN_EINVAL;
+    if (!(std::isfinite(scale))) return SINKATTN_EINVAL;
+  }
+  if (a.rope_on && !(rope_base > 0.f && std::isfinite(rope_base))) return SINKATTN_EINVAL;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  if (a.rope_on) fill_turns(a, rope_base);
+  return SINKATTN_OK;
+}
+
+template <int BN, int NQ, int NKV>
+sinkattn_status launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                       const AttnArgs &a, int grid, cudaStream_t stream) {
+  using Ly = Layout<BN, NQ, NKV>;
+  auto kern = sa::sinkattn_fwd_kernel<BN, NQ, NKV>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(Ly::kDynSmem)) != cudaSuccess)
+    return SINKATTN_ECUDA;
+  kern<<<grid, sa::kThreads, Ly::kDynSmem, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+}
+
+struct DecodePlan {
+  int32_t chunk = 0, splits = 0, rows = 0;
+  size_t bytes = 0;
+};
+
+// Split-KV plan: chunks of `chunk` keys (a multiple of 128) so that the whole
+// batch yields about 8192 chunk-sized work items at the longest cache.
+DecodePlan decode_plan(int32_t batch, int32_t T, int32_t hq, int32_t hkv, int32_t max_seqlen,
+                       int32_t window) {
+  DecodePlan p;
+  const int64_t range = window > 0 ? std::min<int64_t>(max_seqlen, int64_t(T) + window - 1)
+                                   : int64_t(max_seqlen);
+  const int64_t units = int64_t(batch) * hkv;
+  int64_t chunk = (range * units + 8191) / 8192;
+  chunk = ((chunk + 127) / 128) * 128;
+  chunk = std::max<int64_t>(256, std::min<int64_t>(16384, chunk));
+  p.chunk = static_cast<int32_t>(chunk);
+  p.splits = static_cast<int32_t>(std::max<int64_t>(1, (range + chunk - 1) / chunk));
+  p.rows = T * (hq / hkv);
+  p.bytes = static_cast<size_t>(units) * p.splits * p.rows * (sa::kDv + 4) * sizeof(float);
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sinkattn_version(void) { return kVersion; }
+
+const char *sinkattn_status_string(sinkattn_status s) {
+  switch (s) {
+    case SINKATTN_OK: return "ok";
+    case SINKATTN_EINVAL: return "invalid argument";
+    case SINKATTN_EUNSUPPORTED: return "unsupported shape or device";
+    case SINKATTN_EWORKSPACE: return "workspace missing or too small";
+    case SINKATTN_ECUDA: return "CUDA error";
+    case SINKATTN_ETIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+sinkattn_status sinkattn_get_device_status(uint32_t *detail) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return SINKATTN_ECUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, sa::g_status_word, sizeof word) != cudaSuccess)
+    return SINKATTN_ECUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(sa::g_status_word, &zero, sizeof zero) != cudaSuccess)
+    return SINKATTN_ECUDA;
+  if (detail) *detail = word;
+  return (word & 1u) ? SINKATTN_ETIMEOUT : SINKATTN_OK;
+}
+
+sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v, const float *sink,
+                                    const int32_t *cu_seqlens, int32_t batch, int32_t total,
+                                    int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t window, float rope_base, const sinkattn_params *params,
+                                    void *out, float *lse, sinkattn_stream_t stream) {
+  // ------------------------------------------------ host-side checks (no CUDA call)
+  if (batch < 0 || total < 0 || max_seqlen < 0 || window < 0) return SINKATTN_EINVAL;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return SINKATTN_EINVAL;
+  if (!pow2_upto_128(num_q_heads / num_kv_heads)) return SINKATTN_EUNSUPPORTED;
+  if (num_q_heads > 65535 || num_kv_heads > 65535) return SINKATTN_EUNSUPPORTED;
+  if (total > 0 && max_seqlen == 0) return SINKATTN_EINVAL;
+  if (batch == 0 || total == 0) return SINKATTN_OK;
+  if (!q || !k || !v || !sink || !cu_seqlens || !out || !lse) return SINKATTN_EINVAL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(sink, 4) || !aligned(cu_seqlens, 4))
+    return SINKATTN_EINVAL;
+  AttnArgs a;
+  if (sinkattn_status st = fill_common(a, params, rope_base, num_q_heads, num_kv_heads, window))
+    return st;
+
+  // ------------------------------------------------ schedule
+  const int32_t G = a.G;
+  const int32_t tile_tokens = 128 / G;
+  // Sliding windows that fit one 144-key block per tile take the single-block
+  // kernel; global or wide windows take the multi-block online-softmax kernel.
+  const bool wide = window > 0 && window + tile_tokens - 1 <= kBNWide;
+  const int32_t BN = wide ? kBNWide : kBN;
+  a.mode = sa::kModePrefill;
+  a.batch = batch;
+  a.tile_tokens = tile_tokens;
+  a.tiles_per_seq = (max_seqlen + tile_tokens - 1) / tile_tokens;
+  const int64_t n_items = int64_t(batch) * num_kv_heads * a.tiles_per_seq;
+  if (n_items > INT32_MAX) return SINKATTN_EUNSUPPORTED;
+  a.n_items = static_cast<int32_t>(n_items);
+  a.lpt_order = window == 0 ? 1 : 0;
+  a.q_tx_bytes = 3u * 64u * 2u * static_cast<uint32_t>(G * tile_tokens);
+  a.cu_seqlens = cu_seqlens;
+  a.sink = sink;
+  a.out = static_cast<__nv_bfloat16 *>(out);
+  a.lse = lse;
+
+  DeviceInfo dev;
+  if (!device_info(dev)) return SINKATTN_ECUDA;
+  if (dev.major != 10 || dev.minor != 3) return SINKATTN_EUNSUPPORTED;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, 192, num_q_heads, total, G, tile_tokens) ||
+      !make_map(&mk, k, 192, num_kv_heads, total, 1, BN) ||
+      !make_map(&mv, v, 128, num_kv_heads, total, 1, BN))
+    return SINKATTN_ECUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(n_items, dev.sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (wide) return launch<kBNWide, 2, 1>(mq, mk, mv, a, grid, s);
+  return launch<kBN, 1, 2>(mq, mk, mv, a, grid, s);
+}
+
+sinkattn_status sinkattn_prefill(const void *q, const void *k, const void *v, const float *sink,
+                                 const int32_t *cu_seqlens, int32_t batch, int32_t total,
+                                 int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t window, float rope_base, void *out, float *lse,
+                                 sinkattn_stream_t stream) {
+  return sinkattn_prefill_ex(q, k, v, sink, cu_seqlens, batch, total, max_seqlen, num_q_heads,
+                             num_kv_heads, window, rope_base, nullptr, out, lse, stream);
+}
+
+size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t max_seqlen, int32_t window) {
+  if (batch <= 0 || T <= 0 || max_seqlen < 0 || window < 0) return 0;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (!pow2_upto_128(G) || T * G > 128) return 0;
+  return decode_plan(batch, T, num_q_heads, num_kv_heads, max_seqlen, window).bytes;
+}
+
+sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void *vcache,
+                                   const int32_t *seqlens, const float *sink, int32_t window,
+                                   float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                   int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                   const sinkattn_params *params, void *workspace,
+                                   size_t workspace_bytes, void *out, float *lse,
+                                   sinkattn_stream_t stream) {
+  if (batch < 0 || T <= 0 || S_cap <= 0 || max_seqlen < 0 || window < 0) return SINKATTN_EINVAL;
+  if (max_seqlen > S_cap) return SINKATTN_EINVAL;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return SINKATTN_EINVAL;
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (!pow2_upto_128(G)) return SINKATTN_EUNSUPPORTED;
+  if (T * G > 128) return SINKATTN_EUNSUPPORTED;
+  if (int64_t(batch) * S_cap > INT32_MAX || int64_t(batch) * T > INT32_MAX)
+    return SINKATTN_EUNSUPPORTED;
+  if (batch == 0) return SINKATTN_OK;
+  if (!q || !kcache || !vcache || !seqlens || !sink || !out || !lse) return SINKATTN_EINVAL;
+  if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(vcache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(sink, 4) || !aligned(seqlens, 4))
+    return SINKATTN_EINVAL;
+  const DecodePlan plan = decode_plan(batch, T, num_q_heads, num_kv_heads, max_seqlen, window);
+  if (!workspace || workspace_bytes < plan.bytes || !aligned(workspace, 256))
+    return SINKATTN_EWORKSPACE;
+  AttnArgs a;
+  if (sinkattn_status st = fill_common(a, params, rope_base, num_q_heads, num_kv_heads, window))
+    return st;
+
+  a.mode = sa::kModeDecodePartial;
+  a.batch = batch;
+  a.tile_tokens = T;
+  a.T = T;
+  a.S_cap = S_cap;
+  a.chunk = plan.chunk;
+  a.tiles_per_seq = plan.splits;
+  const int64_t n_items = int64_t(batch) * num_kv_heads * plan.splits;
+  if (n_items > INT32_MAX) return SINKATTN_EUNSUPPORTED;
+  a.n_items = static_cast<int32_t>(n_items);
+  a.part_rows = plan.rows;
+  a.q_tx_bytes = 3u * 64u * 2u * static_cast<uint32_t>(G * T);
+  a.seqlens = seqlens;
+  a.sink = sink;
+  a.part_o = static_cast<float *>(workspace);
+  a.part_ml = static_cast<float *>(workspace) +
+              static_cast<size_t>(batch) * num_kv_heads * plan.splits * plan.rows * sa::kDv;
+
+  DeviceInfo dev;
+  if (!device_info(dev)) return SINKATTN_ECUDA;
+  if (dev.major != 10 || dev.minor != 3) return SINKATTN_EUNSUPPORTED;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, 192, num_q_heads, uint64_t(batch) * T, G, T) ||
+      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, kBN) ||
+      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, kBN))
+    return SINKATTN_ECUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(n_items, dev.sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (sinkattn_status st = launch<kBN, 1, 2>(mq, mk, mv, a, grid, s)) return st;
+
+  const int64_t rows = int64_t(batch) * T * num_q_heads;
+  if (rows > INT32_MAX) return SINKATTN_EUNSUPPORTED;
+  sa::sinkattn_combine_kernel<<<static_cast<unsigned>(rows), sa::kDv, 0, s>>>(
+      a.part_o, a.part_ml, seqlens, sink, T, num_q_heads, num_kv_heads, window, plan.chunk,
+      plan.splits, plan.rows, static_cast<__nv_bfloat16 *>(out), lse);
+  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+}
+
+sinkattn_status sinkattn_decode(const void *q, const void *kcache, const void *vcache,
+                                const int32_t *seqlens, const float *sink, int32_t window,
+                                float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                void *workspace, size_t workspace_bytes, void *out, float *lse,
+                                sinkattn_stream_t stream) {
+  return sinkattn_decode_ex(q, kcache, vcache, seqlens, sink, window, rope_base, batch, T, S_cap,
+                            max_seqlen, num_q_heads, num_kv_heads, nullptr, workspace,
+                            workspace_bytes, out, lse, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+"""Host-only checks of the C ABI: the library builds for sm_103a, loads, exports
+every function include/sinkattn.h declares, and rejects bad arguments before
+touching the GPU (these calls never reach a CUDA API)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sinkattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sliding_window_sink_bias_b300 import build
+    build.build()
+    import sliding_window_sink_bias_b300 as sa
+    return sa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(sinkattn_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_lists_the_api():
+    names = declared_functions()
+    for n in ("sinkattn_prefill", "sinkattn_decode", "sinkattn_decode_workspace_size"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    import sliding_window_sink_bias_b300 as sa
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert set(sa.EXPORTED) == set(declared_functions())
+
+
+def test_status_strings_and_version(L):
+    import sliding_window_sink_bias_b300 as sa
+    assert sa.version() >= 100
+    for code in range(6):
+        s = L.sinkattn_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.sinkattn_status_string(99).decode() == "unknown status"
+
+
+def _prefill(L, q=1, k=1, v=1, sink=1, cu=1, batch=1, total=16, max_seqlen=16, hq=64, hkv=8,
+             window=128, base=1e4, out=1, lse=1):
+    P = ctypes.c_void_p
+    f = lambda x: None if x is None else P(16 * x)  # fake, 16-byte-aligned pointers
+    return L.sinkattn_prefill(f(q), f(k), f(v), f(sink), f(cu), batch, total, max_seqlen, hq, hkv,
+                              window, base, f(out), f(lse), None)
+
+
+def test_prefill_argument_checks(L):
+    import sliding_window_sink_bias_b300 as sa
+    assert _prefill(L, batch=-1) == sa.EINVAL
+    assert _prefill(L, total=-5) == sa.EINVAL
+    assert _prefill(L, window=-1) == sa.EINVAL
+    assert _prefill(L, hq=64, hkv=5) == sa.EINVAL         # not a multiple
+    assert _prefill(L, hq=0) == sa.EINVAL
+    assert _prefill(L, hq=24, hkv=8) == sa.EUNSUPPORTED   # group of 3
+    assert _prefill(L, hq=256, hkv=1) == sa.EUNSUPPORTED  # group above 128
+    assert _prefill(L, q=None) == sa.EINVAL
+    assert _prefill(L, lse=None) == sa.EINVAL
+    assert _prefill(L, max_seqlen=0) == sa.EINVAL
+    assert _prefill(L, base=0.0) == sa.EINVAL
+    assert _prefill(L, base=float("nan")) == sa.EINVAL
+    # nothing to do: no launch, no CUDA call
+    assert _prefill(L, batch=0, total=0, max_seqlen=0, q=None) == sa.OK
+    assert _prefill(L, total=0, max_seqlen=0, q=None) == sa.OK
+    # misaligned q (8 bytes off)
+    P = ctypes.c_void_p
+    st = L.sinkattn_prefill(P(24), P(16), P(16), P(16), P(16), 1, 16, 16, 64, 8, 128, 1e4,
+                            P(16), P(16), None)
+    assert st == sa.EINVAL
+
+
+def test_prefill_ex_params_checks(L):
+    import sliding_window_sink_bias_b300 as sa
+    P = ctypes.c_void_p
+    bad = sa.Params(0.0, 0, 7, 0)
+    st = L.sinkattn_prefill_ex(P(16), P(16), P(16), P(16), P(16), 1, 16, 16, 64, 8, 128, 1e4,
+                               ctypes.byref(bad), P(16), P(16), None)
+    assert st == sa.EINVAL
+    inf_scale = sa.Params(float("inf"), 0, 0, 0)
+    st = L.sinkattn_prefill_ex(P(16), P(16), P(16), P(16), P(16), 1, 16, 16, 64, 8, 128, 1e4,
+                               ctypes.byref(inf_scale), P(16), P(16), None)
+    assert st == sa.EINVAL
+
+
+def test_decode_workspace_size(L):
+    ws = L.sinkattn_decode_workspace_size
+    assert ws(0, 4, 64, 4, 1000, 0) == 0
+    assert ws(2, 0, 64, 4, 1000, 0) == 0
+    assert ws(2, 9, 64, 4, 1000, 0) == 0        # 9 tokens x 16 heads > 128 rows
+    assert ws(2, 4, 64, 5, 1000, 0) == 0
+    a = ws(64, 4, 64, 4, 262144, 0)
+    b = ws(64, 4, 64, 4, 65536, 0)
+    assert a > 0 and b > 0 and a >= b
+    # the window bounds the keys a sequence needs
+    assert ws(64, 4, 64, 8, 262144, 128) < ws(64, 4, 64, 8, 262144, 0)
+    # partial rows = T * G, 132 fp32 each (128 values + max, two sums, pad), units * splits
+    assert a % (64 * 4 * 16 * 132 * 4) == 0
+
+
+def _decode(L, q=1, kc=1, vc=1, sl=1, sink=1, window=0, base=5e6, b=2, t=4, s_cap=100,
+            max_seqlen=100, hq=64, hkv=4, ws=1, ws_bytes=None, out=1, lse=1):
+    P = ctypes.c_void_p
+    f = lambda x: None if x is None else P(256 * x)
+    if ws_bytes is None:
+        ws_bytes = L.sinkattn_decode_workspace_size(b, t, hq, hkv, max_seqlen, window)
+    return L.sinkattn_decode(f(q), f(kc), f(vc), f(sl), f(sink), window, base, b, t, s_cap,
+                             max_seqlen, hq, hkv, f(ws), ws_bytes, f(out), f(lse), None)
+
+
+def test_decode_argument_checks(L):
+    import sliding_window_sink_bias_b300 as sa
+    assert _decode(L, t=0) == sa.EINVAL
+    assert _decode(L, b=-1) == sa.EINVAL
+    assert _decode(L, max_seqlen=101) == sa.EINVAL     # longer than the cache
+    assert _decode(L, hkv=3) == sa.EINVAL
+    assert _decode(L, t=9) == sa.EUNSUPPORTED          # 9 x 16 rows > 128
+    assert _decode(L, kc=None) == sa.EINVAL
+    assert _decode(L, ws=None) == sa.EWORKSPACE
+    assert _decode(L, ws_bytes=8) == sa.EWORKSPACE
+    assert _decode(L, b=0) == sa.OK
