@@ -1,0 +1,432 @@
+"""Benchmark of the sink-bias GQA attention forward on B300.
+
+Default (N = 1): the headline workload is SWA prefill, batch 4 x 32768 tokens,
+64 query / 8 KV heads, window 128, RoPE base 1e4 (one SWA layer of the
+MiMo-V2-Flash model at its 32K native context).  One step = one
+sinkattn_prefill call over that batch.  The same JSON line also reports the
+global-attention prefill (1 x 131072 tokens, 64/4 heads) and the MTP-verify
+decode (batch 64, 4 query tokens, caches of 64K-256K tokens; GA and SWA layers),
+each timed the same way.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference there is) on a
+bounded sample of the same workload, on the host cores.
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: every rank
+runs the whole workload on its own GPU; value = work of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sink-attn prefill TFLOP/s & decode KV GB/s on 1 B300; % of roofline"
+MAIN = "swa_prefill_4x32768"
+FLOP_PER_PAIR_HEAD = 2 * 192 + 2 * 128  # QK^T + PV per visible (query, key) pair and head
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--main-only", action="store_true", help="skip the GA prefill and decode lines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ environment
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event (throttle) reasons of this
+    process's GPU through NVML every 5 ms while the timed region runs."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []
+        self.max_mhz = None
+        self._stop = None
+        self.error = None
+
+    def _handle(self):
+        import pynvml
+        import torch
+        pynvml.nvmlInit()
+        p = torch.cuda.get_device_properties(self.cuda_index)
+        try:
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+            return pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = int(vis.split(",")[self.cuda_index]) if vis and vis.split(",")[0].isdigit() \
+                else self.cuda_index
+            return pynvml.nvmlDeviceGetHandleByIndex(idx)
+
+    def __enter__(self):
+        import threading
+        try:
+            import pynvml
+            h = self._handle()
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # no NVML: the line says "unsampled" and why
+            self.error = f"{type(e).__name__}: {e}"
+            return self
+        self._stop = threading.Event()
+
+        def loop():
+            while not self._stop.is_set():
+                try:
+                    mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                    rs = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                    self.samples.append((mhz, rs))
+                except Exception as e:
+                    self.error = f"{type(e).__name__}: {e}"
+                time.sleep(0.005)
+
+        self._t = threading.Thread(target=loop, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._stop is not None:
+            self._stop.set()
+            self._t.join(timeout=2)
+        return False
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0, "error": self.error}
+        mhz = [s[0] for s in self.samples]
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz), "source": "nvml"}
+
+
+# ------------------------------------------------------------------ workloads
+def prefill_work(wl):
+    from sliding_window_sink_bias_b300 import synth
+    pairs = synth.algorithmic_pairs_prefill(wl["seqlens"], wl["window"])
+    total = sum(wl["seqlens"])
+    hq, hkv = wl["hq"], wl["hkv"]
+    flops = pairs * hq * FLOP_PER_PAIR_HEAD
+    bytes_ = total * (hq * 192 * 2 + hkv * 192 * 2 + hkv * 128 * 2 + hq * 128 * 2 + hq * 4)
+    return flops, bytes_, total
+
+
+def time_calls(fn, steps, warmup, ws):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(ws)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    barrier(ws)
+    return max_over_ranks(total_ms, ws) / steps, per
+
+
+def bench_prefill(name, steps, warmup, ws, local, with_e2e):
+    import torch
+
+    import sliding_window_sink_bias_b300 as sa
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[name]
+    dev = f"cuda:{local}"
+    inp = synth.prefill_inputs(wl["seqlens"], wl["hq"], wl["hkv"], window=wl["window"],
+                               rope_base=wl["rope_base"], seed=0, device=dev)
+    out = torch.empty(inp.total, wl["hq"], 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(inp.total, wl["hq"], dtype=torch.float32, device=dev)
+
+    def call():
+        sa.prefill(inp.q, inp.k, inp.v, inp.sink, inp.cu_seqlens, max_seqlen=inp.max_seqlen,
+                   window=wl["window"], rope_base=wl["rope_base"], out=out, lse=lse)
+
+    with ClockSampler(local) as clk:
+        ms, per = time_calls(call, steps, warmup, ws)
+    st, word = sa.device_status()
+    if st != sa.OK:
+        raise RuntimeError(f"device status {st} word {word:#x} after {name}")
+    flops, bytes_, total = prefill_work(wl)
+    res = {"name": name, "ms": ms, "per_launch_ms": per, "flops": flops, "bytes": bytes_,
+           "tokens": total, "clocks": clk.summary(), "launches": steps}
+    if with_e2e:
+        pin = lambda t: t.cpu().pin_memory()
+        qh, kh, vh, sh, ch = pin(inp.q), pin(inp.k), pin(inp.v), pin(inp.sink), pin(inp.cu_seqlens)
+        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_call():
+            inp.q.copy_(qh, non_blocking=True)
+            inp.k.copy_(kh, non_blocking=True)
+            inp.v.copy_(vh, non_blocking=True)
+            inp.sink.copy_(sh, non_blocking=True)
+            inp.cu_seqlens.copy_(ch, non_blocking=True)
+            call()
+            oh.copy_(out, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        e_ms, _ = time_calls(e2e_call, max(3, steps // 4), 1, ws)
+        res["e2e_ms"] = e_ms
+        res["h2d"] = sum(t.numel() * t.element_size() for t in (qh, kh, vh, sh, ch))
+        res["d2h"] = sum(t.numel() * t.element_size() for t in (oh, lh))
+        del qh, kh, vh, oh, lh
+    del inp, out, lse
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode(name, steps, warmup, ws, local):
+    import torch
+
+    import sliding_window_sink_bias_b300 as sa
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[name]
+    dev = f"cuda:{local}"
+    lens = synth.uniform_lengths(wl["batch"], wl["len_lo"], wl["len_hi"], seed=0)
+    inp = synth.decode_inputs(lens, wl["t"], wl["s_cap"], wl["hq"], wl["hkv"],
+                              window=wl["window"], rope_base=wl["rope_base"], seed=0, device=dev)
+    ws_bytes = sa.decode_workspace_size(wl["batch"], wl["t"], wl["hq"], wl["hkv"], max(lens),
+                                        wl["window"])
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(wl["batch"], wl["t"], wl["hq"], 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(wl["batch"], wl["t"], wl["hq"], dtype=torch.float32, device=dev)
+
+    def call():
+        sa.decode(inp.q, inp.kcache, inp.vcache, inp.seqlens, inp.sink, max_seqlen=max(lens),
+                  window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
+                  lse=lse)
+
+    # the decode working set can sit in L2 for the SWA layer: flush between steps
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    import sliding_window_sink_bias_b300 as _sa  # noqa: F401
+    times = []
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(ws)
+    stream = torch.cuda.current_stream()
+    with ClockSampler(local) as clk:
+        for _ in range(steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+    barrier(ws)
+    ms = max_over_ranks(sum(times) / len(times), ws)
+    st, word = sa.device_status()
+    if st != sa.OK:
+        raise RuntimeError(f"device status {st} word {word:#x} after {name}")
+    hkv, t, hq, W = wl["hkv"], wl["t"], wl["hq"], wl["window"]
+    keys = [min(L, t + W - 1) if W > 0 else L for L in lens]
+    kv_bytes = sum(keys) * hkv * (192 + 128) * 2
+    io_bytes = wl["batch"] * t * hq * (192 * 2 + 128 * 2 + 4)
+    pairs = synth.algorithmic_pairs_decode(lens, t, W)
+    res = {"name": name, "ms": ms, "kv_bytes": kv_bytes, "bytes": kv_bytes + io_bytes,
+           "flops": pairs * hq * FLOP_PER_PAIR_HEAD, "clocks": clk.summary(),
+           "launches": 2 * steps, "tokens": wl["batch"] * t}
+    del inp, work, out, lse, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample_prefill(wl, n_tokens, seed=0):
+    """Run the oracle on the first n_tokens tokens of sequence 0 (every head);
+    returns (seconds, flops, threads)."""
+    import numpy as np
+
+    import oracle
+    from sliding_window_sink_bias_b300 import synth
+    oracle.build()
+    L = min(n_tokens, wl["seqlens"][0])
+    inp = synth.prefill_inputs([L], wl["hq"], wl["hkv"], window=wl["window"],
+                               rope_base=wl["rope_base"], seed=seed, device="cpu")
+    t0 = time.perf_counter()
+    oracle.prefill(inp.q, inp.k, inp.v, inp.sink, np.array([0, L], dtype=np.int32),
+                   window=wl["window"], rope_base=wl["rope_base"])
+    dt = time.perf_counter() - t0
+    pairs = synth.algorithmic_pairs_prefill([L], wl["window"])
+    return dt, pairs * wl["hq"] * FLOP_PER_PAIR_HEAD, oracle.max_threads()
+
+
+def cpu_baseline(target_s=12.0):
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[MAIN]
+    dt, fl, thr = oracle_sample_prefill(wl, 256)
+    n = int(min(32768, max(256, 256 * target_s / max(dt, 1e-3))))
+    dt, fl, thr = oracle_sample_prefill(wl, n)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": f"first {n} tokens of sequence 0 of {MAIN}, all 64 heads "
+                      f"({fl / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[MAIN]
+    n = 512
+    for _ in range(args.warmup):
+        oracle_sample_prefill(wl, n)
+    times, flops = [], 0
+    thr = 0
+    for _ in range(args.steps):
+        dt, fl, thr = oracle_sample_prefill(wl, n)
+        times.append(dt)
+        flops = fl
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms / 1e3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": MAIN, "sample_tokens_per_step": n, "window": 128,
+                   "heads": "64q/8kv", "head_dims": "192/128"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                         "sample": f"first {n} tokens of sequence 0 of {MAIN}, all 64 heads, "
+                                   "per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+def roofline_obj(bound, achieved, peak, unit, traffic=None):
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak if peak else None, "traffic": traffic}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    ws, rank, local = dist_setup()
+    from sliding_window_sink_bias_b300 import build
+    if rank == 0:
+        build.build()
+    barrier(ws)
+    peaks = load_peaks()
+    m = bench_prefill(MAIN, args.steps, args.warmup, ws, local, with_e2e=True)
+    tflops = ws * m["flops"] / (m["ms"] / 1e3) / 1e12
+    gbs = m["bytes"] / (m["ms"] / 1e3) / 1e9  # per GPU, per launch (one launch per step)
+    e2e_tflops = ws * m["flops"] / (m["e2e_ms"] / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": MAIN, "batch": 4, "seq_len": 32768, "heads": "64q/8kv",
+                   "head_dims": "192/128", "window": 128, "rope_base": 1e4,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (6.07 GB per step), no flush"},
+        "tokens_per_s": ws * m["tokens"] / (m["ms"] / 1e3),
+        "roofline": roofline_obj("hbm", gbs, peaks["hbm_gbs"], "GB/s"),
+        "peaks_source": peaks["source"],
+        "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"], "ms_per_step": m["e2e_ms"]},
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
+    }
+    if not args.main_only:
+        extra = {}
+        g = bench_prefill("ga_prefill_1x131072", max(3, args.steps // 4), args.warmup, ws, local,
+                          with_e2e=False)
+        g_tf = g["flops"] / (g["ms"] / 1e3) / 1e12
+        extra["ga_prefill_1x131072"] = {
+            "value": ws * g_tf, "unit": "TFLOP/s", "ms_per_step": g["ms"],
+            "roofline": roofline_obj("tensor", g_tf, peaks["bf16_tflops"], "TFLOP/s"),
+            "clocks": g["clocks"]}
+        for name in ("mtp_decode_ga_b64_t4", "mtp_decode_swa_b64_t4"):
+            d = bench_decode(name, args.steps, args.warmup, ws, local)
+            d_gbs = d["bytes"] / (d["ms"] / 1e3) / 1e9
+            extra[name] = {"value": ws * d_gbs, "unit": "GB/s", "ms_per_step": d["ms"],
+                           "kv_bytes": d["kv_bytes"],
+                           "tflops": d["flops"] / (d["ms"] / 1e3) / 1e12,
+                           "roofline": roofline_obj("hbm", d_gbs, peaks["hbm_gbs"], "GB/s"),
+                           "clocks": d["clocks"], "l2": "256 MB flush between steps"}
+        line["other_workloads"] = extra
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
