@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--main-only", action="store_true", help="skip the GA prefill and decode lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None,
+                    help="time only this workload of synth.WORKLOADS (one line, no e2e, no "
+                         "CPU baseline); used for the reduced profiler captures")
     return ap.parse_args()
 
 
@@ -88,7 +91,8 @@ def load_peaks():
 
 class ClockSampler:
     """Samples the SM clock and the clock-event (throttle) reasons of this
-    process's GPU through NVML every 5 ms while the timed region runs."""
+    process's GPU while the timed region runs: through NVML every 5 ms when the
+    pynvml module imports, else through `nvidia-smi -lms 50` in a subprocess."""
 
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
                0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
@@ -98,31 +102,22 @@ class ClockSampler:
         self.samples = []
         self.max_mhz = None
         self._stop = None
+        self._proc = None
         self.error = None
+        self.source = None
 
-    def _handle(self):
-        import pynvml
+    def _bus_id(self):
         import torch
-        pynvml.nvmlInit()
         p = torch.cuda.get_device_properties(self.cuda_index)
-        try:
-            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
-            return pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
-        except Exception:
-            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-            idx = int(vis.split(",")[self.cuda_index]) if vis and vis.split(",")[0].isdigit() \
-                else self.cuda_index
-            return pynvml.nvmlDeviceGetHandleByIndex(idx)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
 
-    def __enter__(self):
+    def _start_nvml(self):
         import threading
-        try:
-            import pynvml
-            h = self._handle()
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # no NVML: the line says "unsampled" and why
-            self.error = f"{type(e).__name__}: {e}"
-            return self
+
+        import pynvml
+        pynvml.nvmlInit()
+        h = pynvml.nvmlDeviceGetHandleByPciBusId(self._bus_id().encode())
+        self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
         self._stop = threading.Event()
 
         def loop():
@@ -137,11 +132,55 @@ class ClockSampler:
 
         self._t = threading.Thread(target=loop, daemon=True)
         self._t.start()
+        self.source = "nvml"
+
+    def _start_smi(self):
+        import subprocess
+        import threading
+        q = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+        self._proc = subprocess.Popen(
+            ["nvidia-smi", "-i", self._bus_id(), f"--query-gpu={q}",
+             "--format=csv,noheader,nounits", "-lms", "50"],
+            stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        first = threading.Event()
+
+        def reader():
+            for line in self._proc.stdout:
+                parts = [x.strip() for x in line.split(",")]
+                try:
+                    mhz, mx, rs = float(parts[0]), float(parts[1]), int(parts[2], 16)
+                except (ValueError, IndexError):
+                    continue
+                self.max_mhz = mx
+                self.samples.append((mhz, rs))
+                first.set()
+
+        self._t = threading.Thread(target=reader, daemon=True)
+        self._t.start()
+        first.wait(timeout=5.0)
+        self.source = "nvidia-smi"
+
+    def __enter__(self):
+        try:
+            self._start_nvml()
+        except Exception as e:
+            self.error = f"nvml: {type(e).__name__}: {e}"
+            try:
+                self._start_smi()
+            except Exception as e2:  # no sampler at all: the line says "unsampled" and why
+                self.error += f"; nvidia-smi: {type(e2).__name__}: {e2}"
         return self
 
     def __exit__(self, *exc):
         if self._stop is not None:
             self._stop.set()
+            self._t.join(timeout=2)
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
             self._t.join(timeout=2)
         return False
 
@@ -153,7 +192,7 @@ class ClockSampler:
         reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items()
                           if r & bit})
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(mhz), "source": "nvml"}
+                "reasons": reasons, "samples": len(mhz), "source": self.source}
 
 
 # ------------------------------------------------------------------ workloads
@@ -363,6 +402,25 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ main
+def single_workload(args, ws, rank, local, peaks):
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    if wl["kind"] == "prefill":
+        r = bench_prefill(args.workload, args.steps, args.warmup, ws, local, with_e2e=False)
+        tf = r["flops"] / (r["ms"] / 1e3) / 1e12
+        gbs = r["bytes"] / (r["ms"] / 1e3) / 1e9
+        line = {"workload": args.workload, "ms": r["ms"], "tflops": tf, "gbs": gbs,
+                "frac_tensor": tf / peaks["bf16_tflops"], "frac_hbm": gbs / peaks["hbm_gbs"],
+                "clocks": r["clocks"]}
+    else:
+        r = bench_decode(args.workload, args.steps, args.warmup, ws, local)
+        gbs = r["bytes"] / (r["ms"] / 1e3) / 1e9
+        line = {"workload": args.workload, "ms": r["ms"], "gbs": gbs,
+                "frac_hbm": gbs / peaks["hbm_gbs"], "clocks": r["clocks"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def roofline_obj(bound, achieved, peak, unit, traffic=None):
     return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak if peak else None, "traffic": traffic}
@@ -380,6 +438,9 @@ def main():
         build.build()
     barrier(ws)
     peaks = load_peaks()
+    if args.workload:
+        single_workload(args, ws, rank, local, peaks)
+        return
     m = bench_prefill(MAIN, args.steps, args.warmup, ws, local, with_e2e=True)
     tflops = ws * m["flops"] / (m["ms"] / 1e3) / 1e12
     gbs = m["bytes"] / (m["ms"] / 1e3) / 1e9  # per GPU, per launch (one launch per step)

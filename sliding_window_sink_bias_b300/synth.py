@@ -131,6 +131,11 @@ WORKLOADS = {
                                  len_lo=65536, len_hi=262144, **GA),
     "mtp_decode_swa_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=262144,
                                   len_lo=65536, len_hi=262144, **SWA),
+    # reduced shapes of the same kernels, for profiler captures (a few GB on the device)
+    "swa_prefill_1x32768": dict(kind="prefill", seqlens=[32768], **SWA),
+    "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),
+    "mtp_decode_ga_b8_t4": dict(kind="decode", batch=8, t=4, s_cap=131072,
+                                len_lo=65536, len_hi=131072, **GA),
 }
 
 
