@@ -30,28 +30,10 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
-#include "ptx.cuh"
+#include "common.cuh"
 
 namespace sa {
-
-constexpr int kThreads = 384;
-constexpr int kDqk = 192;
-constexpr int kDv = 128;
-constexpr uint32_t kRowBytes = 128;                     // one 64-element bf16 row of a box
-constexpr uint32_t kQBoxBytes = 128 * kRowBytes;        // 128 packed query rows
-constexpr uint32_t kQStageBytes = 3 * kQBoxBytes;       // dims 0..191
-constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t tmem_s_col(uint32_t buf) { return buf ? 192u : 0u; }
-constexpr uint32_t kTmemO = 384;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;        // 4 s per wait
-constexpr uint64_t kDrainLimitNs = 200000000ull;        // 0.2 s to drain after an abort
-
 enum : int32_t { kModePrefill = 0, kModeDecodePartial = 1 };
-
-// Device status word: bit 0 = a wait timed out; bits 8..15 = the wait site.
-__device__ uint32_t g_status_word;
 
 struct AttnArgs {
   int32_t Hq, Hkv, G;
@@ -142,153 +124,6 @@ __device__ __forceinline__ Item make_item(const AttnArgs &a, int32_t w, int32_t 
     it.valid = 1;
   }
   return it;
-}
-
-// Bounded mbarrier wait.  Returns false if this CTA is aborting.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                      uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  uint32_t n = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (++n == 32) {
-      n = 0;
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1u;
-        atomicOr(&g_status_word, 1u | (site << 8));
-        return false;
-      }
-    }
-  }
-}
-
-// Warp-uniform form: every lane polls, then the warp agrees, so warp-collective
-// tcgen05.ld/st that follow never run with part of the warp gone.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
-                                              volatile uint32_t *abort_flag, uint32_t site) {
-  const bool ok = wait_bar(bar, parity, abort_flag, site);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Wait used only while draining: ignores the abort flag, short limit.
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kDrainLimitNs) {
-      atomicOr(&g_status_word, 1u | (0xFFu << 8));
-      return;
-    }
-  }
-}
-
-// cos/sin of pos * theta_t from a 64-bit fixed-point angle in turns: the product
-// wraps modulo one full turn exactly, so the angle is exact before the final
-// conversion to a float in [-pi, pi).
-__device__ __forceinline__ void rope_cs(int32_t pos, unsigned long long turns_fp, float &c,
-                                        float &s) {
-  const unsigned long long prod =
-      static_cast<unsigned long long>(static_cast<long long>(pos)) * turns_fp;
-  const int32_t hi = static_cast<int32_t>(prod >> 32);
-  const float ang = static_cast<float>(hi) * 1.4629180792671596e-09f;  // 2 pi / 2^32
-  __sincosf(ang, &s, &c);
-}
-
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// The rotated dims 0..63 are written back as fp16, not bf16: the 64-dim part of
-// q.k then runs as its own fp16 x fp16 MMA k-steps (fp32 accumulate), and the
-// rotation's re-rounding error drops 8-fold (11 vs 8 significant bits).
-// Rotate the four (2t, 2t+1) pairs stored in one 16-byte chunk (pairs 4c..4c+3).
-__device__ __forceinline__ void rot_chunk_interleaved(uint4 *p, const float (&cs)[4],
-                                                      const float (&sn)[4]) {
-  uint4 v = *p;
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float x = bf16lo(w[e]), y = bf16hi(w[e]);
-    w[e] = pack_f16x2(x * cs[e] - y * sn[e], x * sn[e] + y * cs[e]);
-  }
-  *p = make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Rotate the eight (t, t+32) pairs held by chunk c (dims 8c..8c+7) and chunk
-// c+4 (dims 32+8c..32+8c+7).
-__device__ __forceinline__ void rot_chunks_half(uint4 *pa, uint4 *pb, const float (&cs)[8],
-                                                const float (&sn)[8]) {
-  uint4 va = *pa, vb = *pb;
-  uint32_t a[4] = {va.x, va.y, va.z, va.w};
-  uint32_t b[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float x0 = bf16lo(a[e]), y0 = bf16lo(b[e]);
-    const float x1 = bf16hi(a[e]), y1 = bf16hi(b[e]);
-    const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
-    a[e] = pack_f16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
-    b[e] = pack_f16x2(x0 * s0 + y0 * c0, x1 * s1 + y1 * c1);
-  }
-  *pa = make_uint4(a[0], a[1], a[2], a[3]);
-  *pb = make_uint4(b[0], b[1], b[2], b[3]);
-}
-
-// Address of 16-byte chunk c of row r in a 128B-swizzled box (1024-byte aligned).
-__device__ __forceinline__ uint4 *swz_chunk(uint8_t *box, int32_t r, int32_t c) {
-  return reinterpret_cast<uint4 *>(box + r * kRowBytes + ((c ^ (r & 7)) << 4));
-}
-
-// RoPE on dims 0..63 (box 0) of the Q tile: rows r = t * G + g share the angle
-// of token t, so each (token, chunk) unit computes its angles once.
-__device__ void rope_q_tile(uint8_t *box0, const Item &it, const AttnArgs &a,
-                            const unsigned long long *turns, int32_t tid) {
-  const int32_t G = a.G, nt = it.n_tok;
-  const int32_t nch = a.rope_style == 0 ? 8 : 4;
-  const int32_t units = nt * nch;
-  int32_t hsplit = units >= 128 ? 1 : min(G, 128 / units);
-  const int32_t hper = (G + hsplit - 1) / hsplit;
-  for (int32_t u = tid; u < units * hsplit; u += 128) {
-    const int32_t hs = u / units, tc = u % units;
-    const int32_t t = tc / nch, c = tc % nch;
-    const int32_t pos = it.pos0 + t;
-    const int32_t g0 = hs * hper, g1 = min(G, g0 + hper);
-    if (a.rope_style == 0) {
-      float cs[4], sn[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) rope_cs(pos, turns[4 * c + e], cs[e], sn[e]);
-      for (int32_t g = g0; g < g1; ++g) rot_chunk_interleaved(swz_chunk(box0, t * G + g, c), cs, sn);
-    } else {
-      float cs[8], sn[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) rope_cs(pos, turns[8 * c + e], cs[e], sn[e]);
-      for (int32_t g = g0; g < g1; ++g) {
-        const int32_t r = t * G + g;
-        rot_chunks_half(swz_chunk(box0, r, c), swz_chunk(box0, r, c + 4), cs, sn);
-      }
-    }
-  }
-}
-
-// RoPE on dims 0..63 (box 0) of a K block of `rows` keys at positions kpos0 + row.
-__device__ void rope_k_block(uint8_t *box0, int32_t rows, int32_t kpos0, const AttnArgs &a,
-                             const unsigned long long *turns, int32_t tid) {
-  if (a.rope_style == 0) {
-    for (int32_t u = tid; u < rows * 8; u += 128) {
-      const int32_t r = u >> 3, c = u & 7;
-      float cs[4], sn[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) rope_cs(kpos0 + r, turns[4 * c + e], cs[e], sn[e]);
-      rot_chunk_interleaved(swz_chunk(box0, r, c), cs, sn);
-    }
-  } else {
-    for (int32_t u = tid; u < rows * 4; u += 128) {
-      const int32_t r = u >> 2, c = u & 3;
-      float cs[8], sn[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) rope_cs(kpos0 + r, turns[8 * c + e], cs[e], sn[e]);
-      rot_chunks_half(swz_chunk(box0, r, c), swz_chunk(box0, r, c + 4), cs, sn);
-    }
-  }
 }
 
 template <int BN, int NQ, int NKV>
@@ -661,7 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!it.valid) continue;
       const uint32_t qs = gq % NQ;
       if (!(ok = wait_bar_warp(B_QFULL(qs), (gq / NQ) & 1, abort_flag, 10))) break;
-      if (args.rope_on) rope_q_tile(smem + Ly::kQOff + qs * kQStageBytes, it, args, turns, tid);
+      if (args.rope_on)
+        rope_q_tile(smem + Ly::kQOff + qs * kQStageBytes, G, it.n_tok, it.pos0, args.rope_style,
+                    turns, tid);
       fence_proxy_async_smem();
       mbar_arrive(B_QREADY(qs));
       ++gq;
@@ -669,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ks = gk % NKV;
         if (!(ok = wait_bar_warp(B_KVFULL(ks), (gk / NKV) & 1, abort_flag, 11))) break;
         if (args.rope_on)
-          rope_k_block(smem + Ly::kKVOff + ks * Ly::kKVStage, BN, it.kstart + j * BN, args, turns,
-                       tid);
+          rope_k_rows(smem + Ly::kKVOff + ks * Ly::kKVStage, BN, it.kstart + j * BN,
+                      args.rope_style, turns, tid);
         fence_proxy_async_smem();
         mbar_arrive(B_KREADY(ks));
         ++gk;

@@ -1,0 +1,537 @@
+// band_kernel.cuh -- sliding-window (SWA) prefill for 8 query heads per KV head.
+//
+// Computes the attention layer of the MiMo-V2-Flash Technical Report (§2.2
+// eqs. (1)-(3), shapes of §2.1 Table 1) for the sliding-window layers: key j
+// is visible to query i iff i - W < j <= i, W <= 128.
+//
+// A tile is 16 consecutive tokens x the 8 query heads of one KV head (128 MMA
+// rows, row r = token * 8 + head).  Its keys are the 16-key segments
+// [t0 - 128, t0 + 16) (W = 128: 9 segments, 144 keys), so one QK^T MMA of
+// N = 144 and one PV of K = 144 cover the whole band of the tile.
+//
+// Each CTA walks a contiguous run of tiles of one (sequence, KV head) lane at a
+// time (the flattened tile list is cut into gridDim.x equal pieces), and keeps
+// the keys and values of the band in a shared-memory ring of 12 segments: a
+// tile loads only its own 16 new keys, so K and V are read from memory once,
+// and the loads run up to three tiles ahead of the MMAs.
+//
+// Warp roles (384 threads, one CTA per SM):
+//   warp 0       TMA producer: Q tile (3 boxes of 64 dims, 2 stages), new K/V segments.
+//   warp 1       MMA issuer: S = Q K^T into TMEM (two MMAs when the band wraps
+//                around the end of the ring), then O = P V with P read from TMEM.
+//   warp 2       TMEM allocator (S0, S1, O).
+//   warp 3       set-up: locates this CTA's first tile.
+//   warps 4-7    softmax + epilogue, one row per thread: max over the band with
+//                the sink (eq. (2)), P = 2^(s*scale*log2e - m) as bf16 into TMEM,
+//                l = 2^(sink - m) + sum P, then o = O / l and the log-sum-exp.
+//   warps 8-11   RoPE on dims 0..63 of the Q tile and of each new K segment.
+#pragma once
+#include "common.cuh"
+
+namespace sa {
+
+constexpr int32_t kBandSeg = 16;   // keys per ring segment = tokens per tile
+constexpr int32_t kBandRing = 12;  // segments in the K/V ring
+constexpr int32_t kBandMaxWin = 9; // segments of a full window, W <= 128
+constexpr int32_t kBandG = 8;      // query heads per KV head
+
+struct BandArgs {
+  int32_t Hq, Hkv;
+  int32_t window;      // 1..128
+  int32_t batch;
+  int32_t nseg;        // segments of a full window: ceil((window - 1) / 16) + 1
+  int32_t rope_on, rope_style;
+  float scale_log2;    // logit scale * log2(e), > 0
+  const int32_t *cu_seqlens;
+  const float *sink;
+  __nv_bfloat16 *out;
+  float *lse;
+  unsigned long long rope_turns[32];
+};
+
+struct BandLayout {
+  static constexpr uint32_t kSegBox = kBandSeg * kRowBytes;   // 16 keys x 64 dims: 2 KB
+  static constexpr uint32_t kRingBox = kBandRing * kSegBox;   // 24 KB
+  static constexpr uint32_t kQOff = 0;                        // 2 stages x 48 KB
+  static constexpr uint32_t kKOff = 2 * kQStageBytes;         // 3 ring boxes (dims 0..191)
+  static constexpr uint32_t kVOff = kKOff + 3 * kRingBox;     // 2 ring boxes (dims 0..127)
+  static constexpr uint32_t kBarOff = kVOff + 2 * kRingBox;
+  // q_full[2] q_ready[2] q_empty[2] seg_full[R] seg_ready[R] seg_empty[R]
+  // s_full[2] p_full[2] pv_done o_empty drain
+  static constexpr uint32_t kNumBars = 6 + 3 * kBandRing + 7;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem, abort, cursor[4]
+  static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;
+  static constexpr uint32_t kBytes = kTurnsOff + 32 * 8;
+  static constexpr uint32_t kDynSmem = kBytes + 1024;
+};
+static_assert(BandLayout::kDynSmem <= 232448, "band kernel shared memory");
+
+// Position in the flattened tile list: tile i of sequence b, KV head kvh.
+struct BandCursor {
+  int32_t b, kvh, i;
+  int32_t ntile;   // tiles of sequence b
+  int32_t s0, L;   // first packed row and length of sequence b
+  int32_t left;    // tiles of this CTA not yet passed (the current one included)
+  int32_t run;     // 1 if this tile starts a run (first of the CTA or of its lane)
+};
+
+__device__ __forceinline__ void band_load_seq(BandCursor &c, const BandArgs &a) {
+  c.s0 = __ldg(a.cu_seqlens + c.b);
+  c.L = __ldg(a.cu_seqlens + c.b + 1) - c.s0;
+  c.ntile = (c.L + kBandSeg - 1) / kBandSeg;
+}
+
+__device__ __forceinline__ void band_next(BandCursor &c, const BandArgs &a) {
+  c.run = 0;
+  if (--c.left <= 0) return;
+  if (++c.i < c.ntile) return;
+  c.i = 0;
+  c.run = 1;
+  if (++c.kvh < a.Hkv) return;
+  c.kvh = 0;
+  do {
+    ++c.b;
+    band_load_seq(c, a);
+  } while (c.ntile == 0 && c.b + 1 < a.batch);
+}
+
+// Window of the cursor's tile: nwin segments starting at segment i - nwin + 1.
+__device__ __forceinline__ int32_t band_nwin(const BandCursor &c, const BandArgs &a) {
+  return min(c.i + 1, a.nseg);
+}
+
+// Set-up (one warp): the exact number of tiles, this CTA's share of the
+// flattened list and the (sequence, KV head, tile) it starts at.
+__device__ void band_locate(const BandArgs &a, int32_t lane, int32_t *cur) {
+  uint32_t ct = 0;
+  for (int32_t b = lane; b < a.batch; b += 32) {
+    const int32_t L = __ldg(a.cu_seqlens + b + 1) - __ldg(a.cu_seqlens + b);
+    ct += static_cast<uint32_t>((L + kBandSeg - 1) / kBandSeg);
+  }
+  ct = __reduce_add_sync(0xffffffffu, ct);
+  const int64_t T = int64_t(ct) * a.Hkv;
+  const int64_t f0 = T * blockIdx.x / gridDim.x;
+  const int64_t f1 = T * (blockIdx.x + 1) / gridDim.x;
+  int32_t sb = 0, skvh = 0, si = 0;
+  bool found = false;
+  int64_t run = 0;
+  for (int32_t base = 0; base < a.batch && !found && f1 > f0; base += 32) {
+    const int32_t b = base + lane;
+    int32_t c = 0;
+    if (b < a.batch) {
+      const int32_t L = __ldg(a.cu_seqlens + b + 1) - __ldg(a.cu_seqlens + b);
+      c = (L + kBandSeg - 1) / kBandSeg;
+    }
+    const int64_t w = int64_t(c) * a.Hkv;
+    int64_t incl = w;
+#pragma unroll
+    for (int32_t o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, w > 0 && run + incl > f0);
+    if (m) {
+      const int32_t j = __ffs(m) - 1;
+      const int64_t incl_j = __shfl_sync(0xffffffffu, incl, j);
+      const int64_t w_j = __shfl_sync(0xffffffffu, w, j);
+      const int32_t c_j = __shfl_sync(0xffffffffu, c, j);
+      const int64_t off = f0 - (run + incl_j - w_j);
+      sb = base + j;
+      skvh = static_cast<int32_t>(off / c_j);
+      si = static_cast<int32_t>(off % c_j);
+      found = true;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    cur[0] = sb;
+    cur[1] = skvh;
+    cur[2] = si;
+    cur[3] = found ? static_cast<int32_t>(f1 - f0) : 0;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sinkattn_band_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ BandArgs args) {
+  using Ly = BandLayout;
+  constexpr int32_t R = kBandRing;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const int32_t warp = threadIdx.x >> 5;
+  const int32_t lane = threadIdx.x & 31;
+
+  auto bar = [&](uint32_t i) { return sbase + Ly::kBarOff + i * 8; };
+  auto B_QFULL = [&](uint32_t s) { return bar(s); };
+  auto B_QREADY = [&](uint32_t s) { return bar(2 + s); };
+  auto B_QEMPTY = [&](uint32_t s) { return bar(4 + s); };
+  auto B_SEGFULL = [&](uint32_t s) { return bar(6 + s); };
+  auto B_SEGREADY = [&](uint32_t s) { return bar(6 + R + s); };
+  auto B_SEGEMPTY = [&](uint32_t s) { return bar(6 + 2 * R + s); };
+  auto B_SFULL = [&](uint32_t b) { return bar(6 + 3 * R + b); };
+  auto B_PFULL = [&](uint32_t b) { return bar(6 + 3 * R + 2 + b); };
+  const uint32_t B_PVDONE = bar(6 + 3 * R + 4);
+  const uint32_t B_OEMPTY = bar(6 + 3 * R + 5);
+  const uint32_t B_DRAIN = bar(6 + 3 * R + 6);
+
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
+  int32_t *cur_smem = reinterpret_cast<int32_t *>(smem + Ly::kMiscOff + 16);
+  unsigned long long *turns = reinterpret_cast<unsigned long long *>(smem + Ly::kTurnsOff);
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < 2; ++s) {
+      mbar_init(B_QFULL(s), 1);
+      mbar_init(B_QREADY(s), 128);
+      mbar_init(B_QEMPTY(s), 1);
+      mbar_init(B_SFULL(s), 1);
+      mbar_init(B_PFULL(s), 128);
+    }
+    for (uint32_t s = 0; s < R; ++s) {
+      mbar_init(B_SEGFULL(s), 1);
+      mbar_init(B_SEGREADY(s), 128);
+      mbar_init(B_SEGEMPTY(s), 1);
+    }
+    mbar_init(B_PVDONE, 1);
+    mbar_init(B_OEMPTY, 128);
+    mbar_init(B_DRAIN, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) turns[threadIdx.x] = args.rope_turns[threadIdx.x];
+  if (warp == 2) {
+    tmem_alloc(sbase + Ly::kMiscOff, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 3) band_locate(args, lane, cur_smem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  BandCursor c0;
+  c0.b = cur_smem[0];
+  c0.kvh = cur_smem[1];
+  c0.i = cur_smem[2];
+  c0.left = cur_smem[3];
+  c0.run = 1;
+  if (c0.left > 0) band_load_seq(c0, args);
+  const int32_t W = args.window;
+  // Registers: the launch gives 168 per thread (64,512 in all).  The softmax
+  // warpgroup holds a 144-column band row and takes 240; the producer/MMA and
+  // RoPE warpgroups give back to 88 each: (88 + 240 + 88) x 128 = 53,248.  Each
+  // warpgroup changes its count inside its own branch (so ptxas compiles each
+  // role under its own limit) and returns to 168 before the common teardown.
+  if (warp < 4) {
+    setmaxnreg_dec<88>();
+    if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0 && c0.left > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t gq = 0, gseg = 0;
+      bool ok = true;
+      for (BandCursor c = c0; ok && c.left > 0; band_next(c, args)) {
+        const uint32_t qs = gq & 1;
+        if (!(ok = wait_bar(B_QEMPTY(qs), ((gq >> 1) & 1) ^ 1, abort_flag, 1))) break;
+        mbar_arrive_expect_tx(B_QFULL(qs), 3u * kQBoxBytes);
+        const uint32_t qdst = sbase + Ly::kQOff + qs * kQStageBytes;
+        const int32_t qrow = c.s0 + c.i * kBandSeg;
+#pragma unroll
+        for (int cc = 0; cc < 3; ++cc)
+          tma_load_3d(qdst + cc * kQBoxBytes, &tm_q, cc * 64, c.kvh * kBandG, qrow, B_QFULL(qs));
+        ++gq;
+        const int32_t nwin = band_nwin(c, args);
+        const int32_t nload = c.run ? nwin : 1;
+        for (int32_t j = 0; j < nload; ++j) {
+          const int32_t seg = c.i - nload + 1 + j;
+          const uint32_t slot = gseg % R;
+          if (!(ok = wait_bar(B_SEGEMPTY(slot), ((gseg / R) & 1) ^ 1, abort_flag, 2))) break;
+          mbar_arrive_expect_tx(B_SEGFULL(slot), 5u * Ly::kSegBox);
+          const int32_t krow = c.s0 + seg * kBandSeg;
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc)
+            tma_load_3d(sbase + Ly::kKOff + cc * Ly::kRingBox + slot * Ly::kSegBox, &tm_k, cc * 64,
+                        c.kvh, krow, B_SEGFULL(slot));
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            tma_load_3d(sbase + Ly::kVOff + cc * Ly::kRingBox + slot * Ly::kSegBox, &tm_v, cc * 64,
+                        c.kvh, krow, B_SEGFULL(slot));
+          ++gseg;
+        }
+      }
+      // Drain: the last copy into each stage and slot must land before the CTA exits.
+      for (uint32_t s = 0; s < 2; ++s)
+        if (gq > s) drain_wait(B_QFULL(s), ((gq - 1 - s) >> 1) & 1);
+      for (uint32_t s = 0; s < R; ++s)
+        if (gseg > s) drain_wait(B_SEGFULL(s), ((gseg - 1 - s) / R) & 1);
+    }
+    } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0 && c0.left > 0) {
+      constexpr uint32_t kIdescPV = idesc_f32acc(128, kDv, 1, 0, 1);
+      uint32_t gt = 0, gseg = 0;
+      bool ok = true;
+      // the previous tile, whose PV is issued after the next tile's QK^T
+      int32_t p_nwin = 0;
+      uint32_t p_first = 0;
+      auto issue_pv = [&](uint32_t t, int32_t nwin, uint32_t g_first, int32_t nfree) -> bool {
+        const uint32_t buf = t & 1;
+        if (!wait_bar(B_PFULL(buf), (t >> 1) & 1, abort_flag, 4)) return false;
+        tc_fence_after();
+        if (!wait_bar(B_OEMPTY, (t & 1) ^ 1, abort_flag, 5)) return false;
+        tc_fence_after();
+        for (int32_t kk = 0; kk < nwin; ++kk) {
+          const uint32_t slot = (g_first + kk) % R;
+          // B = V, MN-major: the two 64-column halves of dv are one ring box
+          // apart (LBO); the two 8-key groups of the k-step 1024 B apart (SBO).
+          const uint64_t bdesc =
+              smem_desc_sw128(sbase + Ly::kVOff + slot * Ly::kSegBox, Ly::kRingBox, 1024);
+          mma_ts(tmem + kTmemO, tmem + tmem_s_col(buf) + kk * 8, bdesc, kIdescPV, kk > 0 ? 1u : 0u);
+        }
+        for (int32_t kk = 0; kk < nfree; ++kk) mma_commit(B_SEGEMPTY((g_first + kk) % R));
+        mma_commit(B_PVDONE);
+        return true;
+      };
+      for (BandCursor c = c0; ok && c.left > 0; band_next(c, args)) {
+        const int32_t nwin = band_nwin(c, args);
+        const int32_t nload = c.run ? nwin : 1;
+        if (gt > 0 && c.run) {
+          // a new run reloads the whole band: the previous tile's segments must
+          // be released (its PV issued) before this tile's loads can land
+          if (!(ok = issue_pv(gt - 1, p_nwin, p_first, p_nwin))) break;
+        }
+        const uint32_t qs = gt & 1;
+        if (!(ok = wait_bar(B_QREADY(qs), (gt >> 1) & 1, abort_flag, 3))) break;
+        for (int32_t j = 0; j < nload && ok; ++j) {
+          const uint32_t g = gseg + j;
+          ok = wait_bar(B_SEGREADY(g % R), (g / R) & 1, abort_flag, 6);
+        }
+        if (!ok) break;
+        tc_fence_after();
+        gseg += nload;
+        const uint32_t g_first = gseg - nwin;
+        const uint32_t buf = gt & 1;
+        const uint32_t slot0 = g_first % R;
+        const int32_t n1 = min(nwin, R - static_cast<int32_t>(slot0));
+        const int32_t n2 = nwin - n1;
+        const uint32_t rot = args.rope_on ? 0u : 1u;  // rotated dims are fp16
+        const uint32_t id1 = idesc_f32acc(128, n1 * kBandSeg, 1, 0, 0);
+        const uint32_t id1r = idesc_f32acc(128, n1 * kBandSeg, rot, 0, 0);
+        const uint32_t id2 = idesc_f32acc(128, (n2 > 0 ? n2 : 1) * kBandSeg, 1, 0, 0);
+        const uint32_t id2r = idesc_f32acc(128, (n2 > 0 ? n2 : 1) * kBandSeg, rot, 0, 0);
+        const uint32_t qaddr = sbase + Ly::kQOff + qs * kQStageBytes;
+        const uint32_t s_t = tmem + tmem_s_col(buf);
+#pragma unroll
+        for (int kstep = 0; kstep < kDqk / 16; ++kstep) {
+          const uint32_t box = kstep >> 2, off = (kstep & 3) * 32;
+          const uint64_t adesc = smem_desc_sw128(qaddr + box * kQBoxBytes + off, 16, 1024);
+          const uint32_t kb = sbase + Ly::kKOff + box * Ly::kRingBox + off;
+          mma_ss(s_t, adesc, smem_desc_sw128(kb + slot0 * Ly::kSegBox, 16, 1024),
+                 box == 0 ? id1r : id1, kstep > 0 ? 1u : 0u);
+          if (n2 > 0)
+            mma_ss(s_t + n1 * kBandSeg, adesc, smem_desc_sw128(kb, 16, 1024), box == 0 ? id2r : id2,
+                   kstep > 0 ? 1u : 0u);
+        }
+        mma_commit(B_SFULL(buf));
+        mma_commit(B_QEMPTY(qs));
+        if (gt > 0 && !c.run) {
+          // same lane: the oldest segment of the previous band leaves the window
+          // once the band is full
+          const int32_t nfree = nwin == p_nwin ? 1 : 0;
+          if (!(ok = issue_pv(gt - 1, p_nwin, p_first, nfree))) break;
+        }
+        p_nwin = nwin;
+        p_first = g_first;
+        ++gt;
+      }
+      if (ok && gt > 0) ok = issue_pv(gt - 1, p_nwin, p_first, p_nwin);
+      if (gt > 0) {
+        mma_commit(B_DRAIN);
+        drain_wait(B_DRAIN, 0);
+      }
+    }
+    }
+    __syncwarp();
+    setmaxnreg_inc<168>();
+  } else if (warp < 8) {
+    setmaxnreg_inc<240>();
+    // ============================================================ softmax + epilogue
+    // Tile i's softmax runs before tile i-1's epilogue, so these warps never
+    // wait on a PV: by the time tile i's P is stored, PV(i-1) has long finished.
+    const int32_t row = threadIdx.x - 128;  // query row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int32_t t = row / kBandG, g = row % kBandG;
+    const float sc = args.scale_log2;
+    const uint32_t o_t = tmem + lane_off + kTmemO;
+    uint32_t gt = 0;
+    bool ok = true;
+    // the tile whose epilogue is pending
+    bool p_valid = false;
+    size_t p_orow = 0;
+    float p_m = 0.f, p_l = 0.f;
+    auto epilogue = [&](uint32_t tt) -> bool {
+      if (!wait_bar_warp(B_PVDONE, tt & 1, abort_flag, 9)) return false;
+      tc_fence_after();
+      uint32_t o[kDv];
+#pragma unroll
+      for (int32_t cb = 0; cb < kDv; cb += 32) tmem_ld32p(o_t + cb, o + cb);
+      tmem_wait_ld();
+      reg_fence<kDv>(o);
+      // O is in registers: the next PV may overwrite it
+      tc_fence_before();
+      mbar_arrive(B_OEMPTY);
+      if (p_valid) {
+        // eq. (3) with the denominator of eq. (2): o = O / l, lse = (m + log2 l) ln 2
+        const float inv_l = p_l > 0.f ? 1.f / p_l : 0.f;
+        uint4 *dst = reinterpret_cast<uint4 *>(args.out + p_orow * kDv);
+#pragma unroll
+        for (int32_t q4 = 0; q4 < kDv / 8; ++q4) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int32_t e = 0; e < 4; ++e)
+            w4[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
+                                __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
+          dst[q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        args.lse[p_orow] = p_l > 0.f ? (p_m + __log2f(p_l)) * kLn2 : -INFINITY;
+      }
+      return true;
+    };
+    constexpr int32_t NC = kBandMaxWin * kBandSeg;  // 144 columns at most
+    for (BandCursor c = c0; ok && c.left > 0; band_next(c, args)) {
+      const int32_t head = c.kvh * kBandG + g;
+      const int32_t pos = c.i * kBandSeg + t;
+      const bool rvalid = pos < c.L;
+      const int32_t nwin = band_nwin(c, args);
+      const int32_t kstart = (c.i - nwin + 1) * kBandSeg;
+      int32_t lo = max(0, pos - W + 1) - kstart;  // visible columns [lo, hi]
+      int32_t hi = pos - kstart;
+      if (!rvalid) { lo = 1; hi = 0; }
+      const float sk2 = __ldg(args.sink + head) * kLog2e;  // -inf stays -inf
+      const uint32_t buf = gt & 1;
+      if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
+      tc_fence_after();
+      const uint32_t s_t = tmem + lane_off + tmem_s_col(buf);
+      // The whole band row in registers with one wait (columns past the
+      // window hold stale values and are masked: hi < nwin * 16 always).
+      uint32_t r[NC];
+#pragma unroll
+      for (int32_t cb = 0; cb < 128; cb += 32) tmem_ld32p(s_t + cb, r + cb);
+      tmem_ld16p(s_t + 128, r + 128);
+      tmem_wait_ld();
+      reg_fence<NC>(r);
+      // Interior rows of a full W = 128 band see columns [lo, hi] with lo <= 16
+      // and hi >= 127: only the first and last 16 columns need a mask.
+      const bool interior = lo <= 16 && hi >= 127;
+      const bool fast = __all_sync(0xffffffffu, interior);
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (fast) {
+#pragma unroll
+        for (int32_t k = 0; k < 16; ++k) {
+          mx0 = fmaxf(mx0, k >= lo ? __uint_as_float(r[k]) : -INFINITY);
+          mx1 = fmaxf(mx1, 128 + k <= hi ? __uint_as_float(r[128 + k]) : -INFINITY);
+        }
+#pragma unroll
+        for (int32_t k = 16; k < 128; k += 2) {
+          mx0 = fmaxf(mx0, __uint_as_float(r[k]));
+          mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
+        }
+      } else {
+#pragma unroll
+        for (int32_t k = 0; k < NC; k += 2) {
+          mx0 = fmaxf(mx0, (k >= lo && k <= hi) ? __uint_as_float(r[k]) : -INFINITY);
+          mx1 = fmaxf(mx1, (k + 1 >= lo && k + 1 <= hi) ? __uint_as_float(r[k + 1]) : -INFINITY);
+        }
+      }
+      // eq. (2): m = max(max_j a_ij, sink), in the log2 domain (scale > 0)
+      const float m = fmaxf(fmaxf(mx0, mx1) * sc, sk2);
+      const float mneg = m == -INFINITY ? 0.f : -m;
+      // P = 2^(s * scale * log2e - m), packed bf16 in place, then into TMEM over S
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int32_t k = 0; k < NC; k += 2) {
+        float p0 = ex2(fmaf(__uint_as_float(r[k]), sc, mneg));
+        float p1 = ex2(fmaf(__uint_as_float(r[k + 1]), sc, mneg));
+        if (fast) {
+          if (k < 16) {
+            if (k < lo) p0 = 0.f;
+            if (k + 1 < lo) p1 = 0.f;
+          } else if (k >= 128) {
+            if (k > hi) p0 = 0.f;
+            if (k + 1 > hi) p1 = 0.f;
+          }
+        } else {
+          if (!(k >= lo && k <= hi)) p0 = 0.f;
+          if (!(k + 1 >= lo && k + 1 <= hi)) p1 = 0.f;
+        }
+        sum0 += p0;
+        sum1 += p1;
+        r[k >> 1] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32p(s_t, r);
+      tmem_st32p(s_t + 32, r + 32);
+      tmem_st8p(s_t + 64, r + 64);
+      tmem_wait_st();
+      const float l = (sk2 == -INFINITY ? 0.f : ex2(sk2 + mneg)) + (sum0 + sum1);
+      tc_fence_before();
+      mbar_arrive(B_PFULL(buf));
+      if (gt > 0 && !(ok = epilogue(gt - 1))) break;
+      p_valid = rvalid;
+      p_orow = static_cast<size_t>(c.s0 + pos) * args.Hq + head;
+      p_m = m;
+      p_l = l;
+      ++gt;
+    }
+    if (ok && gt > 0) epilogue(gt - 1);
+    __syncwarp();
+    setmaxnreg_dec<168>();
+  } else {
+    setmaxnreg_dec<88>();
+    // ============================================================ RoPE
+    const int32_t tid = threadIdx.x - 256;
+    uint32_t gq = 0, gseg = 0;
+    bool ok = true;
+    for (BandCursor c = c0; ok && c.left > 0; band_next(c, args)) {
+      const uint32_t qs = gq & 1;
+      if (!(ok = wait_bar_warp(B_QFULL(qs), (gq >> 1) & 1, abort_flag, 10))) break;
+      if (args.rope_on)
+        rope_q_tile(smem + Ly::kQOff + qs * kQStageBytes, kBandG, min(kBandSeg, c.L - c.i * kBandSeg),
+                    c.i * kBandSeg, args.rope_style, turns, tid);
+      fence_proxy_async_smem();
+      mbar_arrive(B_QREADY(qs));
+      ++gq;
+      const int32_t nwin = band_nwin(c, args);
+      const int32_t nload = c.run ? nwin : 1;
+      for (int32_t j = 0; j < nload; ++j) {
+        const int32_t seg = c.i - nload + 1 + j;
+        const uint32_t slot = gseg % R;
+        if (!(ok = wait_bar_warp(B_SEGFULL(slot), (gseg / R) & 1, abort_flag, 11))) break;
+        if (args.rope_on)
+          rope_k_rows(smem + Ly::kKOff + slot * Ly::kSegBox, kBandSeg, seg * kBandSeg,
+                      args.rope_style, turns, tid);
+        fence_proxy_async_smem();
+        mbar_arrive(B_SEGREADY(slot));
+        ++gseg;
+      }
+    }
+    __syncwarp();
+    setmaxnreg_inc<168>();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace sa

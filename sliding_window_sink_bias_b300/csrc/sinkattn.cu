@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "attn_kernel.cuh"
+#include "band_kernel.cuh"
 #include "sinkattn.h"
 
 namespace {
@@ -119,6 +120,43 @@ sinkattn_status launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
+// Sliding-window prefill with 8 query heads per KV head and W <= 128: the
+// banded kernel with the K/V ring.
+sinkattn_status launch_band(const void *q, const void *k, const void *v, const AttnArgs &a,
+                            const int32_t *cu_seqlens, int32_t batch, int32_t total,
+                            const DeviceInfo &dev, cudaStream_t stream) {
+  sa::BandArgs b;
+  std::memset(&b, 0, sizeof b);
+  b.Hq = a.Hq;
+  b.Hkv = a.Hkv;
+  b.window = a.window;
+  b.batch = batch;
+  b.nseg = (a.window - 1 + sa::kBandSeg - 1) / sa::kBandSeg + 1;
+  b.rope_on = a.rope_on;
+  b.rope_style = a.rope_style;
+  b.scale_log2 = a.scale_log2;
+  b.cu_seqlens = cu_seqlens;
+  b.sink = a.sink;
+  b.out = a.out;
+  b.lse = a.lse;
+  std::memcpy(b.rope_turns, a.rope_turns, sizeof b.rope_turns);
+  // upper bound of the tile count: sum_b ceil(L_b / 16) <= (total + 15 * batch) / 16
+  const int64_t tiles = int64_t(a.Hkv) * ((int64_t(total) + 15 * int64_t(batch)) / sa::kBandSeg);
+  if (tiles > INT32_MAX) return SINKATTN_EUNSUPPORTED;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, 192, a.Hq, total, sa::kBandG, sa::kBandSeg) ||
+      !make_map(&mk, k, 192, a.Hkv, total, 1, sa::kBandSeg) ||
+      !make_map(&mv, v, 128, a.Hkv, total, 1, sa::kBandSeg))
+    return SINKATTN_ECUDA;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, dev.sms)));
+  auto kern = sa::sinkattn_band_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sa::BandLayout::kDynSmem)) != cudaSuccess)
+    return SINKATTN_ECUDA;
+  kern<<<grid, sa::kThreads, sa::BandLayout::kDynSmem, stream>>>(mq, mk, mv, b);
+  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+}
+
 struct DecodePlan {
   int32_t chunk = 0, splits = 0, rows = 0;
   size_t bytes = 0;
@@ -217,13 +255,17 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
   if (!device_info(dev)) return SINKATTN_ECUDA;
   if (dev.major != 10 || dev.minor != 3) return SINKATTN_EUNSUPPORTED;
 
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (G == sa::kBandG && window >= 1 && window <= sa::kBandMaxWin * sa::kBandSeg - sa::kBandSeg &&
+      a.scale_log2 > 0.f)
+    return launch_band(q, k, v, a, cu_seqlens, batch, total, dev, s);
+
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, num_q_heads, total, G, tile_tokens) ||
       !make_map(&mk, k, 192, num_kv_heads, total, 1, BN) ||
       !make_map(&mv, v, 128, num_kv_heads, total, 1, BN))
     return SINKATTN_ECUDA;
   const int grid = static_cast<int>(std::min<int64_t>(n_items, dev.sms));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (wide) return launch<kBNWide, 2, 1>(mq, mk, mv, a, grid, s);
   return launch<kBN, 1, 2>(mq, mk, mv, a, grid, s);
 }
