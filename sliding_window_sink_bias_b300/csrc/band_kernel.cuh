@@ -15,16 +15,20 @@
 // tile loads only its own 16 new keys, so K and V are read from memory once,
 // and the loads run up to three tiles ahead of the MMAs.
 //
-// Warp roles (384 threads, one CTA per SM):
+// Warp roles (512 threads, one CTA per SM):
 //   warp 0       TMA producer: Q tile (3 boxes of 64 dims, 2 stages), new K/V segments.
 //   warp 1       MMA issuer: S = Q K^T into TMEM (two MMAs when the band wraps
 //                around the end of the ring), then O = P V with P read from TMEM.
 //   warp 2       TMEM allocator (S0, S1, O).
 //   warp 3       set-up: locates this CTA's first tile.
-//   warps 4-7    softmax + epilogue, one row per thread: max over the band with
-//                the sink (eq. (2)), P = 2^(s*scale*log2e - m) as bf16 into TMEM,
-//                l = 2^(sink - m) + sum P, then o = O / l and the log-sum-exp.
-//   warps 8-11   RoPE on dims 0..63 of the Q tile and of each new K segment.
+//   warps 4-11   softmax + epilogue, two threads per row (TMEM lane): warps 4-7
+//                take band columns 0..71 and output dims 0..63, warps 8-11 band
+//                columns 72..143 and output dims 64..127.  Per tile: row max over
+//                the band with the sink (eq. (2); partial maxima swapped through
+//                shared memory), P = 2^(s*scale*log2e - m) as bf16 into TMEM, then
+//                for the previous tile o = O / l with l = 2^(sink - m) + sum P,
+//                and the log-sum-exp.
+//   warps 12-15  RoPE on dims 0..63 of the Q tile and of each new K segment.
 #pragma once
 #include "common.cuh"
 
@@ -34,6 +38,9 @@ constexpr int32_t kBandSeg = 16;   // keys per ring segment = tokens per tile
 constexpr int32_t kBandRing = 12;  // segments in the K/V ring
 constexpr int32_t kBandMaxWin = 9; // segments of a full window, W <= 128
 constexpr int32_t kBandG = 8;      // query heads per KV head
+constexpr int32_t kBandThreads = 512;
+constexpr int32_t kBandHalf = 72;  // band columns per softmax thread
+constexpr uint32_t kBandPCol = 36; // TMEM column of P (bf16 pairs) within an S buffer
 
 struct BandArgs {
   int32_t Hq, Hkv;
@@ -57,11 +64,14 @@ struct BandLayout {
   static constexpr uint32_t kVOff = kKOff + 3 * kRingBox;     // 2 ring boxes (dims 0..127)
   static constexpr uint32_t kBarOff = kVOff + 2 * kRingBox;
   // q_full[2] q_ready[2] q_empty[2] seg_full[R] seg_ready[R] seg_empty[R]
-  // s_full[2] p_full[2] pv_done o_empty drain
-  static constexpr uint32_t kNumBars = 6 + 3 * kBandRing + 7;
+  // s_full[2] p_full[2] pv_done o_empty drain pair[2][4]
+  static constexpr uint32_t kPairBar = 6 + 3 * kBandRing + 7;
+  static constexpr uint32_t kNumBars = kPairBar + 8;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem, abort, cursor[4]
   static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;
-  static constexpr uint32_t kBytes = kTurnsOff + 32 * 8;
+  // partial (max, sum) of each row half, double-buffered by tile parity
+  static constexpr uint32_t kXchgOff = kTurnsOff + 32 * 8;
+  static constexpr uint32_t kBytes = kXchgOff + 2 * 2 * 128 * 8;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
 static_assert(BandLayout::kDynSmem <= 232448, "band kernel shared memory");
@@ -151,7 +161,213 @@ __device__ void band_locate(const BandArgs &a, int32_t lane, int32_t *cur) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Softmax + epilogue of one half of every row (half 0: band columns 0..71 and
+// output dims 0..63; half 1: band columns 72..143 and output dims 64..127).
+// The two threads of a row swap their partial maximum of tile i and their
+// partial sum of tile i-1 through shared memory, paired by an mbarrier.  Both
+// halves run the same code (half is a runtime value) to keep the hot loop
+// small in the instruction cache.
+//
+// Band columns are read from TMEM in the chunks below (sizes and column
+// offsets are multiples of the chunk size): half 0: 32 + 32 + 8, half 1:
+// 8 + 16 + 32 + 16.
+__device__ __forceinline__ void band_ld_chunk(uint32_t s_t, int32_t half, int32_t ch,
+                                              uint32_t *r, int32_t &n) {
+  if (half == 0) {
+    if (ch == 0) { tmem_ld32p(s_t, r); n = 32; }
+    else if (ch == 1) { tmem_ld32p(s_t + 32, r); n = 32; }
+    else if (ch == 2) { tmem_ld8p(s_t + 64, r); n = 8; }
+    else n = 0;
+  } else {
+    if (ch == 0) { tmem_ld8p(s_t + 72, r); n = 8; }
+    else if (ch == 1) { tmem_ld16p(s_t + 80, r); n = 16; }
+    else if (ch == 2) { tmem_ld32p(s_t + 96, r); n = 32; }
+    else { tmem_ld16p(s_t + 128, r); n = 16; }
+  }
+}
+
+__device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCursor &c0,
+                                             uint32_t tmem, uint32_t sbase, uint8_t *smem,
+                                             volatile uint32_t *abort_flag) {
+  using Ly = BandLayout;
+  constexpr int32_t R = kBandRing;
+  const uint32_t bars = sbase + Ly::kBarOff;
+  auto B_SFULL = [&](uint32_t b) { return bars + (6 + 3 * R + b) * 8; };
+  auto B_PFULL = [&](uint32_t b) { return bars + (6 + 3 * R + 2 + b) * 8; };
+  const uint32_t B_PVDONE = bars + (6 + 3 * R + 4) * 8;
+  const uint32_t B_OEMPTY = bars + (6 + 3 * R + 5) * 8;
+  const int32_t warp = threadIdx.x >> 5;
+  const int32_t half = warp >= 8 ? 1 : 0;
+  const int32_t c0col = half * kBandHalf;  // first band column of this half
+  const int32_t row = (warp & 3) * 32 + (threadIdx.x & 31);  // query row == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  auto B_PAIR = [&](uint32_t par) { return bars + (Ly::kPairBar + par * 4 + (warp & 3)) * 8; };
+  float2 *xchg = reinterpret_cast<float2 *>(smem + Ly::kXchgOff);  // [parity][half][row]
+  const int32_t t = row / kBandG, g = row % kBandG;
+  const float sc = args.scale_log2;
+  const int32_t W = args.window;
+  const uint32_t o_t = tmem + lane_off + kTmemO + half * 64;
+  uint32_t gt = 0;
+  bool ok = true;
+  // the tile whose epilogue is pending
+  bool p_valid = false;
+  size_t p_orow = 0;
+  float p_m = 0.f, p_sk = 0.f, p_sum = 0.f;
+
+  // Swap (partial max of this tile, partial sum of the previous tile) with the
+  // other thread of the row; returns the other's pair.
+  auto swap = [&](uint32_t tt, float mx, float sum, float2 &other) -> bool {
+    const uint32_t par = tt & 1;
+    xchg[(par * 2 + half) * 128 + row] = make_float2(mx, sum);
+    tc_fence_before();
+    mbar_arrive(B_PAIR(par));
+    if (!wait_bar_warp(B_PAIR(par), (tt >> 1) & 1, abort_flag, 12)) return false;
+    tc_fence_after();
+    other = xchg[(par * 2 + (1 - half)) * 128 + row];
+    return true;
+  };
+
+  // One pass per tile, plus a last pass that only finishes the last epilogue.
+  BandCursor c = c0;
+  for (uint32_t step = 0; ok; ++step) {
+    const bool have = c.left > 0;  // a tile to run the softmax of
+    if (!have && step == 0) break;
+    float mx = -INFINITY, m = 0.f, sk2 = 0.f, sum = 0.f;
+    bool rvalid = false;
+    size_t orow = 0;
+    uint32_t s_t = 0, buf = 0;
+    int32_t lo = 0;
+    uint32_t span = 0;  // visible band columns of this half: k - lo <= span (unsigned)
+    if (have) {
+      const int32_t head = c.kvh * kBandG + g;
+      const int32_t pos = c.i * kBandSeg + t;
+      rvalid = pos < c.L;
+      orow = static_cast<size_t>(c.s0 + pos) * args.Hq + head;
+      const int32_t nwin = band_nwin(c, args);
+      const int32_t kstart = (c.i - nwin + 1) * kBandSeg;
+      // visible band columns [lo, hi] (hi < nwin * 16: columns past the
+      // window hold stale values and are masked), shifted to this half
+      lo = max(0, pos - W + 1) - kstart - c0col;
+      const int32_t hi = pos - kstart - c0col;
+      span = static_cast<uint32_t>(hi - lo);
+      if (!rvalid) { lo = 1 << 20; span = 0; }
+      sk2 = __ldg(args.sink + head) * kLog2e;  // -inf stays -inf
+      buf = gt & 1;
+      if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
+      tc_fence_after();
+      s_t = tmem + lane_off + tmem_s_col(buf);
+      // pass 1: row max of the visible columns of this half, chunk by chunk
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      int32_t k0 = 0;
+#pragma unroll 1
+      for (int32_t ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        int32_t n;
+        band_ld_chunk(s_t, half, ch, r, n);
+        if (n == 0) break;
+        tmem_wait_ld();
+        reg_fence<32>(r);
+#pragma unroll
+        for (int32_t k = 0; k < 32; k += 2) {
+          if (k < n) {
+            if (static_cast<uint32_t>(k0 + k - lo) <= span) mx0 = fmaxf(mx0, __uint_as_float(r[k]));
+            if (static_cast<uint32_t>(k0 + k + 1 - lo) <= span)
+              mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
+          }
+        }
+        k0 += n;
+      }
+      mx = fmaxf(mx0, mx1);
+    }
+    float2 other = make_float2(-INFINITY, 0.f);
+    if (!(ok = swap(step, mx, p_sum, other))) break;
+    if (have) {
+      // eq. (2): m = max(max_j a_ij, sink), in the log2 domain (scale > 0)
+      m = fmaxf(fmaxf(mx, other.x) * sc, sk2);
+      const float mneg = m == -INFINITY ? 0.f : -m;
+      // pass 2, chunk by chunk: P = 2^(s * scale * log2e - m) (0 when masked),
+      // packed bf16 into TMEM: band column k -> TMEM column kBandPCol + k / 2.
+      // With that offset each half's P covers only its own S columns (half 0:
+      // 36..71, half 1: 72..107), and walking the chunks downwards (half 0) or
+      // upwards (half 1) overwrites only columns that were already read.
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll 1
+      for (int32_t idx = 0; idx < 4; ++idx) {
+        const int32_t ch = half == 0 ? 2 - idx : idx;
+        if (ch < 0) break;
+        const int32_t k0 = half == 0 ? ch * 32 : (ch == 0 ? 0 : ch == 1 ? 8 : ch == 2 ? 24 : 56);
+        uint32_t r[32];
+        int32_t n;
+        band_ld_chunk(s_t, half, ch, r, n);
+        tmem_wait_ld();
+        reg_fence<32>(r);
+#pragma unroll
+        for (int32_t k = 0; k < 32; k += 2) {
+          if (k < n) {
+            float p0 = ex2(fmaf(__uint_as_float(r[k]), sc, mneg));
+            float p1 = ex2(fmaf(__uint_as_float(r[k + 1]), sc, mneg));
+            if (static_cast<uint32_t>(k0 + k - lo) > span) p0 = 0.f;
+            if (static_cast<uint32_t>(k0 + k + 1 - lo) > span) p1 = 0.f;
+            sum0 += p0;
+            sum1 += p1;
+            r[k >> 1] = pack_bf16x2(p0, p1);
+          }
+        }
+        const uint32_t pcol = s_t + kBandPCol + (c0col + k0) / 2;
+        if (n == 32) tmem_st16p(pcol, r);
+        else if (n == 16) tmem_st8p(pcol, r);
+        else tmem_st4p(pcol, r);
+      }
+      sum = sum0 + sum1;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(B_PFULL(buf));
+    }
+    if (step > 0) {
+      // ---------------- epilogue of the previous tile (eqs. (2)-(3)):
+      // o = O / l with l = 2^(sink - m) + sum_j P_j, lse = (m + log2 l) ln 2
+      if (!(ok = wait_bar_warp(B_PVDONE, (step - 1) & 1, abort_flag, 9))) break;
+      tc_fence_after();
+      const float l = (p_sk == -INFINITY ? 0.f : ex2(p_sk - p_m)) + (p_sum + other.y);
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      uint4 *dst = reinterpret_cast<uint4 *>(args.out + p_orow * kDv + half * 64);
+#pragma unroll
+      for (int32_t oc = 0; oc < 2; ++oc) {
+        uint32_t o[32];
+        tmem_ld32p(o_t + oc * 32, o);
+        tmem_wait_ld();
+        reg_fence<32>(o);
+        if (oc == 1) {
+          // O is in registers: the next PV may overwrite it
+          tc_fence_before();
+          mbar_arrive(B_OEMPTY);
+        }
+        if (p_valid) {
+#pragma unroll
+          for (int32_t q4 = 0; q4 < 4; ++q4) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int32_t e = 0; e < 4; ++e)
+              w4[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
+                                  __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
+            dst[oc * 4 + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+      if (p_valid && half == 0) args.lse[p_orow] = l > 0.f ? (p_m + __log2f(l)) * kLn2 : -INFINITY;
+    }
+    if (!have) break;
+    p_valid = rvalid;
+    p_orow = orow;
+    p_m = m;
+    p_sk = sk2;
+    p_sum = sum;
+    ++gt;
+    band_next(c, args);
+  }
+}
+
+__global__ void __launch_bounds__(kBandThreads, 1)
     sinkattn_band_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
@@ -190,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B_QREADY(s), 128);
       mbar_init(B_QEMPTY(s), 1);
       mbar_init(B_SFULL(s), 1);
-      mbar_init(B_PFULL(s), 128);
+      mbar_init(B_PFULL(s), 256);
     }
     for (uint32_t s = 0; s < R; ++s) {
       mbar_init(B_SEGFULL(s), 1);
@@ -198,8 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B_SEGEMPTY(s), 1);
     }
     mbar_init(B_PVDONE, 1);
-    mbar_init(B_OEMPTY, 128);
+    mbar_init(B_OEMPTY, 256);
     mbar_init(B_DRAIN, 1);
+    for (uint32_t i = 0; i < 8; ++i) mbar_init(bar(Ly::kPairBar + i), 64);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -222,13 +439,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   c0.run = 1;
   if (c0.left > 0) band_load_seq(c0, args);
   const int32_t W = args.window;
-  // Registers: the launch gives 168 per thread (64,512 in all).  The softmax
-  // warpgroup holds a 144-column band row and takes 240; the producer/MMA and
-  // RoPE warpgroups give back to 88 each: (88 + 240 + 88) x 128 = 53,248.  Each
-  // warpgroup changes its count inside its own branch (so ptxas compiles each
-  // role under its own limit) and returns to 168 before the common teardown.
+  // Registers: the launch gives 128 per thread (65,536 in all).  The softmax
+  // warpgroups hold a 72-column half row and take 160; the producer/MMA and
+  // RoPE warpgroups give back to 64: (64 + 160 + 160 + 64) x 128 = 57,344.  Each
+  // warpgroup changes its count inside its own branch (ptxas then compiles each
+  // role under its own limit) and returns to 128 before the common teardown.
   if (warp < 4) {
-    setmaxnreg_dec<88>();
     if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0 && c0.left > 0) {
@@ -293,7 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // apart (LBO); the two 8-key groups of the k-step 1024 B apart (SBO).
           const uint64_t bdesc =
               smem_desc_sw128(sbase + Ly::kVOff + slot * Ly::kSegBox, Ly::kRingBox, 1024);
-          mma_ts(tmem + kTmemO, tmem + tmem_s_col(buf) + kk * 8, bdesc, kIdescPV, kk > 0 ? 1u : 0u);
+          mma_ts(tmem + kTmemO, tmem + tmem_s_col(buf) + kBandPCol + kk * 8, bdesc, kIdescPV,
+                 kk > 0 ? 1u : 0u);
         }
         for (int32_t kk = 0; kk < nfree; ++kk) mma_commit(B_SEGEMPTY((g_first + kk) % R));
         mma_commit(B_PVDONE);
@@ -358,144 +575,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     }
-    __syncwarp();
-    setmaxnreg_inc<168>();
-  } else if (warp < 8) {
-    setmaxnreg_inc<240>();
+  } else if (warp < 12) {
     // ============================================================ softmax + epilogue
     // Tile i's softmax runs before tile i-1's epilogue, so these warps never
     // wait on a PV: by the time tile i's P is stored, PV(i-1) has long finished.
-    const int32_t row = threadIdx.x - 128;  // query row == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int32_t t = row / kBandG, g = row % kBandG;
-    const float sc = args.scale_log2;
-    const uint32_t o_t = tmem + lane_off + kTmemO;
-    uint32_t gt = 0;
-    bool ok = true;
-    // the tile whose epilogue is pending
-    bool p_valid = false;
-    size_t p_orow = 0;
-    float p_m = 0.f, p_l = 0.f;
-    auto epilogue = [&](uint32_t tt) -> bool {
-      if (!wait_bar_warp(B_PVDONE, tt & 1, abort_flag, 9)) return false;
-      tc_fence_after();
-      uint32_t o[kDv];
-#pragma unroll
-      for (int32_t cb = 0; cb < kDv; cb += 32) tmem_ld32p(o_t + cb, o + cb);
-      tmem_wait_ld();
-      reg_fence<kDv>(o);
-      // O is in registers: the next PV may overwrite it
-      tc_fence_before();
-      mbar_arrive(B_OEMPTY);
-      if (p_valid) {
-        // eq. (3) with the denominator of eq. (2): o = O / l, lse = (m + log2 l) ln 2
-        const float inv_l = p_l > 0.f ? 1.f / p_l : 0.f;
-        uint4 *dst = reinterpret_cast<uint4 *>(args.out + p_orow * kDv);
-#pragma unroll
-        for (int32_t q4 = 0; q4 < kDv / 8; ++q4) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int32_t e = 0; e < 4; ++e)
-            w4[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
-                                __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
-          dst[q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        args.lse[p_orow] = p_l > 0.f ? (p_m + __log2f(p_l)) * kLn2 : -INFINITY;
-      }
-      return true;
-    };
-    constexpr int32_t NC = kBandMaxWin * kBandSeg;  // 144 columns at most
-    for (BandCursor c = c0; ok && c.left > 0; band_next(c, args)) {
-      const int32_t head = c.kvh * kBandG + g;
-      const int32_t pos = c.i * kBandSeg + t;
-      const bool rvalid = pos < c.L;
-      const int32_t nwin = band_nwin(c, args);
-      const int32_t kstart = (c.i - nwin + 1) * kBandSeg;
-      int32_t lo = max(0, pos - W + 1) - kstart;  // visible columns [lo, hi]
-      int32_t hi = pos - kstart;
-      if (!rvalid) { lo = 1; hi = 0; }
-      const float sk2 = __ldg(args.sink + head) * kLog2e;  // -inf stays -inf
-      const uint32_t buf = gt & 1;
-      if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
-      tc_fence_after();
-      const uint32_t s_t = tmem + lane_off + tmem_s_col(buf);
-      // The whole band row in registers with one wait (columns past the
-      // window hold stale values and are masked: hi < nwin * 16 always).
-      uint32_t r[NC];
-#pragma unroll
-      for (int32_t cb = 0; cb < 128; cb += 32) tmem_ld32p(s_t + cb, r + cb);
-      tmem_ld16p(s_t + 128, r + 128);
-      tmem_wait_ld();
-      reg_fence<NC>(r);
-      // Interior rows of a full W = 128 band see columns [lo, hi] with lo <= 16
-      // and hi >= 127: only the first and last 16 columns need a mask.
-      const bool interior = lo <= 16 && hi >= 127;
-      const bool fast = __all_sync(0xffffffffu, interior);
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      if (fast) {
-#pragma unroll
-        for (int32_t k = 0; k < 16; ++k) {
-          mx0 = fmaxf(mx0, k >= lo ? __uint_as_float(r[k]) : -INFINITY);
-          mx1 = fmaxf(mx1, 128 + k <= hi ? __uint_as_float(r[128 + k]) : -INFINITY);
-        }
-#pragma unroll
-        for (int32_t k = 16; k < 128; k += 2) {
-          mx0 = fmaxf(mx0, __uint_as_float(r[k]));
-          mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
-        }
-      } else {
-#pragma unroll
-        for (int32_t k = 0; k < NC; k += 2) {
-          mx0 = fmaxf(mx0, (k >= lo && k <= hi) ? __uint_as_float(r[k]) : -INFINITY);
-          mx1 = fmaxf(mx1, (k + 1 >= lo && k + 1 <= hi) ? __uint_as_float(r[k + 1]) : -INFINITY);
-        }
-      }
-      // eq. (2): m = max(max_j a_ij, sink), in the log2 domain (scale > 0)
-      const float m = fmaxf(fmaxf(mx0, mx1) * sc, sk2);
-      const float mneg = m == -INFINITY ? 0.f : -m;
-      // P = 2^(s * scale * log2e - m), packed bf16 in place, then into TMEM over S
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int32_t k = 0; k < NC; k += 2) {
-        float p0 = ex2(fmaf(__uint_as_float(r[k]), sc, mneg));
-        float p1 = ex2(fmaf(__uint_as_float(r[k + 1]), sc, mneg));
-        if (fast) {
-          if (k < 16) {
-            if (k < lo) p0 = 0.f;
-            if (k + 1 < lo) p1 = 0.f;
-          } else if (k >= 128) {
-            if (k > hi) p0 = 0.f;
-            if (k + 1 > hi) p1 = 0.f;
-          }
-        } else {
-          if (!(k >= lo && k <= hi)) p0 = 0.f;
-          if (!(k + 1 >= lo && k + 1 <= hi)) p1 = 0.f;
-        }
-        sum0 += p0;
-        sum1 += p1;
-        r[k >> 1] = pack_bf16x2(p0, p1);
-      }
-      tmem_st32p(s_t, r);
-      tmem_st32p(s_t + 32, r + 32);
-      tmem_st8p(s_t + 64, r + 64);
-      tmem_wait_st();
-      const float l = (sk2 == -INFINITY ? 0.f : ex2(sk2 + mneg)) + (sum0 + sum1);
-      tc_fence_before();
-      mbar_arrive(B_PFULL(buf));
-      if (gt > 0 && !(ok = epilogue(gt - 1))) break;
-      p_valid = rvalid;
-      p_orow = static_cast<size_t>(c.s0 + pos) * args.Hq + head;
-      p_m = m;
-      p_l = l;
-      ++gt;
-    }
-    if (ok && gt > 0) epilogue(gt - 1);
-    __syncwarp();
-    setmaxnreg_dec<168>();
+    band_softmax(args, c0, tmem, sbase, smem, abort_flag);
   } else {
-    setmaxnreg_dec<88>();
     // ============================================================ RoPE
-    const int32_t tid = threadIdx.x - 256;
+    const int32_t tid = threadIdx.x - 384;
     uint32_t gq = 0, gseg = 0;
     bool ok = true;
     for (BandCursor c = c0; ok && c.left > 0; band_next(c, args)) {
@@ -521,8 +608,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gseg;
       }
     }
-    __syncwarp();
-    setmaxnreg_inc<168>();
   }
 
   // ---------------------------------------------------------------- teardown

@@ -153,7 +153,7 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(sa::BandLayout::kDynSmem)) != cudaSuccess)
     return SINKATTN_ECUDA;
-  kern<<<grid, sa::kThreads, sa::BandLayout::kDynSmem, stream>>>(mq, mk, mv, b);
+  kern<<<grid, sa::kBandThreads, sa::BandLayout::kDynSmem, stream>>>(mq, mk, mv, b);
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
