@@ -186,6 +186,21 @@ __device__ __forceinline__ void band_ld_chunk(uint32_t s_t, int32_t half, int32_
   }
 }
 
+// Writes a chunk read by band_ld_chunk back to the same TMEM columns.
+__device__ __forceinline__ void band_st_chunk(uint32_t s_t, int32_t half, int32_t ch,
+                                              const uint32_t *r) {
+  if (half == 0) {
+    if (ch == 0) tmem_st32p(s_t, r);
+    else if (ch == 1) tmem_st32p(s_t + 32, r);
+    else tmem_st8p(s_t + 64, r);
+  } else {
+    if (ch == 0) tmem_st8p(s_t + 72, r);
+    else if (ch == 1) tmem_st16p(s_t + 80, r);
+    else if (ch == 2) tmem_st32p(s_t + 96, r);
+    else tmem_st16p(s_t + 128, r);
+  }
+}
+
 __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCursor &c0,
                                              uint32_t tmem, uint32_t sbase, uint8_t *smem,
                                              volatile uint32_t *abort_flag) {
@@ -256,8 +271,12 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
       tc_fence_after();
       s_t = tmem + lane_off + tmem_s_col(buf);
-      // pass 1: row max of the visible columns of this half, chunk by chunk
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      // pass 1, chunk by chunk: masked columns become -inf and are written
+      // back to TMEM (so pass 2 needs no mask: 2^-inf = 0); the row max is taken
+      // with 3-input max.  Chunks that the whole warp sees completely (all but
+      // one for interior rows of a full W = 128 band) skip the mask.
+      constexpr uint32_t kNegInf = 0xff800000u;
+      float mxa = -INFINITY, mxb = -INFINITY;
       int32_t k0 = 0;
 #pragma unroll 1
       for (int32_t ch = 0; ch < 4; ++ch) {
@@ -267,17 +286,25 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
         if (n == 0) break;
         tmem_wait_ld();
         reg_fence<32>(r);
+        const bool whole = static_cast<uint32_t>(k0 - lo) <= span &&
+                           static_cast<uint32_t>(k0 + n - 1 - lo) <= span;
+        if (!__all_sync(0xffffffffu, whole)) {
 #pragma unroll
-        for (int32_t k = 0; k < 32; k += 2) {
+          for (int32_t k = 0; k < 32; ++k)
+            if (static_cast<uint32_t>(k0 + k - lo) > span) r[k] = kNegInf;
+          band_st_chunk(s_t, half, ch, r);
+        }
+#pragma unroll
+        for (int32_t k = 0; k < 32; k += 4) {
           if (k < n) {
-            if (static_cast<uint32_t>(k0 + k - lo) <= span) mx0 = fmaxf(mx0, __uint_as_float(r[k]));
-            if (static_cast<uint32_t>(k0 + k + 1 - lo) <= span)
-              mx1 = fmaxf(mx1, __uint_as_float(r[k + 1]));
+            mxa = fmax3(mxa, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+            mxb = fmax3(mxb, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
           }
         }
         k0 += n;
       }
-      mx = fmaxf(mx0, mx1);
+      mx = fmaxf(mxa, mxb);
+      tmem_wait_st();
     }
     float2 other = make_float2(-INFINITY, 0.f);
     if (!(ok = swap(step, mx, p_sum, other))) break;
@@ -304,10 +331,8 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
 #pragma unroll
         for (int32_t k = 0; k < 32; k += 2) {
           if (k < n) {
-            float p0 = ex2(fmaf(__uint_as_float(r[k]), sc, mneg));
-            float p1 = ex2(fmaf(__uint_as_float(r[k + 1]), sc, mneg));
-            if (static_cast<uint32_t>(k0 + k - lo) > span) p0 = 0.f;
-            if (static_cast<uint32_t>(k0 + k + 1 - lo) > span) p1 = 0.f;
+            const float p0 = ex2(fmaf(__uint_as_float(r[k]), sc, mneg));
+            const float p1 = ex2(fmaf(__uint_as_float(r[k + 1]), sc, mneg));
             sum0 += p0;
             sum1 += p1;
             r[k >> 1] = pack_bf16x2(p0, p1);

@@ -32,18 +32,16 @@ __device__ uint32_t g_status_word;
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                       uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
+  // each try_wait sleeps up to its suspend hint (1 ms), so checking the clock
+  // and the abort flag once per round costs nothing
   const uint64_t t0 = global_timer_ns();
-  uint32_t n = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (++n == 32) {
-      n = 0;
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1u;
-        atomicOr(&g_status_word, 1u | (site << 8));
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1u;
+      atomicOr(&g_status_word, 1u | (site << 8));
+      return false;
     }
   }
 }
