@@ -49,6 +49,7 @@ struct BandArgs {
   int32_t nseg;        // segments of a full window: ceil((window - 1) / 16) + 1
   int32_t rope_on, rope_style;
   float scale_log2;    // logit scale * log2(e), > 0
+  int32_t out_v8;      // 1: out is 32-byte aligned (whole-sector stores)
   const int32_t *cu_seqlens;
   const float *sink;
   __nv_bfloat16 *out;
@@ -168,37 +169,66 @@ __device__ void band_locate(const BandArgs &a, int32_t lane, int32_t *cur) {
 // halves run the same code (half is a runtime value) to keep the hot loop
 // small in the instruction cache.
 //
-// Band columns are read from TMEM in the chunks below (sizes and column
-// offsets are multiples of the chunk size): half 0: 32 + 32 + 8, half 1:
-// 8 + 16 + 32 + 16.
-__device__ __forceinline__ void band_ld_chunk(uint32_t s_t, int32_t half, int32_t ch,
-                                              uint32_t *r, int32_t &n) {
-  if (half == 0) {
-    if (ch == 0) { tmem_ld32p(s_t, r); n = 32; }
-    else if (ch == 1) { tmem_ld32p(s_t + 32, r); n = 32; }
-    else if (ch == 2) { tmem_ld8p(s_t + 64, r); n = 8; }
-    else n = 0;
-  } else {
-    if (ch == 0) { tmem_ld8p(s_t + 72, r); n = 8; }
-    else if (ch == 1) { tmem_ld16p(s_t + 80, r); n = 16; }
-    else if (ch == 2) { tmem_ld32p(s_t + 96, r); n = 32; }
-    else { tmem_ld16p(s_t + 128, r); n = 16; }
+// TMEM loads/stores of N consecutive 32-bit columns (N = 4, 8, 16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t *r) {
+  if (N == 32) tmem_ld32p(taddr, r);
+  else if (N == 16) tmem_ld16p(taddr, r);
+  else if (N == 8) tmem_ld8p(taddr, r);
+  else tmem_ld4p(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t *r) {
+  if (N == 32) tmem_st32p(taddr, r);
+  else if (N == 16) tmem_st16p(taddr, r);
+  else if (N == 8) tmem_st8p(taddr, r);
+  else tmem_st4p(taddr, r);
+}
+
+// Pass 1 over band columns C .. C+N-1 of a row (kc: their index within this
+// thread's half): masked columns become -inf and, if the warp has any, the
+// chunk is written back to TMEM (so pass 2 needs no mask: 2^-inf = 0); the
+// running max is taken with 3-input max.  Column offsets and sizes are
+// multiples of the chunk size.
+template <int C, int N>
+__device__ __forceinline__ void band_pass1(uint32_t s_t, int32_t kc, int32_t lo, uint32_t span,
+                                           float &mxa, float &mxb) {
+  constexpr uint32_t kNegInf = 0xff800000u;
+  uint32_t r[N];
+  tmem_ld_n<N>(s_t + C, r);
+  tmem_wait_ld();
+  reg_fence<N>(r);
+  const bool whole = static_cast<uint32_t>(kc - lo) <= span &&
+                     static_cast<uint32_t>(kc + N - 1 - lo) <= span;
+  if (!__all_sync(0xffffffffu, whole)) {
+#pragma unroll
+    for (int32_t k = 0; k < N; ++k)
+      if (static_cast<uint32_t>(kc + k - lo) > span) r[k] = kNegInf;
+    tmem_st_n<N>(s_t + C, r);
+  }
+#pragma unroll
+  for (int32_t k = 0; k < N; k += 4) {
+    mxa = fmax3(mxa, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+    mxb = fmax3(mxb, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
   }
 }
 
-// Writes a chunk read by band_ld_chunk back to the same TMEM columns.
-__device__ __forceinline__ void band_st_chunk(uint32_t s_t, int32_t half, int32_t ch,
-                                              const uint32_t *r) {
-  if (half == 0) {
-    if (ch == 0) tmem_st32p(s_t, r);
-    else if (ch == 1) tmem_st32p(s_t + 32, r);
-    else tmem_st8p(s_t + 64, r);
-  } else {
-    if (ch == 0) tmem_st8p(s_t + 72, r);
-    else if (ch == 1) tmem_st16p(s_t + 80, r);
-    else if (ch == 2) tmem_st32p(s_t + 96, r);
-    else tmem_st16p(s_t + 128, r);
+// Pass 2 over band columns C .. C+N-1: P = 2^(s * scale * log2e - m) summed
+// and stored as bf16 pairs at TMEM column kBandPCol + C/2.
+template <int C, int N>
+__device__ __forceinline__ void band_pass2(uint32_t s_t, float2 sc2, float2 mneg2, float2 &sum2) {
+  uint32_t r[N];
+  tmem_ld_n<N>(s_t + C, r);
+  tmem_wait_ld();
+  reg_fence<N>(r);
+#pragma unroll
+  for (int32_t k = 0; k < N; k += 2) {
+    const float2 y = ffma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, mneg2);
+    const float2 p = make_float2(ex2(y.x), ex2(y.y));
+    sum2 = fadd2(sum2, p);
+    r[k >> 1] = pack_bf16x2(p.x, p.y);
   }
+  tmem_st_n<N / 2>(s_t + kBandPCol + C / 2, r);
 }
 
 __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCursor &c0,
@@ -271,37 +301,18 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
       tc_fence_after();
       s_t = tmem + lane_off + tmem_s_col(buf);
-      // pass 1, chunk by chunk: masked columns become -inf and are written
-      // back to TMEM (so pass 2 needs no mask: 2^-inf = 0); the row max is taken
-      // with 3-input max.  Chunks that the whole warp sees completely (all but
-      // one for interior rows of a full W = 128 band) skip the mask.
-      constexpr uint32_t kNegInf = 0xff800000u;
+      // pass 1 (see band_pass1); chunks of half 0: 32 + 32 + 8 columns, of
+      // half 1: 8 + 16 + 32 + 16 (TMEM offsets are multiples of the size)
       float mxa = -INFINITY, mxb = -INFINITY;
-      int32_t k0 = 0;
-#pragma unroll 1
-      for (int32_t ch = 0; ch < 4; ++ch) {
-        uint32_t r[32];
-        int32_t n;
-        band_ld_chunk(s_t, half, ch, r, n);
-        if (n == 0) break;
-        tmem_wait_ld();
-        reg_fence<32>(r);
-        const bool whole = static_cast<uint32_t>(k0 - lo) <= span &&
-                           static_cast<uint32_t>(k0 + n - 1 - lo) <= span;
-        if (!__all_sync(0xffffffffu, whole)) {
-#pragma unroll
-          for (int32_t k = 0; k < 32; ++k)
-            if (static_cast<uint32_t>(k0 + k - lo) > span) r[k] = kNegInf;
-          band_st_chunk(s_t, half, ch, r);
-        }
-#pragma unroll
-        for (int32_t k = 0; k < 32; k += 4) {
-          if (k < n) {
-            mxa = fmax3(mxa, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
-            mxb = fmax3(mxb, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
-          }
-        }
-        k0 += n;
+      if (half == 0) {
+        band_pass1<0, 32>(s_t, 0, lo, span, mxa, mxb);
+        band_pass1<32, 32>(s_t, 32, lo, span, mxa, mxb);
+        band_pass1<64, 8>(s_t, 64, lo, span, mxa, mxb);
+      } else {
+        band_pass1<72, 8>(s_t, 0, lo, span, mxa, mxb);
+        band_pass1<80, 16>(s_t, 8, lo, span, mxa, mxb);
+        band_pass1<96, 32>(s_t, 24, lo, span, mxa, mxb);
+        band_pass1<128, 16>(s_t, 56, lo, span, mxa, mxb);
       }
       mx = fmaxf(mxa, mxb);
       tmem_wait_st();
@@ -312,38 +323,23 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       // eq. (2): m = max(max_j a_ij, sink), in the log2 domain (scale > 0)
       m = fmaxf(fmaxf(mx, other.x) * sc, sk2);
       const float mneg = m == -INFINITY ? 0.f : -m;
-      // pass 2, chunk by chunk: P = 2^(s * scale * log2e - m) (0 when masked),
-      // packed bf16 into TMEM: band column k -> TMEM column kBandPCol + k / 2.
-      // With that offset each half's P covers only its own S columns (half 0:
-      // 36..71, half 1: 72..107), and walking the chunks downwards (half 0) or
+      // pass 2 (see band_pass2): P of band column k lands at TMEM column
+      // kBandPCol + k/2, so each half's P covers only its own S columns (half 0:
+      // 36..71, half 1: 72..107); walking the chunks downwards (half 0) or
       // upwards (half 1) overwrites only columns that were already read.
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll 1
-      for (int32_t idx = 0; idx < 4; ++idx) {
-        const int32_t ch = half == 0 ? 2 - idx : idx;
-        if (ch < 0) break;
-        const int32_t k0 = half == 0 ? ch * 32 : (ch == 0 ? 0 : ch == 1 ? 8 : ch == 2 ? 24 : 56);
-        uint32_t r[32];
-        int32_t n;
-        band_ld_chunk(s_t, half, ch, r, n);
-        tmem_wait_ld();
-        reg_fence<32>(r);
-#pragma unroll
-        for (int32_t k = 0; k < 32; k += 2) {
-          if (k < n) {
-            const float p0 = ex2(fmaf(__uint_as_float(r[k]), sc, mneg));
-            const float p1 = ex2(fmaf(__uint_as_float(r[k + 1]), sc, mneg));
-            sum0 += p0;
-            sum1 += p1;
-            r[k >> 1] = pack_bf16x2(p0, p1);
-          }
-        }
-        const uint32_t pcol = s_t + kBandPCol + (c0col + k0) / 2;
-        if (n == 32) tmem_st16p(pcol, r);
-        else if (n == 16) tmem_st8p(pcol, r);
-        else tmem_st4p(pcol, r);
+      const float2 sc2 = make_float2(sc, sc), mneg2 = make_float2(mneg, mneg);
+      float2 sum2 = make_float2(0.f, 0.f);
+      if (half == 0) {
+        band_pass2<64, 8>(s_t, sc2, mneg2, sum2);
+        band_pass2<32, 32>(s_t, sc2, mneg2, sum2);
+        band_pass2<0, 32>(s_t, sc2, mneg2, sum2);
+      } else {
+        band_pass2<72, 8>(s_t, sc2, mneg2, sum2);
+        band_pass2<80, 16>(s_t, sc2, mneg2, sum2);
+        band_pass2<96, 32>(s_t, sc2, mneg2, sum2);
+        band_pass2<128, 16>(s_t, sc2, mneg2, sum2);
       }
-      sum = sum0 + sum1;
+      sum = sum2.x + sum2.y;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(B_PFULL(buf));
@@ -368,14 +364,24 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
           mbar_arrive(B_OEMPTY);
         }
         if (p_valid) {
+          // 32 output dims -> 64 bytes: two whole 32-byte sectors when out is
+          // 32-byte aligned (rows are 256 bytes), else four 16-byte stores
+          uint32_t w[16];
 #pragma unroll
-          for (int32_t q4 = 0; q4 < 4; ++q4) {
-            uint32_t w4[4];
+          for (int32_t e = 0; e < 16; ++e) {
+            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])),
+                                   make_float2(inv_l, inv_l));
+            w[e] = pack_bf16x2(v.x, v.y);
+          }
+          if (args.out_v8) {
+            uint32_t (&w0)[8] = *reinterpret_cast<uint32_t(*)[8]>(w);
+            uint32_t (&w1)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8);
+            st_global_v8(dst + oc * 4, w0);
+            st_global_v8(dst + oc * 4 + 2, w1);
+          } else {
 #pragma unroll
-            for (int32_t e = 0; e < 4; ++e)
-              w4[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
-                                  __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
-            dst[oc * 4 + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            for (int32_t q4 = 0; q4 < 4; ++q4)
+              dst[oc * 4 + q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
           }
         }
       }
@@ -517,27 +523,39 @@ __global__ void __launch_bounds__(kBandThreads, 1)
     // ============================================================ MMA issuer
     if (lane == 0 && c0.left > 0) {
       constexpr uint32_t kIdescPV = idesc_f32acc(128, kDv, 1, 0, 1);
+      // Shared-memory matrix descriptors (128-byte swizzle, SBO = 1024 B), as
+      // (low, high) words: the low word holds start address >> 4 and LBO >> 4,
+      // so every operand offset below is a single 32-bit add.
+      constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      const uint32_t q_lo = ((sbase + Ly::kQOff) >> 4) | (1u << 16);
+      const uint32_t k_lo = ((sbase + Ly::kKOff) >> 4) | (1u << 16);
+      // V is MN-major: LBO = one ring box (the two 64-column halves of dv)
+      const uint32_t v_lo = ((sbase + Ly::kVOff) >> 4) | ((Ly::kRingBox >> 4) << 16);
+      constexpr uint32_t kSegLo = Ly::kSegBox >> 4;
+      const uint32_t rot = args.rope_on ? 0u : 1u;  // rotated dims are fp16
       uint32_t gt = 0, gseg = 0;
       bool ok = true;
       // the previous tile, whose PV is issued after the next tile's QK^T
       int32_t p_nwin = 0;
-      uint32_t p_first = 0;
-      auto issue_pv = [&](uint32_t t, int32_t nwin, uint32_t g_first, int32_t nfree) -> bool {
+      uint32_t p_slot = 0;
+      auto issue_pv = [&](uint32_t t, int32_t nwin, uint32_t slot, int32_t nfree) -> bool {
         const uint32_t buf = t & 1;
         if (!wait_bar(B_PFULL(buf), (t >> 1) & 1, abort_flag, 4)) return false;
         tc_fence_after();
         if (!wait_bar(B_OEMPTY, (t & 1) ^ 1, abort_flag, 5)) return false;
         tc_fence_after();
+        const uint32_t p_t = tmem + tmem_s_col(buf) + kBandPCol;
+        uint32_t sl = slot;
         for (int32_t kk = 0; kk < nwin; ++kk) {
-          const uint32_t slot = (g_first + kk) % R;
-          // B = V, MN-major: the two 64-column halves of dv are one ring box
-          // apart (LBO); the two 8-key groups of the k-step 1024 B apart (SBO).
-          const uint64_t bdesc =
-              smem_desc_sw128(sbase + Ly::kVOff + slot * Ly::kSegBox, Ly::kRingBox, 1024);
-          mma_ts(tmem + kTmemO, tmem + tmem_s_col(buf) + kBandPCol + kk * 8, bdesc, kIdescPV,
-                 kk > 0 ? 1u : 0u);
+          mma_ts2(tmem + kTmemO, p_t + kk * 8, v_lo + sl * kSegLo, kDescHi, kIdescPV,
+                  kk > 0 ? 1u : 0u);
+          sl = sl + 1 == R ? 0 : sl + 1;
         }
-        for (int32_t kk = 0; kk < nfree; ++kk) mma_commit(B_SEGEMPTY((g_first + kk) % R));
+        sl = slot;
+        for (int32_t kk = 0; kk < nfree; ++kk) {
+          mma_commit(B_SEGEMPTY(sl));
+          sl = sl + 1 == R ? 0 : sl + 1;
+        }
         mma_commit(B_PVDONE);
         return true;
       };
@@ -547,7 +565,7 @@ __global__ void __launch_bounds__(kBandThreads, 1)
         if (gt > 0 && c.run) {
           // a new run reloads the whole band: the previous tile's segments must
           // be released (its PV issued) before this tile's loads can land
-          if (!(ok = issue_pv(gt - 1, p_nwin, p_first, p_nwin))) break;
+          if (!(ok = issue_pv(gt - 1, p_nwin, p_slot, p_nwin))) break;
         }
         const uint32_t qs = gt & 1;
         if (!(ok = wait_bar(B_QREADY(qs), (gt >> 1) & 1, abort_flag, 3))) break;
@@ -558,28 +576,29 @@ __global__ void __launch_bounds__(kBandThreads, 1)
         if (!ok) break;
         tc_fence_after();
         gseg += nload;
-        const uint32_t g_first = gseg - nwin;
+        const uint32_t slot0 = (gseg - nwin) % R;
         const uint32_t buf = gt & 1;
-        const uint32_t slot0 = g_first % R;
         const int32_t n1 = min(nwin, R - static_cast<int32_t>(slot0));
         const int32_t n2 = nwin - n1;
-        const uint32_t rot = args.rope_on ? 0u : 1u;  // rotated dims are fp16
         const uint32_t id1 = idesc_f32acc(128, n1 * kBandSeg, 1, 0, 0);
         const uint32_t id1r = idesc_f32acc(128, n1 * kBandSeg, rot, 0, 0);
         const uint32_t id2 = idesc_f32acc(128, (n2 > 0 ? n2 : 1) * kBandSeg, 1, 0, 0);
         const uint32_t id2r = idesc_f32acc(128, (n2 > 0 ? n2 : 1) * kBandSeg, rot, 0, 0);
-        const uint32_t qaddr = sbase + Ly::kQOff + qs * kQStageBytes;
+        const uint32_t a_lo = q_lo + qs * (kQStageBytes >> 4);
+        const uint32_t b1_lo = k_lo + slot0 * kSegLo;
         const uint32_t s_t = tmem + tmem_s_col(buf);
+        // S = Q K^T: 12 k-steps of 16 dims (3 boxes of 64); when the band wraps
+        // the end of the ring, segments slot0.. and 0.. are two MMAs
 #pragma unroll
         for (int kstep = 0; kstep < kDqk / 16; ++kstep) {
           const uint32_t box = kstep >> 2, off = (kstep & 3) * 32;
-          const uint64_t adesc = smem_desc_sw128(qaddr + box * kQBoxBytes + off, 16, 1024);
-          const uint32_t kb = sbase + Ly::kKOff + box * Ly::kRingBox + off;
-          mma_ss(s_t, adesc, smem_desc_sw128(kb + slot0 * Ly::kSegBox, 16, 1024),
-                 box == 0 ? id1r : id1, kstep > 0 ? 1u : 0u);
+          const uint32_t ao = (box * kQBoxBytes + off) >> 4;
+          const uint32_t bo = (box * Ly::kRingBox + off) >> 4;
+          mma_ss2(s_t, a_lo + ao, kDescHi, b1_lo + bo, kDescHi, box == 0 ? id1r : id1,
+                  kstep > 0 ? 1u : 0u);
           if (n2 > 0)
-            mma_ss(s_t + n1 * kBandSeg, adesc, smem_desc_sw128(kb, 16, 1024), box == 0 ? id2r : id2,
-                   kstep > 0 ? 1u : 0u);
+            mma_ss2(s_t + n1 * kBandSeg, a_lo + ao, kDescHi, k_lo + bo, kDescHi,
+                    box == 0 ? id2r : id2, kstep > 0 ? 1u : 0u);
         }
         mma_commit(B_SFULL(buf));
         mma_commit(B_QEMPTY(qs));
@@ -587,13 +606,13 @@ __global__ void __launch_bounds__(kBandThreads, 1)
           // same lane: the oldest segment of the previous band leaves the window
           // once the band is full
           const int32_t nfree = nwin == p_nwin ? 1 : 0;
-          if (!(ok = issue_pv(gt - 1, p_nwin, p_first, nfree))) break;
+          if (!(ok = issue_pv(gt - 1, p_nwin, p_slot, nfree))) break;
         }
         p_nwin = nwin;
-        p_first = g_first;
+        p_slot = slot0;
         ++gt;
       }
-      if (ok && gt > 0) ok = issue_pv(gt - 1, p_nwin, p_first, p_nwin);
+      if (ok && gt > 0) ok = issue_pv(gt - 1, p_nwin, p_slot, p_nwin);
       if (gt > 0) {
         mma_commit(B_DRAIN);
         drain_wait(B_DRAIN, 0);

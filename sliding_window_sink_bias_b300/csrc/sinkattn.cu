@@ -135,6 +135,7 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
   b.rope_on = a.rope_on;
   b.rope_style = a.rope_style;
   b.scale_log2 = a.scale_log2;
+  b.out_v8 = aligned(a.out, 32) ? 1 : 0;
   b.cu_seqlens = cu_seqlens;
   b.sink = a.sink;
   b.out = a.out;
