@@ -143,6 +143,36 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
                                    size_t workspace_bytes, void *out, float *lse,
                                    sinkattn_stream_t stream);
 
+/*
+ * sinkattn_decode_noalloc -- sinkattn_decode for callers that cannot allocate.
+ *
+ * This entry point has no counterpart in the report; it exists for callers that
+ * must not allocate device memory when they decode (an allocator-free region,
+ * a fixed memory pool that may not grow, a host without a device allocator).  It takes the same arguments as sinkattn_decode
+ * minus the workspace: the split-KV partials go to one fixed buffer of
+ * SINKATTN_NOALLOC_SCRATCH_BYTES that is part of the library's device image, so
+ * every GPU that loads the library holds that memory until the process exits.
+ * Nothing is allocated or freed by this call.
+ *
+ *   - Sizes whose partials need more than SINKATTN_NOALLOC_SCRATCH_BYTES (see
+ *     sinkattn_decode_workspace_size) are rejected with SINKATTN_EWORKSPACE
+ *     before anything is launched.
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress on that device); make that first call before any
+ *     stream capture.
+ *   - All calls share the one buffer per device: calls that overlap on the GPU
+ *     (other streams, other host threads) race and give wrong results.  Calls
+ *     on one stream are ordered and safe.
+ *   - The buffer keeps the previous call's contents; no call needs it cleared.
+ */
+#define SINKATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+sinkattn_status sinkattn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
+                                        const int32_t *seqlens, const float *sink, int32_t window,
+                                        float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                        int32_t max_seqlen, int32_t num_q_heads,
+                                        int32_t num_kv_heads, void *out, float *lse,
+                                        sinkattn_stream_t stream);
+
 /* A static string naming a status code. */
 const char *sinkattn_status_string(sinkattn_status status);
 

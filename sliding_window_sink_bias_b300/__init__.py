@@ -24,8 +24,11 @@ OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA, ETIMEOUT = range(6)
 EXPORTED = (
     "sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode_workspace_size",
     "sinkattn_decode", "sinkattn_decode_ex", "sinkattn_status_string",
-    "sinkattn_get_device_status", "sinkattn_version",
+    "sinkattn_get_device_status", "sinkattn_version", "sinkattn_decode_noalloc",
 )
+
+# bytes of the library's fixed decode scratch (include/sinkattn.h)
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class SinkAttnError(RuntimeError):
@@ -61,12 +64,14 @@ def lib() -> ctypes.CDLL:
                                       P, ctypes.c_size_t, P, P, P]
         L.sinkattn_decode_ex.argtypes = [P, P, P, P, P, i32, f32, i32, i32, i32, i32, i32, i32,
                                          ctypes.POINTER(Params), P, ctypes.c_size_t, P, P, P]
+        L.sinkattn_decode_noalloc.argtypes = [P, P, P, P, P, i32, f32, i32, i32, i32, i32, i32, i32,
+                                              P, P, P]
         L.sinkattn_status_string.argtypes = [i32]
         L.sinkattn_status_string.restype = ctypes.c_char_p
         L.sinkattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.sinkattn_version.restype = i32
         for name in ("sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode",
-                     "sinkattn_decode_ex", "sinkattn_get_device_status"):
+                     "sinkattn_decode_ex", "sinkattn_get_device_status", "sinkattn_decode_noalloc"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -176,6 +181,38 @@ def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, ro
     else:
         st = lib().sinkattn_decode_ex(*args, ctypes.byref(p), *tail)
     _check("sinkattn_decode", st)
+    return out, lse
+
+
+def decode_noalloc(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int,
+                   rope_base: float, out=None, lse=None, stream=None):
+    """MTP-verify decode through sinkattn_decode_noalloc: same inputs and results
+    as decode(), but the split-KV partials go to the library's fixed device
+    buffer (NOALLOC_SCRATCH_BYTES per GPU) instead of a workspace, so the call
+    itself allocates nothing.  For callers that cannot allocate device memory
+    where they decode.  Calls that overlap on the GPU share that buffer and
+    race; the first call on a device should come before any stream capture.
+    out / lse are the caller's outputs (allocated here only if not given)."""
+    _require(q, "q", torch.bfloat16, 4)
+    _require(kcache, "kcache", torch.bfloat16, 4)
+    _require(vcache, "vcache", torch.bfloat16, 4)
+    _require(seqlens, "seqlens", torch.int32, 1)
+    _require(sink, "sink", torch.float32, 1)
+    b, t, hq, dqk = q.shape
+    s_cap, hkv = kcache.shape[1], kcache.shape[2]
+    if dqk != 192 or kcache.shape != (b, s_cap, hkv, 192) or vcache.shape != (b, s_cap, hkv, 128):
+        raise ValueError("expected q [B,T,Hq,192], kcache [B,S,Hkv,192], vcache [B,S,Hkv,128]")
+    if out is None:
+        out = torch.empty(b, t, hq, 128, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(b, t, hq, dtype=torch.float32, device=q.device)
+    _require(out, "out", torch.bfloat16, 4)
+    _require(lse, "lse", torch.float32, 3)
+    st = lib().sinkattn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens),
+                                       _ptr(sink), int(window), float(rope_base), b, t, s_cap,
+                                       int(max_seqlen), hq, hkv, _ptr(out), _ptr(lse),
+                                       _stream(stream))
+    _check("sinkattn_decode_noalloc", st)
     return out, lse
 
 

@@ -367,3 +367,59 @@ sinkattn_status sinkattn_decode(const void *q, const void *kcache, const void *v
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------
+// Decode without any allocation by the caller or the library.
+//
+// Some callers cannot allocate device memory at the point where they run
+// decode: code inside an allocator-free region (a memory pool that must not
+// grow, a real-time path that forbids cudaMalloc and its implicit
+// synchronisation), or a host that owns no device allocator at all.  For them,
+// the split-KV partials live in one fixed buffer that is part of the library's
+// own device image: every GPU that loads the library holds these
+// SINKATTN_NOALLOC_SCRATCH_BYTES until the process exits.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SINKATTN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (host code only sees a host-side stand-in for the symbol).
+sinkattn_status noalloc_scratch(void **ptr) {
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SINKATTN_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SINKATTN_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SINKATTN_ECUDA;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return SINKATTN_OK;
+}
+
+}  // namespace
+
+extern "C" sinkattn_status sinkattn_decode_noalloc(
+    const void *q, const void *kcache, const void *vcache, const int32_t *seqlens,
+    const float *sink, int32_t window, float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+    int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads, void *out, float *lse,
+    sinkattn_stream_t stream) {
+  const size_t need =
+      sinkattn_decode_workspace_size(batch, T, num_q_heads, num_kv_heads, max_seqlen, window);
+  if (need > SINKATTN_NOALLOC_SCRATCH_BYTES) return SINKATTN_EWORKSPACE;
+  if (batch == 0) return sinkattn_decode(q, kcache, vcache, seqlens, sink, window, rope_base, batch,
+                                         T, S_cap, max_seqlen, num_q_heads, num_kv_heads, nullptr,
+                                         0, out, lse, stream);
+  void *scratch = nullptr;
+  if (sinkattn_status st = noalloc_scratch(&scratch)) return st;
+  // Every partial the combine step reads is written first by the same call, so
+  // the buffer needs no clearing between calls.
+  return sinkattn_decode(q, kcache, vcache, seqlens, sink, window, rope_base, batch, T, S_cap,
+                         max_seqlen, num_q_heads, num_kv_heads, scratch,
+                         SINKATTN_NOALLOC_SCRATCH_BYTES, out, lse, stream);
+}
