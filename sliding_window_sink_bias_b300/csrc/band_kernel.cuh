@@ -351,37 +351,59 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       tc_fence_after();
       const float l = (p_sk == -INFINITY ? 0.f : ex2(p_sk - p_m)) + (p_sum + other.y);
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      uint4 *dst = reinterpret_cast<uint4 *>(args.out + p_orow * kDv + half * 64);
-#pragma unroll
-      for (int32_t oc = 0; oc < 2; ++oc) {
-        uint32_t o[32];
-        tmem_ld32p(o_t + oc * 32, o);
+      uint32_t w[32];  // this half-row as bf16 pairs: four 32-byte sectors of 8 words
+      {
+        uint32_t o[64];
+        tmem_ld32p(o_t, o);
+        tmem_ld32p(o_t + 32, o + 32);
         tmem_wait_ld();
-        reg_fence<32>(o);
-        if (oc == 1) {
-          // O is in registers: the next PV may overwrite it
-          tc_fence_before();
-          mbar_arrive(B_OEMPTY);
+        reg_fence<64>(o);
+        // O is in registers: the next PV may overwrite it
+        tc_fence_before();
+        mbar_arrive(B_OEMPTY);
+#pragma unroll
+        for (int32_t e = 0; e < 32; ++e) {
+          const float2 v = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])),
+                                 make_float2(inv_l, inv_l));
+          w[e] = pack_bf16x2(v.x, v.y);
         }
-        if (p_valid) {
-          // 32 output dims -> 64 bytes: two whole 32-byte sectors when out is
-          // 32-byte aligned (rows are 256 bytes), else four 16-byte stores
-          uint32_t w[16];
+      }
+      // Each half-row is one 128-byte line of out.  Transpose the 4 x 4 sectors
+      // within each quad of lanes (rows 4k..4k+3, consecutive heads of one
+      // token): afterwards lane q holds sector q of rows 4k..4k+3, so each of
+      // the four stores below writes 8 whole lines per warp instead of 32
+      // partial ones.
+      const int32_t q = threadIdx.x & 3;
 #pragma unroll
-          for (int32_t e = 0; e < 16; ++e) {
-            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])),
-                                   make_float2(inv_l, inv_l));
-            w[e] = pack_bf16x2(v.x, v.y);
-          }
+      for (int32_t j = 0; j < 2; ++j) {  // partner q ^ 2: sectors {0,1} <-> {2,3}
+#pragma unroll
+        for (int32_t e = 0; e < 8; ++e) {
+          const uint32_t send = (q & 2) ? w[8 * j + e] : w[8 * (j + 2) + e];
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+          if (q & 2) w[8 * j + e] = recv; else w[8 * (j + 2) + e] = recv;
+        }
+      }
+#pragma unroll
+      for (int32_t j = 0; j < 4; j += 2) {  // partner q ^ 1: positions j <-> j + 1
+#pragma unroll
+        for (int32_t e = 0; e < 8; ++e) {
+          const uint32_t send = (q & 1) ? w[8 * j + e] : w[8 * (j + 1) + e];
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+          if (q & 1) w[8 * j + e] = recv; else w[8 * (j + 1) + e] = recv;
+        }
+      }
+      if (p_valid) {
+        // rows of a quad share the token; row 4k+p is head (g & ~3) + p
+        __nv_bfloat16 *row0 = args.out + (p_orow - q) * kDv + half * 64 + q * 16;
+#pragma unroll
+        for (int32_t pq = 0; pq < 4; ++pq) {
+          uint32_t (&sec)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8 * pq);
           if (args.out_v8) {
-            uint32_t (&w0)[8] = *reinterpret_cast<uint32_t(*)[8]>(w);
-            uint32_t (&w1)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8);
-            st_global_v8(dst + oc * 4, w0);
-            st_global_v8(dst + oc * 4 + 2, w1);
+            st_global_v8(row0 + pq * kDv, sec);
           } else {
-#pragma unroll
-            for (int32_t q4 = 0; q4 < 4; ++q4)
-              dst[oc * 4 + q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+            uint4 *d4 = reinterpret_cast<uint4 *>(row0 + pq * kDv);
+            d4[0] = make_uint4(sec[0], sec[1], sec[2], sec[3]);
+            d4[1] = make_uint4(sec[4], sec[5], sec[6], sec[7]);
           }
         }
       }
