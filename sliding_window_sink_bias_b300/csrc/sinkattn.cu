@@ -22,6 +22,8 @@ using sa::Layout;
 constexpr int32_t kVersion = 100;  // 0.1.0
 constexpr int32_t kBNWide = 144;   // one key block covers a 128-key window + 16-token tile
 constexpr int32_t kBN = 128;
+constexpr int32_t kBNDecode = 64;  // decode streams the cache in 64-key blocks, 4 in flight
+constexpr int32_t kDecodeStages = 4;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool pow2_upto_128(int32_t x) { return x >= 1 && x <= 128 && (x & (x - 1)) == 0; }
@@ -340,12 +342,12 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, num_q_heads, uint64_t(batch) * T, G, T) ||
-      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, kBN) ||
-      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, kBN))
+      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, kBNDecode) ||
+      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, kBNDecode))
     return SINKATTN_ECUDA;
   const int grid = static_cast<int>(std::min<int64_t>(n_items, dev.sms));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (sinkattn_status st = launch<kBN, 1, 2>(mq, mk, mv, a, grid, s)) return st;
+  if (sinkattn_status st = launch<kBNDecode, 1, kDecodeStages>(mq, mk, mv, a, grid, s)) return st;
 
   const int64_t rows = int64_t(batch) * T * num_q_heads;
   if (rows > INT32_MAX) return SINKATTN_EUNSUPPORTED;
