@@ -12,6 +12,7 @@
 
 #include "attn_kernel.cuh"
 #include "band_kernel.cuh"
+#include "decode_kernel.cuh"
 #include "sinkattn.h"
 
 namespace {
@@ -347,7 +348,16 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
     return SINKATTN_ECUDA;
   const int grid = static_cast<int>(std::min<int64_t>(n_items, dev.sms));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (sinkattn_status st = launch<kBNDecode, 1, kDecodeStages>(mq, mk, mv, a, grid, s)) return st;
+  if (a.scale_log2 > 0.f) {
+    auto kern = sa::sinkattn_decode_kernel;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sa::DecLayout::kDynSmem)) != cudaSuccess)
+      return SINKATTN_ECUDA;
+    kern<<<grid, sa::kThreads, sa::DecLayout::kDynSmem, s>>>(mq, mk, mv, a);
+    if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
+  } else if (sinkattn_status st = launch<kBNDecode, 1, kDecodeStages>(mq, mk, mv, a, grid, s)) {
+    return st;
+  }
 
   const int64_t rows = int64_t(batch) * T * num_q_heads;
   if (rows > INT32_MAX) return SINKATTN_EUNSUPPORTED;
