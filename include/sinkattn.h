@@ -103,9 +103,15 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
                                     void *out, float *lse, sinkattn_stream_t stream);
 
 /*
- * Bytes of device workspace sinkattn_decode needs for these sizes (the split-KV
- * partials of §2.3.1's multi-token verify: each KV chunk's running max, sum and
- * unnormalised output).  Returns 0 for arguments sinkattn_decode would reject.
+ * Bytes of device workspace sinkattn_decode needs for these sizes.  The decode
+ * cuts every unit's (sequence, KV head) visible keys into 64-key blocks and
+ * splits the list of all blocks evenly over at most 160 CTAs; the workspace
+ * holds the per-unit block offsets (batch * num_kv_heads + 1 int32, padded to
+ * 256 bytes) and, per CTA, two partial slots of T * (num_q_heads / num_kv_heads)
+ * rows x 132 fp32 for the units a CTA boundary cuts (their running max, sum and
+ * unnormalised output; §2.3.1's multi-token verify split over the cache).  It
+ * does not depend on the cache lengths or the window.  Returns 0 for arguments
+ * sinkattn_decode would reject.
  */
 size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_heads,
                                       int32_t num_kv_heads, int32_t max_seqlen, int32_t window);
@@ -125,7 +131,10 @@ size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_he
  *   max_seqlen  host bound on max(seqlens).
  *   T        1 <= T and T * (num_q_heads / num_kv_heads) <= 128.
  *   workspace, workspace_bytes  device scratch of at least
- *            sinkattn_decode_workspace_size(...) bytes, 256-byte aligned.
+ *            sinkattn_decode_workspace_size(...) bytes, 256-byte aligned; it
+ *            needs no clearing and its contents are rewritten by every call.
+ *   The logit scale must be positive (sinkattn_decode_ex with a scale <= 0
+ *   returns SINKATTN_EINVAL).
  *   out      bf16 [batch, T, num_q_heads, 128];  lse fp32 [batch, T, num_q_heads]
  */
 sinkattn_status sinkattn_decode(const void *q, const void *kcache, const void *vcache,

@@ -491,12 +491,6 @@ __global__ void __launch_bounds__(kBandThreads, 1)
   c0.left = cur_smem[3];
   c0.run = 1;
   if (c0.left > 0) band_load_seq(c0, args);
-  const int32_t W = args.window;
-  // Registers: the launch gives 128 per thread (65,536 in all).  The softmax
-  // warpgroups hold a 72-column half row and take 160; the producer/MMA and
-  // RoPE warpgroups give back to 64: (64 + 160 + 160 + 64) x 128 = 57,344.  Each
-  // warpgroup changes its count inside its own branch (ptxas then compiles each
-  // role under its own limit) and returns to 128 before the common teardown.
   if (warp < 4) {
     if (warp == 0) {
     // ============================================================ TMA producer

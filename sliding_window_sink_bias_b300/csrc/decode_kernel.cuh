@@ -1,28 +1,35 @@
 // decode_kernel.cuh -- split-KV partials of the multi-token (MTP-verify) decode.
 //
 // The MiMo-V2-Flash Technical Report (§2.3.1) verifies 1 + K draft tokens in
-// one pass over the KV cache; this kernel computes, for one chunk of the cache
-// of one (sequence, KV head) at a time, the unnormalised attention partials of
-// eqs. (1)-(3) of §2.2 for the T new tokens x G query heads of that KV head:
-// the running max m, the sum l of 2^(a - m) and O = sum 2^(a - m) v, without
-// the sink (sinkattn_combine_kernel adds it once, over all chunks).
+// one pass over the KV cache.  For each unit (sequence b, KV head) the T new
+// tokens x G query heads of that KV head form T * G <= 128 packed rows, and the
+// unit's visible keys are cut into 64-key blocks.  The flattened list of all
+// units' blocks is split into gridDim.x equal contiguous ranges, one per CTA,
+// so every CTA streams the same number of cache blocks whatever the sequence
+// lengths.  A unit that lies entirely inside one CTA's range is finished there
+// (eqs. (1)-(3) of §2.2, the sink added once); a unit cut by a range boundary
+// leaves, per CTA, its running max m, the sum l of 2^(a - m) and the
+// unnormalised O = sum 2^(a - m) v without the sink, and
+// sinkattn_decode_combine_kernel merges those and adds the sink once.
 //
 // The cache is streamed in 64-key blocks, four in flight (TMA into a shared
 // memory ring); S = Q K^T and O += P V run on tcgen05 with S, P and O in TMEM.
-// Only the T * G <= 128 packed rows that exist are touched by the softmax.
+// Only the T * G packed rows that exist are touched by the softmax.
 //
 // Warp roles (384 threads, one CTA per SM):
 //   warp 0       TMA producer: Q tile once per chunk, K/V blocks.
 //   warp 1       MMA issuer: S = Q K^T (12 k-steps), then O += P V.
 //   warp 2       TMEM allocator (S0, S1, O: 256 columns).
+//   warp 3       set-up: this CTA's block range and first unit (CTA 0 also writes
+//                the per-unit block offsets the combine step reads).
 //   warps 4-7    online softmax, one row per thread: the block's masked max
 //                (3-input max), lazy running max (moves only when a block
 //                exceeds it by more than 2^8), P = 2^(s * scale * log2e - m) as
 //                bf16 pairs into TMEM, l, and the rescale of this row's O when
-//                m moves; at the end of a chunk the partial row is written.
+//                m moves; at the end of a unit's segment the row is finished
+//                (with the sink) or its partial is written.
 //   warps 8-11   RoPE on dims 0..63 of the Q tile and of every K block.
 #pragma once
-#include "attn_kernel.cuh"
 #include "common.cuh"
 
 namespace sa {
@@ -31,6 +38,136 @@ constexpr int32_t kDecBN = 64;      // keys per block
 constexpr int32_t kDecStages = 4;   // K/V blocks in flight
 constexpr uint32_t kDecTmemCols = 256;
 constexpr uint32_t kDecTmemO = 128;
+constexpr int32_t kDecMaxGrid = 160;  // CTAs at most (2 partial slots each)
+
+struct DecArgs {
+  int32_t Hq, Hkv, G, T;
+  int32_t R;              // T * G packed rows
+  int32_t window;
+  int32_t batch, S_cap;
+  int32_t n_units;        // batch * Hkv
+  int32_t rope_on, rope_style;
+  uint32_t q_tx_bytes;
+  float scale_log2;       // > 0
+  const int32_t *seqlens;
+  const float *sink;
+  __nv_bfloat16 *out;
+  float *lse;
+  int32_t *unit_blk;      // [n_units + 1] block offsets (written by CTA 0)
+  float *part_o;          // [gridDim.x * 2, R, 128] unnormalised O
+  float *part_ml;         // [gridDim.x * 2, R, 4] (m, l, 0, 0), log2 domain
+  unsigned long long rope_turns[32];
+};
+
+// Visible keys of unit u = b * Hkv + kvh: [lo, L) with L = seqlens[b]; with a
+// window only the last T + W - 1 keys can be seen by the T queries.
+__device__ __forceinline__ void dec_unit_keys(const DecArgs &a, int32_t u, int32_t &L, int32_t &lo,
+                                              int32_t &nblk) {
+  L = __ldg(a.seqlens + u / a.Hkv);
+  lo = a.window > 0 ? max(0, L - a.T - a.window + 1) : 0;
+  nblk = L > lo ? (L - lo + kDecBN - 1) / kDecBN : 0;
+}
+
+// One segment: blocks [blk0, blk0 + nblk) of unit u, processed by this CTA.
+struct DecSeg {
+  int32_t u, b, kvh, L, lo;
+  int32_t blk0, nblk, nblk_u;
+  int32_t first;  // the CTA's first segment (partial slot 0, else slot 1)
+};
+
+struct DecCursor {
+  int32_t u, blk;  // next block to process
+  int32_t left;    // blocks of this CTA not yet handed out
+  int32_t first;
+};
+
+// The next segment of the cursor (returns false when the CTA's range is done).
+__device__ __forceinline__ bool dec_next(DecCursor &c, const DecArgs &a, DecSeg &sg) {
+  while (c.left > 0 && c.u < a.n_units) {
+    int32_t L, lo, nb;
+    dec_unit_keys(a, c.u, L, lo, nb);
+    if (c.blk >= nb) {
+      ++c.u;
+      c.blk = 0;
+      continue;
+    }
+    sg.u = c.u;
+    sg.b = c.u / a.Hkv;
+    sg.kvh = c.u % a.Hkv;
+    sg.L = L;
+    sg.lo = lo;
+    sg.nblk_u = nb;
+    sg.blk0 = c.blk;
+    sg.nblk = min(nb - c.blk, c.left);
+    sg.first = c.first;
+    c.first = 0;
+    c.left -= sg.nblk;
+    c.blk += sg.nblk;
+    return true;
+  }
+  return false;
+}
+
+// Set-up (one warp): block offsets of all units (a warp scan), this CTA's range
+// [f0, f1) of the flattened block list, and the unit/block it starts at.
+// CTA 0 also stores the offsets for the combine step.
+__device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
+  int64_t run = 0;
+  // pass 1: total blocks (and, for CTA 0, the offset table)
+  for (int32_t base = 0; base < a.n_units; base += 32) {
+    const int32_t u = base + lane;
+    int32_t nb = 0;
+    if (u < a.n_units) {
+      int32_t L, lo;
+      dec_unit_keys(a, u, L, lo, nb);
+    }
+    int32_t incl = nb;
+#pragma unroll
+    for (int32_t o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (blockIdx.x == 0 && u < a.n_units) a.unit_blk[u] = static_cast<int32_t>(run + incl - nb);
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (blockIdx.x == 0 && lane == 0) a.unit_blk[a.n_units] = static_cast<int32_t>(run);
+  const int64_t T = run;
+  const int64_t f0 = T * blockIdx.x / gridDim.x;
+  const int64_t f1 = T * (blockIdx.x + 1) / gridDim.x;
+  // pass 2: the unit holding block f0
+  int32_t su = a.n_units, sblk = 0;
+  run = 0;
+  bool found = false;
+  for (int32_t base = 0; base < a.n_units && !found && f1 > f0; base += 32) {
+    const int32_t u = base + lane;
+    int32_t nb = 0;
+    if (u < a.n_units) {
+      int32_t L, lo;
+      dec_unit_keys(a, u, L, lo, nb);
+    }
+    int32_t incl = nb;
+#pragma unroll
+    for (int32_t o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, nb > 0 && run + incl > f0);
+    if (m) {
+      const int32_t j = __ffs(m) - 1;
+      const int32_t incl_j = __shfl_sync(0xffffffffu, incl, j);
+      const int32_t nb_j = __shfl_sync(0xffffffffu, nb, j);
+      su = base + j;
+      sblk = static_cast<int32_t>(f0 - (run + incl_j - nb_j));
+      found = true;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    cur[0] = su;
+    cur[1] = sblk;
+    cur[2] = found ? static_cast<int32_t>(f1 - f0) : 0;
+  }
+}
 
 struct DecLayout {
   static constexpr uint32_t kKBox = kDecBN * kRowBytes;    // 64 keys x 64 dims: 8 KB
@@ -40,8 +177,8 @@ struct DecLayout {
   static constexpr uint32_t kBarOff = kKVOff + kDecStages * kKVStage;
   // q_full q_ready q_empty | kv_full[S] k_ready[S] kv_empty[S] | s_full[2] p_full[2] pv_done o_empty drain
   static constexpr uint32_t kNumBars = 3 + 3 * kDecStages + 7;
-  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
-  static constexpr uint32_t kTurnsOff = (kMiscOff + 16 + 7) & ~7u;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag, cursor
+  static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;  // + cursor[3]
   static constexpr uint32_t kBytes = kTurnsOff + 32 * 8;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
@@ -51,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sinkattn_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
-                           const __grid_constant__ AttnArgs args) {
+                           const __grid_constant__ DecArgs args) {
   using Ly = DecLayout;
   constexpr int32_t S = kDecStages;
   constexpr int32_t BN = kDecBN;
@@ -75,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
+  int32_t *cur_smem = reinterpret_cast<int32_t *>(smem + Ly::kMiscOff + 8);
   unsigned long long *turns = reinterpret_cast<unsigned long long *>(smem + Ly::kTurnsOff);
 
   // ---------------------------------------------------------------- set-up
@@ -102,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sbase + Ly::kMiscOff, kDecTmemCols);
     tmem_relinquish();
   }
+  if (warp == 3) dec_locate(args, lane, cur_smem);
   // The Q tile has T * G rows; the MMA reads all 128, so the rest stay zero.
   for (uint32_t i = threadIdx.x; i < kQStageBytes / 16; i += kThreads)
     reinterpret_cast<uint4 *>(smem + Ly::kQOff)[i] = make_uint4(0, 0, 0, 0);
@@ -111,7 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int32_t G = args.G;
-  const int32_t R = args.part_rows;  // T * G packed rows
+  const int32_t R = args.R;
+  DecCursor c0;
+  c0.u = cur_smem[0];
+  c0.blk = cur_smem[1];
+  c0.left = cur_smem[2];
+  c0.first = 1;
 
   if (warp == 0) {
     // ============================================================ TMA producer
@@ -121,27 +265,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       uint32_t gq = 0, gk = 0;
       bool ok = true;
-      for (int32_t w = blockIdx.x; ok && w < args.n_items; w += gridDim.x) {
-        const Item it = make_item(args, w, BN);
-        if (!it.valid) continue;
+      DecCursor c = c0;
+      DecSeg sg;
+      while (ok && dec_next(c, args, sg)) {
         if (!(ok = wait_bar(B_QEMPTY, (gq & 1) ^ 1, abort_flag, 1))) break;
         mbar_arrive_expect_tx(B_QFULL, args.q_tx_bytes);
 #pragma unroll
-        for (int c = 0; c < 3; ++c)
-          tma_load_3d(sbase + Ly::kQOff + c * kQBoxBytes, &tm_q, c * 64, it.kvh * G, it.q_row, B_QFULL);
+        for (int cc = 0; cc < 3; ++cc)
+          tma_load_3d(sbase + Ly::kQOff + cc * kQBoxBytes, &tm_q, cc * 64, sg.kvh * G, sg.b * args.T,
+                      B_QFULL);
         ++gq;
-        for (int32_t j = 0; j < it.n_blk; ++j) {
+        const int32_t krow0 = sg.b * args.S_cap + sg.lo + sg.blk0 * BN;
+        for (int32_t j = 0; j < sg.nblk; ++j) {
           const uint32_t st = gk % S;
           if (!(ok = wait_bar(B_KVEMPTY(st), ((gk / S) & 1) ^ 1, abort_flag, 2))) break;
           mbar_arrive_expect_tx(B_KVFULL(st), Ly::kKVStage);
           const uint32_t dst = sbase + Ly::kKVOff + st * Ly::kKVStage;
-          const int32_t krow = it.kv_row0 + it.kstart + j * BN;
 #pragma unroll
-          for (int c = 0; c < 3; ++c)
-            tma_load_3d(dst + c * Ly::kKBox, &tm_k, c * 64, it.kvh, krow, B_KVFULL(st));
+          for (int cc = 0; cc < 3; ++cc)
+            tma_load_3d(dst + cc * Ly::kKBox, &tm_k, cc * 64, sg.kvh, krow0 + j * BN, B_KVFULL(st));
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(dst + (3 + c) * Ly::kKBox, &tm_v, c * 64, it.kvh, krow, B_KVFULL(st));
+          for (int cc = 0; cc < 2; ++cc)
+            tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, sg.kvh, krow0 + j * BN,
+                        B_KVFULL(st));
           ++gk;
         }
       }
@@ -180,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(B_PVDONE);
         return true;
       };
-      for (int32_t w = blockIdx.x; ok && w < args.n_items; w += gridDim.x) {
-        const Item it = make_item(args, w, BN);
-        if (!it.valid) continue;
+      DecCursor c = c0;
+      DecSeg sg;
+      while (ok && dec_next(c, args, sg)) {
         if (!(ok = wait_bar(B_QREADY, gq & 1, abort_flag, 3))) break;
         tc_fence_after();
-        for (int32_t j = 0; ok && j < it.n_blk; ++j) {
+        for (int32_t j = 0; ok && j < sg.nblk; ++j) {
           const uint32_t st = (gk + j) % S;
           if (!(ok = wait_bar(B_KREADY(st), ((gk + j) / S) & 1, abort_flag, 6))) break;
           tc_fence_after();
@@ -199,13 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           issued = true;
           mma_commit(B_SFULL((gs + j) & 1));
-          if (j == it.n_blk - 1) mma_commit(B_QEMPTY);
+          if (j == sg.nblk - 1) mma_commit(B_QEMPTY);
           if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
         }
-        if (ok) ok = issue_pv(gs + it.n_blk - 1, (gk + it.n_blk - 1) % S, it.n_blk == 1);
+        if (ok) ok = issue_pv(gs + sg.nblk - 1, (gk + sg.nblk - 1) % S, sg.nblk == 1);
         ++gq;
-        gk += it.n_blk;
-        gs += it.n_blk;
+        gk += sg.nblk;
+        gs += sg.nblk;
         ++gt;
       }
       if (issued) {
@@ -223,18 +369,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t W = args.window;
     uint32_t gs = 0, gpv = 0;
     bool ok = true;
-    for (int32_t w = blockIdx.x; ok && w < args.n_items; w += gridDim.x) {
-      const Item it = make_item(args, w, BN);
-      if (!it.valid) continue;
-      // query t sits at position L - T + t and sees keys [max(0, pos - W + 1), pos]
-      // of the cache, here limited to this chunk's keys [key_lo, key_hi)
-      const int32_t pos = it.pos0 + t;
+    DecCursor c = c0;
+    DecSeg sg;
+    while (ok && dec_next(c, args, sg)) {
+      // query t sits at position L - T + t and sees cache keys
+      // [max(0, pos - W + 1), pos], here limited to this segment's keys
+      const int32_t pos = sg.L - args.T + t;
+      const int32_t kfirst = sg.lo + sg.blk0 * BN;
+      const int32_t klast = min(kfirst + sg.nblk * BN, sg.L) - 1;
       const bool rvalid = row < R && pos >= 0;
-      int32_t qlo = max(it.key_lo, W > 0 ? pos - W + 1 : 0);
-      int32_t qhi = min(pos, it.key_hi - 1);
-      if (!rvalid) { qlo = 1 << 30; qhi = 1 << 30; }
+      int32_t qlo = max(kfirst, W > 0 ? pos - W + 1 : 0);
+      int32_t qhi = min(pos, klast);
+      // no visible key in this segment (or no such row): nothing is visible
+      if (!rvalid || qhi < qlo) { qlo = 1 << 30; qhi = 1 << 30; }
       float m = -INFINITY, l = 0.f;
-      for (int32_t j = 0; ok && j < it.n_blk; ++j) {
+      for (int32_t j = 0; ok && j < sg.nblk; ++j) {
         const uint32_t buf = gs & 1;
         if (!(ok = wait_bar_warp(B_SFULL(buf), (gs >> 1) & 1, abort_flag, 7))) break;
         tc_fence_after();
@@ -248,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           reg_fence<BN>(r);
           // visible columns of this block: k - lo <= span (unsigned)
-          const int32_t kb = it.kstart + j * BN;
+          const int32_t kb = kfirst + j * BN;
           const int32_t lo = qlo - kb;
           const uint32_t span = static_cast<uint32_t>(qhi - qlo);
           const bool whole = lo <= 0 && lo + static_cast<int32_t>(span) >= BN - 1;
@@ -296,19 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the running max moved: rescale this row's O before PV(j) adds to it
             const uint32_t o_t = tmem + lane_off + kDecTmemO;
 #pragma unroll 1
-            for (int32_t c0 = 0; c0 < kDv; c0 += 32) {
+            for (int32_t cb = 0; cb < kDv; cb += 32) {
               uint32_t o[32];
-              tmem_ld32p(o_t + c0, o);
+              tmem_ld32p(o_t + cb, o);
               tmem_wait_ld();
               reg_fence<32>(o);
 #pragma unroll
-              for (int32_t c = 0; c < 32; c += 2) {
-                const float2 v = fmul2(make_float2(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
+              for (int32_t k = 0; k < 32; k += 2) {
+                const float2 v = fmul2(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])),
                                        make_float2(alpha_row, alpha_row));
-                o[c] = __float_as_uint(v.x);
-                o[c + 1] = __float_as_uint(v.y);
+                o[k] = __float_as_uint(v.x);
+                o[k + 1] = __float_as_uint(v.y);
               }
-              tmem_st32p(o_t + c0, o);
+              tmem_st32p(o_t + cb, o);
             }
             tmem_wait_st();
           }
@@ -318,29 +467,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gs;
       }
       if (!ok) break;
-      // ---------------- the chunk's partial: unnormalised O, m and l (log2 domain)
-      if (!(ok = wait_bar_warp(B_PVDONE, (gpv + it.n_blk - 1) & 1, abort_flag, 9))) break;
-      gpv += it.n_blk;
+      // ---------------- end of the segment
+      if (!(ok = wait_bar_warp(B_PVDONE, (gpv + sg.nblk - 1) & 1, abort_flag, 9))) break;
+      gpv += sg.nblk;
       tc_fence_after();
+      const bool whole_unit = sg.blk0 == 0 && sg.nblk == sg.nblk_u;
       if (warp_active) {
         const uint32_t o_t = tmem + lane_off + kDecTmemO;
-        const size_t prow = static_cast<size_t>(it.out_idx) * R + row;
-        float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kDv);
+        const int32_t head = sg.kvh * G + g;
+        // whole unit: eqs. (2)-(3) with the sink added once,
+        //   M = max(m, sink), L = l 2^(m - M) + 2^(sink - M), o = O 2^(m - M) / L;
+        // else the unnormalised partial (m, l, O) for the combine step
+        float scale_o = 1.f, lse_v = 0.f;
+        if (whole_unit) {
+          const float sk2 = __ldg(args.sink + head) * kLog2e;
+          const float M = fmaxf(m, sk2);
+          if (M == -INFINITY) {
+            scale_o = 0.f;
+            lse_v = -INFINITY;
+          } else {
+            const float a1 = m == -INFINITY ? 0.f : ex2(m - M);
+            const float a2 = sk2 == -INFINITY ? 0.f : ex2(sk2 - M);
+            const float Lw = l * a1 + a2;
+            scale_o = a1 / Lw;
+            lse_v = (M + __log2f(Lw)) * kLn2;
+          }
+        }
+        const size_t orow = (static_cast<size_t>(sg.b) * args.T + t) * args.Hq + head;
+        const size_t prow = (static_cast<size_t>(blockIdx.x) * 2 + (sg.first ? 0 : 1)) * R + row;
 #pragma unroll 1
-        for (int32_t c0 = 0; c0 < kDv; c0 += 32) {
+        for (int32_t cb = 0; cb < kDv; cb += 32) {
           uint32_t o[32];
-          tmem_ld32p(o_t + c0, o);
+          tmem_ld32p(o_t + cb, o);
           tmem_wait_ld();
           reg_fence<32>(o);
           if (row < R) {
+            if (whole_unit) {
+              uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv + cb);
 #pragma unroll
-            for (int32_t q4 = 0; q4 < 8; ++q4)
-              dst[c0 / 4 + q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
-                                             __uint_as_float(o[4 * q4 + 2]),
-                                             __uint_as_float(o[4 * q4 + 3]));
+              for (int32_t q4 = 0; q4 < 4; ++q4) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int32_t e = 0; e < 4; ++e)
+                  w4[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * scale_o,
+                                      __uint_as_float(o[q4 * 8 + 2 * e + 1]) * scale_o);
+                dst[q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            } else {
+              float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kDv + cb);
+#pragma unroll
+              for (int32_t q4 = 0; q4 < 8; ++q4)
+                dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                      __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+            }
           }
         }
-        if (row < R) reinterpret_cast<float4 *>(args.part_ml)[prow] = make_float4(m, l, l, 0.f);
+        if (row < R) {
+          if (whole_unit)
+            args.lse[orow] = lse_v;
+          else
+            reinterpret_cast<float4 *>(args.part_ml)[prow] = make_float4(m, l, 0.f, 0.f);
+        }
       }
       tc_fence_before();
       mbar_arrive(B_OEMPTY);
@@ -350,20 +537,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t tid = threadIdx.x - 256;
     uint32_t gq = 0, gk = 0;
     bool ok = true;
-    for (int32_t w = blockIdx.x; ok && w < args.n_items; w += gridDim.x) {
-      const Item it = make_item(args, w, BN);
-      if (!it.valid) continue;
+    DecCursor c = c0;
+    DecSeg sg;
+    while (ok && dec_next(c, args, sg)) {
       if (!(ok = wait_bar_warp(B_QFULL, gq & 1, abort_flag, 10))) break;
       if (args.rope_on)
-        rope_q_tile(smem + Ly::kQOff, G, it.n_tok, it.pos0, args.rope_style, turns, tid);
+        rope_q_tile(smem + Ly::kQOff, G, args.T, sg.L - args.T, args.rope_style, turns, tid);
       fence_proxy_async_smem();
       mbar_arrive(B_QREADY);
       ++gq;
-      for (int32_t j = 0; j < it.n_blk; ++j) {
+      const int32_t kpos0 = sg.lo + sg.blk0 * BN;
+      for (int32_t j = 0; j < sg.nblk; ++j) {
         const uint32_t st = gk % S;
         if (!(ok = wait_bar_warp(B_KVFULL(st), (gk / S) & 1, abort_flag, 11))) break;
         if (args.rope_on)
-          rope_k_rows(smem + Ly::kKVOff + st * Ly::kKVStage, BN, it.kstart + j * BN, args.rope_style,
+          rope_k_rows(smem + Ly::kKVOff + st * Ly::kKVStage, BN, kpos0 + j * BN, args.rope_style,
                       turns, tid);
         fence_proxy_async_smem();
         mbar_arrive(B_KREADY(st));
@@ -379,6 +567,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kDecTmemCols);
   }
+}
+
+// Combine step: for each output row of a unit that a CTA-range boundary cut,
+// merge the per-CTA partials (m_c, l_c, O_c), computed without the sink, and
+// add the sink exactly once (eq. (2) over a partition of the keys):
+//   M = max(sink, max_c m_c),  L = 2^(sink - M) + sum_c l_c 2^(m_c - M),
+//   o = sum_c 2^(m_c - M) O_c / L,  lse = (M + log2 L) ln 2   (log2 domain).
+// Rows of units the decode kernel finished return at once; rows of units with
+// no visible key get o = 0 and lse = sink.  One CTA of 128 threads (one per
+// value dim) per output row; the CTAs are visited in a fixed order.
+__global__ void __launch_bounds__(128)
+    sinkattn_decode_combine_kernel(const __grid_constant__ DecArgs a, int32_t grid) {
+  const int32_t rowid = blockIdx.x;  // (b * T + t) * Hq + h
+  const int32_t h = rowid % a.Hq, bt = rowid / a.Hq;
+  const int32_t t = bt % a.T, b = bt / a.T;
+  const int32_t u = b * a.Hkv + h / a.G, r = t * a.G + (h % a.G);
+  const int32_t F0 = a.unit_blk[u], F1 = a.unit_blk[u + 1];
+  const int64_t Tb = a.unit_blk[a.n_units];
+  const int32_t e = threadIdx.x;
+  const float sk_raw = __ldg(a.sink + h);
+  const float sk = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
+  if (F1 == F0) {  // no visible key at all: the empty sum
+    a.out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(0.f);
+    if (e == 0) a.lse[rowid] = sk_raw;
+    return;
+  }
+  auto cta_of = [&](int64_t f) { return static_cast<int32_t>(((f + 1) * grid - 1) / Tb); };
+  const int32_t c_first = cta_of(F0), c_last = cta_of(F1 - 1);
+  if (c_first == c_last) return;  // finished by the decode kernel
+  const float4 *ml = reinterpret_cast<const float4 *>(a.part_ml);
+  auto slot = [&](int32_t c) {
+    const int64_t bnd = Tb * c / grid;  // first block of CTA c
+    return (static_cast<size_t>(c) * 2 + ((c == c_first && bnd < F0) ? 1 : 0)) * a.R + r;
+  };
+  // CTAs whose range is empty (fewer blocks than CTAs) hold no partial
+  auto empty = [&](int32_t c) { return Tb * c / grid == Tb * (c + 1) / grid; };
+  float M = sk;
+  for (int32_t c = c_first; c <= c_last; ++c)
+    if (!empty(c)) M = fmaxf(M, ml[slot(c)].x);
+  if (M == -INFINITY) {
+    a.out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(0.f);
+    if (e == 0) a.lse[rowid] = -INFINITY;
+    return;
+  }
+  float Ls = sk == -INFINITY ? 0.f : ex2(sk - M);
+  float acc = 0.f;
+  for (int32_t c = c_first; c <= c_last; ++c) {
+    if (empty(c)) continue;
+    const size_t pr = slot(c);
+    const float4 v = ml[pr];
+    const float wgt = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+    Ls += v.y * wgt;
+    acc += wgt * a.part_o[pr * kDv + e];
+  }
+  a.out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(acc / Ls);
+  if (e == 0) a.lse[rowid] = (M + __log2f(Ls)) * kLn2;
 }
 
 }  // namespace sa

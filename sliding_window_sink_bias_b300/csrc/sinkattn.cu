@@ -23,8 +23,6 @@ using sa::Layout;
 constexpr int32_t kVersion = 100;  // 0.1.0
 constexpr int32_t kBNWide = 144;   // one key block covers a 128-key window + 16-token tile
 constexpr int32_t kBN = 128;
-constexpr int32_t kBNDecode = 64;  // decode streams the cache in 64-key blocks, 4 in flight
-constexpr int32_t kDecodeStages = 4;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool pow2_upto_128(int32_t x) { return x >= 1 && x <= 128 && (x & (x - 1)) == 0; }
@@ -161,26 +159,20 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
+// Decode workspace: the per-unit block offsets (n_units + 1 int32, padded to
+// 256 bytes), then 2 partial slots per CTA of R rows x (128 + 4) fp32, for at
+// most sa::kDecMaxGrid CTAs.
 struct DecodePlan {
-  int32_t chunk = 0, splits = 0, rows = 0;
-  size_t bytes = 0;
+  int32_t rows = 0;
+  size_t tab_bytes = 0, bytes = 0;
 };
 
-// Split-KV plan: chunks of `chunk` keys (a multiple of 128) so that the whole
-// batch yields about 8192 chunk-sized work items at the longest cache.
-DecodePlan decode_plan(int32_t batch, int32_t T, int32_t hq, int32_t hkv, int32_t max_seqlen,
-                       int32_t window) {
+DecodePlan decode_plan(int32_t batch, int32_t T, int32_t hq, int32_t hkv) {
   DecodePlan p;
-  const int64_t range = window > 0 ? std::min<int64_t>(max_seqlen, int64_t(T) + window - 1)
-                                   : int64_t(max_seqlen);
-  const int64_t units = int64_t(batch) * hkv;
-  int64_t chunk = (range * units + 8191) / 8192;
-  chunk = ((chunk + 127) / 128) * 128;
-  chunk = std::max<int64_t>(256, std::min<int64_t>(16384, chunk));
-  p.chunk = static_cast<int32_t>(chunk);
-  p.splits = static_cast<int32_t>(std::max<int64_t>(1, (range + chunk - 1) / chunk));
   p.rows = T * (hq / hkv);
-  p.bytes = static_cast<size_t>(units) * p.splits * p.rows * (sa::kDv + 4) * sizeof(float);
+  p.tab_bytes = ((static_cast<size_t>(batch) * hkv + 1) * sizeof(int32_t) + 255) & ~size_t(255);
+  p.bytes = p.tab_bytes +
+            static_cast<size_t>(sa::kDecMaxGrid) * 2 * p.rows * (sa::kDv + 4) * sizeof(float);
   return p;
 }
 
@@ -289,7 +281,7 @@ size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_he
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
   const int32_t G = num_q_heads / num_kv_heads;
   if (!pow2_upto_128(G) || T * G > 128) return 0;
-  return decode_plan(batch, T, num_q_heads, num_kv_heads, max_seqlen, window).bytes;
+  return decode_plan(batch, T, num_q_heads, num_kv_heads).bytes;
 }
 
 sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void *vcache,
@@ -312,30 +304,38 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
   if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(vcache, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(sink, 4) || !aligned(seqlens, 4))
     return SINKATTN_EINVAL;
-  const DecodePlan plan = decode_plan(batch, T, num_q_heads, num_kv_heads, max_seqlen, window);
+  const DecodePlan plan = decode_plan(batch, T, num_q_heads, num_kv_heads);
   if (!workspace || workspace_bytes < plan.bytes || !aligned(workspace, 256))
     return SINKATTN_EWORKSPACE;
   AttnArgs a;
   if (sinkattn_status st = fill_common(a, params, rope_base, num_q_heads, num_kv_heads, window))
     return st;
+  if (!(a.scale_log2 > 0.f)) return SINKATTN_EINVAL;  // the decode softmax scales after the max
+  if (int64_t(batch) * num_kv_heads > INT32_MAX / 2) return SINKATTN_EUNSUPPORTED;
 
-  a.mode = sa::kModeDecodePartial;
-  a.batch = batch;
-  a.tile_tokens = T;
-  a.T = T;
-  a.S_cap = S_cap;
-  a.chunk = plan.chunk;
-  a.tiles_per_seq = plan.splits;
-  const int64_t n_items = int64_t(batch) * num_kv_heads * plan.splits;
-  if (n_items > INT32_MAX) return SINKATTN_EUNSUPPORTED;
-  a.n_items = static_cast<int32_t>(n_items);
-  a.part_rows = plan.rows;
-  a.q_tx_bytes = 3u * 64u * 2u * static_cast<uint32_t>(G * T);
-  a.seqlens = seqlens;
-  a.sink = sink;
-  a.part_o = static_cast<float *>(workspace);
-  a.part_ml = static_cast<float *>(workspace) +
-              static_cast<size_t>(batch) * num_kv_heads * plan.splits * plan.rows * sa::kDv;
+  sa::DecArgs d;
+  std::memset(&d, 0, sizeof d);
+  d.Hq = num_q_heads;
+  d.Hkv = num_kv_heads;
+  d.G = G;
+  d.T = T;
+  d.R = plan.rows;
+  d.window = window;
+  d.batch = batch;
+  d.S_cap = S_cap;
+  d.n_units = batch * num_kv_heads;
+  d.rope_on = a.rope_on;
+  d.rope_style = a.rope_style;
+  d.q_tx_bytes = 3u * 64u * 2u * static_cast<uint32_t>(G * T);
+  d.scale_log2 = a.scale_log2;
+  d.seqlens = seqlens;
+  d.sink = sink;
+  d.out = static_cast<__nv_bfloat16 *>(out);
+  d.lse = lse;
+  d.unit_blk = static_cast<int32_t *>(workspace);
+  d.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.tab_bytes);
+  d.part_ml = d.part_o + static_cast<size_t>(sa::kDecMaxGrid) * 2 * plan.rows * sa::kDv;
+  std::memcpy(d.rope_turns, a.rope_turns, sizeof d.rope_turns);
 
   DeviceInfo dev;
   if (!device_info(dev)) return SINKATTN_ECUDA;
@@ -343,27 +343,26 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, num_q_heads, uint64_t(batch) * T, G, T) ||
-      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, kBNDecode) ||
-      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, kBNDecode))
+      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, sa::kDecBN) ||
+      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, sa::kDecBN))
     return SINKATTN_ECUDA;
-  const int grid = static_cast<int>(std::min<int64_t>(n_items, dev.sms));
+  // upper bound of the blocks: every unit sees at most max_seqlen (window: T + W - 1) keys
+  const int64_t range = window > 0 ? std::min<int64_t>(max_seqlen, int64_t(T) + window - 1)
+                                   : int64_t(max_seqlen);
+  const int64_t max_blocks = int64_t(d.n_units) * ((range + sa::kDecBN - 1) / sa::kDecBN);
+  const int grid = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(max_blocks, dev.sms), sa::kDecMaxGrid)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a.scale_log2 > 0.f) {
-    auto kern = sa::sinkattn_decode_kernel;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sa::DecLayout::kDynSmem)) != cudaSuccess)
-      return SINKATTN_ECUDA;
-    kern<<<grid, sa::kThreads, sa::DecLayout::kDynSmem, s>>>(mq, mk, mv, a);
-    if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
-  } else if (sinkattn_status st = launch<kBNDecode, 1, kDecodeStages>(mq, mk, mv, a, grid, s)) {
-    return st;
-  }
+  auto kern = sa::sinkattn_decode_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sa::DecLayout::kDynSmem)) != cudaSuccess)
+    return SINKATTN_ECUDA;
+  kern<<<grid, sa::kThreads, sa::DecLayout::kDynSmem, s>>>(mq, mk, mv, d);
+  if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
 
   const int64_t rows = int64_t(batch) * T * num_q_heads;
   if (rows > INT32_MAX) return SINKATTN_EUNSUPPORTED;
-  sa::sinkattn_combine_kernel<<<static_cast<unsigned>(rows), sa::kDv, 0, s>>>(
-      a.part_o, a.part_ml, seqlens, sink, T, num_q_heads, num_kv_heads, window, plan.chunk,
-      plan.splits, plan.rows, static_cast<__nv_bfloat16 *>(out), lse);
+  sa::sinkattn_decode_combine_kernel<<<static_cast<unsigned>(rows), sa::kDv, 0, s>>>(d, grid);
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 

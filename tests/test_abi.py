@@ -101,11 +101,15 @@ def test_decode_workspace_size(L):
     assert ws(2, 4, 64, 5, 1000, 0) == 0
     a = ws(64, 4, 64, 4, 262144, 0)
     b = ws(64, 4, 64, 4, 65536, 0)
-    assert a > 0 and b > 0 and a >= b
-    # the window bounds the keys a sequence needs
-    assert ws(64, 4, 64, 8, 262144, 128) < ws(64, 4, 64, 8, 262144, 0)
-    # partial rows = T * G, 132 fp32 each (128 values + max, two sums, pad), units * splits
-    assert a % (64 * 4 * 16 * 132 * 4) == 0
+    # the layout does not depend on the cache lengths or the window: the block
+    # offsets of the batch*Hkv units (int32, padded to 256 bytes), then two
+    # partial slots of T*G rows x 132 fp32 (128 values, max, sum, pad) per CTA
+    # for at most 160 CTAs
+    assert a == b == ws(64, 4, 64, 4, 262144, 128)
+    tab = ((64 * 4 + 1) * 4 + 255) // 256 * 256
+    assert a == tab + 160 * 2 * (4 * 16) * 132 * 4
+    tab8 = ((64 * 8 + 1) * 4 + 255) // 256 * 256
+    assert ws(64, 4, 64, 8, 262144, 128) == tab8 + 160 * 2 * (4 * 8) * 132 * 4
 
 
 def _decode(L, q=1, kc=1, vc=1, sl=1, sink=1, window=0, base=5e6, b=2, t=4, s_cap=100,
@@ -129,3 +133,17 @@ def test_decode_argument_checks(L):
     assert _decode(L, ws=None) == sa.EWORKSPACE
     assert _decode(L, ws_bytes=8) == sa.EWORKSPACE
     assert _decode(L, b=0) == sa.OK
+
+
+def test_decode_rejects_non_positive_scale(L):
+    """The decode softmax scales the logits after taking their max, so a scale
+    <= 0 is refused before anything is launched."""
+    import sliding_window_sink_bias_b300 as sa
+    P = ctypes.c_void_p
+    f = lambda x: P(256 * x)
+    ws = L.sinkattn_decode_workspace_size(2, 4, 64, 4, 100, 0)
+    for scale in (-0.5, -1e-3):
+        p = sa.Params(scale, 0, 0, 0)
+        st = L.sinkattn_decode_ex(f(1), f(1), f(1), f(1), f(1), 0, 5e6, 2, 4, 100, 100, 64, 4,
+                                  ctypes.byref(p), f(1), ws, f(1), f(1), None)
+        assert st == sa.EINVAL

@@ -40,6 +40,17 @@ def test_mtp_verify_small(oracle_mod, window, hkv, base):
     assert_parity(o, l, ro, rl, f"decode W={window}")
 
 
+@pytest.mark.parametrize("window,hkv,base", [(0, 4, 5e6), (128, 8, 1e4), (16, 4, 1e4)])
+def test_lengths_at_block_edges(oracle_mod, window, hkv, base):
+    # cache lengths on both sides of the 64-key block edges: the blocks are cut
+    # across CTAs, so some CTA segments hold keys that some query rows cannot
+    # see (e.g. a query at position 127 against keys 128..130)
+    seqlens = [1, 2, 3, 4, 5, 63, 64, 65, 66, 67, 68, 127, 128, 129, 130, 131, 132, 191, 192, 193,
+               255, 256, 257]
+    o, l, ro, rl = run_decode(oracle_mod, seqlens, 4, 257, 64, hkv, window, base, seed=9)
+    assert_parity(o, l, ro, rl, f"block edges W={window}")
+
+
 @pytest.mark.parametrize("t", [1, 2, 3, 8])
 def test_token_counts(oracle_mod, t):
     o, l, ro, rl = run_decode(oracle_mod, [t, 700, 1500], t, 1600, 64, 4, 0, 5e6, seed=t)

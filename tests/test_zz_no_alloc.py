@@ -24,10 +24,11 @@ def test_noalloc_rejects_sizes_beyond_its_buffer():
     buffer is refused with SINKATTN_EWORKSPACE before anything is launched."""
     import sliding_window_sink_bias_b300 as sa
     L = sa.lib()
-    need = sa.decode_workspace_size(64, 4, 64, 4, 262144, 0)
+    # 8 query tokens x 16 heads = 128 partial rows per unit: more than the buffer holds
+    need = sa.decode_workspace_size(64, 8, 64, 4, 262144, 0)
     assert need > sa.NOALLOC_SCRATCH_BYTES
     P = ctypes.c_void_p
-    st = L.sinkattn_decode_noalloc(P(256), P(256), P(256), P(256), P(256), 0, 5e6, 64, 4, 262144,
+    st = L.sinkattn_decode_noalloc(P(256), P(256), P(256), P(256), P(256), 0, 5e6, 64, 8, 262144,
                                    262144, 64, 4, P(256), P(256), None)
     assert st == sa.EWORKSPACE
 
