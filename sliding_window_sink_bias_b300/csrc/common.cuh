@@ -125,6 +125,7 @@ __device__ __forceinline__ uint4 *swz_chunk(uint8_t *box, int32_t r, int32_t c) 
 // unit computes its angles once and rotates all G heads.  128 threads.
 __device__ void rope_q_tile(uint8_t *box0, int32_t G, int32_t n_tok, int32_t pos0,
                             int32_t rope_style, const unsigned long long *turns, int32_t tid) {
+  if (n_tok <= 0) return;
   const int32_t nch = rope_style == 0 ? 8 : 4;
   const int32_t units = n_tok * nch;
   const int32_t hsplit = units >= 128 ? 1 : min(G, 128 / units);

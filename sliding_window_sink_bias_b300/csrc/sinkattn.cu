@@ -13,6 +13,7 @@
 #include "attn_kernel.cuh"
 #include "band_kernel.cuh"
 #include "decode_kernel.cuh"
+#include "causal_kernel.cuh"
 #include "sinkattn.h"
 
 namespace {
@@ -23,6 +24,7 @@ using sa::Layout;
 constexpr int32_t kVersion = 100;  // 0.1.0
 constexpr int32_t kBNWide = 144;   // one key block covers a 128-key window + 16-token tile
 constexpr int32_t kBN = 128;
+constexpr uint32_t kQBoxBytesHost = 128 * 128;  // one 64-dim box of a 128-row Q tile
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool pow2_upto_128(int32_t x) { return x >= 1 && x <= 128 && (x & (x - 1)) == 0; }
@@ -162,6 +164,47 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
 // Decode workspace: the per-unit block offsets (n_units + 1 int32, padded to
 // 256 bytes), then 2 partial slots per CTA of R rows x (128 + 4) fp32, for at
 // most sa::kDecMaxGrid CTAs.
+// Global causal prefill with G >= 4 query heads per KV head: pairs of query
+// tiles per CTA, longest first.
+sinkattn_status launch_causal(const void *q, const void *k, const void *v, const AttnArgs &a,
+                              const int32_t *cu_seqlens, int32_t batch, int32_t total,
+                              int32_t max_seqlen, const DeviceInfo &dev, cudaStream_t stream) {
+  sa::CausalArgs c;
+  std::memset(&c, 0, sizeof c);
+  c.Hq = a.Hq;
+  c.Hkv = a.Hkv;
+  c.G = a.G;
+  c.T = 128 / a.G;
+  c.batch = batch;
+  c.max_seqlen = max_seqlen;
+  c.npairs = (max_seqlen + 2 * c.T - 1) / (2 * c.T);
+  const int64_t n_items = int64_t(batch) * a.Hkv * c.npairs;
+  if (n_items > INT32_MAX) return SINKATTN_EUNSUPPORTED;
+  c.n_items = static_cast<int32_t>(n_items);
+  c.rope_on = a.rope_on;
+  c.rope_style = a.rope_style;
+  c.q_tx_bytes = 3u * kQBoxBytesHost;
+  c.scale_log2 = a.scale_log2;
+  c.out_v8 = aligned(a.out, 32) ? 1 : 0;
+  c.cu_seqlens = cu_seqlens;
+  c.sink = a.sink;
+  c.out = a.out;
+  c.lse = a.lse;
+  std::memcpy(c.rope_turns, a.rope_turns, sizeof c.rope_turns);
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, 192, a.Hq, total, a.G, c.T) ||
+      !make_map(&mk, k, 192, a.Hkv, total, 1, sa::kCauBN) ||
+      !make_map(&mv, v, 128, a.Hkv, total, 1, sa::kCauBN))
+    return SINKATTN_ECUDA;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n_items, dev.sms)));
+  auto kern = sa::sinkattn_causal_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sa::CauLayout::kDynSmem)) != cudaSuccess)
+    return SINKATTN_ECUDA;
+  kern<<<grid, sa::kCauThreads, sa::CauLayout::kDynSmem, stream>>>(mq, mk, mv, c);
+  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+}
+
 struct DecodePlan {
   int32_t rows = 0;
   size_t tab_bytes = 0, bytes = 0;
@@ -255,6 +298,8 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
   if (G == sa::kBandG && window >= 1 && window <= sa::kBandMaxWin * sa::kBandSeg - sa::kBandSeg &&
       a.scale_log2 > 0.f)
     return launch_band(q, k, v, a, cu_seqlens, batch, total, dev, s);
+  if (window == 0 && G >= 4 && a.scale_log2 > 0.f)
+    return launch_causal(q, k, v, a, cu_seqlens, batch, total, max_seqlen, dev, s);
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, num_q_heads, total, G, tile_tokens) ||
