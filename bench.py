@@ -276,6 +276,50 @@ def bench_prefill(name, steps, warmup, ws, local, with_e2e):
     return res
 
 
+def bench_hybrid(name, steps, warmup, ws, local):
+    """One hybrid block (5 SWA layers, 1 GA layer) over a ragged batch: every
+    step runs the six layer prefills back to back on the same stream."""
+    import torch
+
+    import sliding_window_sink_bias_b300 as sa
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[name]
+    dev = f"cuda:{local}"
+    lens = synth.log_uniform_lengths(wl["n_seq"], wl["len_lo"], wl["len_hi"], seed=0)
+    hq = wl["hq"]
+    swa = synth.prefill_inputs(lens, hq, wl["swa_hkv"], window=wl["window"],
+                               rope_base=wl["swa_base"], seed=0, device=dev)
+    ga = synth.prefill_inputs(lens, hq, wl["ga_hkv"], window=0, rope_base=wl["ga_base"], seed=1,
+                              device=dev)
+    n_layers = wl["swa_layers"] + wl["ga_layers"]
+    sinks = [synth.sink_vector(hq, seed=10 + i, device=dev) for i in range(n_layers)]
+    total = sum(lens)
+    out = torch.empty(total, hq, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(total, hq, dtype=torch.float32, device=dev)
+
+    def call():
+        for i in range(wl["swa_layers"]):
+            sa.prefill(swa.q, swa.k, swa.v, sinks[i], swa.cu_seqlens, max_seqlen=max(lens),
+                       window=wl["window"], rope_base=wl["swa_base"], out=out, lse=lse)
+        for i in range(wl["ga_layers"]):
+            sa.prefill(ga.q, ga.k, ga.v, sinks[wl["swa_layers"] + i], ga.cu_seqlens,
+                       max_seqlen=max(lens), window=0, rope_base=wl["ga_base"], out=out, lse=lse)
+
+    with ClockSampler(local) as clk:
+        ms, _ = time_calls(call, steps, warmup, ws)
+    st, word = sa.device_status()
+    if st != sa.OK:
+        raise RuntimeError(f"device status {st} word {word:#x} after {name}")
+    swa_pairs = synth.algorithmic_pairs_prefill(lens, wl["window"])
+    ga_pairs = synth.algorithmic_pairs_prefill(lens, 0)
+    flops = hq * FLOP_PER_PAIR_HEAD * (wl["swa_layers"] * swa_pairs + wl["ga_layers"] * ga_pairs)
+    res = {"name": name, "ms": ms, "flops": flops, "tokens": total, "lens": lens,
+           "clocks": clk.summary(), "launches": n_layers * steps}
+    del swa, ga, out, lse
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_decode(name, steps, warmup, ws, local):
     import torch
 
@@ -405,7 +449,11 @@ def run_reference(args):
 def single_workload(args, ws, rank, local, peaks):
     from sliding_window_sink_bias_b300 import synth
     wl = synth.WORKLOADS[args.workload]
-    if wl["kind"] == "prefill":
+    if wl["kind"] == "hybrid":
+        r = bench_hybrid(args.workload, args.steps, args.warmup, ws, local)
+        line = {"workload": args.workload, "ms": r["ms"], "tokens_per_s": r["tokens"] / (r["ms"] / 1e3),
+                "tflops": r["flops"] / (r["ms"] / 1e3) / 1e12, "lens": r["lens"], "clocks": r["clocks"]}
+    elif wl["kind"] == "prefill":
         r = bench_prefill(args.workload, args.steps, args.warmup, ws, local, with_e2e=False)
         tf = r["flops"] / (r["ms"] / 1e3) / 1e12
         gbs = r["bytes"] / (r["ms"] / 1e3) / 1e9
@@ -419,6 +467,41 @@ def single_workload(args, ws, rank, local, peaks):
                 "frac_hbm": gbs / peaks["hbm_gbs"], "clocks": r["clocks"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+# DRAM bytes per launch measured by ncu (profiles/dram_traffic.json), keyed by
+# kernel; each entry holds the sha256 of the kernel sources it was measured on
+# and is ignored (traffic null) once those sources change.
+KERNEL_SOURCES = {
+    "band": ["band_kernel.cuh", "common.cuh", "ptx.cuh"],
+    "causal": ["causal_kernel.cuh", "common.cuh", "ptx.cuh"],
+    "decode": ["decode_kernel.cuh", "common.cuh", "ptx.cuh"],
+}
+
+
+def kernel_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sliding_window_sink_bias_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_for(key, tokens):
+    """DRAM bytes of one launch of the benchmarked workload, or None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    e = tab.get(key)
+    if not e or e.get("sha256") != kernel_hash(e["kernel"]):
+        return None
+    b = e["dram_bytes_per_launch"]
+    if tokens and e.get("tokens"):  # measured on a smaller case: scale by the units processed
+        b = b * tokens / e["tokens"]
+    return b
 
 
 def roofline_obj(bound, achieved, peak, unit, traffic=None):
@@ -455,7 +538,8 @@ def main():
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (6.07 GB per step), no flush"},
         "tokens_per_s": ws * m["tokens"] / (m["ms"] / 1e3),
-        "roofline": roofline_obj("hbm", gbs, peaks["hbm_gbs"], "GB/s"),
+        "roofline": roofline_obj("hbm", gbs, peaks["hbm_gbs"], "GB/s",
+                                 traffic_for("band", m["tokens"])),
         "peaks_source": peaks["source"],
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": m["h2d"],
                 "d2h_bytes_per_step": m["d2h"], "ms_per_step": m["e2e_ms"]},
@@ -469,7 +553,10 @@ def main():
         g_tf = g["flops"] / (g["ms"] / 1e3) / 1e12
         extra["ga_prefill_1x131072"] = {
             "value": ws * g_tf, "unit": "TFLOP/s", "ms_per_step": g["ms"],
-            "roofline": roofline_obj("tensor", g_tf, peaks["bf16_tflops"], "TFLOP/s"),
+            "roofline": roofline_obj("tensor", g_tf, peaks["bf16_tflops"], "TFLOP/s",
+                                     traffic_for("causal", g["tokens"])),
+            "frac_of_sustained_peak": (g_tf / peaks["bf16_tflops_sustained"]
+                                       if peaks.get("bf16_tflops_sustained") else None),
             "clocks": g["clocks"]}
         for name in ("mtp_decode_ga_b64_t4", "mtp_decode_swa_b64_t4"):
             d = bench_decode(name, args.steps, args.warmup, ws, local)
@@ -477,8 +564,16 @@ def main():
             extra[name] = {"value": ws * d_gbs, "unit": "GB/s", "ms_per_step": d["ms"],
                            "kv_bytes": d["kv_bytes"],
                            "tflops": d["flops"] / (d["ms"] / 1e3) / 1e12,
-                           "roofline": roofline_obj("hbm", d_gbs, peaks["hbm_gbs"], "GB/s"),
+                           "roofline": roofline_obj("hbm", d_gbs, peaks["hbm_gbs"], "GB/s",
+                                                    traffic_for("decode_" + name, None)),
                            "clocks": d["clocks"], "l2": "256 MB flush between steps"}
+        h = bench_hybrid("hybrid_block_ragged_8seq", max(3, args.steps // 4), args.warmup, ws,
+                         local)
+        extra["hybrid_block_ragged_8seq"] = {
+            "value": ws * h["tokens"] / (h["ms"] / 1e3), "unit": "tokens/s",
+            "ms_per_step": h["ms"], "tflops": h["flops"] / (h["ms"] / 1e3) / 1e12,
+            "seq_lens": h["lens"], "layers": "5 SWA (64/8, W=128) + 1 GA (64/4)",
+            "clocks": h["clocks"]}
         line["other_workloads"] = extra
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

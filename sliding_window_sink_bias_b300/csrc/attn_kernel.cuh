@@ -1,4 +1,9 @@
-// attn_kernel.cuh -- the sink-bias GQA attention forward kernel for sm_103a.
+// attn_kernel.cuh -- the general sink-bias GQA prefill kernel for sm_103a.
+//
+// The shapes of the model run on specialised kernels (band_kernel.cuh: sliding
+// window, 8 heads per KV head, W <= 128; causal_kernel.cuh: global causal with
+// >= 4 heads per KV head).  This kernel covers every other supported prefill:
+// other group sizes, wider windows and non-positive logit scales.
 //
 // Computes, for one tile of 128 packed query rows at a time, the attention of
 // the MiMo-V2-Flash Technical Report (§2.2 eqs. (1)-(3); shapes from §2.1
@@ -33,29 +38,22 @@
 #include "common.cuh"
 
 namespace sa {
-enum : int32_t { kModePrefill = 0, kModeDecodePartial = 1 };
 
 struct AttnArgs {
   int32_t Hq, Hkv, G;
-  int32_t tile_tokens;     // tokens per tile: 128 / G (prefill) or T (decode)
-  int32_t mode;
+  int32_t tile_tokens;     // tokens per tile: 128 / G
   int32_t window;
   int32_t batch;
   int32_t n_items;         // virtual work items (some are empty and skipped)
-  int32_t tiles_per_seq;   // prefill: ceil(max_seqlen / tile_tokens); decode: splits per unit
+  int32_t tiles_per_seq;   // ceil(max_seqlen / tile_tokens)
   int32_t lpt_order;       // 1: walk tiles longest-first (global causal prefill)
-  int32_t T, S_cap, chunk; // decode only
   int32_t rope_on, rope_style;
-  int32_t part_rows;       // decode: T * G rows per partial
   uint32_t q_tx_bytes;     // bytes of one Q tile load (3 boxes)
   float scale_log2;        // logit scale * log2(e)
   const int32_t *cu_seqlens;
-  const int32_t *seqlens;
   const float *sink;
   __nv_bfloat16 *out;
   float *lse;
-  float *part_o;           // decode: [units * splits, part_rows, 128] unnormalised O
-  float *part_ml;          // decode: [units * splits, part_rows, 4] (m, l, l_rounded, 0), log2 domain
   unsigned long long rope_turns[32];  // round(theta_t / (2 pi) * 2^64), t = 0..31
 };
 
@@ -70,59 +68,35 @@ struct Item {
   int32_t kstart;   // key position of column 0 of block 0
   int32_t n_blk;
   int32_t key_lo, key_hi;  // keys this item may use: [key_lo, key_hi)
-  int32_t out_idx;  // decode: partial slot
 };
 
 __device__ __forceinline__ Item make_item(const AttnArgs &a, int32_t w, int32_t BN) {
   Item it;
   it.valid = 0;
-  if (a.mode == kModePrefill) {
-    int32_t i, r;
-    if (a.lpt_order) {
-      const int32_t per = a.batch * a.Hkv;
-      i = a.tiles_per_seq - 1 - w / per;
-      r = w % per;
-    } else {
-      i = w % a.tiles_per_seq;
-      r = w / a.tiles_per_seq;
-    }
-    it.kvh = r % a.Hkv;
-    it.b = r / a.Hkv;
-    const int32_t s0 = __ldg(a.cu_seqlens + it.b);
-    const int32_t L = __ldg(a.cu_seqlens + it.b + 1) - s0;
-    it.pos0 = i * a.tile_tokens;
-    if (it.pos0 >= L) return it;
-    it.n_tok = min(a.tile_tokens, L - it.pos0);
-    it.q_row = s0 + it.pos0;
-    it.kv_row0 = s0;
-    const int32_t hi = it.pos0 + it.n_tok;
-    it.kstart = a.window > 0 ? max(0, it.pos0 - a.window + 1) : 0;
-    it.n_blk = (hi - it.kstart + BN - 1) / BN;
-    it.key_lo = 0;
-    it.key_hi = hi;
-    it.out_idx = 0;
-    it.valid = 1;
+  int32_t i, r;
+  if (a.lpt_order) {
+    const int32_t per = a.batch * a.Hkv;
+    i = a.tiles_per_seq - 1 - w / per;
+    r = w % per;
   } else {
-    const int32_t s = w % a.tiles_per_seq;
-    const int32_t u = w / a.tiles_per_seq;
-    it.kvh = u % a.Hkv;
-    it.b = u / a.Hkv;
-    const int32_t L = __ldg(a.seqlens + it.b);
-    const int32_t lo = a.window > 0 ? max(0, L - a.T - a.window + 1) : 0;
-    const int32_t c0 = lo + s * a.chunk;
-    const int32_t c1 = min(c0 + a.chunk, L);
-    if (c0 >= c1) return it;
-    it.n_tok = a.T;
-    it.pos0 = L - a.T;
-    it.q_row = it.b * a.T;
-    it.kv_row0 = it.b * a.S_cap;
-    it.kstart = c0;
-    it.n_blk = (c1 - c0 + BN - 1) / BN;
-    it.key_lo = c0;
-    it.key_hi = c1;
-    it.out_idx = u * a.tiles_per_seq + s;
-    it.valid = 1;
+    i = w % a.tiles_per_seq;
+    r = w / a.tiles_per_seq;
   }
+  it.kvh = r % a.Hkv;
+  it.b = r / a.Hkv;
+  const int32_t s0 = __ldg(a.cu_seqlens + it.b);
+  const int32_t L = __ldg(a.cu_seqlens + it.b + 1) - s0;
+  it.pos0 = i * a.tile_tokens;
+  if (it.pos0 >= L) return it;
+  it.n_tok = min(a.tile_tokens, L - it.pos0);
+  it.q_row = s0 + it.pos0;
+  it.kv_row0 = s0;
+  const int32_t hi = it.pos0 + it.n_tok;
+  it.kstart = a.window > 0 ? max(0, it.pos0 - a.window + 1) : 0;
+  it.n_blk = (hi - it.kstart + BN - 1) / BN;
+  it.key_lo = 0;
+  it.key_hi = hi;
+  it.valid = 1;
   return it;
 }
 
@@ -349,12 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t hi = min(pos, it.key_hi - 1);
       if (!rvalid) { lo = 1; hi = 0; }
       // Running max starts at the sink and the denominator at exp(sink - m) = 1
-      // (eq. (2)); a -inf sink starts from the empty sum.  Decode partials carry
-      // no sink: the combine adds it once.  Two denominators are kept: `l` sums
-      // the fp32 weights (for lse), `lr` sums the bf16-rounded weights that the
-      // PV MMA actually multiplies, so O / lr cancels the rounding of P.
+      // (eq. (2)); a -inf sink starts from the empty sum.  Two denominators are
+      // kept: `l` sums the fp32 weights (for lse), `lr` sums the bf16-rounded
+      // weights that the PV MMA actually multiplies, so O / lr cancels the
+      // rounding of P.
       float m = -INFINITY, l = 0.f, lr = 0.f;
-      if (args.mode == kModePrefill) {
+      {
         const float sk = __ldg(args.sink + head);
         if (sk != -INFINITY) { m = sk * kLog2e; l = 1.f; lr = 1.f; }
       }
@@ -371,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           if (BN - c0 >= 32) tmem_ld32(s_t + c0, r); else tmem_ld16(s_t + c0, r);
           tmem_wait_ld();
+          reg_fence<32>(r);
 #pragma unroll
           for (int32_t c = 0; c < 32; ++c) {
             if (c0 + c < BN) {
@@ -393,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool full = BN - c0 >= 32;
           if (full) tmem_ld32(s_t + c0, r); else tmem_ld16(s_t + c0, r);
           tmem_wait_ld();
+          reg_fence<32>(r);
           uint32_t pk[16];
 #pragma unroll
           for (int32_t c = 0; c < 32; c += 2) {
@@ -426,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t r[32];
               tmem_ld32(o_t + c0, r);
               tmem_wait_ld();
+              reg_fence<32>(r);
 #pragma unroll
               for (int32_t c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
               tmem_st32(o_t + c0, r);
@@ -438,51 +415,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gs;
       }
       if (!ok) break;
-      // ---------------- epilogue: O / l and lse, or the raw partial
+      // ---------------- epilogue: O / l and lse
       if (!(ok = wait_bar_warp(B_PVDONE, gp & 1, abort_flag, 9))) break;
       ++gp;
       tc_fence_after();
       const uint32_t o_t = tmem + lane_off + kTmemO;
-      if (args.mode == kModePrefill) {
-        const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
-        const size_t orow = static_cast<size_t>(it.q_row + t) * args.Hq + head;
-        uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv);
+      const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+      const size_t orow = static_cast<size_t>(it.q_row + t) * args.Hq + head;
+      uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv);
 #pragma unroll
-        for (int32_t c0 = 0; c0 < kDv; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(o_t + c0, r);
-          tmem_wait_ld();
-          if (rvalid) {
+      for (int32_t c0 = 0; c0 < kDv; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(o_t + c0, r);
+        tmem_wait_ld();
+        reg_fence<32>(r);
+        if (rvalid) {
 #pragma unroll
-            for (int32_t q4 = 0; q4 < 4; ++q4) {
-              uint32_t w4[4];
+          for (int32_t q4 = 0; q4 < 4; ++q4) {
+            uint32_t w4[4];
 #pragma unroll
-              for (int32_t e = 0; e < 4; ++e)
-                w4[e] = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2 * e]) * inv_l,
-                                    __uint_as_float(r[q4 * 8 + 2 * e + 1]) * inv_l);
-              dst[c0 / 8 + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+            for (int32_t e = 0; e < 4; ++e)
+              w4[e] = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2 * e]) * inv_l,
+                                  __uint_as_float(r[q4 * 8 + 2 * e + 1]) * inv_l);
+            dst[c0 / 8 + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
-        if (rvalid) args.lse[orow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-      } else {
-        const size_t prow = static_cast<size_t>(it.out_idx) * args.part_rows + row;
-        float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kDv);
-#pragma unroll
-        for (int32_t c0 = 0; c0 < kDv; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(o_t + c0, r);
-          tmem_wait_ld();
-          if (rvalid) {
-#pragma unroll
-            for (int32_t q4 = 0; q4 < 8; ++q4)
-              dst[c0 / 4 + q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
-                                             __uint_as_float(r[4 * q4 + 2]),
-                                             __uint_as_float(r[4 * q4 + 3]));
-          }
-        }
-        if (rvalid) reinterpret_cast<float4 *>(args.part_ml)[prow] = make_float4(m, l, lr, 0.f);
       }
+      if (rvalid) args.lse[orow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(B_OEMPTY);
     }
@@ -522,52 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// Split-KV combine (decode): merge the per-chunk partials (m_s, l_s, O_s),
-// computed without the sink, and add the sink exactly once:
-//   M = max(sink, max_s m_s),  Lsum = 2^(sink - M) + sum_s l_s 2^(m_s - M),
-//   o = sum_s 2^(m_s - M) O_s / Lsum,  lse = (M + log2 Lsum) ln 2   (log2 domain).
-// o divides by the sum of the rounded weights (l_rounded), lse uses the fp32 sum.
-// One CTA of 128 threads (one per value dim) per output row, fixed split order.
-__global__ void __launch_bounds__(128)
-    sinkattn_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
-                            const int32_t *__restrict__ seqlens, const float *__restrict__ sink,
-                            int32_t T, int32_t Hq, int32_t Hkv, int32_t window, int32_t chunk,
-                            int32_t splits, int32_t R, __nv_bfloat16 *__restrict__ out,
-                            float *__restrict__ lse) {
-  const int32_t rowid = blockIdx.x;  // (b * T + t) * Hq + h
-  const int32_t G = Hq / Hkv;
-  const int32_t h = rowid % Hq, bt = rowid / Hq;
-  const int32_t t = bt % T, b = bt / T;
-  const int32_t u = b * Hkv + h / G, r = t * G + (h % G);
-  const int32_t L = __ldg(seqlens + b);
-  const int32_t lo = window > 0 ? max(0, L - T - window + 1) : 0;
-  const int32_t ns = L > lo ? (L - lo + chunk - 1) / chunk : 0;
-  const float sk_raw = __ldg(sink + h);
-  const float sk = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
-  const float4 *ml = reinterpret_cast<const float4 *>(part_ml);
-  float M = sk;
-  for (int32_t s = 0; s < ns; ++s) M = fmaxf(M, ml[static_cast<size_t>(u * splits + s) * R + r].x);
-  const int32_t e = threadIdx.x;
-  if (M == -INFINITY) {
-    out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(0.f);
-    if (e == 0) lse[rowid] = -INFINITY;
-    return;
-  }
-  const float s0 = sk == -INFINITY ? 0.f : ex2(sk - M);
-  float Ls = s0, Lr = s0;
-  float acc = 0.f;
-  for (int32_t s = 0; s < ns; ++s) {
-    const size_t pr = static_cast<size_t>(u * splits + s) * R + r;
-    const float4 v = ml[pr];
-    const float wgt = v.x == -INFINITY ? 0.f : ex2(v.x - M);
-    Ls += v.y * wgt;
-    Lr += v.z * wgt;
-    acc += wgt * part_o[pr * kDv + e];
-  }
-  out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(acc / Lr);
-  if (e == 0) lse[rowid] = (M + __log2f(Ls)) * kLn2;
 }
 
 }  // namespace sa

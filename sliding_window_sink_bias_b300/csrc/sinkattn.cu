@@ -276,7 +276,6 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
   // kernel; global or wide windows take the multi-block online-softmax kernel.
   const bool wide = window > 0 && window + tile_tokens - 1 <= kBNWide;
   const int32_t BN = wide ? kBNWide : kBN;
-  a.mode = sa::kModePrefill;
   a.batch = batch;
   a.tile_tokens = tile_tokens;
   a.tiles_per_seq = (max_seqlen + tile_tokens - 1) / tile_tokens;

@@ -131,6 +131,11 @@ WORKLOADS = {
                                  len_lo=65536, len_hi=262144, **GA),
     "mtp_decode_swa_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=262144,
                                   len_lo=65536, len_hi=262144, **SWA),
+    # one hybrid block of the model (§2.1: 5 SWA layers then 1 GA layer) over a
+    # varlen batch of 8 sequences, lengths log-uniform in [4096, 131072]
+    "hybrid_block_ragged_8seq": dict(kind="hybrid", n_seq=8, len_lo=4096, len_hi=131072,
+                                     swa_layers=5, ga_layers=1, hq=64, swa_hkv=8, ga_hkv=4,
+                                     window=128, swa_base=1e4, ga_base=5e6),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)
     "swa_prefill_1x32768": dict(kind="prefill", seqlens=[32768], **SWA),
     "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),
