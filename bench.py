@@ -373,7 +373,7 @@ def bench_decode(name, steps, warmup, ws, local):
     pairs = synth.algorithmic_pairs_decode(lens, t, W)
     res = {"name": name, "ms": ms, "kv_bytes": kv_bytes, "bytes": kv_bytes + io_bytes,
            "flops": pairs * hq * FLOP_PER_PAIR_HEAD, "clocks": clk.summary(),
-           "launches": 2 * steps, "tokens": wl["batch"] * t}
+           "launches": 2 * steps, "tokens": wl["batch"] * t, "vis_keys": sum(keys)}
     del inp, work, out, lse, flush
     torch.cuda.empty_cache()
     return res
@@ -565,7 +565,7 @@ def main():
                            "kv_bytes": d["kv_bytes"],
                            "tflops": d["flops"] / (d["ms"] / 1e3) / 1e12,
                            "roofline": roofline_obj("hbm", d_gbs, peaks["hbm_gbs"], "GB/s",
-                                                    traffic_for("decode_" + name, None)),
+                                                    traffic_for("decode_" + name, d["vis_keys"])),
                            "clocks": d["clocks"], "l2": "256 MB flush between steps"}
         h = bench_hybrid("hybrid_block_ragged_8seq", max(3, args.steps // 4), args.warmup, ws,
                          local)

@@ -162,14 +162,7 @@ __device__ void band_locate(const BandArgs &a, int32_t lane, int32_t *cur) {
   }
 }
 
-// Softmax + epilogue of one half of every row (half 0: band columns 0..71 and
-// output dims 0..63; half 1: band columns 72..143 and output dims 64..127).
-// The two threads of a row swap their partial maximum of tile i and their
-// partial sum of tile i-1 through shared memory, paired by an mbarrier.  Both
-// halves run the same code (half is a runtime value) to keep the hot loop
-// small in the instruction cache.
-//
-// TMEM loads/stores of N consecutive 32-bit columns (N = 4, 8, 16 or 32).
+// TMEM loads of N consecutive 32-bit columns (N = 4, 8, 16 or 32).
 template <int N>
 __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t *r) {
   if (N == 32) tmem_ld32p(taddr, r);
@@ -177,60 +170,31 @@ __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t *r) {
   else if (N == 8) tmem_ld8p(taddr, r);
   else tmem_ld4p(taddr, r);
 }
-template <int N>
-__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t *r) {
-  if (N == 32) tmem_st32p(taddr, r);
-  else if (N == 16) tmem_st16p(taddr, r);
-  else if (N == 8) tmem_st8p(taddr, r);
-  else tmem_st4p(taddr, r);
-}
 
-// Pass 1 over band columns C .. C+N-1 of a row (kc: their index within this
-// thread's half): masked columns become -inf and, if the warp has any, the
-// chunk is written back to TMEM (so pass 2 needs no mask: 2^-inf = 0); the
-// running max is taken with 3-input max.  Column offsets and sizes are
-// multiples of the chunk size.
-template <int C, int N>
-__device__ __forceinline__ void band_pass1(uint32_t s_t, int32_t kc, int32_t lo, uint32_t span,
-                                           float &mxa, float &mxb) {
+// Pass-1 mask of band columns 8K .. 8K+7 of this thread's half (TMEM column
+// s_col): columns that are not visible (k - lo > span as unsigned) become
+// -inf and, unless the whole warp sees all 8, the group is written back to
+// TMEM so that pass 2 needs no mask (2^-inf = 0).
+template <int K>
+__device__ __forceinline__ void band_mask8(uint32_t *r, uint32_t s_col, int32_t lo, uint32_t span) {
   constexpr uint32_t kNegInf = 0xff800000u;
-  uint32_t r[N];
-  tmem_ld_n<N>(s_t + C, r);
-  tmem_wait_ld();
-  reg_fence<N>(r);
-  const bool whole = static_cast<uint32_t>(kc - lo) <= span &&
-                     static_cast<uint32_t>(kc + N - 1 - lo) <= span;
+  const bool whole = static_cast<uint32_t>(8 * K - lo) <= span &&
+                     static_cast<uint32_t>(8 * K + 7 - lo) <= span;
   if (!__all_sync(0xffffffffu, whole)) {
 #pragma unroll
-    for (int32_t k = 0; k < N; ++k)
-      if (static_cast<uint32_t>(kc + k - lo) > span) r[k] = kNegInf;
-    tmem_st_n<N>(s_t + C, r);
-  }
-#pragma unroll
-  for (int32_t k = 0; k < N; k += 4) {
-    mxa = fmax3(mxa, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
-    mxb = fmax3(mxb, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
+    for (int32_t k = 0; k < 8; ++k)
+      if (static_cast<uint32_t>(8 * K + k - lo) > span) r[8 * K + k] = kNegInf;
+    tmem_st8p(s_col + 8 * K, r + 8 * K);
   }
 }
 
-// Pass 2 over band columns C .. C+N-1: P = 2^(s * scale * log2e - m) summed
-// and stored as bf16 pairs at TMEM column kBandPCol + C/2.
-template <int C, int N>
-__device__ __forceinline__ void band_pass2(uint32_t s_t, float2 sc2, float2 mneg2, float2 &sum2) {
-  uint32_t r[N];
-  tmem_ld_n<N>(s_t + C, r);
-  tmem_wait_ld();
-  reg_fence<N>(r);
-#pragma unroll
-  for (int32_t k = 0; k < N; k += 2) {
-    const float2 y = ffma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, mneg2);
-    const float2 p = make_float2(ex2(y.x), ex2(y.y));
-    sum2 = fadd2(sum2, p);
-    r[k >> 1] = pack_bf16x2(p.x, p.y);
-  }
-  tmem_st_n<N / 2>(s_t + kBandPCol + C / 2, r);
-}
-
+// Softmax + epilogue of one half of every row (half 0: band columns 0..71 and
+// output dims 0..63; half 1: band columns 72..143 and output dims 64..127).
+// Each of the two passes over the 72 logits of the half issues all its TMEM
+// loads before one wait: pass 1 masks (writing masked groups back) and takes
+// the maximum, pass 2 forms P.  The two threads of a row swap their partial maximum of tile i and their partial sum of tile i-1
+// through shared memory, paired by an mbarrier.  Both halves run the same code
+// (half is a runtime value) to keep the hot loop small in the instruction cache.
 __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCursor &c0,
                                              uint32_t tmem, uint32_t sbase, uint8_t *smem,
                                              volatile uint32_t *abort_flag) {
@@ -301,18 +265,35 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
       tc_fence_after();
       s_t = tmem + lane_off + tmem_s_col(buf);
-      // pass 1 (see band_pass1); chunks of half 0: 32 + 32 + 8 columns, of
-      // half 1: 8 + 16 + 32 + 16 (TMEM offsets are multiples of the size)
-      float mxa = -INFINITY, mxb = -INFINITY;
+      // pass 1: the 72 logits of this half in one batch of loads (TMEM
+      // offsets are multiples of the load size), the mask, the maximum
+      uint32_t r[72];
       if (half == 0) {
-        band_pass1<0, 32>(s_t, 0, lo, span, mxa, mxb);
-        band_pass1<32, 32>(s_t, 32, lo, span, mxa, mxb);
-        band_pass1<64, 8>(s_t, 64, lo, span, mxa, mxb);
+        tmem_ld_n<32>(s_t, r);
+        tmem_ld_n<32>(s_t + 32, r + 32);
+        tmem_ld_n<8>(s_t + 64, r + 64);
       } else {
-        band_pass1<72, 8>(s_t, 0, lo, span, mxa, mxb);
-        band_pass1<80, 16>(s_t, 8, lo, span, mxa, mxb);
-        band_pass1<96, 32>(s_t, 24, lo, span, mxa, mxb);
-        band_pass1<128, 16>(s_t, 56, lo, span, mxa, mxb);
+        tmem_ld_n<8>(s_t + 72, r);
+        tmem_ld_n<16>(s_t + 80, r + 8);
+        tmem_ld_n<32>(s_t + 96, r + 24);
+        tmem_ld_n<16>(s_t + 128, r + 56);
+      }
+      tmem_wait_ld();
+      reg_fence<72>(r);
+      band_mask8<0>(r, s_t + c0col, lo, span);
+      band_mask8<1>(r, s_t + c0col, lo, span);
+      band_mask8<2>(r, s_t + c0col, lo, span);
+      band_mask8<3>(r, s_t + c0col, lo, span);
+      band_mask8<4>(r, s_t + c0col, lo, span);
+      band_mask8<5>(r, s_t + c0col, lo, span);
+      band_mask8<6>(r, s_t + c0col, lo, span);
+      band_mask8<7>(r, s_t + c0col, lo, span);
+      band_mask8<8>(r, s_t + c0col, lo, span);
+      float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+      for (int32_t k = 0; k < 72; k += 4) {
+        mxa = fmax3(mxa, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+        mxb = fmax3(mxb, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
       }
       mx = fmaxf(mxa, mxb);
       tmem_wait_st();
@@ -323,22 +304,34 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       // eq. (2): m = max(max_j a_ij, sink), in the log2 domain (scale > 0)
       m = fmaxf(fmaxf(mx, other.x) * sc, sk2);
       const float mneg = m == -INFINITY ? 0.f : -m;
-      // pass 2 (see band_pass2): P of band column k lands at TMEM column
-      // kBandPCol + k/2, so each half's P covers only its own S columns (half 0:
-      // 36..71, half 1: 72..107); walking the chunks downwards (half 0) or
-      // upwards (half 1) overwrites only columns that were already read.
+      // P = 2^(s * scale * log2e - m) as bf16 pairs at TMEM column
+      // kBandPCol + 36 * half, over S columns this thread has already read
       const float2 sc2 = make_float2(sc, sc), mneg2 = make_float2(mneg, mneg);
       float2 sum2 = make_float2(0.f, 0.f);
+      uint32_t r[72];
       if (half == 0) {
-        band_pass2<64, 8>(s_t, sc2, mneg2, sum2);
-        band_pass2<32, 32>(s_t, sc2, mneg2, sum2);
-        band_pass2<0, 32>(s_t, sc2, mneg2, sum2);
+        tmem_ld_n<32>(s_t, r);
+        tmem_ld_n<32>(s_t + 32, r + 32);
+        tmem_ld_n<8>(s_t + 64, r + 64);
       } else {
-        band_pass2<72, 8>(s_t, sc2, mneg2, sum2);
-        band_pass2<80, 16>(s_t, sc2, mneg2, sum2);
-        band_pass2<96, 32>(s_t, sc2, mneg2, sum2);
-        band_pass2<128, 16>(s_t, sc2, mneg2, sum2);
+        tmem_ld_n<8>(s_t + 72, r);
+        tmem_ld_n<16>(s_t + 80, r + 8);
+        tmem_ld_n<32>(s_t + 96, r + 24);
+        tmem_ld_n<16>(s_t + 128, r + 56);
       }
+      tmem_wait_ld();
+      reg_fence<72>(r);
+#pragma unroll
+      for (int32_t k = 0; k < 72; k += 2) {
+        const float2 y = ffma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, mneg2);
+        const float2 p = make_float2(ex2(y.x), ex2(y.y));
+        sum2 = fadd2(sum2, p);
+        r[k >> 1] = pack_bf16x2(p.x, p.y);
+      }
+      const uint32_t p_t = s_t + kBandPCol + static_cast<uint32_t>(half) * 36u;
+      tmem_st16p(p_t, r);
+      tmem_st16p(p_t + 16, r + 16);
+      tmem_st4p(p_t + 32, r + 32);
       sum = sum2.x + sum2.y;
       tmem_wait_st();
       tc_fence_before();

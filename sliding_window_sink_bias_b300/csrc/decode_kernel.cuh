@@ -574,55 +574,67 @@ __global__ void __launch_bounds__(kThreads, 1)
 // add the sink exactly once (eq. (2) over a partition of the keys):
 //   M = max(sink, max_c m_c),  L = 2^(sink - M) + sum_c l_c 2^(m_c - M),
 //   o = sum_c 2^(m_c - M) O_c / L,  lse = (M + log2 L) ln 2   (log2 domain).
-// Rows of units the decode kernel finished return at once; rows of units with
-// no visible key get o = 0 and lse = sink.  One CTA of 128 threads (one per
-// value dim) per output row; the CTAs are visited in a fixed order.
-__global__ void __launch_bounds__(128)
+// Units the decode kernel finished return at once; rows of units with no
+// visible key get o = 0 and lse = sink.  Grid (units, kCombParts), 512 threads:
+// thread (w, e) takes value dim e of rows part * 4 + w, + 16, + 32, ...; the
+// partials are visited in a fixed order.
+constexpr int32_t kCombParts = 4;
+constexpr int32_t kCombThreads = 512;
+
+__global__ void __launch_bounds__(kCombThreads)
     sinkattn_decode_combine_kernel(const __grid_constant__ DecArgs a, int32_t grid) {
-  const int32_t rowid = blockIdx.x;  // (b * T + t) * Hq + h
-  const int32_t h = rowid % a.Hq, bt = rowid / a.Hq;
-  const int32_t t = bt % a.T, b = bt / a.T;
-  const int32_t u = b * a.Hkv + h / a.G, r = t * a.G + (h % a.G);
+  const int32_t u = blockIdx.x;
   const int32_t F0 = a.unit_blk[u], F1 = a.unit_blk[u + 1];
   const int64_t Tb = a.unit_blk[a.n_units];
-  const int32_t e = threadIdx.x;
-  const float sk_raw = __ldg(a.sink + h);
-  const float sk = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
-  if (F1 == F0) {  // no visible key at all: the empty sum
-    a.out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(0.f);
-    if (e == 0) a.lse[rowid] = sk_raw;
-    return;
-  }
   auto cta_of = [&](int64_t f) { return static_cast<int32_t>(((f + 1) * grid - 1) / Tb); };
-  const int32_t c_first = cta_of(F0), c_last = cta_of(F1 - 1);
-  if (c_first == c_last) return;  // finished by the decode kernel
+  const bool empty_unit = F1 == F0;
+  int32_t c_first = 0, c_last = 0;
+  if (!empty_unit) {
+    c_first = cta_of(F0);
+    c_last = cta_of(F1 - 1);
+    if (c_first == c_last) return;  // finished by the decode kernel
+  }
+  const int32_t b = u / a.Hkv, kvh = u % a.Hkv;
+  const int32_t e = threadIdx.x & (kDv - 1);
   const float4 *ml = reinterpret_cast<const float4 *>(a.part_ml);
-  auto slot = [&](int32_t c) {
+  // CTAs whose range is empty (fewer blocks than CTAs) hold no partial
+  auto has_part = [&](int32_t c) { return Tb * c / grid != Tb * (c + 1) / grid; };
+  auto slot = [&](int32_t c, int32_t r) {
     const int64_t bnd = Tb * c / grid;  // first block of CTA c
     return (static_cast<size_t>(c) * 2 + ((c == c_first && bnd < F0) ? 1 : 0)) * a.R + r;
   };
-  // CTAs whose range is empty (fewer blocks than CTAs) hold no partial
-  auto empty = [&](int32_t c) { return Tb * c / grid == Tb * (c + 1) / grid; };
-  float M = sk;
-  for (int32_t c = c_first; c <= c_last; ++c)
-    if (!empty(c)) M = fmaxf(M, ml[slot(c)].x);
-  if (M == -INFINITY) {
-    a.out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(0.f);
-    if (e == 0) a.lse[rowid] = -INFINITY;
-    return;
+  constexpr int32_t kStride = kCombParts * (kCombThreads / kDv);
+  for (int32_t r = blockIdx.y * (kCombThreads / kDv) + (threadIdx.x >> 7); r < a.R; r += kStride) {
+    const int32_t t = r / a.G, h = kvh * a.G + r % a.G;
+    const size_t rowid = (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
+    const float sk_raw = __ldg(a.sink + h);
+    const float sk = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
+    if (empty_unit) {  // no visible key at all: the empty sum
+      a.out[rowid * kDv + e] = __float2bfloat16_rn(0.f);
+      if (e == 0) a.lse[rowid] = sk_raw;
+      continue;
+    }
+    float M = sk;
+    for (int32_t c = c_first; c <= c_last; ++c)
+      if (has_part(c)) M = fmaxf(M, ml[slot(c, r)].x);
+    if (M == -INFINITY) {
+      a.out[rowid * kDv + e] = __float2bfloat16_rn(0.f);
+      if (e == 0) a.lse[rowid] = -INFINITY;
+      continue;
+    }
+    float Ls = sk == -INFINITY ? 0.f : ex2(sk - M);
+    float acc = 0.f;
+    for (int32_t c = c_first; c <= c_last; ++c) {
+      if (!has_part(c)) continue;
+      const size_t pr = slot(c, r);
+      const float4 v = ml[pr];
+      const float wgt = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+      Ls += v.y * wgt;
+      acc += wgt * a.part_o[pr * kDv + e];
+    }
+    a.out[rowid * kDv + e] = __float2bfloat16_rn(acc / Ls);
+    if (e == 0) a.lse[rowid] = (M + __log2f(Ls)) * kLn2;
   }
-  float Ls = sk == -INFINITY ? 0.f : ex2(sk - M);
-  float acc = 0.f;
-  for (int32_t c = c_first; c <= c_last; ++c) {
-    if (empty(c)) continue;
-    const size_t pr = slot(c);
-    const float4 v = ml[pr];
-    const float wgt = v.x == -INFINITY ? 0.f : ex2(v.x - M);
-    Ls += v.y * wgt;
-    acc += wgt * a.part_o[pr * kDv + e];
-  }
-  a.out[static_cast<size_t>(rowid) * kDv + e] = __float2bfloat16_rn(acc / Ls);
-  if (e == 0) a.lse[rowid] = (M + __log2f(Ls)) * kLn2;
 }
 
 }  // namespace sa

@@ -404,9 +404,8 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
   kern<<<grid, sa::kThreads, sa::DecLayout::kDynSmem, s>>>(mq, mk, mv, d);
   if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
 
-  const int64_t rows = int64_t(batch) * T * num_q_heads;
-  if (rows > INT32_MAX) return SINKATTN_EUNSUPPORTED;
-  sa::sinkattn_decode_combine_kernel<<<static_cast<unsigned>(rows), sa::kDv, 0, s>>>(d, grid);
+  sa::sinkattn_decode_combine_kernel<<<dim3(static_cast<unsigned>(d.n_units), sa::kCombParts),
+                                       sa::kCombThreads, 0, s>>>(d, grid);
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
