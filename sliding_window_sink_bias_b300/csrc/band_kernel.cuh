@@ -162,37 +162,25 @@ __device__ void band_locate(const BandArgs &a, int32_t lane, int32_t *cur) {
   }
 }
 
-// TMEM loads of N consecutive 32-bit columns (N = 4, 8, 16 or 32).
-template <int N>
-__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t *r) {
-  if (N == 32) tmem_ld32p(taddr, r);
-  else if (N == 16) tmem_ld16p(taddr, r);
-  else if (N == 8) tmem_ld8p(taddr, r);
-  else tmem_ld4p(taddr, r);
-}
 
-// Pass-1 mask of band columns 8K .. 8K+7 of this thread's half (TMEM column
-// s_col): columns that are not visible (k - lo > span as unsigned) become
-// -inf and, unless the whole warp sees all 8, the group is written back to
-// TMEM so that pass 2 needs no mask (2^-inf = 0).
-template <int K>
-__device__ __forceinline__ void band_mask8(uint32_t *r, uint32_t s_col, int32_t lo, uint32_t span) {
+// Mask of the 8 band columns k0 .. k0+7 of this thread's half held in r:
+// columns that are not visible (k - lo > span as unsigned) become -inf,
+// unless the whole warp sees all 8.
+__device__ __forceinline__ void band_mask8(uint32_t (&r)[8], int32_t k0, int32_t lo, uint32_t span) {
   constexpr uint32_t kNegInf = 0xff800000u;
-  const bool whole = static_cast<uint32_t>(8 * K - lo) <= span &&
-                     static_cast<uint32_t>(8 * K + 7 - lo) <= span;
+  const bool whole = static_cast<uint32_t>(k0 - lo) <= span &&
+                     static_cast<uint32_t>(k0 + 7 - lo) <= span;
   if (!__all_sync(0xffffffffu, whole)) {
 #pragma unroll
     for (int32_t k = 0; k < 8; ++k)
-      if (static_cast<uint32_t>(8 * K + k - lo) > span) r[8 * K + k] = kNegInf;
-    tmem_st8p(s_col + 8 * K, r + 8 * K);
+      if (static_cast<uint32_t>(k0 + k - lo) > span) r[k] = kNegInf;
   }
 }
 
 // Softmax + epilogue of one half of every row (half 0: band columns 0..71 and
 // output dims 0..63; half 1: band columns 72..143 and output dims 64..127).
-// Each of the two passes over the 72 logits of the half issues all its TMEM
-// loads before one wait: pass 1 masks (writing masked groups back) and takes
-// the maximum, pass 2 forms P.  The two threads of a row swap their partial maximum of tile i and their partial sum of tile i-1
+// Each of the two passes walks the 72 logits of the half in chunks of 8 and
+// masks them in registers: pass 1 takes the maximum, pass 2 forms P.  The two threads of a row swap their partial maximum of tile i and their partial sum of tile i-1
 // through shared memory, paired by an mbarrier.  Both halves run the same code
 // (half is a runtime value) to keep the hot loop small in the instruction cache.
 __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCursor &c0,
@@ -222,6 +210,10 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
   bool p_valid = false;
   size_t p_orow = 0;
   float p_m = 0.f, p_sk = 0.f, p_sum = 0.f;
+  // sink of this thread's head, reloaded only when the KV head changes (a
+  // global load in the loop would queue behind the epilogue's output stores)
+  int32_t sk_kvh = -1;
+  float sk_cur = 0.f;
 
   // Swap (partial max of this tile, partial sum of the previous tile) with the
   // other thread of the row; returns the other's pair.
@@ -260,43 +252,33 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       const int32_t hi = pos - kstart - c0col;
       span = static_cast<uint32_t>(hi - lo);
       if (!rvalid) { lo = 1 << 20; span = 0; }
-      sk2 = __ldg(args.sink + head) * kLog2e;  // -inf stays -inf
+      if (c.kvh != sk_kvh) {
+        sk_kvh = c.kvh;
+        sk_cur = __ldg(args.sink + head) * kLog2e;  // -inf stays -inf
+      }
+      sk2 = sk_cur;
       buf = gt & 1;
       if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
       tc_fence_after();
       s_t = tmem + lane_off + tmem_s_col(buf);
-      // pass 1: the 72 logits of this half in one batch of loads (TMEM
-      // offsets are multiples of the load size), the mask, the maximum
-      uint32_t r[72];
-      if (half == 0) {
-        tmem_ld_n<32>(s_t, r);
-        tmem_ld_n<32>(s_t + 32, r + 32);
-        tmem_ld_n<8>(s_t + 64, r + 64);
-      } else {
-        tmem_ld_n<8>(s_t + 72, r);
-        tmem_ld_n<16>(s_t + 80, r + 8);
-        tmem_ld_n<32>(s_t + 96, r + 24);
-        tmem_ld_n<16>(s_t + 128, r + 56);
-      }
-      tmem_wait_ld();
-      reg_fence<72>(r);
-      band_mask8<0>(r, s_t + c0col, lo, span);
-      band_mask8<1>(r, s_t + c0col, lo, span);
-      band_mask8<2>(r, s_t + c0col, lo, span);
-      band_mask8<3>(r, s_t + c0col, lo, span);
-      band_mask8<4>(r, s_t + c0col, lo, span);
-      band_mask8<5>(r, s_t + c0col, lo, span);
-      band_mask8<6>(r, s_t + c0col, lo, span);
-      band_mask8<7>(r, s_t + c0col, lo, span);
-      band_mask8<8>(r, s_t + c0col, lo, span);
+      // pass 1: the mask and the maximum, 8 columns per TMEM load (a compact
+      // loop: the kernel's speed is bound by its instruction-cache footprint,
+      // and a TMEM load round trip costs only tens of cycles)
+      const uint32_t s_h = s_t + c0col;
       float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll
-      for (int32_t k = 0; k < 72; k += 4) {
-        mxa = fmax3(mxa, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
-        mxb = fmax3(mxb, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
+#pragma unroll 1
+      for (int32_t k0 = 0; k0 < kBandHalf; k0 += 8) {
+        uint32_t r[8];
+        tmem_ld8p(s_h + k0, r);
+        tmem_wait_ld();
+        reg_fence<8>(r);
+        band_mask8(r, k0, lo, span);
+        mxa = fmax3(mxa, __uint_as_float(r[0]), __uint_as_float(r[1]));
+        mxb = fmax3(mxb, __uint_as_float(r[2]), __uint_as_float(r[3]));
+        mxa = fmax3(mxa, __uint_as_float(r[4]), __uint_as_float(r[5]));
+        mxb = fmax3(mxb, __uint_as_float(r[6]), __uint_as_float(r[7]));
       }
       mx = fmaxf(mxa, mxb);
-      tmem_wait_st();
     }
     float2 other = make_float2(-INFINITY, 0.f);
     if (!(ok = swap(step, mx, p_sum, other))) break;
@@ -304,34 +286,32 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       // eq. (2): m = max(max_j a_ij, sink), in the log2 domain (scale > 0)
       m = fmaxf(fmaxf(mx, other.x) * sc, sk2);
       const float mneg = m == -INFINITY ? 0.f : -m;
-      // P = 2^(s * scale * log2e - m) as bf16 pairs at TMEM column
-      // kBandPCol + 36 * half, over S columns this thread has already read
+      // pass 2: P = 2^(s * scale * log2e - m) as bf16 pairs; P of band column
+      // k lands at TMEM column kBandPCol + k/2, so each half's P covers only
+      // its own S columns (half 0: 36..71, half 1: 72..107); walking the
+      // chunks downwards (half 0) or upwards (half 1) overwrites only columns
+      // that were already read
       const float2 sc2 = make_float2(sc, sc), mneg2 = make_float2(mneg, mneg);
       float2 sum2 = make_float2(0.f, 0.f);
-      uint32_t r[72];
-      if (half == 0) {
-        tmem_ld_n<32>(s_t, r);
-        tmem_ld_n<32>(s_t + 32, r + 32);
-        tmem_ld_n<8>(s_t + 64, r + 64);
-      } else {
-        tmem_ld_n<8>(s_t + 72, r);
-        tmem_ld_n<16>(s_t + 80, r + 8);
-        tmem_ld_n<32>(s_t + 96, r + 24);
-        tmem_ld_n<16>(s_t + 128, r + 56);
-      }
-      tmem_wait_ld();
-      reg_fence<72>(r);
+      const uint32_t s_h = s_t + c0col;
+      const uint32_t p_h = s_t + kBandPCol + static_cast<uint32_t>(c0col >> 1);
+#pragma unroll 1
+      for (int32_t j = 0; j < kBandHalf; j += 8) {
+        const int32_t k0 = half ? j : kBandHalf - 8 - j;
+        uint32_t r[8];
+        tmem_ld8p(s_h + k0, r);
+        tmem_wait_ld();
+        reg_fence<8>(r);
+        band_mask8(r, k0, lo, span);
 #pragma unroll
-      for (int32_t k = 0; k < 72; k += 2) {
-        const float2 y = ffma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, mneg2);
-        const float2 p = make_float2(ex2(y.x), ex2(y.y));
-        sum2 = fadd2(sum2, p);
-        r[k >> 1] = pack_bf16x2(p.x, p.y);
+        for (int32_t k = 0; k < 8; k += 2) {
+          const float2 y = ffma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, mneg2);
+          const float2 pp = make_float2(ex2(y.x), ex2(y.y));
+          sum2 = fadd2(sum2, pp);
+          r[k >> 1] = pack_bf16x2(pp.x, pp.y);
+        }
+        tmem_st4p(p_h + (k0 >> 1), r);
       }
-      const uint32_t p_t = s_t + kBandPCol + static_cast<uint32_t>(half) * 36u;
-      tmem_st16p(p_t, r);
-      tmem_st16p(p_t + 16, r + 16);
-      tmem_st4p(p_t + 32, r + 32);
       sum = sum2.x + sum2.y;
       tmem_wait_st();
       tc_fence_before();

@@ -28,10 +28,10 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;        // 0.2 s to drain after 
 // Device status word: bit 0 = a wait timed out; bits 8..15 = the wait site.
 __device__ uint32_t g_status_word;
 
-// Bounded mbarrier wait.  Returns false if this CTA is aborting.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                      uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded mbarrier wait, slow path: the timed loop.  Returns false if this CTA
+// is aborting.
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity,
+                                           volatile uint32_t *abort_flag, uint32_t site) {
   // each try_wait sleeps up to its suspend hint (1 ms), so checking the clock
   // and the abort flag once per round costs nothing
   const uint64_t t0 = global_timer_ns();
@@ -46,6 +46,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Bounded mbarrier wait.  The first try_wait (which itself sleeps up to its
+// hint) almost always succeeds; the timed loop lives out of line so the hot
+// loops stay small in the instruction cache.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                         uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, abort_flag, site);
+}
 // Warp-uniform form: every lane polls, then the warp agrees, so warp-collective
 // tcgen05.ld/st that follow never run with part of the warp gone.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
