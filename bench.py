@@ -320,6 +320,52 @@ def bench_hybrid(name, steps, warmup, ws, local):
     return res
 
 
+def bench_ratio(name, warmup, ws, local):
+    """Attention time of the hybrid design against all-global attention: one
+    SWA layer and one GA layer timed on a single sequence per length; the
+    block (5 SWA + 1 GA) and model (39 SWA + 9 GA) ratios are the all-GA time
+    of the same layer count over the hybrid time.  The KV-cache ratio counts
+    the keys a decode must keep: L per GA layer, the 128-key window per SWA
+    layer."""
+    import torch
+
+    import sliding_window_sink_bias_b300 as sa
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[name]
+    dev = f"cuda:{local}"
+    hq = wl["hq"]
+    (bs, bg), (ms_, mg) = wl["block"], wl["model"]
+    rows = []
+    for L in wl["lens"]:
+        res = {"seq_len": L}
+        for tag, hkv, win, base in (("swa", wl["swa_hkv"], wl["window"], wl["swa_base"]),
+                                    ("ga", wl["ga_hkv"], 0, wl["ga_base"])):
+            inp = synth.prefill_inputs([L], hq, hkv, window=win, rope_base=base, seed=0,
+                                       device=dev)
+            out = torch.empty(L, hq, 128, dtype=torch.bfloat16, device=dev)
+            lse = torch.empty(L, hq, dtype=torch.float32, device=dev)
+
+            def call():
+                sa.prefill(inp.q, inp.k, inp.v, inp.sink, inp.cu_seqlens, max_seqlen=L,
+                           window=win, rope_base=base, out=out, lse=lse)
+
+            steps = 5 if (tag == "swa" or L <= 32768) else 2
+            ms, _ = time_calls(call, steps, min(warmup, 2) if tag == "swa" else 1, ws)
+            st, word = sa.device_status()
+            if st != sa.OK:
+                raise RuntimeError(f"device status {st} word {word:#x} after {name}")
+            res[f"{tag}_ms"] = ms
+            del inp, out, lse
+            torch.cuda.empty_cache()
+        s_, g_ = res["swa_ms"], res["ga_ms"]
+        res["block_ratio"] = (bs + bg) * g_ / (bs * s_ + bg * g_)
+        res["model_ratio"] = (ms_ + mg) * g_ / (ms_ * s_ + mg * g_)
+        kv_ga, kv_swa = L * wl["ga_hkv"], min(L, wl["window"]) * wl["swa_hkv"]
+        res["model_kv_ratio"] = (ms_ + mg) * kv_ga / (ms_ * kv_swa + mg * kv_ga)
+        rows.append(res)
+    return rows
+
+
 def bench_decode(name, steps, warmup, ws, local):
     import torch
 
@@ -339,7 +385,7 @@ def bench_decode(name, steps, warmup, ws, local):
     def call():
         sa.decode(inp.q, inp.kcache, inp.vcache, inp.seqlens, inp.sink, max_seqlen=max(lens),
                   window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
-                  lse=lse)
+                  lse=lse, kv_ring=wl.get("kv_ring", False))
 
     # the decode working set can sit in L2 for the SWA layer: flush between steps
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -449,7 +495,9 @@ def run_reference(args):
 def single_workload(args, ws, rank, local, peaks):
     from sliding_window_sink_bias_b300 import synth
     wl = synth.WORKLOADS[args.workload]
-    if wl["kind"] == "hybrid":
+    if wl["kind"] == "ratio":
+        line = {"workload": args.workload, "rows": bench_ratio(args.workload, args.warmup, ws, local)}
+    elif wl["kind"] == "hybrid":
         r = bench_hybrid(args.workload, args.steps, args.warmup, ws, local)
         line = {"workload": args.workload, "ms": r["ms"], "tokens_per_s": r["tokens"] / (r["ms"] / 1e3),
                 "tflops": r["flops"] / (r["ms"] / 1e3) / 1e12, "lens": r["lens"], "clocks": r["clocks"]}
@@ -558,7 +606,7 @@ def main():
             "frac_of_sustained_peak": (g_tf / peaks["bf16_tflops_sustained"]
                                        if peaks.get("bf16_tflops_sustained") else None),
             "clocks": g["clocks"]}
-        for name in ("mtp_decode_ga_b64_t4", "mtp_decode_swa_b64_t4"):
+        for name in ("mtp_decode_ga_b64_t4", "mtp_decode_swa_b64_t4", "mtp_decode_swa_ring_b64_t4"):
             d = bench_decode(name, args.steps, args.warmup, ws, local)
             d_gbs = d["bytes"] / (d["ms"] / 1e3) / 1e9
             extra[name] = {"value": ws * d_gbs, "unit": "GB/s", "ms_per_step": d["ms"],
@@ -574,6 +622,11 @@ def main():
             "ms_per_step": h["ms"], "tflops": h["flops"] / (h["ms"] / 1e3) / 1e12,
             "seq_lens": h["lens"], "layers": "5 SWA (64/8, W=128) + 1 GA (64/4)",
             "clocks": h["clocks"]}
+        extra["hybrid_vs_all_ga"] = {
+            "rows": bench_ratio("hybrid_vs_all_ga", args.warmup, ws, local),
+            "note": "ratio = all-GA attention time / hybrid attention time for the same layer "
+                    "count; block = 5 SWA + 1 GA, model = 39 SWA + 9 GA; the pages claim "
+                    "nearly 6x (context, not a target)"}
         line["other_workloads"] = extra
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

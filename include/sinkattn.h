@@ -67,7 +67,9 @@ typedef struct {
     float scale;        /* logit scale; 0 -> 1/sqrt(192) (eq. (1) with d = 192) */
     int32_t rope_off;   /* 1 -> no rotary embedding at all (positions ignored) */
     int32_t rope_style; /* 0 -> pairs (2t, 2t+1) (default); 1 -> pairs (t, t+32) */
-    int32_t reserved;
+    int32_t kv_ring;    /* decode only (prefill rejects it): 1 -> kcache/vcache are rings of
+                           S_cap slots holding the latest keys, position j at slot j % S_cap
+                           (the KV cache of a sliding-window layer keeps only its window) */
 } sinkattn_params;
 
 /*
@@ -127,7 +129,8 @@ size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_he
  *   kcache   bf16 [batch, S_cap, num_kv_heads, 192], unrotated keys at positions 0..
  *   vcache   bf16 [batch, S_cap, num_kv_heads, 128]
  *   seqlens  int32 [batch], device: cached tokens including the T new ones,
- *            T <= seqlens[b] <= S_cap (shorter caches give empty rows).
+ *            T <= seqlens[b] <= S_cap (shorter caches give empty rows).  Cache
+ *            rows at or past seqlens[b] are never used and may hold anything.
  *   max_seqlen  host bound on max(seqlens).
  *   T        1 <= T and T * (num_q_heads / num_kv_heads) <= 128.
  *   workspace, workspace_bytes  device scratch of at least
@@ -135,6 +138,14 @@ size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_he
  *            needs no clearing and its contents are rewritten by every call.
  *   The logit scale must be positive (sinkattn_decode_ex with a scale <= 0
  *   returns SINKATTN_EINVAL).
+ *   Ring cache (sinkattn_decode_ex with params->kv_ring = 1; the KV cache of an
+ *   SWA layer, §2.1: only the window is ever read): kcache/vcache hold S_cap
+ *   slots per sequence and the key at position j sits at slot j % S_cap, so
+ *   seqlens[b] may exceed S_cap.  Positions keep their absolute values for
+ *   RoPE and the mask.  Requires window > 0, S_cap >= window + T - 1 (the T
+ *   queries see the last window + T - 1 positions) and S_cap a multiple of 16;
+ *   otherwise SINKATTN_EINVAL.  Slots outside the visible positions may hold
+ *   anything.
  *   out      bf16 [batch, T, num_q_heads, 128];  lse fp32 [batch, T, num_q_heads]
  */
 sinkattn_status sinkattn_decode(const void *q, const void *kcache, const void *vcache,

@@ -40,7 +40,7 @@ class SinkAttnError(RuntimeError):
 class Params(ctypes.Structure):
     """sinkattn_params: scale (0 = 1/sqrt(192)), rope_off, rope_style."""
     _fields_ = [("scale", ctypes.c_float), ("rope_off", ctypes.c_int32),
-                ("rope_style", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("rope_style", ctypes.c_int32), ("kv_ring", ctypes.c_int32)]
 
 
 _lib = None
@@ -92,10 +92,10 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _params(scale, rope_style, rope_off):
-    if scale is None and rope_style == 0 and not rope_off:
+def _params(scale, rope_style, rope_off, kv_ring=False):
+    if scale is None and rope_style == 0 and not rope_off and not kv_ring:
         return None
-    return Params(float(scale or 0.0), int(bool(rope_off)), int(rope_style), 0)
+    return Params(float(scale or 0.0), int(bool(rope_off)), int(rope_style), int(bool(kv_ring)))
 
 
 def _require(t, name, dtype, ndim):
@@ -151,10 +151,12 @@ def decode_workspace_size(batch: int, t: int, hq: int, hkv: int, max_seqlen: int
 
 def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, rope_base: float,
            workspace=None, out=None, lse=None, scale=None, rope_style: int = 0,
-           rope_off: bool = False, stream=None):
+           rope_off: bool = False, kv_ring: bool = False, stream=None):
     """MTP-verify decode.  q [B, T, Hq, 192]; kcache [B, S_cap, Hkv, 192];
     vcache [B, S_cap, Hkv, 128] bf16; seqlens int32 [B] (cached tokens including
-    the T new ones); sink fp32 [Hq].  Returns (out [B, T, Hq, 128], lse [B, T, Hq])."""
+    the T new ones); sink fp32 [Hq].  Returns (out [B, T, Hq, 128], lse [B, T, Hq]).
+    kv_ring=True: the caches are rings of S_cap slots, position j at slot
+    j % S_cap (sliding-window layers; seqlens may exceed S_cap)."""
     _require(q, "q", torch.bfloat16, 4)
     _require(kcache, "kcache", torch.bfloat16, 4)
     _require(vcache, "vcache", torch.bfloat16, 4)
@@ -171,7 +173,7 @@ def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, ro
         out = torch.empty(b, t, hq, 128, dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty(b, t, hq, dtype=torch.float32, device=q.device)
-    p = _params(scale, rope_style, rope_off)
+    p = _params(scale, rope_style, rope_off, kv_ring)
     args = (_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(sink), int(window),
             float(rope_base), b, t, s_cap, int(max_seqlen), hq, hkv)
     tail = (_ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),

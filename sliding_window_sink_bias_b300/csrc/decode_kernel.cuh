@@ -46,6 +46,7 @@ struct DecArgs {
   int32_t window;
   int32_t batch, S_cap;
   int32_t n_units;        // batch * Hkv
+  int32_t kv_ring;        // 1: the cache is a ring of S_cap slots, position j at slot j % S_cap
   int32_t rope_on, rope_style;
   uint32_t q_tx_bytes;
   float scale_log2;       // > 0
@@ -65,6 +66,9 @@ __device__ __forceinline__ void dec_unit_keys(const DecArgs &a, int32_t u, int32
                                               int32_t &nblk) {
   L = __ldg(a.seqlens + u / a.Hkv);
   lo = a.window > 0 ? max(0, L - a.T - a.window + 1) : 0;
+  // a ring cache is read in 16-key pieces that must not straddle the ring's
+  // end: blocks start on a multiple of 16 (the keys before lo are masked)
+  if (a.kv_ring) lo &= ~15;
   nblk = L > lo ? (L - lo + kDecBN - 1) / kDecBN : 0;
 }
 
@@ -275,19 +279,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sbase + Ly::kQOff + cc * kQBoxBytes, &tm_q, cc * 64, sg.kvh * G, sg.b * args.T,
                       B_QFULL);
         ++gq;
-        const int32_t krow0 = sg.b * args.S_cap + sg.lo + sg.blk0 * BN;
+        const int32_t kpos0 = sg.lo + sg.blk0 * BN;
+        const int32_t krow0 = sg.b * args.S_cap + kpos0;
         for (int32_t j = 0; j < sg.nblk; ++j) {
           const uint32_t st = gk % S;
           if (!(ok = wait_bar(B_KVEMPTY(st), ((gk / S) & 1) ^ 1, abort_flag, 2))) break;
           mbar_arrive_expect_tx(B_KVFULL(st), Ly::kKVStage);
           const uint32_t dst = sbase + Ly::kKVOff + st * Ly::kKVStage;
+          if (!args.kv_ring) {
 #pragma unroll
-          for (int cc = 0; cc < 3; ++cc)
-            tma_load_3d(dst + cc * Ly::kKBox, &tm_k, cc * 64, sg.kvh, krow0 + j * BN, B_KVFULL(st));
+            for (int cc = 0; cc < 3; ++cc)
+              tma_load_3d(dst + cc * Ly::kKBox, &tm_k, cc * 64, sg.kvh, krow0 + j * BN, B_KVFULL(st));
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
-            tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, sg.kvh, krow0 + j * BN,
-                        B_KVFULL(st));
+            for (int cc = 0; cc < 2; ++cc)
+              tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, sg.kvh, krow0 + j * BN,
+                          B_KVFULL(st));
+          } else {
+            // four 16-key pieces (the maps' boxes are 16 rows), each at its slot
+#pragma unroll 1
+            for (int32_t pc = 0; pc < BN; pc += 16) {
+              const int32_t row = sg.b * args.S_cap + (kpos0 + j * BN + pc) % args.S_cap;
+#pragma unroll
+              for (int cc = 0; cc < 3; ++cc)
+                tma_load_3d(dst + cc * Ly::kKBox + pc * kRowBytes, &tm_k, cc * 64, sg.kvh, row,
+                            B_KVFULL(st));
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc)
+                tma_load_3d(dst + (3 + cc) * Ly::kKBox + pc * kRowBytes, &tm_v, cc * 64, sg.kvh, row,
+                            B_KVFULL(st));
+            }
+          }
           ++gk;
         }
       }
@@ -547,12 +568,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(B_QREADY);
       ++gq;
       const int32_t kpos0 = sg.lo + sg.blk0 * BN;
+      // keys no query of the unit can see: below the window or past the cache
+      const int32_t vis_lo = args.window > 0 ? max(0, sg.L - args.T - args.window + 1) : 0;
       for (int32_t j = 0; j < sg.nblk; ++j) {
         const uint32_t st = gk % S;
         if (!(ok = wait_bar_warp(B_KVFULL(st), (gk / S) & 1, abort_flag, 11))) break;
-        if (args.rope_on)
-          rope_k_rows(smem + Ly::kKVOff + st * Ly::kKVStage, BN, kpos0 + j * BN, args.rope_style,
-                      turns, tid);
+        uint8_t *kv = smem + Ly::kKVOff + st * Ly::kKVStage;
+        const int32_t kp = kpos0 + j * BN;
+        if (args.rope_on) rope_k_rows(kv, BN, kp, args.rope_style, turns, tid);
+        // Their scores are masked, but P = 0 times a NaN value is NaN: zero
+        // the value rows of keys outside [vis_lo, L), whose cache rows (past
+        // the sequence, or old ring slots) may hold anything.
+        const int32_t r0 = min(BN, max(0, vis_lo - kp)), r1 = max(r0, min(BN, sg.L - kp));
+        if (r0 > 0 || r1 < BN) {
+          for (int32_t u = tid; u < BN * 16; u += 128) {
+            const int32_t r = u >> 4, ch = u & 15;  // row, 16-byte chunk of its 256 bytes
+            if (r < r0 || r >= r1)
+              *reinterpret_cast<uint4 *>(kv + (3 + (ch >> 3)) * Ly::kKBox + r * kRowBytes +
+                                         (ch & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
         fence_proxy_async_smem();
         mbar_arrive(B_KREADY(st));
         ++gk;

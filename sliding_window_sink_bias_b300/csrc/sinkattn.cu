@@ -266,6 +266,7 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
       !aligned(lse, 4) || !aligned(sink, 4) || !aligned(cu_seqlens, 4))
     return SINKATTN_EINVAL;
   AttnArgs a;
+  if (params && params->kv_ring) return SINKATTN_EINVAL;  // a prefill reads no cache
   if (sinkattn_status st = fill_common(a, params, rope_base, num_q_heads, num_kv_heads, window))
     return st;
 
@@ -336,7 +337,15 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
                                    size_t workspace_bytes, void *out, float *lse,
                                    sinkattn_stream_t stream) {
   if (batch < 0 || T <= 0 || S_cap <= 0 || max_seqlen < 0 || window < 0) return SINKATTN_EINVAL;
-  if (max_seqlen > S_cap) return SINKATTN_EINVAL;
+  const bool ring = params && params->kv_ring;
+  if (params && params->kv_ring != 0 && params->kv_ring != 1) return SINKATTN_EINVAL;
+  if (ring) {
+    // the visible positions [L - T - W + 1, L) must sit in distinct slots, read
+    // in 16-key pieces that never straddle the ring's end
+    if (window <= 0 || int64_t(S_cap) < int64_t(window) + T - 1 || S_cap % 16) return SINKATTN_EINVAL;
+  } else if (max_seqlen > S_cap) {
+    return SINKATTN_EINVAL;
+  }
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return SINKATTN_EINVAL;
   const int32_t G = num_q_heads / num_kv_heads;
   if (!pow2_upto_128(G)) return SINKATTN_EUNSUPPORTED;
@@ -368,6 +377,7 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
   d.batch = batch;
   d.S_cap = S_cap;
   d.n_units = batch * num_kv_heads;
+  d.kv_ring = ring ? 1 : 0;
   d.rope_on = a.rope_on;
   d.rope_style = a.rope_style;
   d.q_tx_bytes = 3u * 64u * 2u * static_cast<uint32_t>(G * T);
@@ -387,11 +397,12 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, num_q_heads, uint64_t(batch) * T, G, T) ||
-      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, sa::kDecBN) ||
-      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, sa::kDecBN))
+      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, ring ? 16 : sa::kDecBN) ||
+      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, ring ? 16 : sa::kDecBN))
     return SINKATTN_ECUDA;
-  // upper bound of the blocks: every unit sees at most max_seqlen (window: T + W - 1) keys
-  const int64_t range = window > 0 ? std::min<int64_t>(max_seqlen, int64_t(T) + window - 1)
+  // upper bound of the blocks: every unit sees at most max_seqlen (window: T + W - 1) keys,
+  // plus up to 15 before them when a ring cache aligns its first block
+  const int64_t range = window > 0 ? std::min<int64_t>(max_seqlen, int64_t(T) + window - 1 + (ring ? 15 : 0))
                                    : int64_t(max_seqlen);
   const int64_t max_blocks = int64_t(d.n_units) * ((range + sa::kDecBN - 1) / sa::kDecBN);
   const int grid = static_cast<int>(

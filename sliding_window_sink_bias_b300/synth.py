@@ -131,11 +131,21 @@ WORKLOADS = {
                                  len_lo=65536, len_hi=262144, **GA),
     "mtp_decode_swa_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=262144,
                                   len_lo=65536, len_hi=262144, **SWA),
+    # the same SWA layer with the KV cache an SWA layer needs: a ring of 144
+    # slots (>= W + T - 1 = 131, a multiple of 16) per sequence
+    "mtp_decode_swa_ring_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=144, kv_ring=True,
+                                       len_lo=65536, len_hi=262144, **SWA),
     # one hybrid block of the model (§2.1: 5 SWA layers then 1 GA layer) over a
     # varlen batch of 8 sequences, lengths log-uniform in [4096, 131072]
     "hybrid_block_ragged_8seq": dict(kind="hybrid", n_seq=8, len_lo=4096, len_hi=131072,
                                      swa_layers=5, ga_layers=1, hq=64, swa_hkv=8, ga_hkv=4,
                                      window=128, swa_base=1e4, ga_base=5e6),
+    # one SWA layer and one GA layer of the model timed on a single sequence at
+    # 32K, 128K and 256K tokens: attention time of a hybrid block (5 SWA + 1 GA)
+    # and of the 48-layer stack (39 SWA + 9 GA) against all-global attention
+    "hybrid_vs_all_ga": dict(kind="ratio", lens=[32768, 131072, 262144], hq=64, swa_hkv=8,
+                             ga_hkv=4, window=128, swa_base=1e4, ga_base=5e6,
+                             block=(5, 1), model=(39, 9)),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)
     "swa_prefill_1x32768": dict(kind="prefill", seqlens=[32768], **SWA),
     "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),

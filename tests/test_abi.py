@@ -147,3 +147,30 @@ def test_decode_rejects_non_positive_scale(L):
         st = L.sinkattn_decode_ex(f(1), f(1), f(1), f(1), f(1), 0, 5e6, 2, 4, 100, 100, 64, 4,
                                   ctypes.byref(p), f(1), ws, f(1), f(1), None)
         assert st == sa.EINVAL
+
+
+def test_ring_cache_argument_checks(L):
+    """A ring KV cache (params kv_ring = 1) is a decode-only option for windowed
+    layers; its slot count must hold the T + W - 1 visible positions and be a
+    multiple of 16.  Everything here is refused on the host, before any launch."""
+    import sliding_window_sink_bias_b300 as sa
+    P = ctypes.c_void_p
+    f = lambda x: P(256 * x)
+    ws = L.sinkattn_decode_workspace_size(2, 4, 64, 8, 5000, 128)
+
+    def dec(window, s_cap, max_seqlen, ring=1, t=4):
+        p = sa.Params(0.0, 0, 0, ring)
+        return L.sinkattn_decode_ex(f(1), f(1), f(1), f(1), f(1), window, 1e4, 2, t, s_cap,
+                                    max_seqlen, 64, 8, ctypes.byref(p), f(1), ws, f(1), f(1),
+                                    None)
+
+    assert dec(0, 256, 5000) == sa.EINVAL      # global attention has no ring
+    assert dec(128, 130, 5000) == sa.EINVAL    # fewer slots than T + W - 1 = 131
+    assert dec(128, 136, 5000) == sa.EINVAL    # not a multiple of 16
+    assert dec(128, 256, 5000, ring=2) == sa.EINVAL
+    assert dec(128, 256, 5000, ring=0) == sa.EINVAL  # a plain cache must hold max_seqlen
+    # the prefill reads no cache
+    p = sa.Params(0.0, 0, 0, 1)
+    st = L.sinkattn_prefill_ex(f(1), f(1), f(1), f(1), f(1), 1, 16, 16, 64, 8, 128, 1e4,
+                               ctypes.byref(p), f(1), f(1), None)
+    assert st == sa.EINVAL

@@ -121,3 +121,61 @@ def test_mtp_decode_full_size_sampled(oracle_mod):
             assert_parity(out[b:b + 1], lse[b:b + 1], ro, rl, f"{name} b={b}")
         del inp, out, lse
         torch.cuda.empty_cache()
+
+
+def _nan_past_end(cache, seqlens):
+    for b, L in enumerate(seqlens):
+        cache[b, L:] = float("nan")
+
+
+@pytest.mark.parametrize("window,hkv,base", [(0, 4, 5e6), (128, 8, 1e4)])
+def test_cache_rows_past_the_end_are_never_used(oracle_mod, window, hkv, base):
+    """Rows at or past seqlens[b] may hold anything (NaN here): the last 64-key
+    block of a sequence reads some of them, and the result must not change."""
+    import sliding_window_sink_bias_b300 as sa
+    seqlens = [4, 65, 130, 1000, 1001, 77]
+    inp = synth.decode_inputs(seqlens, 4, 1100, 64, hkv, window=window, rope_base=base, seed=11,
+                              device="cpu")
+    _nan_past_end(inp.kcache, seqlens)
+    _nan_past_end(inp.vcache, seqlens)
+    out, lse = sa.decode(inp.q.to(DEV), inp.kcache.to(DEV), inp.vcache.to(DEV),
+                         inp.seqlens.to(DEV), inp.sink.to(DEV), max_seqlen=max(seqlens),
+                         window=window, rope_base=base)
+    torch.cuda.synchronize()
+    assert sa.device_status()[0] == sa.OK
+    ro, rl = oracle_mod.decode(inp.q, inp.kcache, inp.vcache, inp.seqlens, inp.sink,
+                               window=window, rope_base=base)
+    assert_parity(out, lse, ro, rl, f"NaN past the end W={window}")
+
+
+def _ring_of(full, seqlens, cap, keep):
+    """The ring a sliding-window layer keeps: slot j % cap holds position j for
+    the last `keep` positions; every other slot holds NaN."""
+    ring = torch.full((full.shape[0], cap) + tuple(full.shape[2:]), float("nan"),
+                      dtype=full.dtype)
+    for b, L in enumerate(seqlens):
+        idx = torch.arange(max(0, L - keep), L)
+        ring[b, idx % cap] = full[b, idx]
+    return ring
+
+
+@pytest.mark.parametrize("cap,window,t", [(144, 128, 4), (256, 128, 4), (144, 128, 1),
+                                          (144, 128, 8), (32, 16, 4)])
+def test_ring_cache_matches_full_cache(oracle_mod, cap, window, t):
+    """A ring of `cap` slots holding only the last T + W - 1 positions gives the
+    decode of the full cache; lengths below, at and far past the ring size put
+    the ring's seam at every offset of the 64-key blocks."""
+    import sliding_window_sink_bias_b300 as sa
+    seqlens = [t, 100, cap - 1, cap, cap + 1, 300, 1000, 5003, 4099 + t]
+    full = synth.decode_inputs(seqlens, t, max(seqlens), 64, 8, window=window, rope_base=1e4,
+                               seed=12 + t, device="cpu")
+    keep = window + t - 1
+    kr, vr = _ring_of(full.kcache, seqlens, cap, keep), _ring_of(full.vcache, seqlens, cap, keep)
+    out, lse = sa.decode(full.q.to(DEV), kr.to(DEV), vr.to(DEV), full.seqlens.to(DEV),
+                         full.sink.to(DEV), max_seqlen=max(seqlens), window=window,
+                         rope_base=1e4, kv_ring=True)
+    torch.cuda.synchronize()
+    assert sa.device_status()[0] == sa.OK
+    ro, rl = oracle_mod.decode(full.q, full.kcache, full.vcache, full.seqlens, full.sink,
+                               window=window, rope_base=1e4)
+    assert_parity(out, lse, ro, rl, f"ring cap={cap} W={window} T={t}")
