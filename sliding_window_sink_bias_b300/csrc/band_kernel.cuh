@@ -163,24 +163,71 @@ __device__ void band_locate(const BandArgs &a, int32_t lane, int32_t *cur) {
 }
 
 
-// Mask of the 8 band columns k0 .. k0+7 of this thread's half held in r:
-// columns that are not visible (k - lo > span as unsigned) become -inf,
-// unless the whole warp sees all 8.
-__device__ __forceinline__ void band_mask8(uint32_t (&r)[8], int32_t k0, int32_t lo, uint32_t span) {
+// Mask of the N band columns k0 .. k0+N-1 of this thread's half held in r,
+// by groups of 8: columns that are not visible (k - lo > span as unsigned)
+// become -inf, unless the whole warp sees all 8 of the group.
+template <int N>
+__device__ __forceinline__ void band_mask(uint32_t (&r)[N], int32_t k0, int32_t lo, uint32_t span) {
   constexpr uint32_t kNegInf = 0xff800000u;
-  const bool whole = static_cast<uint32_t>(k0 - lo) <= span &&
-                     static_cast<uint32_t>(k0 + 7 - lo) <= span;
-  if (!__all_sync(0xffffffffu, whole)) {
 #pragma unroll
-    for (int32_t k = 0; k < 8; ++k)
-      if (static_cast<uint32_t>(k0 + k - lo) > span) r[k] = kNegInf;
+  for (int32_t g = 0; g < N; g += 8) {
+    const bool whole = static_cast<uint32_t>(k0 + g - lo) <= span &&
+                       static_cast<uint32_t>(k0 + g + 7 - lo) <= span;
+    if (!__all_sync(0xffffffffu, whole)) {
+#pragma unroll
+      for (int32_t k = 0; k < 8; ++k)
+        if (static_cast<uint32_t>(k0 + g + k - lo) > span) r[g + k] = kNegInf;
+    }
   }
+}
+
+// TMEM load of N (8 or 16) columns.
+template <int N>
+__device__ __forceinline__ void band_ld(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 16) tmem_ld16p(taddr, r);
+  else tmem_ld8p(taddr, r);
+  tmem_wait_ld();
+  reg_fence<N>(r);
+}
+
+// Pass 1 on N columns at k0: mask, then the running maximum.
+template <int N>
+__device__ __forceinline__ void band_p1(uint32_t s_h, int32_t k0, int32_t lo, uint32_t span,
+                                        float &mxa, float &mxb) {
+  uint32_t r[N];
+  band_ld<N>(s_h + k0, r);
+  band_mask<N>(r, k0, lo, span);
+#pragma unroll
+  for (int32_t k = 0; k < N; k += 4) {
+    mxa = fmax3(mxa, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+    mxb = fmax3(mxb, __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
+  }
+}
+
+// Pass 2 on N columns at k0: P = 2^(s * scale * log2e - m) summed and stored
+// as bf16 pairs at p_h + k0/2.
+template <int N>
+__device__ __forceinline__ void band_p2(uint32_t s_h, uint32_t p_h, int32_t k0, int32_t lo,
+                                        uint32_t span, float2 sc2, float2 mneg2, float2 &sum2) {
+  uint32_t r[N];
+  band_ld<N>(s_h + k0, r);
+  band_mask<N>(r, k0, lo, span);
+#pragma unroll
+  for (int32_t k = 0; k < N; k += 2) {
+    const float2 y = ffma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, mneg2);
+    const float2 pp = make_float2(ex2(y.x), ex2(y.y));
+    sum2 = fadd2(sum2, pp);
+    r[k >> 1] = pack_bf16x2(pp.x, pp.y);
+  }
+  if constexpr (N == 16) tmem_st8p(p_h + (k0 >> 1), r);
+  else tmem_st4p(p_h + (k0 >> 1), r);
 }
 
 // Softmax + epilogue of one half of every row (half 0: band columns 0..71 and
 // output dims 0..63; half 1: band columns 72..143 and output dims 64..127).
-// Each of the two passes walks the 72 logits of the half in chunks of 8 and
-// masks them in registers: pass 1 takes the maximum, pass 2 forms P.  The two threads of a row swap their partial maximum of tile i and their partial sum of tile i-1
+// Each of the two passes walks the 72 logits of the half in one chunk of 8 and
+// four of 16, masking them in registers: pass 1 takes the maximum, pass 2
+// forms P.  The two threads of a row swap their partial maximum of tile i and their partial sum of tile i-1
 // through shared memory, paired by an mbarrier.  Both halves run the same code
 // (half is a runtime value) to keep the hot loop small in the instruction cache.
 __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCursor &c0,
@@ -261,23 +308,17 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       if (!(ok = wait_bar_warp(B_SFULL(buf), (gt >> 1) & 1, abort_flag, 7))) break;
       tc_fence_after();
       s_t = tmem + lane_off + tmem_s_col(buf);
-      // pass 1: the mask and the maximum, 8 columns per TMEM load (a compact
-      // loop: the kernel's speed is bound by its instruction-cache footprint,
-      // and a TMEM load round trip costs only tens of cycles)
+      // pass 1: the mask and the maximum, one TMEM load of 8 then four of 16
+      // columns (compact loops: the kernel's speed is bound by its
+      // instruction-cache footprint, and a TMEM load round trip costs only tens
+      // of cycles); every load offset is a multiple of its size
       const uint32_t s_h = s_t + c0col;
+      const int32_t k8 = half ? 0 : kBandHalf - 8;   // the 8-column chunk
+      const int32_t k16 = half ? 8 : 0;              // the first 16-column chunk
       float mxa = -INFINITY, mxb = -INFINITY;
+      band_p1<8>(s_h, k8, lo, span, mxa, mxb);
 #pragma unroll 1
-      for (int32_t k0 = 0; k0 < kBandHalf; k0 += 8) {
-        uint32_t r[8];
-        tmem_ld8p(s_h + k0, r);
-        tmem_wait_ld();
-        reg_fence<8>(r);
-        band_mask8(r, k0, lo, span);
-        mxa = fmax3(mxa, __uint_as_float(r[0]), __uint_as_float(r[1]));
-        mxb = fmax3(mxb, __uint_as_float(r[2]), __uint_as_float(r[3]));
-        mxa = fmax3(mxa, __uint_as_float(r[4]), __uint_as_float(r[5]));
-        mxb = fmax3(mxb, __uint_as_float(r[6]), __uint_as_float(r[7]));
-      }
+      for (int32_t i = 0; i < 4; ++i) band_p1<16>(s_h, k16 + 16 * i, lo, span, mxa, mxb);
       mx = fmaxf(mxa, mxb);
     }
     float2 other = make_float2(-INFINITY, 0.f);
@@ -289,28 +330,18 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
       // pass 2: P = 2^(s * scale * log2e - m) as bf16 pairs; P of band column
       // k lands at TMEM column kBandPCol + k/2, so each half's P covers only
       // its own S columns (half 0: 36..71, half 1: 72..107); walking the
-      // chunks downwards (half 0) or upwards (half 1) overwrites only columns
-      // that were already read
+      // chunks downwards (half 0: 64, 48, 32, 16, 0) or upwards (half 1: 0, 8,
+      // 24, 40, 56) overwrites only columns that were already read
       const float2 sc2 = make_float2(sc, sc), mneg2 = make_float2(mneg, mneg);
       float2 sum2 = make_float2(0.f, 0.f);
       const uint32_t s_h = s_t + c0col;
       const uint32_t p_h = s_t + kBandPCol + static_cast<uint32_t>(c0col >> 1);
+      const int32_t k8 = half ? 0 : kBandHalf - 8;
+      band_p2<8>(s_h, p_h, k8, lo, span, sc2, mneg2, sum2);
 #pragma unroll 1
-      for (int32_t j = 0; j < kBandHalf; j += 8) {
-        const int32_t k0 = half ? j : kBandHalf - 8 - j;
-        uint32_t r[8];
-        tmem_ld8p(s_h + k0, r);
-        tmem_wait_ld();
-        reg_fence<8>(r);
-        band_mask8(r, k0, lo, span);
-#pragma unroll
-        for (int32_t k = 0; k < 8; k += 2) {
-          const float2 y = ffma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, mneg2);
-          const float2 pp = make_float2(ex2(y.x), ex2(y.y));
-          sum2 = fadd2(sum2, pp);
-          r[k >> 1] = pack_bf16x2(pp.x, pp.y);
-        }
-        tmem_st4p(p_h + (k0 >> 1), r);
+      for (int32_t i = 0; i < 4; ++i) {
+        const int32_t k0 = half ? 8 + 16 * i : 48 - 16 * i;
+        band_p2<16>(s_h, p_h, k0, lo, span, sc2, mneg2, sum2);
       }
       sum = sum2.x + sum2.y;
       tmem_wait_st();
