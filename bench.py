@@ -335,11 +335,12 @@ def bench_ratio(name, warmup, ws, local):
     dev = f"cuda:{local}"
     hq = wl["hq"]
     (bs, bg), (ms_, mg) = wl["block"], wl["model"]
-    rows = []
-    for L in wl["lens"]:
-        res = {"seq_len": L}
-        for tag, hkv, win, base in (("swa", wl["swa_hkv"], wl["window"], wl["swa_base"]),
-                                    ("ga", wl["ga_hkv"], 0, wl["ga_base"])):
+    rows = [{"seq_len": L} for L in wl["lens"]]
+    # all SWA layers first: a GA layer leaves the GPU at its power cap for a while
+    for tag, hkv, win, base in (("swa", wl["swa_hkv"], wl["window"], wl["swa_base"]),
+                                ("ga", wl["ga_hkv"], 0, wl["ga_base"])):
+        for res in rows:
+            L = res["seq_len"]
             inp = synth.prefill_inputs([L], hq, hkv, window=win, rope_base=base, seed=0,
                                        device=dev)
             out = torch.empty(L, hq, 128, dtype=torch.bfloat16, device=dev)
@@ -357,12 +358,13 @@ def bench_ratio(name, warmup, ws, local):
             res[f"{tag}_ms"] = ms
             del inp, out, lse
             torch.cuda.empty_cache()
+    for res in rows:
+        L = res["seq_len"]
         s_, g_ = res["swa_ms"], res["ga_ms"]
         res["block_ratio"] = (bs + bg) * g_ / (bs * s_ + bg * g_)
         res["model_ratio"] = (ms_ + mg) * g_ / (ms_ * s_ + mg * g_)
         kv_ga, kv_swa = L * wl["ga_hkv"], min(L, wl["window"]) * wl["swa_hkv"]
         res["model_kv_ratio"] = (ms_ + mg) * kv_ga / (ms_ * kv_swa + mg * kv_ga)
-        rows.append(res)
     return rows
 
 
