@@ -399,7 +399,10 @@ def bench_decode(name, steps, warmup, ws, local):
     torch.cuda.synchronize()
     barrier(ws)
     stream = torch.cuda.current_stream()
+    # every step is enqueued without waiting for the previous one (the flush
+    # kernel keeps the GPU busy while the host prepares the next call)
     with ClockSampler(local) as clk:
+        evs = []
         for _ in range(steps):
             flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
@@ -407,8 +410,9 @@ def bench_decode(name, steps, warmup, ws, local):
             e0.record(stream)
             call()
             e1.record(stream)
-            e1.synchronize()
-            times.append(e0.elapsed_time(e1))
+            evs.append((e0, e1))
+        evs[-1][1].synchronize()
+        times = [a.elapsed_time(b) for a, b in evs]
     barrier(ws)
     ms = max_over_ranks(sum(times) / len(times), ws)
     st, word = sa.device_status()

@@ -3,10 +3,13 @@
 // The MiMo-V2-Flash Technical Report (§2.3.1) verifies 1 + K draft tokens in
 // one pass over the KV cache.  For each unit (sequence b, KV head) the T new
 // tokens x G query heads of that KV head form T * G <= 128 packed rows, and the
-// unit's visible keys are cut into 64-key blocks.  The flattened list of all
-// units' blocks is split into gridDim.x equal contiguous ranges, one per CTA,
-// so every CTA streams the same number of cache blocks whatever the sequence
-// lengths.  A unit that lies entirely inside one CTA's range is finished there
+// unit's visible keys are cut into 64-key blocks.  Each KV head has its own
+// list of its units' blocks (sequence by sequence), cut into equal contiguous
+// ranges over the same number of CTAs: every CTA streams the same number of
+// cache blocks whatever the sequence lengths, and the CTAs of the different
+// KV heads walk each sequence's cache rows together (a head's 384-byte key
+// slice shares 256-byte DRAM bursts with its neighbours', so walking them at
+// different times fetches those bursts twice).  A unit that lies entirely inside one CTA's range is finished there
 // (eqs. (1)-(3) of §2.2, the sink added once); a unit cut by a range boundary
 // leaves, per CTA, its running max m, the sum l of 2^(a - m) and the
 // unnormalised O = sum 2^(a - m) v without the sink, and
@@ -46,6 +49,11 @@ struct DecArgs {
   int32_t window;
   int32_t batch, S_cap;
   int32_t n_units;        // batch * Hkv
+  // The work is n_sub independent block lists of n_k units each (n_sub = Hkv:
+  // one list per KV head, so the KV heads of a sequence stream its cache rows
+  // at the same time; n_sub = 1: one list over all units).  Unit k of list s
+  // is u = k * n_sub + s; CTA c works on list c % n_sub.
+  int32_t n_sub, n_k;
   int32_t kv_ring;        // 1: the cache is a ring of S_cap slots, position j at slot j % S_cap
   int32_t rope_on, rope_style;
   uint32_t q_tx_bytes;
@@ -54,7 +62,7 @@ struct DecArgs {
   const float *sink;
   __nv_bfloat16 *out;
   float *lse;
-  int32_t *unit_blk;      // [n_units + 1] block offsets (written by CTA 0)
+  int32_t *unit_blk;      // [n_k + 1] block offsets of the units of a list (written by CTA 0)
   float *part_o;          // [gridDim.x * 2, R, 128] unnormalised O
   float *part_ml;         // [gridDim.x * 2, R, 4] (m, l, 0, 0), log2 domain
   unsigned long long rope_turns[32];
@@ -80,24 +88,26 @@ struct DecSeg {
 };
 
 struct DecCursor {
-  int32_t u, blk;  // next block to process
+  int32_t k, blk;  // next block to process: unit k of this CTA's list, block blk
+  int32_t s;       // the list (unit u = k * n_sub + s)
   int32_t left;    // blocks of this CTA not yet handed out
   int32_t first;
 };
 
 // The next segment of the cursor (returns false when the CTA's range is done).
 __device__ __forceinline__ bool dec_next(DecCursor &c, const DecArgs &a, DecSeg &sg) {
-  while (c.left > 0 && c.u < a.n_units) {
+  while (c.left > 0 && c.k < a.n_k) {
+    const int32_t u = c.k * a.n_sub + c.s;
     int32_t L, lo, nb;
-    dec_unit_keys(a, c.u, L, lo, nb);
+    dec_unit_keys(a, u, L, lo, nb);
     if (c.blk >= nb) {
-      ++c.u;
+      ++c.k;
       c.blk = 0;
       continue;
     }
-    sg.u = c.u;
-    sg.b = c.u / a.Hkv;
-    sg.kvh = c.u % a.Hkv;
+    sg.u = u;
+    sg.b = u / a.Hkv;
+    sg.kvh = u % a.Hkv;
     sg.L = L;
     sg.lo = lo;
     sg.nblk_u = nb;
@@ -112,18 +122,23 @@ __device__ __forceinline__ bool dec_next(DecCursor &c, const DecArgs &a, DecSeg 
   return false;
 }
 
-// Set-up (one warp): block offsets of all units (a warp scan), this CTA's range
-// [f0, f1) of the flattened block list, and the unit/block it starts at.
-// CTA 0 also stores the offsets for the combine step.
+// Set-up (one warp): block offsets of the units of this CTA's list (a warp
+// scan), this CTA's range [f0, f1) of the list's blocks (the list's G =
+// gridDim.x / n_sub CTAs split it evenly) and the unit/block it starts at.
+// Every list has the same block counts (a unit's keys depend on its sequence
+// only when n_sub = Hkv), so CTA 0 stores one offset table for the combine.
 __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
+  const int32_t sl = static_cast<int32_t>(blockIdx.x) % a.n_sub;
+  const int32_t g = static_cast<int32_t>(blockIdx.x) / a.n_sub;
+  const int32_t G = static_cast<int32_t>(gridDim.x) / a.n_sub;
   int64_t run = 0;
-  // pass 1: total blocks (and, for CTA 0, the offset table)
-  for (int32_t base = 0; base < a.n_units; base += 32) {
-    const int32_t u = base + lane;
+  // pass 1: total blocks of the list (and, for CTA 0, the offset table)
+  for (int32_t base = 0; base < a.n_k; base += 32) {
+    const int32_t k = base + lane;
     int32_t nb = 0;
-    if (u < a.n_units) {
+    if (k < a.n_k) {
       int32_t L, lo;
-      dec_unit_keys(a, u, L, lo, nb);
+      dec_unit_keys(a, k * a.n_sub + sl, L, lo, nb);
     }
     int32_t incl = nb;
 #pragma unroll
@@ -131,23 +146,23 @@ __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
       const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    if (blockIdx.x == 0 && u < a.n_units) a.unit_blk[u] = static_cast<int32_t>(run + incl - nb);
+    if (blockIdx.x == 0 && k < a.n_k) a.unit_blk[k] = static_cast<int32_t>(run + incl - nb);
     run += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (blockIdx.x == 0 && lane == 0) a.unit_blk[a.n_units] = static_cast<int32_t>(run);
+  if (blockIdx.x == 0 && lane == 0) a.unit_blk[a.n_k] = static_cast<int32_t>(run);
   const int64_t T = run;
-  const int64_t f0 = T * blockIdx.x / gridDim.x;
-  const int64_t f1 = T * (blockIdx.x + 1) / gridDim.x;
+  const int64_t f0 = T * g / G;
+  const int64_t f1 = T * (g + 1) / G;
   // pass 2: the unit holding block f0
-  int32_t su = a.n_units, sblk = 0;
+  int32_t sk = a.n_k, sblk = 0;
   run = 0;
   bool found = false;
-  for (int32_t base = 0; base < a.n_units && !found && f1 > f0; base += 32) {
-    const int32_t u = base + lane;
+  for (int32_t base = 0; base < a.n_k && !found && f1 > f0; base += 32) {
+    const int32_t k = base + lane;
     int32_t nb = 0;
-    if (u < a.n_units) {
+    if (k < a.n_k) {
       int32_t L, lo;
-      dec_unit_keys(a, u, L, lo, nb);
+      dec_unit_keys(a, k * a.n_sub + sl, L, lo, nb);
     }
     int32_t incl = nb;
 #pragma unroll
@@ -160,16 +175,17 @@ __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
       const int32_t j = __ffs(m) - 1;
       const int32_t incl_j = __shfl_sync(0xffffffffu, incl, j);
       const int32_t nb_j = __shfl_sync(0xffffffffu, nb, j);
-      su = base + j;
+      sk = base + j;
       sblk = static_cast<int32_t>(f0 - (run + incl_j - nb_j));
       found = true;
     }
     run += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) {
-    cur[0] = su;
+    cur[0] = sk;
     cur[1] = sblk;
     cur[2] = found ? static_cast<int32_t>(f1 - f0) : 0;
+    cur[3] = sl;
   }
 }
 
@@ -182,7 +198,7 @@ struct DecLayout {
   // q_full q_ready q_empty | kv_full[S] k_ready[S] kv_empty[S] | s_full[2] p_full[2] pv_done o_empty drain
   static constexpr uint32_t kNumBars = 3 + 3 * kDecStages + 7;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag, cursor
-  static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;  // + cursor[3]
+  static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;  // + cursor[4]
   static constexpr uint32_t kBytes = kTurnsOff + 32 * 8;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
@@ -256,9 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t G = args.G;
   const int32_t R = args.R;
   DecCursor c0;
-  c0.u = cur_smem[0];
+  c0.k = cur_smem[0];
   c0.blk = cur_smem[1];
   c0.left = cur_smem[2];
+  c0.s = cur_smem[3];
   c0.first = 1;
 
   if (warp == 0) {
@@ -619,24 +636,27 @@ constexpr int32_t kCombThreads = 512;
 __global__ void __launch_bounds__(kCombThreads)
     sinkattn_decode_combine_kernel(const __grid_constant__ DecArgs a, int32_t grid) {
   const int32_t u = blockIdx.x;
-  const int32_t F0 = a.unit_blk[u], F1 = a.unit_blk[u + 1];
-  const int64_t Tb = a.unit_blk[a.n_units];
-  auto cta_of = [&](int64_t f) { return static_cast<int32_t>(((f + 1) * grid - 1) / Tb); };
+  const int32_t k = u / a.n_sub, sl = u % a.n_sub;  // unit k of list sl
+  const int32_t G = grid / a.n_sub;                // CTAs of a list; CTA of group g: g * n_sub + sl
+  const int32_t F0 = a.unit_blk[k], F1 = a.unit_blk[k + 1];
+  const int64_t Tb = a.unit_blk[a.n_k];
+  auto grp_of = [&](int64_t f) { return static_cast<int32_t>(((f + 1) * G - 1) / Tb); };
   const bool empty_unit = F1 == F0;
-  int32_t c_first = 0, c_last = 0;
+  int32_t c_first = 0, c_last = 0;  // groups
   if (!empty_unit) {
-    c_first = cta_of(F0);
-    c_last = cta_of(F1 - 1);
+    c_first = grp_of(F0);
+    c_last = grp_of(F1 - 1);
     if (c_first == c_last) return;  // finished by the decode kernel
   }
   const int32_t b = u / a.Hkv, kvh = u % a.Hkv;
   const int32_t e = threadIdx.x & (kDv - 1);
   const float4 *ml = reinterpret_cast<const float4 *>(a.part_ml);
-  // CTAs whose range is empty (fewer blocks than CTAs) hold no partial
-  auto has_part = [&](int32_t c) { return Tb * c / grid != Tb * (c + 1) / grid; };
+  // groups whose range is empty (fewer blocks than CTAs) hold no partial
+  auto has_part = [&](int32_t c) { return Tb * c / G != Tb * (c + 1) / G; };
   auto slot = [&](int32_t c, int32_t r) {
-    const int64_t bnd = Tb * c / grid;  // first block of CTA c
-    return (static_cast<size_t>(c) * 2 + ((c == c_first && bnd < F0) ? 1 : 0)) * a.R + r;
+    const int64_t bnd = Tb * c / G;  // first block of group c
+    const size_t cta = static_cast<size_t>(c) * a.n_sub + sl;
+    return (cta * 2 + ((c == c_first && bnd < F0) ? 1 : 0)) * a.R + r;
   };
   constexpr int32_t kStride = kCombParts * (kCombThreads / kDv);
   for (int32_t r = blockIdx.y * (kCombThreads / kDv) + (threadIdx.x >> 7); r < a.R; r += kStride) {

@@ -404,9 +404,14 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
   // plus up to 15 before them when a ring cache aligns its first block
   const int64_t range = window > 0 ? std::min<int64_t>(max_seqlen, int64_t(T) + window - 1 + (ring ? 15 : 0))
                                    : int64_t(max_seqlen);
-  const int64_t max_blocks = int64_t(d.n_units) * ((range + sa::kDecBN - 1) / sa::kDecBN);
-  const int grid = static_cast<int>(
-      std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(max_blocks, dev.sms), sa::kDecMaxGrid)));
+  // one block list per KV head (its CTAs walk the sequences' cache rows with
+  // the other heads' CTAs) unless there are more KV heads than CTAs
+  const int cap = std::min<int>(dev.sms, sa::kDecMaxGrid);
+  d.n_sub = num_kv_heads <= cap ? num_kv_heads : 1;
+  d.n_k = d.n_units / d.n_sub;
+  const int64_t max_blocks = int64_t(d.n_k) * ((range + sa::kDecBN - 1) / sa::kDecBN);
+  const int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_blocks, cap / d.n_sub)));
+  const int grid = groups * d.n_sub;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto kern = sa::sinkattn_decode_kernel;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
