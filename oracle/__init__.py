@@ -52,6 +52,9 @@ def _load():
         lib.oracle_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32,
                                       ctypes.POINTER(_Cfg), P, i64, P, P, ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_prefill_backward.argtypes = [P, P, P, P, P, i32, i32, i32,
+                                                ctypes.POINTER(_Cfg), P, P, P, P, P, ctypes.c_int]
+        lib.oracle_prefill_backward.restype = ctypes.c_int
         lib.oracle_rope.argtypes = [P, i32, i32, i32, ctypes.c_double, ctypes.c_double, P]
         lib.oracle_rope.restype = None
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -145,6 +148,40 @@ def prefill(q, k, v, sink, cu_seqlens, *, window: int, rope_base: float,
     if rows is None:
         return out.reshape(total, Hq, dv), lse.reshape(total, Hq)
     return out, lse
+
+
+def prefill_backward(q, k, v, sink, cu_seqlens, dout, *, window: int, rope_base: float,
+                     scale: float | None = None, drot: int = 64, rope_style: int = 0,
+                     nthreads: int = 0):
+    """Gradients of L = sum(dout * o) for the prefill above, by the chain rule
+    through eqs. (1)-(3): returns (dq [total, Hq, dqk], dk [total, Hkv, dqk],
+    dv [total, Hkv, dv], dsink [Hq]) as fp64 numpy arrays."""
+    qa, dt_q = _as_input(q)
+    ka, dt_k = _as_input(k)
+    va, dt_v = _as_input(v)
+    da, dt_d = _as_input(dout)
+    if not (dt_q == dt_k == dt_v == dt_d):
+        raise ValueError("q, k, v, dout must share one dtype")
+    total, Hq, dqk = qa.shape
+    Hkv, dv = ka.shape[1], va.shape[2]
+    sk = _f32(sink)
+    cu = _i32(cu_seqlens)
+    B = cu.shape[0] - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(dqk)
+    cfg = _cfg(dqk, dv, drot, rope_style, window, dt_q, rope_base, scale)
+    dq = np.zeros((total, Hq, dqk), dtype=np.float64)
+    dk = np.zeros((total, Hkv, dqk), dtype=np.float64)
+    dvv = np.zeros((total, Hkv, dv), dtype=np.float64)
+    ds = np.zeros((Hq,), dtype=np.float64)
+    rc = _load().oracle_prefill_backward(qa.ctypes.data, ka.ctypes.data, va.ctypes.data,
+                                         sk.ctypes.data, cu.ctypes.data, B, Hq, Hkv,
+                                         ctypes.byref(cfg), da.ctypes.data, dq.ctypes.data,
+                                         dk.ctypes.data, dvv.ctypes.data, ds.ctypes.data,
+                                         int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_prefill_backward failed with {rc}")
+    return dq, dk, dvv, ds
 
 
 def decode(q, kcache, vcache, seqlens, sink, *, window: int, rope_base: float,

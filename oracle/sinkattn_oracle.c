@@ -317,3 +317,141 @@ int oracle_decode(const void *q, const void *kcache, const void *vcache,
 }
 
 int oracle_max_threads(void) { return omp_get_max_threads(); }
+
+/* The inverse rotation: R(pos)^T y, i.e. each dim pair turned by -pos*theta_t.
+ * A gradient with respect to a rotated vector comes back to the raw vector's
+ * coordinates this way (the rotation is orthogonal). */
+static void rope_transpose(const double *y, int32_t d, int32_t drot, int32_t style,
+                           double base, double pos, double *x)
+{
+    oracle_rope(y, d, drot, style, base, -pos, x);
+}
+
+/* Backward pass of the prefill forward above, for the loss L = sum_i dO_i . o_i,
+ * by the chain rule through eqs. (1)-(3) (the pages give the forward only; the
+ * gradient is the plain derivative of that definition):
+ *   s_ij = exp(a_ij - lse_i), s_sink,i = exp(sink_h - lse_i)      (eq. (2))
+ *   D_i = dO_i . o_i,  dP_ij = dO_i . v_j
+ *   dL/dv_j    += s_ij dO_i                                         (eq. (3))
+ *   dL/da_ij    = s_ij (dP_ij - D_i)                                (eq. (2))
+ *   dL/dq~_i   += scale * dL/da_ij k~_j,  dL/dk~_j += scale * dL/da_ij q~_i  (eq. (1))
+ *   dL/dsink_h += -s_sink,i D_i        (the sink's term in the denominator)
+ * where q~, k~ are the rotated vectors; dq, dk are turned back by R^T.
+ * Inputs as oracle_prefill, plus dout [total, Hq, dv] (cfg->dtype).  Outputs
+ * dq [total, Hq, dqk], dk [total, Hkv, dqk], dv [total, Hkv, dv], dsink [Hq],
+ * all fp64 and fully written.  Returns 0, -1 on allocation failure, -2 on bad
+ * arguments.  Parallel over (sequence, kv head) groups; each group's rows are
+ * walked in order, so the result does not depend on the thread count except
+ * for the order of dsink's per-group sums (added in group order). */
+int oracle_prefill_backward(const void *q, const void *k, const void *v, const float *sink,
+                            const int32_t *cu_seqlens, int32_t batch, int32_t Hq,
+                            int32_t Hkv, const oracle_cfg *cfg, const void *dout,
+                            double *dq, double *dk, double *dvo, double *dsink, int nthreads)
+{
+    if (check_cfg(cfg, Hq, Hkv) || batch < 0) return -2;
+    const int64_t total = cu_seqlens[batch];
+    const int32_t dqk = cfg->dqk, dv = cfg->dv, G = Hq / Hkv;
+    memset(dq, 0, (size_t)(total * Hq * dqk) * sizeof(double));
+    memset(dk, 0, (size_t)(total * Hkv * dqk) * sizeof(double));
+    memset(dvo, 0, (size_t)(total * Hkv * dv) * sizeof(double));
+    for (int32_t h = 0; h < Hq; ++h) dsink[h] = 0.0;
+    const int64_t ngroups = (int64_t)batch * Hkv;
+    double *ds_part = (double *)calloc((size_t)(ngroups > 0 ? ngroups : 1) * (size_t)G, sizeof(double));
+    if (!ds_part) return -1;
+    int err = 0;
+#pragma omp parallel num_threads(nthreads)
+    {
+        const int64_t maxl = 1 << 20;
+        double *qr = (double *)malloc((size_t)dqk * sizeof(double));
+        double *tmp = (double *)malloc((size_t)dqk * sizeof(double));
+        double *dqr = (double *)malloc((size_t)dqk * sizeof(double));
+        double *o = (double *)malloc((size_t)dv * sizeof(double));
+        double *dO = (double *)malloc((size_t)dv * sizeof(double));
+        (void)maxl;
+        if (!qr || !tmp || !dqr || !o || !dO) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t gi = 0; gi < ngroups; ++gi) {
+            if (!qr || !tmp || !dqr || !o || !dO) continue;
+            const int32_t b = (int32_t)(gi / Hkv), g = (int32_t)(gi % Hkv);
+            const int64_t s0 = cu_seqlens[b], L = cu_seqlens[b + 1] - s0;
+            if (L <= 0) continue;
+            /* the rotated keys of this sequence and kv head, and their gradients */
+            double *kr = (double *)malloc((size_t)L * (size_t)dqk * sizeof(double));
+            double *dkr = (double *)calloc((size_t)L * (size_t)dqk, sizeof(double));
+            double *a = (double *)malloc((size_t)L * sizeof(double));
+            if (!kr || !dkr || !a) {
+                free(kr); free(dkr); free(a);
+#pragma omp atomic write
+                err = 1;
+                continue;
+            }
+            for (int64_t j = 0; j < L; ++j) {
+                const int64_t off = ((s0 + j) * Hkv + g) * (int64_t)dqk;
+                for (int32_t e = 0; e < dqk; ++e) tmp[e] = load(k, cfg->dtype, off + e);
+                oracle_rope(tmp, dqk, cfg->drot, cfg->rope_style, cfg->rope_base, (double)j,
+                            kr + j * dqk);
+            }
+            for (int64_t p = 0; p < L; ++p) {
+                const int64_t lo = cfg->window > 0 ? (p - cfg->window + 1 > 0 ? p - cfg->window + 1 : 0) : 0;
+                for (int32_t hh = 0; hh < G; ++hh) {
+                    const int32_t h = g * G + hh;
+                    const double sk = (double)sink[h];
+                    const int64_t row = (s0 + p) * Hq + h;
+                    for (int32_t e = 0; e < dqk; ++e) tmp[e] = load(q, cfg->dtype, row * dqk + e);
+                    oracle_rope(tmp, dqk, cfg->drot, cfg->rope_style, cfg->rope_base, (double)p, qr);
+                    for (int32_t e = 0; e < dv; ++e) dO[e] = load(dout, cfg->dtype, row * dv + e);
+                    /* forward again: logits, max with the sink, denominator, o */
+                    double m = sk;
+                    for (int64_t j = lo; j <= p; ++j) {
+                        double acc = 0.0;
+                        for (int32_t e = 0; e < dqk; ++e) acc += qr[e] * kr[j * dqk + e];
+                        a[j] = acc * cfg->scale;
+                        if (a[j] > m) m = a[j];
+                    }
+                    if (m == -INFINITY) continue; /* nothing visible, no sink: o = 0, no gradient */
+                    double den = exp(sk - m);
+                    for (int64_t j = lo; j <= p; ++j) den += exp(a[j] - m);
+                    const double lse_i = m + log(den);
+                    for (int32_t e = 0; e < dv; ++e) o[e] = 0.0;
+                    for (int64_t j = lo; j <= p; ++j) {
+                        const double s = exp(a[j] - lse_i);
+                        const int64_t voff = ((s0 + j) * Hkv + g) * (int64_t)dv;
+                        for (int32_t e = 0; e < dv; ++e) o[e] += s * load(v, cfg->dtype, voff + e);
+                    }
+                    double D = 0.0;
+                    for (int32_t e = 0; e < dv; ++e) D += dO[e] * o[e];
+                    /* the sink's gradient, per head of this group */
+                    ds_part[gi * G + hh] += -exp(sk - lse_i) * D;
+                    for (int32_t e = 0; e < dqk; ++e) dqr[e] = 0.0;
+                    for (int64_t j = lo; j <= p; ++j) {
+                        const double s = exp(a[j] - lse_i);
+                        const int64_t voff = ((s0 + j) * Hkv + g) * (int64_t)dv;
+                        double dP = 0.0;
+                        for (int32_t e = 0; e < dv; ++e) dP += dO[e] * load(v, cfg->dtype, voff + e);
+                        for (int32_t e = 0; e < dv; ++e) dvo[voff + e] += s * dO[e];
+                        const double dS = s * (dP - D);
+                        for (int32_t e = 0; e < dqk; ++e) {
+                            dqr[e] += cfg->scale * dS * kr[j * dqk + e];
+                            dkr[j * dqk + e] += cfg->scale * dS * qr[e];
+                        }
+                    }
+                    rope_transpose(dqr, dqk, cfg->drot, cfg->rope_style, cfg->rope_base, (double)p,
+                                   dq + row * dqk);
+                }
+            }
+            for (int64_t j = 0; j < L; ++j)
+                rope_transpose(dkr + j * dqk, dqk, cfg->drot, cfg->rope_style, cfg->rope_base,
+                               (double)j, dk + ((s0 + j) * Hkv + g) * (int64_t)dqk);
+            free(kr); free(dkr); free(a);
+        }
+        free(qr); free(tmp); free(dqr); free(o); free(dO);
+    }
+    /* dsink: the per-group sums in group order */
+    for (int64_t gi = 0; gi < ngroups; ++gi)
+        for (int32_t hh = 0; hh < G; ++hh) dsink[(gi % Hkv) * G + hh] += ds_part[gi * G + hh];
+    free(ds_part);
+    return err ? -1 : 0;
+}
