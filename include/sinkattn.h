@@ -193,6 +193,40 @@ sinkattn_status sinkattn_decode_noalloc(const void *q, const void *kcache, const
                                         int32_t num_kv_heads, void *out, float *lse,
                                         sinkattn_stream_t stream);
 
+/*
+ * Backward pass of sinkattn_prefill (the sink logits are learned, §2.2; the
+ * pages define the forward, eqs. (1)-(3), and this is its plain derivative for
+ * the loss L = sum dout . out):
+ *   dq, dk, dv  gradients of L with respect to q, k, v (raw, unrotated inputs)
+ *   dsink       gradient with respect to sink: -sum_i exp(sink_h - lse_i) (dout_i . out_i)
+ *
+ *   q, k, v, sink, cu_seqlens, batch, total, max_seqlen, num_q_heads,
+ *   num_kv_heads, window, rope_base, params   as for sinkattn_prefill_ex (params
+ *              may be NULL; kv_ring must be 0)
+ *   out, lse   the forward's outputs for these inputs (bf16 [total, Hq, 128],
+ *              fp32 [total, Hq])
+ *   dout       bf16 [total, num_q_heads, 128]
+ *   workspace, workspace_bytes  device scratch of at least
+ *              sinkattn_prefill_backward_workspace_size(...) bytes, 256-byte
+ *              aligned; no clearing needed.  It holds the rotated q and k and
+ *              the row terms dout_i . out_i.
+ *   dq bf16 [total, Hq, 192], dk bf16 [total, Hkv, 192], dv bf16 [total, Hkv, 128],
+ *   dsink fp32 [Hq]: all fully written.
+ * Needs 1 <= num_q_heads / num_kv_heads <= 64 and a positive scale
+ * (SINKATTN_EUNSUPPORTED / SINKATTN_EINVAL otherwise).  Deterministic.
+ */
+size_t sinkattn_prefill_backward_workspace_size(int32_t total, int32_t num_q_heads,
+                                                int32_t num_kv_heads);
+sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const void *v,
+                                          const float *sink, const int32_t *cu_seqlens,
+                                          int32_t batch, int32_t total, int32_t max_seqlen,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t window, float rope_base,
+                                          const sinkattn_params *params, const void *out,
+                                          const float *lse, const void *dout, void *workspace,
+                                          size_t workspace_bytes, void *dq, void *dk, void *dv,
+                                          float *dsink, sinkattn_stream_t stream);
+
 /* A static string naming a status code. */
 const char *sinkattn_status_string(sinkattn_status status);
 

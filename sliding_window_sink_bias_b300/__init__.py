@@ -25,6 +25,7 @@ EXPORTED = (
     "sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode_workspace_size",
     "sinkattn_decode", "sinkattn_decode_ex", "sinkattn_status_string",
     "sinkattn_get_device_status", "sinkattn_version", "sinkattn_decode_noalloc",
+    "sinkattn_prefill_backward_workspace_size", "sinkattn_prefill_backward",
 )
 
 # bytes of the library's fixed decode scratch (include/sinkattn.h)
@@ -66,12 +67,18 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(Params), P, ctypes.c_size_t, P, P, P]
         L.sinkattn_decode_noalloc.argtypes = [P, P, P, P, P, i32, f32, i32, i32, i32, i32, i32, i32,
                                               P, P, P]
+        L.sinkattn_prefill_backward_workspace_size.argtypes = [i32, i32, i32]
+        L.sinkattn_prefill_backward_workspace_size.restype = ctypes.c_size_t
+        L.sinkattn_prefill_backward.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
+                                                ctypes.POINTER(Params), P, P, P, P,
+                                                ctypes.c_size_t, P, P, P, P, P]
         L.sinkattn_status_string.argtypes = [i32]
         L.sinkattn_status_string.restype = ctypes.c_char_p
         L.sinkattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.sinkattn_version.restype = i32
         for name in ("sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode",
-                     "sinkattn_decode_ex", "sinkattn_get_device_status", "sinkattn_decode_noalloc"):
+                     "sinkattn_decode_ex", "sinkattn_get_device_status", "sinkattn_decode_noalloc",
+                     "sinkattn_prefill_backward"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -147,6 +154,47 @@ def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_bas
 def decode_workspace_size(batch: int, t: int, hq: int, hkv: int, max_seqlen: int,
                           window: int) -> int:
     return int(lib().sinkattn_decode_workspace_size(batch, t, hq, hkv, max_seqlen, window))
+
+
+def prefill_backward_workspace_size(total: int, hq: int, hkv: int) -> int:
+    return int(lib().sinkattn_prefill_backward_workspace_size(total, hq, hkv))
+
+
+def prefill_backward(q, k, v, sink, cu_seqlens, out, lse, dout, *, max_seqlen: int, window: int,
+                     rope_base: float, scale=None, rope_style: int = 0, rope_off: bool = False,
+                     workspace=None, dq=None, dk=None, dv=None, dsink=None, stream=None):
+    """Backward of prefill() for the loss sum(dout * out): returns (dq bf16 [T, Hq, 192],
+    dk bf16 [T, Hkv, 192], dv bf16 [T, Hkv, 128], dsink fp32 [Hq]).  out and lse are the
+    forward's results for the same inputs."""
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k, "k", torch.bfloat16, 3)
+    _require(v, "v", torch.bfloat16, 3)
+    _require(sink, "sink", torch.float32, 1)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _require(out, "out", torch.bfloat16, 3)
+    _require(lse, "lse", torch.float32, 2)
+    _require(dout, "dout", torch.bfloat16, 3)
+    total, hq, _ = q.shape
+    hkv = k.shape[1]
+    if out.shape != (total, hq, 128) or dout.shape != (total, hq, 128) or lse.shape != (total, hq):
+        raise ValueError("expected out/dout [T, Hq, 128] and lse [T, Hq]")
+    need = prefill_backward_workspace_size(total, hq, hkv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    dev = q.device
+    dq = torch.empty(total, hq, 192, dtype=torch.bfloat16, device=dev) if dq is None else dq
+    dk = torch.empty(total, hkv, 192, dtype=torch.bfloat16, device=dev) if dk is None else dk
+    dv = torch.empty(total, hkv, 128, dtype=torch.bfloat16, device=dev) if dv is None else dv
+    dsink = torch.empty(hq, dtype=torch.float32, device=dev) if dsink is None else dsink
+    p = _params(scale, rope_style, rope_off)
+    st = lib().sinkattn_prefill_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, total,
+        int(max_seqlen), hq, hkv, int(window), float(rope_base),
+        None if p is None else ctypes.byref(p), _ptr(out), _ptr(lse), _ptr(dout),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(dsink), _stream(stream))
+    _check("sinkattn_prefill_backward", st)
+    return dq, dk, dv, dsink
 
 
 def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, rope_base: float,

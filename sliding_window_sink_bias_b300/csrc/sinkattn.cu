@@ -13,6 +13,7 @@
 #include "attn_kernel.cuh"
 #include "band_kernel.cuh"
 #include "decode_kernel.cuh"
+#include "backward_kernel.cuh"
 #include "causal_kernel.cuh"
 #include "sinkattn.h"
 
@@ -224,6 +225,153 @@ DecodePlan decode_plan(int32_t batch, int32_t T, int32_t hq, int32_t hkv) {
 extern "C" {
 
 int32_t sinkattn_version(void) { return kVersion; }
+
+// ----------------------------------------------------------------- backward
+// Workspace: q_rot bf16 [total, Hq, 192], k_rot bf16 [total, Hkv, 192],
+// D fp32 [total, Hq], per-chunk sink-gradient partials fp32 [chunks, Hq];
+// each region starts on 256 bytes.
+struct BwdPlan {
+  size_t q_rot = 0, k_rot = 0, D = 0, part = 0, bytes = 0;
+  int32_t chunks = 0;
+};
+
+BwdPlan bwd_plan(int64_t total, int32_t hq, int32_t hkv) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  BwdPlan p;
+  p.chunks = static_cast<int32_t>((total + sa::kBwdChunk - 1) / sa::kBwdChunk);
+  p.q_rot = 0;
+  p.k_rot = p.q_rot + up(static_cast<size_t>(total) * hq * 192 * 2);
+  p.D = p.k_rot + up(static_cast<size_t>(total) * hkv * 192 * 2);
+  p.part = p.D + up(static_cast<size_t>(total) * hq * 4);
+  p.bytes = p.part + up(static_cast<size_t>(p.chunks > 0 ? p.chunks : 1) * hq * 4);
+  return p;
+}
+
+size_t sinkattn_prefill_backward_workspace_size(int32_t total, int32_t num_q_heads,
+                                                int32_t num_kv_heads) {
+  if (total < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+  return bwd_plan(total, num_q_heads, num_kv_heads).bytes;
+}
+
+sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const void *v,
+                                          const float *sink, const int32_t *cu_seqlens,
+                                          int32_t batch, int32_t total, int32_t max_seqlen,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t window, float rope_base,
+                                          const sinkattn_params *params, const void *out,
+                                          const float *lse, const void *dout, void *workspace,
+                                          size_t workspace_bytes, void *dq, void *dk, void *dv,
+                                          float *dsink, sinkattn_stream_t stream) {
+  if (batch < 0 || total < 0 || max_seqlen < 0 || window < 0) return SINKATTN_EINVAL;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return SINKATTN_EINVAL;
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (!pow2_upto_128(G) || G > 64) return SINKATTN_EUNSUPPORTED;
+  if (num_q_heads > 65535 || num_kv_heads > 65535) return SINKATTN_EUNSUPPORTED;
+  if (params && params->kv_ring) return SINKATTN_EINVAL;
+  if (total > 0 && max_seqlen == 0) return SINKATTN_EINVAL;
+  AttnArgs a;
+  if (sinkattn_status st = fill_common(a, params, rope_base, num_q_heads, num_kv_heads, window))
+    return st;
+  if (!(a.scale_log2 > 0.f)) return SINKATTN_EINVAL;
+  if (batch == 0 || total == 0) {
+    if (!dsink) return SINKATTN_EINVAL;
+    return cudaMemsetAsync(dsink, 0, sizeof(float) * num_q_heads,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SINKATTN_OK
+               : SINKATTN_ECUDA;
+  }
+  if (!q || !k || !v || !sink || !cu_seqlens || !out || !lse || !dout || !dq || !dk || !dv || !dsink)
+    return SINKATTN_EINVAL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(sink, 4) || !aligned(dsink, 4) || !aligned(cu_seqlens, 4))
+    return SINKATTN_EINVAL;
+  const BwdPlan plan = bwd_plan(total, num_q_heads, num_kv_heads);
+  if (!workspace || workspace_bytes < plan.bytes || !aligned(workspace, 256))
+    return SINKATTN_EWORKSPACE;
+  const int64_t T = 128 / G;
+  const int64_t dq_tiles = (int64_t(max_seqlen) + T - 1) / T;
+  const int64_t kv_blocks = (int64_t(max_seqlen) + sa::kKvBN - 1) / sa::kKvBN;
+  if (int64_t(batch) * num_kv_heads * dq_tiles > INT32_MAX) return SINKATTN_EUNSUPPORTED;
+
+  sa::BwdArgs b;
+  std::memset(&b, 0, sizeof b);
+  b.Hq = num_q_heads;
+  b.Hkv = num_kv_heads;
+  b.G = G;
+  b.batch = batch;
+  b.total = total;
+  b.window = window;
+  b.rope_on = a.rope_on;
+  b.rope_style = a.rope_style;
+  b.scale_log2 = a.scale_log2;
+  b.scale = static_cast<float>(static_cast<double>(a.scale_log2) / 1.4426950408889634);
+  b.cu_seqlens = cu_seqlens;
+  b.sink = sink;
+  b.q = static_cast<const __nv_bfloat16 *>(q);
+  b.k = static_cast<const __nv_bfloat16 *>(k);
+  b.out = static_cast<const __nv_bfloat16 *>(out);
+  b.dout = static_cast<const __nv_bfloat16 *>(dout);
+  b.lse = lse;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  b.q_rot = reinterpret_cast<__nv_bfloat16 *>(ws + plan.q_rot);
+  b.k_rot = reinterpret_cast<__nv_bfloat16 *>(ws + plan.k_rot);
+  b.D = reinterpret_cast<float *>(ws + plan.D);
+  b.dsink_part = reinterpret_cast<float *>(ws + plan.part);
+  b.n_chunks = plan.chunks;
+  b.dq = static_cast<__nv_bfloat16 *>(dq);
+  b.dk = static_cast<__nv_bfloat16 *>(dk);
+  b.dv = static_cast<__nv_bfloat16 *>(dv);
+  b.dsink = dsink;
+  b.dq_tiles = static_cast<int32_t>(dq_tiles);
+  b.dq_items = static_cast<int32_t>(int64_t(batch) * num_kv_heads * dq_tiles);
+  b.kv_blocks = static_cast<int32_t>(kv_blocks);
+  b.kv_items = static_cast<int32_t>(int64_t(batch) * num_kv_heads * kv_blocks);
+  std::memcpy(b.rope_turns, a.rope_turns, sizeof b.rope_turns);
+
+  DeviceInfo dev;
+  if (!device_info(dev)) return SINKATTN_ECUDA;
+  if (dev.major != 10 || dev.minor != 3) return SINKATTN_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  sa::bwd_pre_kernel<<<static_cast<unsigned>(plan.chunks), 256, 0, s>>>(b);
+  if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
+  sa::bwd_dsink_kernel<<<1, 256, 0, s>>>(b);
+  if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
+
+  CUtensorMap mq, mdo, mk, mv;
+  // dq kernel: 128 packed rows (G heads x 128/G tokens) and 64-key blocks
+  if (!make_map(&mq, b.q_rot, 192, num_q_heads, total, G, static_cast<uint32_t>(T)) ||
+      !make_map(&mdo, dout, 128, num_q_heads, total, G, static_cast<uint32_t>(T)) ||
+      !make_map(&mk, b.k_rot, 192, num_kv_heads, total, 1, sa::kDqBN) ||
+      !make_map(&mv, v, 128, num_kv_heads, total, 1, sa::kDqBN))
+    return SINKATTN_ECUDA;
+  {
+    auto kern = sa::bwd_dq_kernel;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sa::DqLayout::kDynSmem)) != cudaSuccess)
+      return SINKATTN_ECUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(b.dq_items, dev.sms));
+    kern<<<grid, sa::kBwdThreads, sa::DqLayout::kDynSmem, s>>>(mq, mdo, mk, mv, b);
+    if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
+  }
+  // dkdv kernel: 64 packed rows (G heads x 64/G tokens) and 128-key blocks
+  if (!make_map(&mq, b.q_rot, 192, num_q_heads, total, G, static_cast<uint32_t>(sa::kKvRows / G)) ||
+      !make_map(&mdo, dout, 128, num_q_heads, total, G, static_cast<uint32_t>(sa::kKvRows / G)) ||
+      !make_map(&mk, b.k_rot, 192, num_kv_heads, total, 1, sa::kKvBN) ||
+      !make_map(&mv, v, 128, num_kv_heads, total, 1, sa::kKvBN))
+    return SINKATTN_ECUDA;
+  {
+    auto kern = sa::bwd_dkdv_kernel;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sa::KvLayout::kDynSmem)) != cudaSuccess)
+      return SINKATTN_ECUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(b.kv_items, dev.sms));
+    kern<<<grid, sa::kBwdThreads, sa::KvLayout::kDynSmem, s>>>(mq, mdo, mk, mv, b);
+    if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
+  }
+  return SINKATTN_OK;
+}
 
 const char *sinkattn_status_string(sinkattn_status s) {
   switch (s) {
