@@ -368,6 +368,53 @@ def bench_ratio(name, warmup, ws, local):
     return rows
 
 
+FLOP_PER_PAIR_HEAD_BWD = 2 * (3 * 192 + 2 * 128)  # S, dP, dV, dK, dQ per visible pair and head
+
+
+def bench_backward(name, steps, warmup, ws, local):
+    """sinkattn_prefill_backward on a workload: algorithmic FLOPs are the five
+    products per visible (query, key) pair and head; algorithmic bytes read q,
+    k, v, out, dout, lse once and write dq, dk, dv once."""
+    import torch
+
+    import sliding_window_sink_bias_b300 as sa
+    from sliding_window_sink_bias_b300 import synth
+    wl = synth.WORKLOADS[name]
+    dev = f"cuda:{local}"
+    hq, hkv, W, base = wl["hq"], wl["hkv"], wl["window"], wl["rope_base"]
+    inp = synth.prefill_inputs(wl["seqlens"], hq, hkv, window=W, rope_base=base, seed=0,
+                               device=dev)
+    g = torch.Generator(device=dev).manual_seed(7)
+    dout = torch.randn(inp.total, hq, 128, generator=g, device=dev).to(torch.bfloat16)
+    out, lse = sa.prefill(inp.q, inp.k, inp.v, inp.sink, inp.cu_seqlens,
+                          max_seqlen=inp.max_seqlen, window=W, rope_base=base)
+    work = torch.empty(sa.prefill_backward_workspace_size(inp.total, hq, hkv), dtype=torch.uint8,
+                       device=dev)
+    dq = torch.empty(inp.total, hq, 192, dtype=torch.bfloat16, device=dev)
+    dk = torch.empty(inp.total, hkv, 192, dtype=torch.bfloat16, device=dev)
+    dv = torch.empty(inp.total, hkv, 128, dtype=torch.bfloat16, device=dev)
+    dsink = torch.empty(hq, dtype=torch.float32, device=dev)
+
+    def call():
+        sa.prefill_backward(inp.q, inp.k, inp.v, inp.sink, inp.cu_seqlens, out, lse, dout,
+                            max_seqlen=inp.max_seqlen, window=W, rope_base=base, workspace=work,
+                            dq=dq, dk=dk, dv=dv, dsink=dsink)
+
+    with ClockSampler(local) as clk:
+        ms, _ = time_calls(call, steps, warmup, ws)
+    st, word = sa.device_status()
+    if st != sa.OK:
+        raise RuntimeError(f"device status {st} word {word:#x} after {name}")
+    pairs = synth.algorithmic_pairs_prefill(wl["seqlens"], W)
+    total = inp.total
+    bytes_ = total * (hq * (192 + 128 + 128 + 192) * 2 + hq * 4 + hkv * (192 + 128) * 2 * 2)
+    res = {"ms": ms, "flops": pairs * hq * FLOP_PER_PAIR_HEAD_BWD, "bytes": bytes_,
+           "tokens": total, "clocks": clk.summary(), "launches": 4 * steps}
+    del inp, out, lse, dout, work, dq, dk, dv
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_decode(name, steps, warmup, ws, local):
     import torch
 
@@ -501,7 +548,14 @@ def run_reference(args):
 def single_workload(args, ws, rank, local, peaks):
     from sliding_window_sink_bias_b300 import synth
     wl = synth.WORKLOADS[args.workload]
-    if wl["kind"] == "ratio":
+    if wl["kind"] == "backward":
+        r = bench_backward(args.workload, args.steps, args.warmup, ws, local)
+        tf = r["flops"] / (r["ms"] / 1e3) / 1e12
+        gbs = r["bytes"] / (r["ms"] / 1e3) / 1e9
+        line = {"workload": args.workload, "ms": r["ms"], "tflops": tf, "gbs": gbs,
+                "frac_tensor": tf / peaks["bf16_tflops"], "frac_hbm": gbs / peaks["hbm_gbs"],
+                "clocks": r["clocks"]}
+    elif wl["kind"] == "ratio":
         line = {"workload": args.workload, "rows": bench_ratio(args.workload, args.warmup, ws, local)}
     elif wl["kind"] == "hybrid":
         r = bench_hybrid(args.workload, args.steps, args.warmup, ws, local)
@@ -628,6 +682,15 @@ def main():
             "ms_per_step": h["ms"], "tflops": h["flops"] / (h["ms"] / 1e3) / 1e12,
             "seq_lens": h["lens"], "layers": "5 SWA (64/8, W=128) + 1 GA (64/4)",
             "clocks": h["clocks"]}
+        for name, bound in (("swa_backward_4x32768", "hbm"), ("ga_backward_1x32768", "tensor")):
+            r = bench_backward(name, max(3, args.steps // 4), args.warmup, ws, local)
+            tf = r["flops"] / (r["ms"] / 1e3) / 1e12
+            gbs = r["bytes"] / (r["ms"] / 1e3) / 1e9
+            roof = (roofline_obj("hbm", gbs, peaks["hbm_gbs"], "GB/s", None) if bound == "hbm"
+                    else roofline_obj("tensor", tf, peaks["bf16_tflops"], "TFLOP/s", None))
+            extra[name] = {"value": ws * tf, "unit": "TFLOP/s", "ms_per_step": r["ms"],
+                           "gbs": gbs, "roofline": roof, "clocks": r["clocks"],
+                           "outputs": "dq, dk, dv, dsink for sum(dout * out)"}
         extra["hybrid_vs_all_ga"] = {
             "rows": bench_ratio("hybrid_vs_all_ga", args.warmup, ws, local),
             "note": "ratio = all-GA attention time / hybrid attention time for the same layer "

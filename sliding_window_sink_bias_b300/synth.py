@@ -146,6 +146,10 @@ WORKLOADS = {
     "hybrid_vs_all_ga": dict(kind="ratio", lens=[32768, 131072, 262144], hq=64, swa_hkv=8,
                              ga_hkv=4, window=128, swa_base=1e4, ga_base=5e6,
                              block=(5, 1), model=(39, 9)),
+    # backward pass (dq, dk, dv, dsink) of an SWA layer on the bulk batch and of
+    # a GA layer at 32K tokens
+    "swa_backward_4x32768": dict(kind="backward", seqlens=[32768] * 4, **SWA),
+    "ga_backward_1x32768": dict(kind="backward", seqlens=[32768], **GA),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)
     "swa_prefill_1x32768": dict(kind="prefill", seqlens=[32768], **SWA),
     "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),
