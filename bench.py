@@ -425,6 +425,22 @@ def bench_decode(name, steps, warmup, ws, local):
     lens = synth.uniform_lengths(wl["batch"], wl["len_lo"], wl["len_hi"], seed=0)
     inp = synth.decode_inputs(lens, wl["t"], wl["s_cap"], wl["hq"], wl["hkv"],
                               window=wl["window"], rope_base=wl["rope_base"], seed=0, device=dev)
+    fp8 = wl.get("fp8", False)
+    if fp8:
+        # E4M3 cache, one scale per KV head (largest magnitude -> 224)
+        def quant(c):
+            # sequence by sequence, so the fp32 temporaries stay small
+            amax = torch.stack([c[b].abs().amax(dim=(0, 2)).float() for b in range(c.shape[0])])
+            sc = (amax.amax(dim=0) / 224.0).clamp_min(1e-6)
+            q8 = torch.empty(c.shape, dtype=torch.float8_e4m3fn, device=c.device)
+            for b in range(c.shape[0]):
+                q8[b] = (c[b].float() / sc[None, :, None]).to(torch.float8_e4m3fn)
+            return q8, sc.float()
+        k8, ks = quant(inp.kcache)
+        inp.kcache = None
+        v8, vs = quant(inp.vcache)
+        inp.vcache = None
+        torch.cuda.empty_cache()
     ws_bytes = sa.decode_workspace_size(wl["batch"], wl["t"], wl["hq"], wl["hkv"], max(lens),
                                         wl["window"])
     work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -432,9 +448,14 @@ def bench_decode(name, steps, warmup, ws, local):
     lse = torch.empty(wl["batch"], wl["t"], wl["hq"], dtype=torch.float32, device=dev)
 
     def call():
-        sa.decode(inp.q, inp.kcache, inp.vcache, inp.seqlens, inp.sink, max_seqlen=max(lens),
-                  window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
-                  lse=lse, kv_ring=wl.get("kv_ring", False))
+        if fp8:
+            sa.decode_fp8(inp.q, k8, v8, ks, vs, inp.seqlens, inp.sink, max_seqlen=max(lens),
+                          window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
+                          lse=lse)
+        else:
+            sa.decode(inp.q, inp.kcache, inp.vcache, inp.seqlens, inp.sink, max_seqlen=max(lens),
+                      window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
+                      lse=lse, kv_ring=wl.get("kv_ring", False))
 
     # the decode working set can sit in L2 for the SWA layer: flush between steps
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -467,7 +488,7 @@ def bench_decode(name, steps, warmup, ws, local):
         raise RuntimeError(f"device status {st} word {word:#x} after {name}")
     hkv, t, hq, W = wl["hkv"], wl["t"], wl["hq"], wl["window"]
     keys = [min(L, t + W - 1) if W > 0 else L for L in lens]
-    kv_bytes = sum(keys) * hkv * (192 + 128) * 2
+    kv_bytes = sum(keys) * hkv * (192 + 128) * (1 if fp8 else 2)
     io_bytes = wl["batch"] * t * hq * (192 * 2 + 128 * 2 + 4)
     pairs = synth.algorithmic_pairs_decode(lens, t, W)
     res = {"name": name, "ms": ms, "kv_bytes": kv_bytes, "bytes": kv_bytes + io_bytes,
@@ -666,7 +687,8 @@ def main():
             "frac_of_sustained_peak": (g_tf / peaks["bf16_tflops_sustained"]
                                        if peaks.get("bf16_tflops_sustained") else None),
             "clocks": g["clocks"]}
-        for name in ("mtp_decode_ga_b64_t4", "mtp_decode_swa_b64_t4", "mtp_decode_swa_ring_b64_t4"):
+        for name in ("mtp_decode_ga_b64_t4", "mtp_decode_ga_fp8_b64_t4", "mtp_decode_swa_b64_t4",
+                     "mtp_decode_swa_ring_b64_t4"):
             d = bench_decode(name, args.steps, args.warmup, ws, local)
             d_gbs = d["bytes"] / (d["ms"] / 1e3) / 1e9
             extra[name] = {"value": ws * d_gbs, "unit": "GB/s", "ms_per_step": d["ms"],

@@ -164,6 +164,28 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
                                    sinkattn_stream_t stream);
 
 /*
+ * MTP-verify decode over an FP8 KV cache.  The report trains and serves in FP8
+ * (§4.6: training and inference both run FP8) but gives no scale convention;
+ * here the cache holds E4M3 values with one fp32 scale per KV head for K and
+ * one for V (the key is e4m3 * k_scale[kv head], the value e4m3 * v_scale).
+ *   kcache   E4M3 bytes [batch, S_cap, num_kv_heads, 192], unrotated keys
+ *   vcache   E4M3 bytes [batch, S_cap, num_kv_heads, 128]
+ *   k_scale, v_scale  fp32 [num_kv_heads], device
+ * Everything else as sinkattn_decode_ex (same workspace size); params->kv_ring
+ * must be 0.  The cache rows are converted to fp16 on chip (exactly) and the
+ * keys rotated there; q is rounded to fp16 and the products run fp16 x fp16
+ * with fp32 accumulation.  The cache read is half the bf16 cache's.
+ */
+sinkattn_status sinkattn_decode_fp8(const void *q, const void *kcache, const void *vcache,
+                                    const float *k_scale, const float *v_scale,
+                                    const int32_t *seqlens, const float *sink, int32_t window,
+                                    float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                    int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                    const sinkattn_params *params, void *workspace,
+                                    size_t workspace_bytes, void *out, float *lse,
+                                    sinkattn_stream_t stream);
+
+/*
  * sinkattn_decode_noalloc -- sinkattn_decode for callers that cannot allocate.
  *
  * This entry point has no counterpart in the report; it exists for callers that

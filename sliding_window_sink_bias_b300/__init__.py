@@ -26,6 +26,7 @@ EXPORTED = (
     "sinkattn_decode", "sinkattn_decode_ex", "sinkattn_status_string",
     "sinkattn_get_device_status", "sinkattn_version", "sinkattn_decode_noalloc",
     "sinkattn_prefill_backward_workspace_size", "sinkattn_prefill_backward",
+    "sinkattn_decode_fp8",
 )
 
 # bytes of the library's fixed decode scratch (include/sinkattn.h)
@@ -72,13 +73,15 @@ def lib() -> ctypes.CDLL:
         L.sinkattn_prefill_backward.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
                                                 ctypes.POINTER(Params), P, P, P, P,
                                                 ctypes.c_size_t, P, P, P, P, P]
+        L.sinkattn_decode_fp8.argtypes = [P, P, P, P, P, P, P, i32, f32, i32, i32, i32, i32, i32,
+                                          i32, ctypes.POINTER(Params), P, ctypes.c_size_t, P, P, P]
         L.sinkattn_status_string.argtypes = [i32]
         L.sinkattn_status_string.restype = ctypes.c_char_p
         L.sinkattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.sinkattn_version.restype = i32
         for name in ("sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode",
                      "sinkattn_decode_ex", "sinkattn_get_device_status", "sinkattn_decode_noalloc",
-                     "sinkattn_prefill_backward"):
+                     "sinkattn_prefill_backward", "sinkattn_decode_fp8"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -231,6 +234,45 @@ def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, ro
     else:
         st = lib().sinkattn_decode_ex(*args, ctypes.byref(p), *tail)
     _check("sinkattn_decode", st)
+    return out, lse
+
+
+def decode_fp8(q, kcache, vcache, k_scale, v_scale, seqlens, sink, *, max_seqlen: int,
+               window: int, rope_base: float, workspace=None, out=None, lse=None, scale=None,
+               rope_style: int = 0, rope_off: bool = False, stream=None):
+    """MTP-verify decode over an FP8 (E4M3) cache: kcache [B, S_cap, Hkv, 192] and
+    vcache [B, S_cap, Hkv, 128] as torch.float8_e4m3fn (or uint8 bit patterns),
+    k_scale / v_scale fp32 [Hkv] (key = e4m3 * k_scale[kv head]).  Other arguments
+    and the results as decode()."""
+    _require(q, "q", torch.bfloat16, 4)
+    for name, t in (("kcache", kcache), ("vcache", vcache)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or \
+                t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must be a 4-dim CUDA float8_e4m3fn/uint8 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _require(k_scale, "k_scale", torch.float32, 1)
+    _require(v_scale, "v_scale", torch.float32, 1)
+    _require(seqlens, "seqlens", torch.int32, 1)
+    _require(sink, "sink", torch.float32, 1)
+    b, t, hq, dqk = q.shape
+    s_cap, hkv = kcache.shape[1], kcache.shape[2]
+    if dqk != 192 or kcache.shape != (b, s_cap, hkv, 192) or vcache.shape != (b, s_cap, hkv, 128):
+        raise ValueError("expected q [B,T,Hq,192], kcache [B,S,Hkv,192], vcache [B,S,Hkv,128]")
+    need = decode_workspace_size(b, t, hq, hkv, max_seqlen, window)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(b, t, hq, 128, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(b, t, hq, dtype=torch.float32, device=q.device)
+    p = _params(scale, rope_style, rope_off)
+    st = lib().sinkattn_decode_fp8(
+        _ptr(q), kcache.data_ptr(), vcache.data_ptr(), _ptr(k_scale), _ptr(v_scale),
+        _ptr(seqlens), _ptr(sink), int(window), float(rope_base), b, t, s_cap, int(max_seqlen),
+        hq, hkv, None if p is None else ctypes.byref(p), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
+    _check("sinkattn_decode_fp8", st)
     return out, lse
 
 

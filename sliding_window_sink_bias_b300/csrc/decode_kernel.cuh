@@ -56,6 +56,7 @@ struct DecArgs {
   int32_t n_sub, n_k;
   int32_t kv_ring;        // 1: the cache is a ring of S_cap slots, position j at slot j % S_cap
   int32_t rope_on, rope_style;
+  const float *k_scale, *v_scale;  // FP8 cache: per-KV-head dequantisation scales
   uint32_t q_tx_bytes;
   float scale_log2;       // > 0
   const int32_t *seqlens;
@@ -189,28 +190,156 @@ __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
   }
 }
 
-struct DecLayout {
+// Shared memory of the decode kernel.  bf16 cache: four K/V stages the TMA
+// fills directly.  FP8 cache: four staging slots of raw E4M3 rows (TMA) and two
+// fp16 K/V stages the conversion warps fill for the MMA.
+template <bool F8>
+struct DecLayoutT {
+  static constexpr int32_t S = F8 ? 2 : kDecStages;   // K/V stages the MMA reads
+  static constexpr int32_t S8 = F8 ? 4 : 0;           // FP8 staging slots
   static constexpr uint32_t kKBox = kDecBN * kRowBytes;    // 64 keys x 64 dims: 8 KB
   static constexpr uint32_t kQOff = 0;                     // 128 rows x 3 boxes: 48 KB
   static constexpr uint32_t kKVOff = kQStageBytes;
   static constexpr uint32_t kKVStage = 5 * kKBox;          // K: 3 boxes, V: 2 boxes
-  static constexpr uint32_t kBarOff = kKVOff + kDecStages * kKVStage;
-  // q_full q_ready q_empty | kv_full[S] k_ready[S] kv_empty[S] | s_full[2] p_full[2] pv_done o_empty drain
-  static constexpr uint32_t kNumBars = 3 + 3 * kDecStages + 7;
+  static constexpr uint32_t kK8 = kDecBN * kDqk;           // 64 keys x 192 E4M3: 12 KB
+  static constexpr uint32_t kStg = kK8 + kDecBN * kDv;     // + 64 x 128 E4M3: 20 KB
+  static constexpr uint32_t kStgOff = kKVOff + S * kKVStage;
+  static constexpr uint32_t kBarOff = kStgOff + S8 * kStg;
+  // q_full q_ready q_empty | kv_full[S] k_ready[S] kv_empty[S] | s_full[2] p_full[2] pv_done
+  // o_empty drain | stg_full[S8] stg_empty[S8]
+  static constexpr uint32_t kNumBars = 3 + 3 * S + 7 + 2 * S8;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag, cursor
   static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;  // + cursor[4]
   static constexpr uint32_t kBytes = kTurnsOff + 32 * 8;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
-static_assert(DecLayout::kDynSmem <= 232448, "decode kernel shared memory");
+using DecLayout = DecLayoutT<false>;
+static_assert(DecLayoutT<false>::kDynSmem <= 232448, "decode kernel shared memory");
+static_assert(DecLayoutT<true>::kDynSmem <= 232448, "decode kernel shared memory (FP8)");
 
-__global__ void __launch_bounds__(kThreads, 1)
+// ---------------------------------------------------------------- FP8 cache
+// Two E4M3 values (the low byte first) -> f16x2; exact (E4M3 is a subset of f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t d;
+  const uint16_t v = static_cast<uint16_t>(two);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+  return d;
+}
+__device__ __forceinline__ uint4 e4m3x8_to_f16(uint2 v) {
+  return make_uint4(e4m3x2_to_f16x2(v.x & 0xffffu), e4m3x2_to_f16x2(v.x >> 16),
+                    e4m3x2_to_f16x2(v.y & 0xffffu), e4m3x2_to_f16x2(v.y >> 16));
+}
+__device__ __forceinline__ float f16lo(uint32_t w) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(w));
+  return f;
+}
+// Element e (0..7) of an 8 x f16 chunk held as four words.
+__device__ __forceinline__ float f16_at(const uint32_t (&w)[4], int e) {
+  return (e & 1) ? f16hi(w[e >> 1]) : f16lo(w[e >> 1]);
+}
+
+// One FP8 K/V block of 64 keys (staging: 64 rows of 192 E4M3 K values, then 64
+// rows of 128 E4M3 V values) -> the fp16 stage the MMA reads, in the layout the
+// TMA gives a bf16 block (K in 3 boxes, V in 2, 128-byte rows, 128-byte
+// swizzle): RoPE on K dims 0..63 at positions kp + row, V rows outside [r0, r1)
+// (keys no query sees) written as zeros.  nthr threads.
+__device__ void dec_convert_fp8(const uint8_t *stg, uint8_t *kv, int32_t kp, int32_t r0, int32_t r1,
+                                bool rope_on, int32_t style, const unsigned long long *turns,
+                                int32_t tid, int32_t nthr) {
+  constexpr uint32_t kBox = kDecBN * kRowBytes;
+  constexpr uint32_t kK8 = kDecBN * kDqk;
+  // K dims 64..191 (boxes 1, 2) and V (boxes 3, 4): chunks of 8 values
+#pragma unroll 2
+  for (int32_t u = tid; u < kDecBN * 32; u += nthr) {
+    const int32_t r = (u >> 5), c = u & 31;
+    if (c < 16) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(stg + r * kDqk + 64 + c * 8);
+      *swz_chunk(kv + (1 + (c >> 3)) * kBox, r, c & 7) = e4m3x8_to_f16(v);
+    } else {
+      const int32_t cv = c - 16;
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (r >= r0 && r < r1)
+        o = e4m3x8_to_f16(*reinterpret_cast<const uint2 *>(stg + kK8 + r * kDv + cv * 8));
+      *swz_chunk(kv + (3 + (cv >> 3)) * kBox, r, cv & 7) = o;
+    }
+  }
+  // K dims 0..63 (box 0), rotated
+  if (!rope_on || style == 0) {
+    for (int32_t u = tid; u < kDecBN * 8; u += nthr) {
+      const int32_t r = u >> 3, c = u & 7;
+      const uint4 v4 = e4m3x8_to_f16(*reinterpret_cast<const uint2 *>(stg + r * kDqk + c * 8));
+      uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+      if (rope_on) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float cs, sn;
+          rope_cs(kp + r, turns[4 * c + e], cs, sn);
+          const float x = f16lo(w[e]), y = f16hi(w[e]);
+          w[e] = pack_f16x2(x * cs - y * sn, x * sn + y * cs);
+        }
+      }
+      *swz_chunk(kv, r, c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    // pairs (t, t+32): chunk c (dims 8c..8c+7) with chunk c + 4
+    for (int32_t u = tid; u < kDecBN * 4; u += nthr) {
+      const int32_t r = u >> 2, c = u & 3;
+      const uint4 a4 = e4m3x8_to_f16(*reinterpret_cast<const uint2 *>(stg + r * kDqk + c * 8));
+      const uint4 b4 = e4m3x8_to_f16(*reinterpret_cast<const uint2 *>(stg + r * kDqk + (c + 4) * 8));
+      const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w}, b[4] = {b4.x, b4.y, b4.z, b4.w};
+      uint32_t oa[4], ob[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        float cs0, sn0, cs1, sn1;
+        rope_cs(kp + r, turns[8 * c + e], cs0, sn0);
+        rope_cs(kp + r, turns[8 * c + e + 1], cs1, sn1);
+        const float x0 = f16_at(a, e), y0 = f16_at(b, e), x1 = f16_at(a, e + 1), y1 = f16_at(b, e + 1);
+        oa[e >> 1] = pack_f16x2(x0 * cs0 - y0 * sn0, x1 * cs1 - y1 * sn1);
+        ob[e >> 1] = pack_f16x2(x0 * sn0 + y0 * cs0, x1 * sn1 + y1 * cs1);
+      }
+      *swz_chunk(kv, r, c) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+      *swz_chunk(kv, r, c + 4) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    }
+  }
+}
+
+// The Q tile's rows [0, R) to fp16 in place: boxes 1 and 2, and box 0 unless
+// the RoPE pass has already written it as fp16.  nthr threads.
+__device__ void dec_q_to_f16(uint8_t *q, int32_t R, bool box0, int32_t tid, int32_t nthr) {
+  const int32_t first = box0 ? 0 : 1;
+  const int32_t nch = (3 - first) * 8;
+  for (int32_t u = tid; u < R * nch; u += nthr) {
+    const int32_t r = u / nch, c = u % nch + first * 8;
+    uint4 *p = reinterpret_cast<uint4 *>(q + (c >> 3) * kQBoxBytes + r * kRowBytes + (c & 7) * 16);
+    const uint4 v = *p;
+    *p = make_uint4(pack_f16x2(bf16lo(v.x), bf16hi(v.x)), pack_f16x2(bf16lo(v.y), bf16hi(v.y)),
+                    pack_f16x2(bf16lo(v.z), bf16hi(v.z)), pack_f16x2(bf16lo(v.w), bf16hi(v.w)));
+  }
+}
+
+// Threads: 384 (bf16 cache) or 512 (FP8 cache: warps 12-15 join the
+// conversion of the cache blocks).
+template <bool F8>
+struct DecThreads {
+  static constexpr int32_t kAll = F8 ? 512 : kThreads;
+  static constexpr int32_t kConv = kAll - 256;  // warps 8.. : RoPE / conversion
+};
+
+template <bool F8>
+__global__ void __launch_bounds__(512, 1)
     sinkattn_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ DecArgs args) {
-  using Ly = DecLayout;
-  constexpr int32_t S = kDecStages;
+  using Ly = DecLayoutT<F8>;
+  constexpr int32_t S = Ly::S;
+  constexpr int32_t S8 = Ly::S8;
   constexpr int32_t BN = kDecBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -229,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t B_PVDONE = bar(3 + 3 * S + 4);
   const uint32_t B_OEMPTY = bar(3 + 3 * S + 5);
   const uint32_t B_DRAIN = bar(3 + 3 * S + 6);
+  auto B_STGFULL = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + s8); };
+  auto B_STGEMPTY = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + S8 + s8); };
 
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
@@ -238,11 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     mbar_init(B_QFULL, 1);
-    mbar_init(B_QREADY, 128);
+    mbar_init(B_QREADY, DecThreads<F8>::kConv);
     mbar_init(B_QEMPTY, 1);
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(B_KVFULL(s), 1);
-      mbar_init(B_KREADY(s), 128);
+      mbar_init(B_KREADY(s), DecThreads<F8>::kConv);
       mbar_init(B_KVEMPTY(s), 1);
     }
     for (uint32_t b = 0; b < 2; ++b) {
@@ -252,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(B_PVDONE, 1);
     mbar_init(B_OEMPTY, 128);
     mbar_init(B_DRAIN, 1);
+    for (uint32_t s8 = 0; s8 < static_cast<uint32_t>(S8); ++s8) {
+      mbar_init(B_STGFULL(s8), 1);
+      mbar_init(B_STGEMPTY(s8), DecThreads<F8>::kConv);
+    }
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -262,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 3) dec_locate(args, lane, cur_smem);
   // The Q tile has T * G rows; the MMA reads all 128, so the rest stay zero.
-  for (uint32_t i = threadIdx.x; i < kQStageBytes / 16; i += kThreads)
+  for (uint32_t i = threadIdx.x; i < kQStageBytes / 16; i += DecThreads<F8>::kAll)
     reinterpret_cast<uint4 *>(smem + Ly::kQOff)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -299,6 +434,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t kpos0 = sg.lo + sg.blk0 * BN;
         const int32_t krow0 = sg.b * args.S_cap + kpos0;
         for (int32_t j = 0; j < sg.nblk; ++j) {
+          if constexpr (F8) {
+            // raw E4M3 rows into a staging slot; the conversion warps fill the MMA's stage
+            const uint32_t s8 = gk % S8;
+            if (!(ok = wait_bar(B_STGEMPTY(s8), ((gk / S8) & 1) ^ 1, abort_flag, 2))) break;
+            mbar_arrive_expect_tx(B_STGFULL(s8), Ly::kStg);
+            const uint32_t dst = sbase + Ly::kStgOff + s8 * Ly::kStg;
+            tma_load_3d(dst, &tm_k, 0, sg.kvh, krow0 + j * BN, B_STGFULL(s8));
+            tma_load_3d(dst + Ly::kK8, &tm_v, 0, sg.kvh, krow0 + j * BN, B_STGFULL(s8));
+            ++gk;
+            continue;
+          }
           const uint32_t st = gk % S;
           if (!(ok = wait_bar(B_KVEMPTY(st), ((gk / S) & 1) ^ 1, abort_flag, 2))) break;
           mbar_arrive_expect_tx(B_KVFULL(st), Ly::kKVStage);
@@ -330,16 +476,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (gq > 0) drain_wait(B_QFULL, (gq - 1) & 1);
-      for (uint32_t s = 0; s < S; ++s)
-        if (gk > s) drain_wait(B_KVFULL(s), ((gk - 1 - s) / S) & 1);
+      if constexpr (F8) {
+        for (uint32_t s8 = 0; s8 < static_cast<uint32_t>(S8); ++s8)
+          if (gk > s8) drain_wait(B_STGFULL(s8), ((gk - 1 - s8) / S8) & 1);
+      } else {
+        for (uint32_t s = 0; s < S; ++s)
+          if (gk > s) drain_wait(B_KVFULL(s), ((gk - 1 - s) / S) & 1);
+      }
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
       const uint32_t rot = args.rope_on ? 0u : 1u;  // rotated dims are fp16
-      const uint32_t kIdQK = idesc_f32acc(128, BN, 1, 0, 0);
-      const uint32_t kIdQKRot = idesc_f32acc(128, BN, rot, 0, 0);
-      constexpr uint32_t kIdPV = idesc_f32acc(128, kDv, 1, 0, 1);
+      // FP8 cache: every operand (Q, the converted K and V, P) is fp16
+      const uint32_t kIdQK = idesc_f32acc(128, BN, F8 ? 0 : 1, 0, 0);
+      const uint32_t kIdQKRot = idesc_f32acc(128, BN, F8 ? 0 : rot, 0, 0);
+      constexpr uint32_t kIdPV = idesc_f32acc(128, kDv, F8 ? 0 : 1, 0, 1);
       constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
       const uint32_t q_lo = ((sbase + Ly::kQOff) >> 4) | (1u << 16);
       const uint32_t kv_lo = ((sbase + Ly::kKVOff) >> 4) | (1u << 16);
@@ -371,6 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int32_t j = 0; ok && j < sg.nblk; ++j) {
           const uint32_t st = (gk + j) % S;
+          // FP8 cache: the conversion of block j+1 waits for the PV that last
+          // read its fp16 stage, so PV(j-1) goes out before block j's QK^T
+          // waits for block j's conversion
+          if constexpr (F8) {
+            if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
+          }
           if (!(ok = wait_bar(B_KREADY(st), ((gk + j) / S) & 1, abort_flag, 6))) break;
           tc_fence_after();
           const uint32_t s_t = tmem + ((gs + j) & 1) * BN;
@@ -384,7 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = true;
           mma_commit(B_SFULL((gs + j) & 1));
           if (j == sg.nblk - 1) mma_commit(B_QEMPTY);
-          if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
+          if constexpr (!F8) {
+            if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
+          }
         }
         if (ok) ok = issue_pv(gs + sg.nblk - 1, (gk + sg.nblk - 1) % S, sg.nblk == 1);
         ++gq;
@@ -403,7 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const bool warp_active = (warp & 3) * 32 < R;  // the warp holds at least one real row
     const int32_t t = row / G, g = row % G;
-    const float sc = args.scale_log2;
     const int32_t W = args.window;
     uint32_t gs = 0, gpv = 0;
     bool ok = true;
@@ -420,6 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t qhi = min(pos, klast);
       // no visible key in this segment (or no such row): nothing is visible
       if (!rvalid || qhi < qlo) { qlo = 1 << 30; qhi = 1 << 30; }
+      // FP8 cache: the keys' scale folds into the logit scale, the values' into o
+      const float sc = args.scale_log2 * (F8 ? __ldg(args.k_scale + sg.kvh) : 1.f);
       float m = -INFINITY, l = 0.f;
       for (int32_t j = 0; ok && j < sg.nblk; ++j) {
         const uint32_t buf = gs & 1;
@@ -463,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    sc2, mneg2);
             const float2 p = make_float2(ex2(y.x), ex2(y.y));
             sum2 = fadd2(sum2, p);
-            r[k >> 1] = pack_bf16x2(p.x, p.y);
+            r[k >> 1] = F8 ? pack_f16x2(p.x, p.y) : pack_bf16x2(p.x, p.y);
           }
           tmem_st32p(s_t, r);  // P over the S columns already read
           const float alpha = (m_new == m) ? 1.f : ex2(m - m_new);
@@ -531,6 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             lse_v = (M + __log2f(Lw)) * kLn2;
           }
         }
+        // FP8 cache: the values' scale multiplies O (partials included: the
+        // combine is linear in O)
+        const float vs = F8 ? __ldg(args.v_scale + sg.kvh) : 1.f;
+        scale_o *= vs;
         const size_t orow = (static_cast<size_t>(sg.b) * args.T + t) * args.Hq + head;
         const size_t prow = (static_cast<size_t>(blockIdx.x) * 2 + (sg.first ? 0 : 1)) * R + row;
 #pragma unroll 1
@@ -555,8 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kDv + cb);
 #pragma unroll
               for (int32_t q4 = 0; q4 < 8; ++q4)
-                dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
-                                      __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+                dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * vs, __uint_as_float(o[4 * q4 + 1]) * vs,
+                                      __uint_as_float(o[4 * q4 + 2]) * vs, __uint_as_float(o[4 * q4 + 3]) * vs);
             }
           }
         }
@@ -579,8 +744,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     DecSeg sg;
     while (ok && dec_next(c, args, sg)) {
       if (!(ok = wait_bar_warp(B_QFULL, gq & 1, abort_flag, 10))) break;
-      if (args.rope_on)
+      if (args.rope_on && tid < 128)
         rope_q_tile(smem + Ly::kQOff, G, args.T, sg.L - args.T, args.rope_style, turns, tid);
+      if constexpr (F8) {
+        // every MMA operand is fp16 with an FP8 cache (the rotation above
+        // already wrote box 0 as fp16; the conversion touches the other boxes)
+        dec_q_to_f16(smem + Ly::kQOff, R, !args.rope_on, tid, DecThreads<F8>::kConv);
+      }
       fence_proxy_async_smem();
       mbar_arrive(B_QREADY);
       ++gq;
@@ -589,6 +759,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t vis_lo = args.window > 0 ? max(0, sg.L - args.T - args.window + 1) : 0;
       for (int32_t j = 0; j < sg.nblk; ++j) {
         const uint32_t st = gk % S;
+        if constexpr (F8) {
+          const uint32_t s8 = gk % S8;
+          if (!(ok = wait_bar_warp(B_STGFULL(s8), (gk / S8) & 1, abort_flag, 11))) break;
+          // the fp16 stage is free once the PV that last read it completed
+          if (!(ok = wait_bar_warp(B_KVEMPTY(st), ((gk / S) & 1) ^ 1, abort_flag, 12))) break;
+          const int32_t kp = kpos0 + j * BN;
+          const int32_t r0 = min(BN, max(0, vis_lo - kp)), r1 = max(r0, min(BN, sg.L - kp));
+          dec_convert_fp8(smem + Ly::kStgOff + s8 * Ly::kStg, smem + Ly::kKVOff + st * Ly::kKVStage, kp,
+                          r0, r1, args.rope_on, args.rope_style, turns, tid, DecThreads<F8>::kConv);
+          fence_proxy_async_smem();
+          mbar_arrive(B_STGEMPTY(s8));
+          mbar_arrive(B_KREADY(st));
+          ++gk;
+          continue;
+        }
         if (!(ok = wait_bar_warp(B_KVFULL(st), (gk / S) & 1, abort_flag, 11))) break;
         uint8_t *kv = smem + Ly::kKVOff + st * Ly::kKVStage;
         const int32_t kp = kpos0 + j * BN;

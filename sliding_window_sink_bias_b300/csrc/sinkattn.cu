@@ -477,13 +477,34 @@ size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_he
   return decode_plan(batch, T, num_q_heads, num_kv_heads).bytes;
 }
 
-sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void *vcache,
+// A 3-D tensor map over rows of `heads` x `dim_bytes` E4M3 bytes: dims
+// (dim_bytes, heads, rows), a box of one head's whole row x box_rows, no swizzle
+// (the conversion warps read it as plain rows).
+bool make_map_u8(CUtensorMap *m, const void *base, uint64_t dim_bytes, uint64_t heads, uint64_t rows,
+                 uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t gdim[3] = {dim_bytes, heads, rows};
+  const cuuint64_t gstride[2] = {dim_bytes, dim_bytes * heads};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(dim_bytes), 1, box_rows};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), gdim, gstride,
+                        box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Shared by the bf16 and the FP8 decode (k_scale != nullptr: the cache holds
+// E4M3 values, dequantised as value * scale[kv head]).
+static sinkattn_status decode_impl(const void *q, const void *kcache, const void *vcache,
                                    const int32_t *seqlens, const float *sink, int32_t window,
                                    float rope_base, int32_t batch, int32_t T, int32_t S_cap,
                                    int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
                                    const sinkattn_params *params, void *workspace,
                                    size_t workspace_bytes, void *out, float *lse,
-                                   sinkattn_stream_t stream) {
+                                   sinkattn_stream_t stream, const float *k_scale,
+                                   const float *v_scale) {
+  const bool fp8 = k_scale != nullptr;
   if (batch < 0 || T <= 0 || S_cap <= 0 || max_seqlen < 0 || window < 0) return SINKATTN_EINVAL;
   const bool ring = params && params->kv_ring;
   if (params && params->kv_ring != 0 && params->kv_ring != 1) return SINKATTN_EINVAL;
@@ -502,6 +523,7 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
     return SINKATTN_EUNSUPPORTED;
   if (batch == 0) return SINKATTN_OK;
   if (!q || !kcache || !vcache || !seqlens || !sink || !out || !lse) return SINKATTN_EINVAL;
+  if (fp8 && (ring || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4))) return SINKATTN_EINVAL;
   if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(vcache, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(sink, 4) || !aligned(seqlens, 4))
     return SINKATTN_EINVAL;
@@ -526,6 +548,8 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
   d.S_cap = S_cap;
   d.n_units = batch * num_kv_heads;
   d.kv_ring = ring ? 1 : 0;
+  d.k_scale = k_scale;
+  d.v_scale = v_scale;
   d.rope_on = a.rope_on;
   d.rope_style = a.rope_style;
   d.q_tx_bytes = 3u * 64u * 2u * static_cast<uint32_t>(G * T);
@@ -545,8 +569,12 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, num_q_heads, uint64_t(batch) * T, G, T) ||
-      !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1, ring ? 16 : sa::kDecBN) ||
-      !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1, ring ? 16 : sa::kDecBN))
+      (fp8 ? !make_map_u8(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, sa::kDecBN)
+           : !make_map(&mk, kcache, 192, num_kv_heads, uint64_t(batch) * S_cap, 1,
+                       ring ? 16 : sa::kDecBN)) ||
+      (fp8 ? !make_map_u8(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, sa::kDecBN)
+           : !make_map(&mv, vcache, 128, num_kv_heads, uint64_t(batch) * S_cap, 1,
+                       ring ? 16 : sa::kDecBN)))
     return SINKATTN_ECUDA;
   // upper bound of the blocks: every unit sees at most max_seqlen (window: T + W - 1) keys,
   // plus up to 15 before them when a ring cache aligns its first block
@@ -561,16 +589,52 @@ sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void
   const int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_blocks, cap / d.n_sub)));
   const int grid = groups * d.n_sub;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto kern = sa::sinkattn_decode_kernel;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sa::DecLayout::kDynSmem)) != cudaSuccess)
-    return SINKATTN_ECUDA;
-  kern<<<grid, sa::kThreads, sa::DecLayout::kDynSmem, s>>>(mq, mk, mv, d);
+  if (fp8) {
+    auto kern = sa::sinkattn_decode_kernel<true>;
+    constexpr uint32_t smem = sa::DecLayoutT<true>::kDynSmem;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return SINKATTN_ECUDA;
+    kern<<<grid, sa::DecThreads<true>::kAll, smem, s>>>(mq, mk, mv, d);
+  } else {
+    auto kern = sa::sinkattn_decode_kernel<false>;
+    constexpr uint32_t smem = sa::DecLayoutT<false>::kDynSmem;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return SINKATTN_ECUDA;
+    kern<<<grid, sa::kThreads, smem, s>>>(mq, mk, mv, d);
+  }
   if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
 
   sa::sinkattn_decode_combine_kernel<<<dim3(static_cast<unsigned>(d.n_units), sa::kCombParts),
                                        sa::kCombThreads, 0, s>>>(d, grid);
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+}
+
+sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void *vcache,
+                                   const int32_t *seqlens, const float *sink, int32_t window,
+                                   float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                   int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                   const sinkattn_params *params, void *workspace,
+                                   size_t workspace_bytes, void *out, float *lse,
+                                   sinkattn_stream_t stream) {
+  return decode_impl(q, kcache, vcache, seqlens, sink, window, rope_base, batch, T, S_cap,
+                     max_seqlen, num_q_heads, num_kv_heads, params, workspace, workspace_bytes,
+                     out, lse, stream, nullptr, nullptr);
+}
+
+sinkattn_status sinkattn_decode_fp8(const void *q, const void *kcache, const void *vcache,
+                                    const float *k_scale, const float *v_scale,
+                                    const int32_t *seqlens, const float *sink, int32_t window,
+                                    float rope_base, int32_t batch, int32_t T, int32_t S_cap,
+                                    int32_t max_seqlen, int32_t num_q_heads, int32_t num_kv_heads,
+                                    const sinkattn_params *params, void *workspace,
+                                    size_t workspace_bytes, void *out, float *lse,
+                                    sinkattn_stream_t stream) {
+  if (!k_scale || !v_scale) return SINKATTN_EINVAL;
+  return decode_impl(q, kcache, vcache, seqlens, sink, window, rope_base, batch, T, S_cap,
+                     max_seqlen, num_q_heads, num_kv_heads, params, workspace, workspace_bytes,
+                     out, lse, stream, k_scale, v_scale);
 }
 
 sinkattn_status sinkattn_decode(const void *q, const void *kcache, const void *vcache,

@@ -131,6 +131,9 @@ WORKLOADS = {
                                  len_lo=65536, len_hi=262144, **GA),
     "mtp_decode_swa_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=262144,
                                   len_lo=65536, len_hi=262144, **SWA),
+    # the GA decode batch over an FP8 (E4M3) cache, one scale per KV head
+    "mtp_decode_ga_fp8_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=262144, fp8=True,
+                                     len_lo=65536, len_hi=262144, **GA),
     # the same SWA layer with the KV cache an SWA layer needs: a ring of 144
     # slots (>= W + T - 1 = 131, a multiple of 16) per sequence
     "mtp_decode_swa_ring_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=144, kv_ring=True,

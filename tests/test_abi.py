@@ -22,7 +22,7 @@ def L():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"\b(sinkattn_[a-z_]+)\s*\(", text)
+    names = re.findall(r"\b(sinkattn_[a-z0-9_]+)\s*\(", text)
     return sorted(set(names))
 
 
@@ -174,3 +174,21 @@ def test_ring_cache_argument_checks(L):
     st = L.sinkattn_prefill_ex(f(1), f(1), f(1), f(1), f(1), 1, 16, 16, 64, 8, 128, 1e4,
                                ctypes.byref(p), f(1), f(1), None)
     assert st == sa.EINVAL
+
+
+def test_fp8_decode_argument_checks(L):
+    """The FP8 decode needs both scale vectors and has no ring-cache form."""
+    import sliding_window_sink_bias_b300 as sa
+    P = ctypes.c_void_p
+    f = lambda x: P(256 * x)
+    ws = L.sinkattn_decode_workspace_size(2, 4, 64, 4, 100, 0)
+
+    def dec(ks=1, vs=1, ring=0, window=0, s_cap=256):
+        p = sa.Params(0.0, 0, 0, ring)
+        return L.sinkattn_decode_fp8(f(1), f(1), f(1), None if ks is None else f(ks),
+                                     None if vs is None else f(vs), f(1), f(1), window, 5e6, 2, 4,
+                                     s_cap, 100, 64, 4, ctypes.byref(p), f(1), ws, f(1), f(1), None)
+
+    assert dec(ks=None) == sa.EINVAL
+    assert dec(vs=None) == sa.EINVAL
+    assert dec(ring=1, window=128) == sa.EINVAL
