@@ -191,12 +191,13 @@ __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
 }
 
 // Shared memory of the decode kernel.  bf16 cache: four K/V stages the TMA
-// fills directly.  FP8 cache: four staging slots of raw E4M3 rows (TMA) and two
-// fp16 K/V stages the conversion warps fill for the MMA.
+// fills directly.  FP8 cache: two staging slots of raw E4M3 rows (TMA; half the
+// bytes of a bf16 block each) and three fp16 K/V stages the conversion warps
+// fill for the MMA.
 template <bool F8>
 struct DecLayoutT {
-  static constexpr int32_t S = F8 ? 2 : kDecStages;   // K/V stages the MMA reads
-  static constexpr int32_t S8 = F8 ? 4 : 0;           // FP8 staging slots
+  static constexpr int32_t S = F8 ? 3 : kDecStages;   // K/V stages the MMA reads
+  static constexpr int32_t S8 = F8 ? 2 : 0;           // FP8 staging slots
   static constexpr uint32_t kKBox = kDecBN * kRowBytes;    // 64 keys x 64 dims: 8 KB
   static constexpr uint32_t kQOff = 0;                     // 128 rows x 3 boxes: 48 KB
   static constexpr uint32_t kKVOff = kQStageBytes;
