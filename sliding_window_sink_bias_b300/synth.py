@@ -158,6 +158,10 @@ WORKLOADS = {
     "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),
     "mtp_decode_ga_b8_t4": dict(kind="decode", batch=8, t=4, s_cap=131072,
                                 len_lo=65536, len_hi=131072, **GA),
+    "mtp_decode_ga_fp8_b8_t4": dict(kind="decode", batch=8, t=4, s_cap=131072, fp8=True,
+                                    len_lo=65536, len_hi=131072, **GA),
+    "swa_backward_1x32768": dict(kind="backward", seqlens=[32768], **SWA),
+    "ga_backward_1x8192": dict(kind="backward", seqlens=[8192], **GA),
 }
 
 
