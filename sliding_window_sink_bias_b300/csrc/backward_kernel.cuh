@@ -27,16 +27,16 @@
 //                     shared-memory tiles read N-major); epilogue as above.
 //   bwd_dsink_kernel  the per-chunk partials summed in chunk order.
 //
-// The MMA kernels are synchronous (one batch of MMAs in flight; the next K/V
-// block or Q sub-tile is prefetched by TMA while the current one is worked
-// on), 128 threads, one row per thread (TMEM lane); every wait is bounded and
-// every CTA-wide decision is taken with __syncthreads_and.
+// The MMA kernels run 4 warps that own one row each (TMEM lane), a fifth warp
+// whose first thread issues the MMAs and a sixth whose first thread issues the
+// copies, so neither the rows nor the MMAs wait for the other issuing; every
+// wait is bounded and every CTA-wide decision is taken with __syncthreads_and.
 #pragma once
 #include "common.cuh"
 
 namespace sa {
 
-constexpr int32_t kBwdThreads = 128;
+constexpr int32_t kBwdThreads = 192;  // dq / dkdv: 4 row warps, an MMA warp, a copy warp
 constexpr int32_t kBwdChunk = 32;    // tokens per pre-pass CTA
 constexpr int32_t kDqBN = 64;        // keys per block (dq kernel)
 constexpr int32_t kKvBN = 128;       // keys per block (dkdv kernel)
@@ -217,41 +217,95 @@ __device__ __forceinline__ void bwd_store_qk_row(uint32_t t_col, float scale, bo
 }
 
 // ------------------------------------------------------------------ dQ kernel
+// Work item of the dq kernel: one tile of 128/G query tokens x G heads of one
+// KV head, over the 64-key blocks [lo, hi] its rows see.
+struct DqItem {
+  int32_t s0, L, t0, lo, nblk, kvh;
+  bool valid;
+};
+
+__device__ __forceinline__ DqItem dq_item(const BwdArgs &a, int32_t it) {
+  DqItem d{};
+  d.valid = false;
+  const int32_t T = 128 / a.G;
+  const int32_t per_seq = a.Hkv * a.dq_tiles;
+  const int32_t b = it / per_seq, rem = it % per_seq;
+  d.kvh = rem % a.Hkv;
+  // global: tiles in order (windowed) or longest first (causal)
+  const int32_t tile = a.window > 0 ? rem / a.Hkv : a.dq_tiles - 1 - rem / a.Hkv;
+  d.s0 = __ldg(a.cu_seqlens + b);
+  d.L = __ldg(a.cu_seqlens + b + 1) - d.s0;
+  d.t0 = tile * T;
+  if (d.t0 >= d.L) return d;
+  d.lo = a.window > 0 ? max(0, d.t0 - a.window + 1) : 0;
+  const int32_t hi = min(d.L, d.t0 + T) - 1;
+  d.nblk = (hi - d.lo + kDqBN) / kDqBN;
+  d.valid = true;
+  return d;
+}
+
+// The first item at or after `it` (stride gridDim.x) that has rows; `d` gets
+// it (d.valid false when the CTA has no more).
+__device__ __forceinline__ int32_t dq_next_item(const BwdArgs &a, int32_t it, DqItem &d) {
+  d.valid = false;
+  for (; it < a.dq_items; it += gridDim.x) {
+    d = dq_item(a, it);
+    if (d.valid) break;
+  }
+  return it;
+}
+
 struct DqLayout {
+  static constexpr int32_t kStages = 3;                  // K/V blocks in flight
   static constexpr uint32_t kQBox = 128 * kRowBytes;     // 128 rows x 64 dims: 16 KB
   static constexpr uint32_t kKBox = kDqBN * kRowBytes;   // 64 keys x 64 dims: 8 KB
   static constexpr uint32_t kQOff = 0;                   // q_rot tile: 3 boxes
   static constexpr uint32_t kDoOff = 3 * kQBox;          // dO tile: 2 boxes
   static constexpr uint32_t kStOff = 5 * kQBox;          // stages: K 3 boxes, V 2 boxes
   static constexpr uint32_t kStage = 5 * kKBox;
-  static constexpr uint32_t kBarOff = kStOff + 2 * kStage;  // qf, kv[2], mm1, mm2
-  static constexpr uint32_t kMiscOff = kBarOff + 5 * 8;      // tmem slot, abort flag
+  static constexpr uint32_t kBarOff = kStOff + kStages * kStage;  // qf, kv[3], mm1[2], mm2
+  static constexpr uint32_t kMiscOff = kBarOff + 7 * 8;           // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
 static_assert(DqLayout::kDynSmem <= 232448, "dq kernel shared memory");
+// TMEM of the dq kernel: S and dP of key block g in buffer g & 1 (S at 128 b,
+// dP at 128 b + 64), the dQ accumulator at 256..447.
+constexpr uint32_t kDqColAcc = 256;
 
+// Pipeline of the dq kernel (thread 128 issues the MMAs, thread 160 the
+// copies; threads 0..127 own one packed query row each):
+//   S(g+1), dP(g+1) are issued before the rows turn S(g), dP(g) into dS(g), so
+//   the tensor core works while they do; one CTA barrier per key block, after
+//   dS(g) is in TMEM, then dQ += dS(g) K(g).  K/V blocks stream through three
+//   stages, loaded two blocks ahead and across item boundaries; the next
+//   item's Q/dO tile is loaded once the last S/dP of the current item is done.
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ BwdArgs a) {
   using Ly = DqLayout;
+  constexpr int32_t NS = Ly::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int32_t warp = threadIdx.x >> 5;
-  const int32_t row = threadIdx.x;  // packed query row == TMEM lane
-  const bool issuer = threadIdx.x == 0;
-  const uint32_t B_QF = sbase + Ly::kBarOff, B_MM1 = B_QF + 24, B_MM2 = B_QF + 32;
+  const int32_t row = threadIdx.x;  // packed query row == TMEM lane (threads 0..127)
+  const bool compute = threadIdx.x < 128;
+  const bool issuer = threadIdx.x == 128;    // MMAs
+  const bool producer = threadIdx.x == 160;  // copies
+  const uint32_t B_QF = sbase + Ly::kBarOff;
   auto B_KV = [&](uint32_t s) { return B_QF + 8 + 8 * s; };
+  auto B_MM1 = [&](uint32_t b) { return B_QF + 8 + 8 * NS + 8 * b; };
+  const uint32_t B_MM2 = B_QF + 8 + 8 * NS + 16;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
   if (issuer) {
     mbar_init(B_QF, 1);
-    mbar_init(B_KV(0), 1);
-    mbar_init(B_KV(1), 1);
-    mbar_init(B_MM1, 1);
+    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s) mbar_init(B_KV(s), 1);
+    mbar_init(B_MM1(0), 1);
+    mbar_init(B_MM1(1), 1);
     mbar_init(B_MM2, 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -269,111 +323,136 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_t = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const int32_t G = a.G, T = 128 / G;
+  const int32_t G = a.G;
   const int32_t t_row = row / G, g_row = row % G;
   const uint32_t q_lo = ((sbase + Ly::kQOff) >> 4) | (1u << 16);
   const uint32_t do_lo = ((sbase + Ly::kDoOff) >> 4) | (1u << 16);
   constexpr uint32_t kIdS = idesc_f32acc(128, kDqBN, 1, 0, 0);
   constexpr uint32_t kIdQ = idesc_f32acc(128, kDqk, 1, 0, 1);
-  uint32_t n_qf = 0, n_kv[2] = {0, 0}, n_m1 = 0, n_m2 = 0, gk = 0;
+  // issue counts of every barrier, kept alike by all threads
+  uint32_t n_qf = 0, n_kv[NS] = {}, n_m1[2] = {0, 0}, n_m2 = 0;
   bool ok = true;
-  for (int32_t it = blockIdx.x; ok && it < a.dq_items; it += gridDim.x) {
-    // item -> (sequence, KV head, tile); global tiles longest first
-    const int32_t per_seq = a.Hkv * a.dq_tiles;
-    const int32_t b = it / per_seq, rem = it % per_seq;
-    const int32_t kvh = rem % a.Hkv;
-    const int32_t tile = a.window > 0 ? rem / a.Hkv : a.dq_tiles - 1 - rem / a.Hkv;
-    const int32_t s0 = __ldg(a.cu_seqlens + b), L = __ldg(a.cu_seqlens + b + 1) - s0;
-    const int32_t t0 = tile * T;
-    if (t0 >= L) continue;
-    const int32_t lo = a.window > 0 ? max(0, t0 - a.window + 1) : 0;
-    const int32_t hi = min(L, t0 + T) - 1;
-    const int32_t nblk = (hi - lo + kDqBN) / kDqBN;
-    // this thread's row
-    const int32_t ti = t0 + t_row, h = kvh * G + g_row;
-    const bool rvalid = ti < L;
-    const size_t grow = static_cast<size_t>(s0 + ti) * a.Hq + h;
-    const float lse2 = rvalid ? __ldg(a.lse + grow) * kLog2e : 0.f;
-    const float Drow = rvalid ? __ldg(a.D + grow) : 0.f;
-    if (issuer) {
+
+  // ---- K/V loader: walks this CTA's (item, block) sequence ahead of the rows
+  DqItem ld;
+  int32_t ld_it = dq_next_item(a, blockIdx.x, ld), ld_j = 0;
+  uint32_t ld_g = 0;  // global index of the next block to load
+  auto load_next = [&]() {
+    const uint32_t st = ld_g % NS;
+    if (producer) {
+      const uint32_t dst = sbase + Ly::kStOff + st * Ly::kStage;
+      const int32_t krow = ld.s0 + ld.lo + ld_j * kDqBN;
+      mbar_arrive_expect_tx(B_KV(st), Ly::kStage);
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc) tma_load_3d(dst + cc * Ly::kKBox, &tm_k, cc * 64, ld.kvh, krow, B_KV(st));
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, ld.kvh, krow, B_KV(st));
+    }
+    ++n_kv[st];
+    ++ld_g;
+    if (++ld_j >= ld.nblk) {
+      ld_j = 0;
+      ld_it = dq_next_item(a, ld_it + gridDim.x, ld);
+    }
+  };
+  auto load_q = [&](const DqItem &d) {
+    if (producer) {
       mbar_arrive_expect_tx(B_QF, 5 * Ly::kQBox);
 #pragma unroll
       for (int cc = 0; cc < 3; ++cc)
-        tma_load_3d(sbase + Ly::kQOff + cc * Ly::kQBox, &tm_q, cc * 64, kvh * G, s0 + t0, B_QF);
+        tma_load_3d(sbase + Ly::kQOff + cc * Ly::kQBox, &tm_q, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
-        tma_load_3d(sbase + Ly::kDoOff + cc * Ly::kQBox, &tm_do, cc * 64, kvh * G, s0 + t0, B_QF);
+        tma_load_3d(sbase + Ly::kDoOff + cc * Ly::kQBox, &tm_do, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
     }
     ++n_qf;
-    auto load_block = [&](int32_t j, uint32_t st) {
-      const uint32_t dst = sbase + Ly::kStOff + st * Ly::kStage;
-      const int32_t krow = s0 + lo + j * kDqBN;
-      mbar_arrive_expect_tx(B_KV(st), Ly::kStage);
-#pragma unroll
-      for (int cc = 0; cc < 3; ++cc) tma_load_3d(dst + cc * Ly::kKBox, &tm_k, cc * 64, kvh, krow, B_KV(st));
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-        tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, kvh, krow, B_KV(st));
-    };
-    if (issuer) load_block(0, gk & 1);
-    ++n_kv[gk & 1];
-    ok = wait_bar(B_QF, (n_qf - 1) & 1, abort_flag, 20);
-    ok = __syncthreads_and(ok);
-    for (int32_t j = 0; ok && j < nblk; ++j, ++gk) {
-      const uint32_t st = gk & 1;
-      if (j + 1 < nblk) {
-        if (issuer) load_block(j + 1, st ^ 1);
-        ++n_kv[st ^ 1];
-      }
-      ok = wait_bar(B_KV(st), (n_kv[st] - 1) & 1, abort_flag, 21);
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
+  };
+  // S(g) = Q K^T and dP(g) = dO V^T into buffer g & 1 (issued only while
+  // `go`; K/V(g) must be the latest load of its stage).  The counts move on
+  // every thread either way.
+  auto issue_sdp = [&](uint32_t g, bool go) -> bool {
+    const uint32_t st = g % NS, buf = g & 1;
+    ++n_m1[buf];
+    if (issuer && go) {
+      if (!wait_bar(B_KV(st), (n_kv[st] - 1) & 1, abort_flag, 21)) return false;
+      tc_fence_after();
       const uint32_t k_lo = ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) | (1u << 16);
       const uint32_t v_lo = k_lo + ((3 * Ly::kKBox) >> 4);
-      if (issuer) {
-        tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kDqk / 16; ++ks) {
-          const uint32_t ao = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
-          const uint32_t bo = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
-          mma_ss2(tmem + kBwdColS, q_lo + ao, kBwdDescHi, k_lo + bo, kBwdDescHi, kIdS, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < kDv / 16; ++ks) {
-          const uint32_t ao = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
-          const uint32_t bo = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
-          mma_ss2(tmem + kBwdColP, do_lo + ao, kBwdDescHi, v_lo + bo, kBwdDescHi, kIdS, ks > 0);
-        }
-        mma_commit(B_MM1);
+      for (int ks = 0; ks < kDqk / 16; ++ks) {
+        const uint32_t ao = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
+        const uint32_t bo = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
+        mma_ss2(tmem + buf * 128, q_lo + ao, kBwdDescHi, k_lo + bo, kBwdDescHi, kIdS, ks > 0);
       }
-      ++n_m1;
-      ok = wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 22);
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
-      tc_fence_after();
-      {
+#pragma unroll
+      for (int ks = 0; ks < kDv / 16; ++ks) {
+        const uint32_t ao = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
+        const uint32_t bo = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
+        mma_ss2(tmem + buf * 128 + 64, do_lo + ao, kBwdDescHi, v_lo + bo, kBwdDescHi, kIdS, ks > 0);
+      }
+      mma_commit(B_MM1(buf));
+    }
+    return true;
+  };
+
+  DqItem cur;
+  int32_t it = dq_next_item(a, blockIdx.x, cur);
+  if (cur.valid) load_q(cur);
+  while (ld.valid && ld_g < static_cast<uint32_t>(NS)) load_next();
+  uint32_t g0 = 0;  // global index of the current item's first block
+  while (ok && cur.valid) {
+    DqItem nxt;
+    const int32_t it_n = dq_next_item(a, it + gridDim.x, nxt);
+    // this thread's row
+    const int32_t ti = cur.t0 + t_row, h = cur.kvh * G + g_row;
+    const bool rvalid = compute && ti < cur.L;
+    const size_t grow = static_cast<size_t>(cur.s0 + ti) * a.Hq + h;
+    const float lse2 = rvalid ? __ldg(a.lse + grow) * kLog2e : 0.f;
+    const float Drow = rvalid ? __ldg(a.D + grow) : 0.f;
+    if (issuer) ok = wait_bar(B_QF, (n_qf - 1) & 1, abort_flag, 20);
+    ok = issue_sdp(g0, ok) && ok;
+    for (int32_t j = 0; j < cur.nblk; ++j) {
+      const uint32_t g = g0 + j;
+      if (j + 1 < cur.nblk) ok = issue_sdp(g + 1, ok) && ok;
+      // the stage of block g+2 was last read by dQ(g-1), the latest dQ
+      if (producer && ok && n_m2 > 0) ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 23);
+      while (ld.valid && ld_g <= g + 2) load_next();
+      // the last S/dP of this item done: the Q/dO tile can take the next item's
+      if (j == cur.nblk - 1 && nxt.valid) {
+        if (producer && ok) ok = wait_bar(B_MM1(g & 1), (n_m1[g & 1] - 1) & 1, abort_flag, 22);
+        load_q(nxt);
+      }
+      if (compute) {
+        // S(g), dP(g) complete (and with them every earlier MMA but dQ(g-1))
+        if (!wait_bar(B_MM1(g & 1), (n_m1[g & 1] - 1) & 1, abort_flag, 22)) ok = false;
+        tc_fence_after();
+        const uint32_t cs = lane_t + (g & 1) * 128;
         uint32_t sv[64], pv[64];
-        tmem_ld32p(lane_t + kBwdColS, sv);
-        tmem_ld32p(lane_t + kBwdColS + 32, sv + 32);
-        tmem_ld32p(lane_t + kBwdColP, pv);
-        tmem_ld32p(lane_t + kBwdColP + 32, pv + 32);
+        tmem_ld32p(cs, sv);
+        tmem_ld32p(cs + 32, sv + 32);
+        tmem_ld32p(cs + 64, pv);
+        tmem_ld32p(cs + 96, pv + 32);
         tmem_wait_ld();
         reg_fence<64>(sv);
         reg_fence<64>(pv);
-        const int32_t kb = lo + j * kDqBN;
+        // this row sees keys [max(0, ti - W + 1), ti]: columns c with
+        // c - c_lo < span (unsigned) of this block
+        const int32_t kb = cur.lo + j * kDqBN;
+        const int32_t c_lo = (a.window > 0 ? ti - a.window + 1 : 0) - kb;
+        const uint32_t span = rvalid ? static_cast<uint32_t>(ti - kb - c_lo) : 0u;
 #pragma unroll
         for (int32_t c = 0; c < kDqBN; c += 2) {
           float ds[2];
 #pragma unroll
           for (int32_t e = 0; e < 2; ++e) {
-            const int32_t kj = kb + c + e;
-            const bool vis = rvalid && kj <= ti && (a.window == 0 || kj > ti - a.window);
+            const bool vis = static_cast<uint32_t>(c + e - c_lo) <= span && rvalid;
             const float p = vis ? ex2(__uint_as_float(sv[c + e]) * a.scale_log2 - lse2) : 0.f;
             ds[e] = p * (__uint_as_float(pv[c + e]) - Drow);
           }
           sv[c >> 1] = pack_bf16x2(ds[0], ds[1]);
         }
-        tmem_st32p(lane_t + kBwdColS, sv);  // dS as bf16 pairs over S
+        tmem_st32p(cs, sv);  // dS as bf16 pairs over S
         tmem_wait_st();
       }
       tc_fence_before();
@@ -381,31 +460,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       if (issuer) {
         tc_fence_after();
+        const uint32_t st = g % NS;
 #pragma unroll
         for (int ks = 0; ks < kDqBN / 16; ++ks)
-          mma_ts2(tmem + kBwdColAcc, tmem + kBwdColS + ks * 8,
+          mma_ts2(tmem + kDqColAcc, tmem + (g & 1) * 128 + ks * 8,
                   ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) + ks * ((16 * kRowBytes) >> 4) +
                       ((Ly::kKBox >> 4) << 16),
                   kBwdDescHi, kIdQ, (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(B_MM2);
       }
       ++n_m2;
-      ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 23);
-      ok = __syncthreads_and(ok);
     }
     if (!ok) break;
-    tc_fence_after();
-    bwd_store_qk_row(lane_t + kBwdColAcc, a.scale, a.rope_on, a.rope_style, ti, a.rope_turns,
-                     a.dq + grow * kDqk, rvalid);
+    if (compute) {
+      ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 24);
+      tc_fence_after();
+      bwd_store_qk_row(lane_t + kDqColAcc, a.scale, a.rope_on, a.rope_style, ti, a.rope_turns,
+                       a.dq + grow * kDqk, rvalid);
+    }
     tc_fence_before();
     ok = __syncthreads_and(ok);
+    g0 += cur.nblk;
+    cur = nxt;
+    it = it_n;
   }
   // drain: every copy and MMA this CTA issued must land before TMEM and shared
   // memory go back (only an aborted CTA has any left)
   if (n_qf > 0) drain_wait(B_QF, (n_qf - 1) & 1);
-  for (uint32_t s = 0; s < 2; ++s)
+  for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
     if (n_kv[s] > 0) drain_wait(B_KV(s), (n_kv[s] - 1) & 1);
-  if (n_m1 > 0) drain_wait(B_MM1, (n_m1 - 1) & 1);
+  for (uint32_t b = 0; b < 2; ++b)
+    if (n_m1[b] > 0) drain_wait(B_MM1(b), (n_m1[b] - 1) & 1);
   if (n_m2 > 0) drain_wait(B_MM2, (n_m2 - 1) & 1);
   tc_fence_before();
   __syncthreads();
@@ -416,43 +501,91 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ------------------------------------------------------------------ dK / dV kernel
+// Work item of the dk/dv kernel: one block of 128 keys of one KV head, over the
+// sub-tiles of 64 packed query rows (64/G tokens x G heads) that see it.
+struct KvItem {
+  int32_t s0, L, k0, i_lo, nsub, kvh;
+  bool valid;
+};
+
+__device__ __forceinline__ KvItem kv_item(const BwdArgs &a, int32_t it) {
+  KvItem d{};
+  d.valid = false;
+  const int32_t TS = kKvRows / a.G;
+  const int32_t per_seq = a.Hkv * a.kv_blocks;
+  const int32_t b = it / per_seq, rem = it % per_seq;
+  d.kvh = rem % a.Hkv;
+  const int32_t blk = rem / a.Hkv;  // global: the earliest blocks (most queries) first
+  d.s0 = __ldg(a.cu_seqlens + b);
+  d.L = __ldg(a.cu_seqlens + b + 1) - d.s0;
+  d.k0 = blk * kKvBN;
+  if (d.k0 >= d.L) return d;
+  d.i_lo = d.k0;
+  const int32_t i_hi = a.window > 0 ? min(d.L - 1, d.k0 + kKvBN - 1 + a.window - 1) : d.L - 1;
+  d.nsub = (i_hi - d.i_lo + TS) / TS;
+  d.valid = true;
+  return d;
+}
+
+__device__ __forceinline__ int32_t kv_next_item(const BwdArgs &a, int32_t it, KvItem &d) {
+  d.valid = false;
+  for (; it < a.kv_items; it += gridDim.x) {
+    d = kv_item(a, it);
+    if (d.valid) break;
+  }
+  return it;
+}
+
 struct KvLayout {
+  static constexpr int32_t kStages = 3;                  // Q/dO sub-tiles in flight
   static constexpr uint32_t kKBox = kKvBN * kRowBytes;   // 128 keys x 64 dims: 16 KB
   static constexpr uint32_t kQBox = kKvRows * kRowBytes; // 64 rows x 64 dims: 8 KB
   static constexpr uint32_t kKOff = 0;                   // k_rot block: 3 boxes
   static constexpr uint32_t kVOff = 3 * kKBox;           // v block: 2 boxes
   static constexpr uint32_t kStOff = 5 * kKBox;          // stages: q_rot rows 3 boxes, dO rows 2
   static constexpr uint32_t kStage = 5 * kQBox;
-  static constexpr uint32_t kColOff = kStOff + 2 * kStage;  // lse*log2e, D of the sub-tile's rows
-  static constexpr uint32_t kBarOff = kColOff + 2 * kKvRows * 4;  // kf, qs[2], mm1, mm2
-  static constexpr uint32_t kMiscOff = kBarOff + 5 * 8;
+  static constexpr uint32_t kColOff = kStOff + kStages * kStage;  // lse*log2e, D: 2 sub-tiles
+  static constexpr uint32_t kBarOff = kColOff + 2 * 2 * kKvRows * 4;  // kf, qs[3], mm1, mm2
+  static constexpr uint32_t kMiscOff = kBarOff + 6 * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
 static_assert(KvLayout::kDynSmem <= 232448, "dkdv kernel shared memory");
 
+// Pipeline of the dk/dv kernel (thread 128 issues the MMAs, thread 160 the
+// copies; threads 0..127 own one key each).  TMEM: S^T 0..63 and dP^T 64..127 of the current sub-tile, dV
+// 128..255, dK 256..447, and P^T (448..479) and dS^T (480..511) as bf16 pairs.
+// After the one CTA barrier of sub-tile g, S^T/dP^T(g+1) go out first and
+// dV/dK(g) behind them, so the rows work on sub-tile g+1 while dV/dK(g) run;
+// they wait for dV/dK(g) only before writing P^T/dS^T(g+1).  Q/dO sub-tiles
+// stream through three stages, loaded two ahead and across item boundaries;
+// the next item's K/V block is loaded once the last S^T/dP^T of the current
+// item is done.
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ BwdArgs a) {
   using Ly = KvLayout;
+  constexpr int32_t NS = Ly::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int32_t warp = threadIdx.x >> 5;
-  const int32_t lane_row = threadIdx.x;  // key row == TMEM lane
-  const bool issuer = threadIdx.x == 0;
-  const uint32_t B_KF = sbase + Ly::kBarOff, B_MM1 = B_KF + 24, B_MM2 = B_KF + 32;
+  const int32_t lane_row = threadIdx.x;  // key row == TMEM lane (threads 0..127)
+  const bool compute = threadIdx.x < 128;
+  const bool issuer = threadIdx.x == 128;    // MMAs
+  const bool producer = threadIdx.x == 160;  // copies
+  const uint32_t B_KF = sbase + Ly::kBarOff;
   auto B_QS = [&](uint32_t s) { return B_KF + 8 + 8 * s; };
+  const uint32_t B_MM1 = B_KF + 8 + 8 * NS, B_MM2 = B_MM1 + 8;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
-  float *c_lse = reinterpret_cast<float *>(smem + Ly::kColOff);
-  float *c_D = c_lse + kKvRows;
+  float *c_lse = reinterpret_cast<float *>(smem + Ly::kColOff);  // [2][64]
+  float *c_D = c_lse + 2 * kKvRows;                                // [2][64]
   if (issuer) {
     mbar_init(B_KF, 1);
-    mbar_init(B_QS(0), 1);
-    mbar_init(B_QS(1), 1);
+    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s) mbar_init(B_QS(s), 1);
     mbar_init(B_MM1, 1);
     mbar_init(B_MM2, 1);
     *abort_flag = 0u;
@@ -477,140 +610,203 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr uint32_t kIdS = idesc_f32acc(128, kKvRows, 1, 0, 0);
   constexpr uint32_t kIdV = idesc_f32acc(128, kDv, 1, 0, 1);
   constexpr uint32_t kIdK = idesc_f32acc(128, kDqk, 1, 0, 1);
-  constexpr uint32_t kColV = kBwdColAcc, kColK = kBwdColAcc + kDv;  // 128..255, 256..447
-  uint32_t n_kf = 0, n_qs[2] = {0, 0}, n_m1 = 0, n_m2 = 0, gs = 0;
+  constexpr uint32_t kColST = 0, kColPT = 64, kColV = 128, kColK = 256, kColP = 448, kColDS = 480;
+  uint32_t n_kf = 0, n_qs[NS] = {}, n_m1 = 0, n_m2 = 0;
   bool ok = true;
-  for (int32_t it = blockIdx.x; ok && it < a.kv_items; it += gridDim.x) {
-    const int32_t per_seq = a.Hkv * a.kv_blocks;
-    const int32_t b = it / per_seq, rem = it % per_seq;
-    const int32_t kvh = rem % a.Hkv;
-    const int32_t blk = rem / a.Hkv;  // global: the earliest blocks (most queries) first
-    const int32_t s0 = __ldg(a.cu_seqlens + b), L = __ldg(a.cu_seqlens + b + 1) - s0;
-    const int32_t k0 = blk * kKvBN;
-    if (k0 >= L) continue;
-    const int32_t i_lo = k0;
-    const int32_t i_hi = a.window > 0 ? min(L - 1, k0 + kKvBN - 1 + a.window - 1) : L - 1;
-    const int32_t nsub = (i_hi - i_lo + TS) / TS;
-    const int32_t kj = k0 + lane_row;  // this thread's key
-    const bool kvalid = kj < L;
-    if (issuer) {
+
+  // ---- Q/dO loader: walks this CTA's (item, sub-tile) sequence ahead of the keys
+  KvItem ld;
+  int32_t ld_it = kv_next_item(a, blockIdx.x, ld), ld_j = 0;
+  uint32_t ld_g = 0;  // global index of the next sub-tile to load
+  auto load_next = [&]() {
+    const uint32_t st = ld_g % NS;
+    if (producer) {
+      const uint32_t dst = sbase + Ly::kStOff + st * Ly::kStage;
+      const int32_t tok = ld.s0 + ld.i_lo + ld_j * TS;
+      mbar_arrive_expect_tx(B_QS(st), Ly::kStage);
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc)
+        tma_load_3d(dst + cc * Ly::kQBox, &tm_q, cc * 64, ld.kvh * G, tok, B_QS(st));
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        tma_load_3d(dst + (3 + cc) * Ly::kQBox, &tm_do, cc * 64, ld.kvh * G, tok, B_QS(st));
+    }
+    ++n_qs[st];
+    ++ld_g;
+    if (++ld_j >= ld.nsub) {
+      ld_j = 0;
+      ld_it = kv_next_item(a, ld_it + gridDim.x, ld);
+    }
+  };
+  auto load_kv = [&](const KvItem &d) {
+    if (producer) {
       mbar_arrive_expect_tx(B_KF, 5 * Ly::kKBox);
 #pragma unroll
       for (int cc = 0; cc < 3; ++cc)
-        tma_load_3d(sbase + Ly::kKOff + cc * Ly::kKBox, &tm_k, cc * 64, kvh, s0 + k0, B_KF);
+        tma_load_3d(sbase + Ly::kKOff + cc * Ly::kKBox, &tm_k, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
-        tma_load_3d(sbase + Ly::kVOff + cc * Ly::kKBox, &tm_v, cc * 64, kvh, s0 + k0, B_KF);
+        tma_load_3d(sbase + Ly::kVOff + cc * Ly::kKBox, &tm_v, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
     }
     ++n_kf;
-    auto load_sub = [&](int32_t sidx, uint32_t st) {
-      const uint32_t dst = sbase + Ly::kStOff + st * Ly::kStage;
-      const int32_t tok = s0 + i_lo + sidx * TS;
-      mbar_arrive_expect_tx(B_QS(st), Ly::kStage);
-#pragma unroll
-      for (int cc = 0; cc < 3; ++cc) tma_load_3d(dst + cc * Ly::kQBox, &tm_q, cc * 64, kvh * G, tok, B_QS(st));
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-        tma_load_3d(dst + (3 + cc) * Ly::kQBox, &tm_do, cc * 64, kvh * G, tok, B_QS(st));
-    };
-    if (issuer) load_sub(0, gs & 1);
-    ++n_qs[gs & 1];
-    ok = wait_bar(B_KF, (n_kf - 1) & 1, abort_flag, 24);
-    ok = __syncthreads_and(ok);
-    for (int32_t sidx = 0; ok && sidx < nsub; ++sidx, ++gs) {
-      const uint32_t st = gs & 1;
-      if (sidx + 1 < nsub) {
-        if (issuer) load_sub(sidx + 1, st ^ 1);
-        ++n_qs[st ^ 1];
-      }
-      const int32_t i0 = i_lo + sidx * TS;
-      if (threadIdx.x < kKvRows) {
-        const int32_t ti = i0 + threadIdx.x / G, h = kvh * G + threadIdx.x % G;
-        const bool v = ti < L;
-        const size_t grow = static_cast<size_t>(s0 + ti) * a.Hq + h;
-        c_lse[threadIdx.x] = v ? __ldg(a.lse + grow) * kLog2e : 0.f;
-        c_D[threadIdx.x] = v ? __ldg(a.D + grow) : 0.f;
-      }
-      ok = wait_bar(B_QS(st), (n_qs[st] - 1) & 1, abort_flag, 25);
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
+  };
+  // lse * log2(e) and D of the 64 rows of sub-tile sidx of item d (threads
+  // 0..63 load one row each; stage_rows puts them in slot p)
+  float r_lse = 0.f, r_D = 0.f;
+  auto fetch_rows = [&](const KvItem &d, int32_t sidx) {
+    if (threadIdx.x < kKvRows) {
+      const int32_t ti = d.i_lo + sidx * TS + threadIdx.x / G, h = d.kvh * G + threadIdx.x % G;
+      const bool v = ti < d.L;
+      const size_t grow = static_cast<size_t>(d.s0 + ti) * a.Hq + h;
+      r_lse = v ? __ldg(a.lse + grow) * kLog2e : 0.f;
+      r_D = v ? __ldg(a.D + grow) : 0.f;
+    }
+  };
+  auto stage_rows = [&](uint32_t p) {
+    if (threadIdx.x < kKvRows) {
+      c_lse[p * kKvRows + threadIdx.x] = r_lse;
+      c_D[p * kKvRows + threadIdx.x] = r_D;
+    }
+  };
+  // S^T(g) = K Q^T and dP^T(g) = V dO^T (issued only while `go`; Q/dO(g) must be
+  // the latest load of its stage).  The counts move on every thread either way.
+  auto issue_sdp = [&](uint32_t g, bool go) -> bool {
+    const uint32_t st = g % NS;
+    ++n_m1;
+    if (issuer && go) {
+      if (!wait_bar(B_QS(st), (n_qs[st] - 1) & 1, abort_flag, 25)) return false;
+      tc_fence_after();
       const uint32_t q_lo = ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) | (1u << 16);
       const uint32_t do_lo = q_lo + ((3 * Ly::kQBox) >> 4);
-      if (issuer) {
-        tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kDqk / 16; ++ks) {
-          const uint32_t ao = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
-          const uint32_t bo = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
-          mma_ss2(tmem + kBwdColS, k_lo + ao, kBwdDescHi, q_lo + bo, kBwdDescHi, kIdS, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < kDv / 16; ++ks) {
-          const uint32_t ao = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
-          const uint32_t bo = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
-          mma_ss2(tmem + kBwdColP, v_lo + ao, kBwdDescHi, do_lo + bo, kBwdDescHi, kIdS, ks > 0);
-        }
-        mma_commit(B_MM1);
+      for (int ks = 0; ks < kDqk / 16; ++ks) {
+        const uint32_t ao = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
+        const uint32_t bo = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
+        mma_ss2(tmem + kColST, k_lo + ao, kBwdDescHi, q_lo + bo, kBwdDescHi, kIdS, ks > 0);
       }
-      ++n_m1;
-      ok = wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 26);
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint32_t sv[64], pv[64];
-        tmem_ld32p(lane_t + kBwdColS, sv);
-        tmem_ld32p(lane_t + kBwdColS + 32, sv + 32);
-        tmem_ld32p(lane_t + kBwdColP, pv);
-        tmem_ld32p(lane_t + kBwdColP + 32, pv + 32);
+#pragma unroll
+      for (int ks = 0; ks < kDv / 16; ++ks) {
+        const uint32_t ao = ((ks >> 2) * Ly::kKBox + (ks & 3) * 32) >> 4;
+        const uint32_t bo = ((ks >> 2) * Ly::kQBox + (ks & 3) * 32) >> 4;
+        mma_ss2(tmem + kColPT, v_lo + ao, kBwdDescHi, do_lo + bo, kBwdDescHi, kIdS, ks > 0);
+      }
+      mma_commit(B_MM1);
+    }
+    return true;
+  };
+
+  KvItem cur;
+  int32_t it = kv_next_item(a, blockIdx.x, cur);
+  if (cur.valid) {
+    load_kv(cur);
+    fetch_rows(cur, 0);
+    stage_rows(0);
+  }
+  while (ld.valid && ld_g < static_cast<uint32_t>(NS)) load_next();
+  __syncthreads();  // the first sub-tile's rows
+  uint32_t g0 = 0;  // global index of the current item's first sub-tile
+  while (ok && cur.valid) {
+    KvItem nxt;
+    const int32_t it_n = kv_next_item(a, it + gridDim.x, nxt);
+    const int32_t kj = cur.k0 + lane_row;  // this thread's key
+    const bool kvalid = compute && kj < cur.L;
+    if (issuer) ok = wait_bar(B_KF, (n_kf - 1) & 1, abort_flag, 24);
+    ok = issue_sdp(g0, ok) && ok;
+    for (int32_t sidx = 0; sidx < cur.nsub; ++sidx) {
+      const uint32_t g = g0 + sidx;
+      const int32_t i0 = cur.i_lo + sidx * TS;
+      // the last S^T/dP^T of this item done: K/V can take the next item's
+      if (sidx == cur.nsub - 1 && nxt.valid) {
+        if (producer && ok) ok = wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 26);
+        load_kv(nxt);
+      }
+      // the next sub-tile's rows: loads go out now, land in shared memory
+      // before the barrier
+      if (sidx + 1 < cur.nsub)
+        fetch_rows(cur, sidx + 1);
+      else if (nxt.valid)
+        fetch_rows(nxt, 0);
+      uint32_t sv[64], pv[64];
+      if (compute) {
+        // S^T(g), dP^T(g) complete
+        if (!wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 26)) ok = false;
+        tc_fence_after();
+        const float4 *cl4 = reinterpret_cast<const float4 *>(c_lse + (g & 1) * kKvRows);
+        const float4 *cd4 = reinterpret_cast<const float4 *>(c_D + (g & 1) * kKvRows);
+        // column c is query token i0 + c / G: this key is seen by the columns
+        // with i0 + c / G in [kj, min(L, kj + W) - 1], i.e. c in [c_lo, c_hi)
+        // (token counts clamped to one sub-tile first, so no product overflows)
+        const int32_t d0 = kj - i0;
+        const int32_t c_lo = d0 > 0 ? d0 * G : 0;
+        int32_t c_hi = min(cur.L - i0, kKvRows) * G;
+        if (a.window > 0) c_hi = min(c_hi, max(0, min(d0 + a.window, kKvRows)) * G);
+        c_hi = min(c_hi, kKvRows);
+        const uint32_t span = (kvalid && c_hi > c_lo) ? static_cast<uint32_t>(c_hi - c_lo) : 0u;
+        tmem_ld32p(lane_t + kColST, sv);
+        tmem_ld32p(lane_t + kColST + 32, sv + 32);
+        tmem_ld32p(lane_t + kColPT, pv);
+        tmem_ld32p(lane_t + kColPT + 32, pv + 32);
         tmem_wait_ld();
         reg_fence<64>(sv);
         reg_fence<64>(pv);
 #pragma unroll
-        for (int32_t c = 0; c < kKvRows; c += 2) {
-          float pp[2], ds[2];
+        for (int32_t c = 0; c < kKvRows; c += 4) {
+          const float4 l4 = cl4[c >> 2], d4 = cd4[c >> 2];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pp[4], ds[4];
 #pragma unroll
-          for (int32_t e = 0; e < 2; ++e) {
-            const int32_t ti = i0 + (c + e) / G;
-            const bool vis = kvalid && ti < L && kj <= ti && (a.window == 0 || kj > ti - a.window);
-            pp[e] = vis ? ex2(__uint_as_float(sv[c + e]) * a.scale_log2 - c_lse[c + e]) : 0.f;
-            ds[e] = pp[e] * (__uint_as_float(pv[c + e]) - c_D[c + e]);
+          for (int32_t e = 0; e < 4; ++e) {
+            const bool vis = static_cast<uint32_t>(c + e - c_lo) < span;
+            pp[e] = vis ? ex2(__uint_as_float(sv[c + e]) * a.scale_log2 - lv[e]) : 0.f;
+            ds[e] = pp[e] * (__uint_as_float(pv[c + e]) - dv[e]);
           }
           sv[c >> 1] = pack_bf16x2(pp[0], pp[1]);
+          sv[(c >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
           pv[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+          pv[(c >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        tmem_st32p(lane_t + kBwdColS, sv);  // P^T as bf16 pairs over S^T
-        tmem_st32p(lane_t + kBwdColP, pv);  // dS^T as bf16 pairs over dP^T
+      }
+      // dV/dK(g-1) complete: P^T/dS^T and the Q/dO stage of sub-tile g-1 are free
+      if ((compute || producer) && ok && n_m2 > 0)
+        ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 27);
+      while (ld.valid && ld_g <= g + 2) load_next();
+      if (compute) {
+        tc_fence_after();
+        tmem_st32p(lane_t + kColP, sv);   // P^T as bf16 pairs
+        tmem_st32p(lane_t + kColDS, pv);  // dS^T as bf16 pairs
         tmem_wait_st();
       }
+      // slot (g+1) & 1 was last read in sub-tile g-1
+      stage_rows((g + 1) & 1);
       tc_fence_before();
       ok = __syncthreads_and(ok);
       if (!ok) break;
-      if (issuer) {
-        tc_fence_after();
-        const uint32_t stb = (sbase + Ly::kStOff + st * Ly::kStage) >> 4;
+      if (issuer) tc_fence_after();
+      // S^T/dP^T of the next sub-tile first, then dV/dK of this one
+      if (sidx + 1 < cur.nsub) ok = issue_sdp(g + 1, ok) && ok;
+      if (issuer && ok) {
+        const uint32_t stb = (sbase + Ly::kStOff + (g % NS) * Ly::kStage) >> 4;
 #pragma unroll
         for (int ks = 0; ks < kKvRows / 16; ++ks) {
           const uint32_t step = ks * ((16 * kRowBytes) >> 4);
           // dV += P^T dO: B = the dO rows read N-major (LBO = one box)
-          mma_ts2(tmem + kColV, tmem + kBwdColS + ks * 8,
+          mma_ts2(tmem + kColV, tmem + kColP + ks * 8,
                   stb + ((3 * Ly::kQBox) >> 4) + step + ((Ly::kQBox >> 4) << 16), kBwdDescHi, kIdV,
                   (sidx > 0 || ks > 0) ? 1u : 0u);
           // dK += dS^T Q: B = the q_rot rows read N-major
-          mma_ts2(tmem + kColK, tmem + kBwdColP + ks * 8, stb + step + ((Ly::kQBox >> 4) << 16),
+          mma_ts2(tmem + kColK, tmem + kColDS + ks * 8, stb + step + ((Ly::kQBox >> 4) << 16),
                   kBwdDescHi, kIdK, (sidx > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(B_MM2);
       }
       ++n_m2;
-      ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 27);
-      ok = __syncthreads_and(ok);
     }
     if (!ok) break;
-    tc_fence_after();
-    {
+    if (compute) {
+      ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 27);
+      tc_fence_after();
       // dV row: 128 fp32 columns -> bf16
-      __nv_bfloat16 *dst = a.dv + (static_cast<size_t>(s0 + kj) * a.Hkv + kvh) * kDv;
+      __nv_bfloat16 *dst = a.dv + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDv;
 #pragma unroll 1
       for (int32_t cb = 0; cb < kDv; cb += 32) {
         uint32_t r[32];
@@ -627,14 +823,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
+      bwd_store_qk_row(lane_t + kColK, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
+                       a.dk + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDqk, kvalid);
     }
-    bwd_store_qk_row(lane_t + kColK, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
-                     a.dk + (static_cast<size_t>(s0 + kj) * a.Hkv + kvh) * kDqk, kvalid);
     tc_fence_before();
     ok = __syncthreads_and(ok);
+    g0 += cur.nsub;
+    cur = nxt;
+    it = it_n;
   }
   if (n_kf > 0) drain_wait(B_KF, (n_kf - 1) & 1);
-  for (uint32_t s = 0; s < 2; ++s)
+  for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
     if (n_qs[s] > 0) drain_wait(B_QS(s), (n_qs[s] - 1) & 1);
   if (n_m1 > 0) drain_wait(B_MM1, (n_m1 - 1) & 1);
   if (n_m2 > 0) drain_wait(B_MM2, (n_m2 - 1) & 1);

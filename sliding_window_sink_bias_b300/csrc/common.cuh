@@ -46,11 +46,13 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity,
   }
 }
 
-// Bounded mbarrier wait.  The first try_wait (which itself sleeps up to its
-// hint) almost always succeeds; the timed loop lives out of line so the hot
-// loops stay small in the instruction cache.
+// Bounded mbarrier wait.  A phase that has already completed is seen by the
+// non-blocking test; otherwise the first try_wait (which itself sleeps up to
+// its hint) almost always succeeds.  The timed loop lives out of line so the
+// hot loops stay small in the instruction cache.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                          uint32_t site) {
+  if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   return wait_bar_slow(bar, parity, abort_flag, site);
 }

@@ -193,7 +193,7 @@ __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
 // Shared memory of the decode kernel.  bf16 cache: four K/V stages the TMA
 // fills directly.  FP8 cache: two staging slots of raw E4M3 rows (TMA; half the
 // bytes of a bf16 block each) and three fp16 K/V stages the conversion warps
-// fill for the MMA.
+// fill for the MMA (block j+1 is converted while block j is multiplied).
 template <bool F8>
 struct DecLayoutT {
   static constexpr int32_t S = F8 ? 3 : kDecStages;   // K/V stages the MMA reads
@@ -255,20 +255,20 @@ __device__ void dec_convert_fp8(const uint8_t *stg, uint8_t *kv, int32_t kp, int
                                 int32_t tid, int32_t nthr) {
   constexpr uint32_t kBox = kDecBN * kRowBytes;
   constexpr uint32_t kK8 = kDecBN * kDqk;
-  // K dims 64..191 (boxes 1, 2) and V (boxes 3, 4): chunks of 8 values
+  // K dims 64..191 (boxes 1, 2), then V (boxes 3, 4): 16 chunks of 8 values a
+  // row each, in two loops so that no warp splits between K and V
 #pragma unroll 2
-  for (int32_t u = tid; u < kDecBN * 32; u += nthr) {
-    const int32_t r = (u >> 5), c = u & 31;
-    if (c < 16) {
-      const uint2 v = *reinterpret_cast<const uint2 *>(stg + r * kDqk + 64 + c * 8);
-      *swz_chunk(kv + (1 + (c >> 3)) * kBox, r, c & 7) = e4m3x8_to_f16(v);
-    } else {
-      const int32_t cv = c - 16;
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);
-      if (r >= r0 && r < r1)
-        o = e4m3x8_to_f16(*reinterpret_cast<const uint2 *>(stg + kK8 + r * kDv + cv * 8));
-      *swz_chunk(kv + (3 + (cv >> 3)) * kBox, r, cv & 7) = o;
-    }
+  for (int32_t u = tid; u < kDecBN * 16; u += nthr) {
+    const int32_t r = u >> 4, c = u & 15;
+    const uint2 v = *reinterpret_cast<const uint2 *>(stg + r * kDqk + 64 + c * 8);
+    *swz_chunk(kv + (1 + (c >> 3)) * kBox, r, c & 7) = e4m3x8_to_f16(v);
+  }
+#pragma unroll 2
+  for (int32_t u = tid; u < kDecBN * 16; u += nthr) {
+    const int32_t r = u >> 4, c = u & 15;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (r >= r0 && r < r1) o = e4m3x8_to_f16(*reinterpret_cast<const uint2 *>(stg + kK8 + r * kDv + c * 8));
+    *swz_chunk(kv + (3 + (c >> 3)) * kBox, r, c & 7) = o;
   }
   // K dims 0..63 (box 0), rotated
   if (!rope_on || style == 0) {
@@ -384,9 +384,11 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(B_PVDONE, 1);
     mbar_init(B_OEMPTY, 128);
     mbar_init(B_DRAIN, 1);
-    for (uint32_t s8 = 0; s8 < static_cast<uint32_t>(S8); ++s8) {
-      mbar_init(B_STGFULL(s8), 1);
-      mbar_init(B_STGEMPTY(s8), DecThreads<F8>::kConv);
+    if constexpr (F8) {
+      for (uint32_t s8 = 0; s8 < static_cast<uint32_t>(S8); ++s8) {
+        mbar_init(B_STGFULL(s8), 1);
+        mbar_init(B_STGEMPTY(s8), DecThreads<F8>::kConv);
+      }
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -524,12 +526,9 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         for (int32_t j = 0; ok && j < sg.nblk; ++j) {
           const uint32_t st = (gk + j) % S;
-          // FP8 cache: the conversion of block j+1 waits for the PV that last
-          // read its fp16 stage, so PV(j-1) goes out before block j's QK^T
-          // waits for block j's conversion
-          if constexpr (F8) {
-            if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
-          }
+          // QK^T(j) goes out before PV(j-1) waits for the softmax of block
+          // j-1, so the two overlap.  The stage block j needs was last read by
+          // PV(j-S), issued in an earlier pass of this loop.
           if (!(ok = wait_bar(B_KREADY(st), ((gk + j) / S) & 1, abort_flag, 6))) break;
           tc_fence_after();
           const uint32_t s_t = tmem + ((gs + j) & 1) * BN;
@@ -543,9 +542,7 @@ __global__ void __launch_bounds__(512, 1)
           issued = true;
           mma_commit(B_SFULL((gs + j) & 1));
           if (j == sg.nblk - 1) mma_commit(B_QEMPTY);
-          if constexpr (!F8) {
-            if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
-          }
+          if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
         }
         if (ok) ok = issue_pv(gs + sg.nblk - 1, (gk + sg.nblk - 1) % S, sg.nblk == 1);
         ++gq;
