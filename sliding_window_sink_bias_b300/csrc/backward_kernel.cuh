@@ -27,16 +27,17 @@
 //                     shared-memory tiles read N-major); epilogue as above.
 //   bwd_dsink_kernel  the per-chunk partials summed in chunk order.
 //
-// The MMA kernels run 4 warps that own one row each (TMEM lane), a fifth warp
-// whose first thread issues the MMAs and a sixth whose first thread issues the
-// copies, so neither the rows nor the MMAs wait for the other issuing; every
-// wait is bounded and every CTA-wide decision is taken with __syncthreads_and.
+// The MMA kernels run 8 warps that own half a row each (TMEM lane; warps w and
+// w + 4 share the lanes of w % 4), a ninth warp whose first thread issues the
+// MMAs and a tenth whose first thread issues the copies, so neither the rows
+// nor the MMAs wait for the other issuing; every wait is bounded and every
+// CTA-wide decision is taken with __syncthreads_and.
 #pragma once
 #include "common.cuh"
 
 namespace sa {
 
-constexpr int32_t kBwdThreads = 192;  // dq / dkdv: 4 row warps, an MMA warp, a copy warp
+constexpr int32_t kBwdThreads = 320;  // dq / dkdv: 8 row warps, an MMA warp, a copy warp
 constexpr int32_t kBwdChunk = 32;    // tokens per pre-pass CTA
 constexpr int32_t kDqBN = 64;        // keys per block (dq kernel)
 constexpr int32_t kKvBN = 128;       // keys per block (dkdv kernel)
@@ -291,10 +292,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int32_t warp = threadIdx.x >> 5;
-  const int32_t row = threadIdx.x;  // packed query row == TMEM lane (threads 0..127)
-  const bool compute = threadIdx.x < 128;
-  const bool issuer = threadIdx.x == 128;    // MMAs
-  const bool producer = threadIdx.x == 160;  // copies
+  const int32_t row = threadIdx.x & 127;  // packed query row == TMEM lane
+  const int32_t half = threadIdx.x >> 7;    // this thread's 32 keys of a block
+  const bool compute = threadIdx.x < 256;
+  const bool issuer = threadIdx.x == 256;    // MMAs
+  const bool producer = threadIdx.x == 288;  // copies
   const uint32_t B_QF = sbase + Ly::kBarOff;
   auto B_KV = [&](uint32_t s) { return B_QF + 8 + 8 * s; };
   auto B_MM1 = [&](uint32_t b) { return B_QF + 8 + 8 * NS + 8 * b; };
@@ -322,15 +324,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_t = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int32_t G = a.G;
   const int32_t t_row = row / G, g_row = row % G;
   const uint32_t q_lo = ((sbase + Ly::kQOff) >> 4) | (1u << 16);
   const uint32_t do_lo = ((sbase + Ly::kDoOff) >> 4) | (1u << 16);
   constexpr uint32_t kIdS = idesc_f32acc(128, kDqBN, 1, 0, 0);
   constexpr uint32_t kIdQ = idesc_f32acc(128, kDqk, 1, 0, 1);
-  // issue counts of every barrier, kept alike by all threads
-  uint32_t n_qf = 0, n_kv[NS] = {}, n_m1[2] = {0, 0}, n_m2 = 0;
+  // issue counts, kept alike by all threads.  Block g is the (g / NS)-th load
+  // of stage g % NS and the (g / 2)-th S/dP of buffer g & 1, so those phases
+  // follow from g.
+  uint32_t n_qf = 0, n_m2 = 0, n_sdp = 0;
   bool ok = true;
 
   // ---- K/V loader: walks this CTA's (item, block) sequence ahead of the rows
@@ -349,7 +353,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, ld.kvh, krow, B_KV(st));
     }
-    ++n_kv[st];
     ++ld_g;
     if (++ld_j >= ld.nblk) {
       ld_j = 0;
@@ -373,9 +376,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // every thread either way.
   auto issue_sdp = [&](uint32_t g, bool go) -> bool {
     const uint32_t st = g % NS, buf = g & 1;
-    ++n_m1[buf];
+    n_sdp = g + 1;
     if (issuer && go) {
-      if (!wait_bar(B_KV(st), (n_kv[st] - 1) & 1, abort_flag, 21)) return false;
+      if (!wait_bar(B_KV(st), (g / NS) & 1, abort_flag, 21)) return false;
       tc_fence_after();
       const uint32_t k_lo = ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) | (1u << 16);
       const uint32_t v_lo = k_lo + ((3 * Ly::kKBox) >> 4);
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int32_t it_n = dq_next_item(a, it + gridDim.x, nxt);
     // this thread's row
     const int32_t ti = cur.t0 + t_row, h = cur.kvh * G + g_row;
-    const bool rvalid = compute && ti < cur.L;
+    const bool rvalid = compute && ti < cur.L;  // both halves of the row
     const size_t grow = static_cast<size_t>(cur.s0 + ti) * a.Hq + h;
     const float lse2 = rvalid ? __ldg(a.lse + grow) * kLog2e : 0.f;
     const float Drow = rvalid ? __ldg(a.D + grow) : 0.f;
@@ -420,29 +423,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       while (ld.valid && ld_g <= g + 2) load_next();
       // the last S/dP of this item done: the Q/dO tile can take the next item's
       if (j == cur.nblk - 1 && nxt.valid) {
-        if (producer && ok) ok = wait_bar(B_MM1(g & 1), (n_m1[g & 1] - 1) & 1, abort_flag, 22);
+        if (producer && ok) ok = wait_bar(B_MM1(g & 1), (g >> 1) & 1, abort_flag, 22);
         load_q(nxt);
       }
       if (compute) {
         // S(g), dP(g) complete (and with them every earlier MMA but dQ(g-1))
-        if (!wait_bar(B_MM1(g & 1), (n_m1[g & 1] - 1) & 1, abort_flag, 22)) ok = false;
+        if (!wait_bar(B_MM1(g & 1), (g >> 1) & 1, abort_flag, 22)) ok = false;
         tc_fence_after();
-        const uint32_t cs = lane_t + (g & 1) * 128;
-        uint32_t sv[64], pv[64];
+        const uint32_t cs = lane_t + (g & 1) * 128 + 32 * half;
+        uint32_t sv[32], pv[32];
         tmem_ld32p(cs, sv);
-        tmem_ld32p(cs + 32, sv + 32);
         tmem_ld32p(cs + 64, pv);
-        tmem_ld32p(cs + 96, pv + 32);
         tmem_wait_ld();
-        reg_fence<64>(sv);
-        reg_fence<64>(pv);
+        reg_fence<32>(sv);
+        reg_fence<32>(pv);
         // this row sees keys [max(0, ti - W + 1), ti]: columns c with
-        // c - c_lo < span (unsigned) of this block
-        const int32_t kb = cur.lo + j * kDqBN;
+        // c - c_lo < span (unsigned) of this half block
+        const int32_t kb = cur.lo + j * kDqBN + 32 * half;
         const int32_t c_lo = (a.window > 0 ? ti - a.window + 1 : 0) - kb;
         const uint32_t span = rvalid ? static_cast<uint32_t>(ti - kb - c_lo) : 0u;
 #pragma unroll
-        for (int32_t c = 0; c < kDqBN; c += 2) {
+        for (int32_t c = 0; c < 32; c += 2) {
           float ds[2];
 #pragma unroll
           for (int32_t e = 0; e < 2; ++e) {
@@ -452,7 +453,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           sv[c >> 1] = pack_bf16x2(ds[0], ds[1]);
         }
-        tmem_st32p(cs, sv);  // dS as bf16 pairs over S
+        // dS of this half (16 bf16 pairs) over the first 16 of its own S columns
+        tmem_st16p(cs, sv);
         tmem_wait_st();
       }
       tc_fence_before();
@@ -461,9 +463,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (issuer) {
         tc_fence_after();
         const uint32_t st = g % NS;
+        // A = dS: keys 16 ks.. of the block sit at columns 32 (ks / 2) + 8 (ks % 2)
 #pragma unroll
         for (int ks = 0; ks < kDqBN / 16; ++ks)
-          mma_ts2(tmem + kDqColAcc, tmem + (g & 1) * 128 + ks * 8,
+          mma_ts2(tmem + kDqColAcc, tmem + (g & 1) * 128 + (ks >> 1) * 32 + (ks & 1) * 8,
                   ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) + ks * ((16 * kRowBytes) >> 4) +
                       ((Ly::kKBox >> 4) << 16),
                   kBwdDescHi, kIdQ, (j > 0 || ks > 0) ? 1u : 0u);
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++n_m2;
     }
     if (!ok) break;
-    if (compute) {
+    if (compute && half == 0) {
       ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 24);
       tc_fence_after();
       bwd_store_qk_row(lane_t + kDqColAcc, a.scale, a.rope_on, a.rope_style, ti, a.rope_turns,
@@ -488,9 +491,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // memory go back (only an aborted CTA has any left)
   if (n_qf > 0) drain_wait(B_QF, (n_qf - 1) & 1);
   for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
-    if (n_kv[s] > 0) drain_wait(B_KV(s), (n_kv[s] - 1) & 1);
+    if (ld_g > s) drain_wait(B_KV(s), ((ld_g - 1 - s) / NS) & 1);
   for (uint32_t b = 0; b < 2; ++b)
-    if (n_m1[b] > 0) drain_wait(B_MM1(b), (n_m1[b] - 1) & 1);
+    if (n_sdp > b) drain_wait(B_MM1(b), ((n_sdp - 1 - b) >> 1) & 1);
   if (n_m2 > 0) drain_wait(B_MM2, (n_m2 - 1) & 1);
   tc_fence_before();
   __syncthreads();
@@ -572,10 +575,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int32_t warp = threadIdx.x >> 5;
-  const int32_t lane_row = threadIdx.x;  // key row == TMEM lane (threads 0..127)
-  const bool compute = threadIdx.x < 128;
-  const bool issuer = threadIdx.x == 128;    // MMAs
-  const bool producer = threadIdx.x == 160;  // copies
+  const int32_t lane_row = threadIdx.x & 127;  // key row == TMEM lane
+  const int32_t half = threadIdx.x >> 7;         // this thread's 32 query rows of a sub-tile
+  const bool compute = threadIdx.x < 256;
+  const bool issuer = threadIdx.x == 256;    // MMAs
+  const bool producer = threadIdx.x == 288;  // copies
   const uint32_t B_KF = sbase + Ly::kBarOff;
   auto B_QS = [&](uint32_t s) { return B_KF + 8 + 8 * s; };
   const uint32_t B_MM1 = B_KF + 8 + 8 * NS, B_MM2 = B_MM1 + 8;
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_t = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int32_t G = a.G, TS = kKvRows / G;  // tokens per sub-tile
   const uint32_t k_lo = ((sbase + Ly::kKOff) >> 4) | (1u << 16);
   const uint32_t v_lo = ((sbase + Ly::kVOff) >> 4) | (1u << 16);
@@ -611,7 +615,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr uint32_t kIdV = idesc_f32acc(128, kDv, 1, 0, 1);
   constexpr uint32_t kIdK = idesc_f32acc(128, kDqk, 1, 0, 1);
   constexpr uint32_t kColST = 0, kColPT = 64, kColV = 128, kColK = 256, kColP = 448, kColDS = 480;
-  uint32_t n_kf = 0, n_qs[NS] = {}, n_m1 = 0, n_m2 = 0;
+  // issue counts, kept alike by all threads; sub-tile g is the (g / NS)-th
+  // load of stage g % NS
+  uint32_t n_kf = 0, n_m1 = 0, n_m2 = 0;
   bool ok = true;
 
   // ---- Q/dO loader: walks this CTA's (item, sub-tile) sequence ahead of the keys
@@ -631,7 +637,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(dst + (3 + cc) * Ly::kQBox, &tm_do, cc * 64, ld.kvh * G, tok, B_QS(st));
     }
-    ++n_qs[st];
     ++ld_g;
     if (++ld_j >= ld.nsub) {
       ld_j = 0;
@@ -674,7 +679,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t st = g % NS;
     ++n_m1;
     if (issuer && go) {
-      if (!wait_bar(B_QS(st), (n_qs[st] - 1) & 1, abort_flag, 25)) return false;
+      if (!wait_bar(B_QS(st), (g / NS) & 1, abort_flag, 25)) return false;
       tc_fence_after();
       const uint32_t q_lo = ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) | (1u << 16);
       const uint32_t do_lo = q_lo + ((3 * Ly::kQBox) >> 4);
@@ -708,7 +713,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   while (ok && cur.valid) {
     KvItem nxt;
     const int32_t it_n = kv_next_item(a, it + gridDim.x, nxt);
-    const int32_t kj = cur.k0 + lane_row;  // this thread's key
+    const int32_t kj = cur.k0 + lane_row;  // this thread's key (both halves)
     const bool kvalid = compute && kj < cur.L;
     if (issuer) ok = wait_bar(B_KF, (n_kf - 1) & 1, abort_flag, 24);
     ok = issue_sdp(g0, ok) && ok;
@@ -726,31 +731,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fetch_rows(cur, sidx + 1);
       else if (nxt.valid)
         fetch_rows(nxt, 0);
-      uint32_t sv[64], pv[64];
+      uint32_t sv[32], pv[32];
       if (compute) {
         // S^T(g), dP^T(g) complete
         if (!wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 26)) ok = false;
         tc_fence_after();
-        const float4 *cl4 = reinterpret_cast<const float4 *>(c_lse + (g & 1) * kKvRows);
-        const float4 *cd4 = reinterpret_cast<const float4 *>(c_D + (g & 1) * kKvRows);
+        const float4 *cl4 = reinterpret_cast<const float4 *>(c_lse + (g & 1) * kKvRows + 32 * half);
+        const float4 *cd4 = reinterpret_cast<const float4 *>(c_D + (g & 1) * kKvRows + 32 * half);
         // column c is query token i0 + c / G: this key is seen by the columns
         // with i0 + c / G in [kj, min(L, kj + W) - 1], i.e. c in [c_lo, c_hi)
-        // (token counts clamped to one sub-tile first, so no product overflows)
+        // (token counts clamped to one sub-tile first, so no product overflows);
+        // this thread takes columns 32 half .. 32 half + 31
         const int32_t d0 = kj - i0;
-        const int32_t c_lo = d0 > 0 ? d0 * G : 0;
+        const int32_t c_lo = (d0 > 0 ? d0 * G : 0) - 32 * half;
         int32_t c_hi = min(cur.L - i0, kKvRows) * G;
         if (a.window > 0) c_hi = min(c_hi, max(0, min(d0 + a.window, kKvRows)) * G);
-        c_hi = min(c_hi, kKvRows);
+        c_hi = min(c_hi, kKvRows) - 32 * half;
         const uint32_t span = (kvalid && c_hi > c_lo) ? static_cast<uint32_t>(c_hi - c_lo) : 0u;
-        tmem_ld32p(lane_t + kColST, sv);
-        tmem_ld32p(lane_t + kColST + 32, sv + 32);
-        tmem_ld32p(lane_t + kColPT, pv);
-        tmem_ld32p(lane_t + kColPT + 32, pv + 32);
+        tmem_ld32p(lane_t + kColST + 32 * half, sv);
+        tmem_ld32p(lane_t + kColPT + 32 * half, pv);
         tmem_wait_ld();
-        reg_fence<64>(sv);
-        reg_fence<64>(pv);
+        reg_fence<32>(sv);
+        reg_fence<32>(pv);
 #pragma unroll
-        for (int32_t c = 0; c < kKvRows; c += 4) {
+        for (int32_t c = 0; c < 32; c += 4) {
           const float4 l4 = cl4[c >> 2], d4 = cd4[c >> 2];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
           float pp[4], ds[4];
@@ -772,8 +776,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       while (ld.valid && ld_g <= g + 2) load_next();
       if (compute) {
         tc_fence_after();
-        tmem_st32p(lane_t + kColP, sv);   // P^T as bf16 pairs
-        tmem_st32p(lane_t + kColDS, pv);  // dS^T as bf16 pairs
+        tmem_st16p(lane_t + kColP + 16 * half, sv);   // P^T as bf16 pairs
+        tmem_st16p(lane_t + kColDS + 16 * half, pv);  // dS^T as bf16 pairs
         tmem_wait_st();
       }
       // slot (g+1) & 1 was last read in sub-tile g-1
@@ -802,7 +806,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++n_m2;
     }
     if (!ok) break;
-    if (compute) {
+    if (compute && half == 0) {
       ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 27);
       tc_fence_after();
       // dV row: 128 fp32 columns -> bf16
@@ -834,7 +838,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (n_kf > 0) drain_wait(B_KF, (n_kf - 1) & 1);
   for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
-    if (n_qs[s] > 0) drain_wait(B_QS(s), (n_qs[s] - 1) & 1);
+    if (ld_g > s) drain_wait(B_QS(s), ((ld_g - 1 - s) / NS) & 1);
   if (n_m1 > 0) drain_wait(B_MM1, (n_m1 - 1) & 1);
   if (n_m2 > 0) drain_wait(B_MM2, (n_m2 - 1) & 1);
   tc_fence_before();
