@@ -561,7 +561,8 @@ static_assert(KvLayout::kDynSmem <= 232448, "dkdv kernel shared memory");
 // After the one CTA barrier of sub-tile g, S^T/dP^T(g+1) go out first and
 // dV/dK(g) behind them, so the rows work on sub-tile g+1 while dV/dK(g) run;
 // they wait for dV/dK(g) only before writing P^T/dS^T(g+1).  Q/dO sub-tiles
-// stream through three stages, loaded two ahead and across item boundaries;
+// (last query rows first) stream through three stages, loaded two ahead and
+// across item boundaries;
 // the next item's K/V block is loaded once the last S^T/dP^T of the current
 // item is done.
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -620,6 +621,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint32_t n_kf = 0, n_m1 = 0, n_m2 = 0;
   bool ok = true;
 
+  // Sub-tile s of an item starts at query token sub0(d, s): the sub-tiles are
+  // walked from the last query rows down, so the CTAs working on the blocks of
+  // one KV head at the same time stream the same query rows together (L2 then
+  // serves the re-reads; walking up, each CTA would start at its own block).
+  auto sub0 = [&](const KvItem &d, int32_t sidx) { return d.i_lo + (d.nsub - 1 - sidx) * TS; };
   // ---- Q/dO loader: walks this CTA's (item, sub-tile) sequence ahead of the keys
   KvItem ld;
   int32_t ld_it = kv_next_item(a, blockIdx.x, ld), ld_j = 0;
@@ -628,7 +634,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t st = ld_g % NS;
     if (producer) {
       const uint32_t dst = sbase + Ly::kStOff + st * Ly::kStage;
-      const int32_t tok = ld.s0 + ld.i_lo + ld_j * TS;
+      const int32_t tok = ld.s0 + sub0(ld, ld_j);
       mbar_arrive_expect_tx(B_QS(st), Ly::kStage);
 #pragma unroll
       for (int cc = 0; cc < 3; ++cc)
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float r_lse = 0.f, r_D = 0.f;
   auto fetch_rows = [&](const KvItem &d, int32_t sidx) {
     if (threadIdx.x < kKvRows) {
-      const int32_t ti = d.i_lo + sidx * TS + threadIdx.x / G, h = d.kvh * G + threadIdx.x % G;
+      const int32_t ti = sub0(d, sidx) + threadIdx.x / G, h = d.kvh * G + threadIdx.x % G;
       const bool v = ti < d.L;
       const size_t grow = static_cast<size_t>(d.s0 + ti) * a.Hq + h;
       r_lse = v ? __ldg(a.lse + grow) * kLog2e : 0.f;
@@ -719,7 +725,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ok = issue_sdp(g0, ok) && ok;
     for (int32_t sidx = 0; sidx < cur.nsub; ++sidx) {
       const uint32_t g = g0 + sidx;
-      const int32_t i0 = cur.i_lo + sidx * TS;
+      const int32_t i0 = sub0(cur, sidx);
       // the last S^T/dP^T of this item done: K/V can take the next item's
       if (sidx == cur.nsub - 1 && nxt.valid) {
         if (producer && ok) ok = wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 26);
