@@ -297,27 +297,60 @@ def bench_hybrid(name, steps, warmup, ws, local):
     out = torch.empty(total, hq, 128, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(total, hq, dtype=torch.float32, device=dev)
 
-    def call():
+    def swa_layers():
         for i in range(wl["swa_layers"]):
             sa.prefill(swa.q, swa.k, swa.v, sinks[i], swa.cu_seqlens, max_seqlen=max(lens),
                        window=wl["window"], rope_base=wl["swa_base"], out=out, lse=lse)
+
+    def ga_layers():
         for i in range(wl["ga_layers"]):
             sa.prefill(ga.q, ga.k, ga.v, sinks[wl["swa_layers"] + i], ga.cu_seqlens,
                        max_seqlen=max(lens), window=0, rope_base=wl["ga_base"], out=out, lse=lse)
 
+    def call():
+        swa_layers()
+        ga_layers()
+
     with ClockSampler(local) as clk:
         ms, _ = time_calls(call, steps, warmup, ws)
+    # the split of one pass between the SWA layers and the GA layer (events
+    # around each part on the launching stream, three passes averaged)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    swa_ms = ga_ms = 0.0
+    for _ in range(3):
+        ev[0].record()
+        swa_layers()
+        ev[1].record()
+        ga_layers()
+        ev[2].record()
+        torch.cuda.synchronize()
+        swa_ms += ev[0].elapsed_time(ev[1]) / (3 * wl["swa_layers"])
+        ga_ms += ev[1].elapsed_time(ev[2]) / (3 * wl["ga_layers"])
     st, word = sa.device_status()
     if st != sa.OK:
         raise RuntimeError(f"device status {st} word {word:#x} after {name}")
     swa_pairs = synth.algorithmic_pairs_prefill(lens, wl["window"])
     ga_pairs = synth.algorithmic_pairs_prefill(lens, 0)
     flops = hq * FLOP_PER_PAIR_HEAD * (wl["swa_layers"] * swa_pairs + wl["ga_layers"] * ga_pairs)
+    hkv = wl["swa_hkv"]
+    per_layer = {"swa_ms": swa_ms, "ga_ms": ga_ms,
+                 "swa_bytes": total * (hq * 192 * 2 + hkv * 192 * 2 + hkv * 128 * 2 + hq * 128 * 2
+                                       + hq * 4),
+                 "ga_flops": hq * FLOP_PER_PAIR_HEAD * ga_pairs}
     res = {"name": name, "ms": ms, "flops": flops, "tokens": total, "lens": lens,
-           "clocks": clk.summary(), "launches": n_layers * steps}
+           "clocks": clk.summary(), "launches": n_layers * steps, "per_layer": per_layer}
     del swa, ga, out, lse
     torch.cuda.empty_cache()
     return res
+
+
+def per_layer_roofline(pl, peaks):
+    """Time and roofline fraction of one SWA layer (HBM-bound) and one GA layer
+    (tensor-bound) of a hybrid block pass."""
+    swa_gbs = pl["swa_bytes"] / (pl["swa_ms"] / 1e3) / 1e9
+    ga_tf = pl["ga_flops"] / (pl["ga_ms"] / 1e3) / 1e12
+    return {"swa_ms": pl["swa_ms"], "swa_gbs": swa_gbs, "swa_frac_hbm": swa_gbs / peaks["hbm_gbs"],
+            "ga_ms": pl["ga_ms"], "ga_tflops": ga_tf, "ga_frac_tensor": ga_tf / peaks["bf16_tflops"]}
 
 
 def bench_ratio(name, warmup, ws, local):
@@ -581,7 +614,8 @@ def single_workload(args, ws, rank, local, peaks):
     elif wl["kind"] == "hybrid":
         r = bench_hybrid(args.workload, args.steps, args.warmup, ws, local)
         line = {"workload": args.workload, "ms": r["ms"], "tokens_per_s": r["tokens"] / (r["ms"] / 1e3),
-                "tflops": r["flops"] / (r["ms"] / 1e3) / 1e12, "lens": r["lens"], "clocks": r["clocks"]}
+                "tflops": r["flops"] / (r["ms"] / 1e3) / 1e12, "lens": r["lens"],
+                "per_layer": per_layer_roofline(r["per_layer"], peaks), "clocks": r["clocks"]}
     elif wl["kind"] == "prefill":
         r = bench_prefill(args.workload, args.steps, args.warmup, ws, local, with_e2e=False)
         tf = r["flops"] / (r["ms"] / 1e3) / 1e12
@@ -703,7 +737,7 @@ def main():
             "value": ws * h["tokens"] / (h["ms"] / 1e3), "unit": "tokens/s",
             "ms_per_step": h["ms"], "tflops": h["flops"] / (h["ms"] / 1e3) / 1e12,
             "seq_lens": h["lens"], "layers": "5 SWA (64/8, W=128) + 1 GA (64/4)",
-            "clocks": h["clocks"]}
+            "per_layer": per_layer_roofline(h["per_layer"], peaks), "clocks": h["clocks"]}
         for name, bound in (("swa_backward_4x32768", "hbm"), ("ga_backward_1x32768", "tensor")):
             r = bench_backward(name, max(3, args.steps // 4), args.warmup, ws, local)
             tf = r["flops"] / (r["ms"] / 1e3) / 1e12
