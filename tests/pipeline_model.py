@@ -1,0 +1,319 @@
+"""CPU model of the mbarrier pipelines of the backward kernels (dq and dk/dv).
+
+Each kernel role (the copy thread, the MMA thread, the row threads of the two
+column halves) is a generator that yields the operations it performs, in the
+order the kernel performs them:
+
+  ("wait", bar, n)         block until `bar` has completed n phases.  The kernel
+                           waits on the parity of phase n-1, which is only
+                           unambiguous while the barrier has completed at most
+                           n phases: the model fails if it ever sees more.
+  ("arrive", bar)          one arrival (every barrier here completes a phase on
+                           one arrival: a commit or a copy's transaction count).
+  ("tma", res, tag, bar)   an asynchronous copy: later, in any order, `res` gets
+                           `tag` and `bar` completes a phase.
+  ("mma", reads, writes)   an MMA joins the tensor pipe, which executes in issue
+                           order; on execution every (res, tag) it reads must hold
+                           that tag, then every (res, tag) it writes is set.
+  ("commit", bar)          joins the tensor pipe behind the MMAs issued so far;
+                           `bar` completes a phase when it is reached.
+  ("read", res, tag)       a thread reads `res` (TMEM or shared memory): it must
+                           hold `tag` (written and complete, not overwritten yet).
+  ("write", res, tag)      a thread writes `res`.
+  ("sync",)                the CTA barrier: every role must arrive.
+
+A scheduler picks at random among the runnable roles, the copies in flight and
+the head of the tensor pipe, so one run is one interleaving; many runs with
+different seeds explore many.  A run fails on a deadlock, an ambiguous parity
+wait, or a read of a resource that does not hold what the reader expects (a
+read before the write landed, or after the next write replaced it).
+"""
+import random
+
+
+class ModelError(AssertionError):
+    pass
+
+
+class Sim:
+    def __init__(self, roles, rng):
+        self.rng = rng
+        self.roles = dict(roles)              # name -> generator
+        self.pending = {n: None for n in self.roles}  # the op a role is blocked on
+        self.done = set()
+        self.phases = {}                      # barrier -> completed phases
+        self.res = {}                         # resource -> tag
+        self.tma = []                         # copies in flight: (res, tag, bar)
+        self.pipe = []                        # tensor pipe: ("mma", reads, writes) | ("commit", bar)
+        self.sync_waiting = set()
+
+    def _complete(self, bar):
+        self.phases[bar] = self.phases.get(bar, 0) + 1
+
+    def _check_waits(self):
+        for name, op in self.pending.items():
+            if op is not None and op[0] == "wait":
+                _, bar, n = op
+                if self.phases.get(bar, 0) > n:
+                    raise ModelError(f"{name}: waits for phase {n} of {bar}, which has "
+                                     f"completed {self.phases[bar]} (parity wait ambiguous)")
+
+    def _runnable(self, name):
+        op = self.pending[name]
+        if op is None:
+            return True
+        if op[0] == "wait":
+            return self.phases.get(op[1], 0) >= op[2]
+        if op[0] == "sync":
+            return False
+        return True
+
+    def _step_role(self, name):
+        op = self.pending[name]
+        if op is not None:
+            kind = op[0]
+            if kind == "wait":
+                pass  # satisfied (checked by _runnable)
+            elif kind == "arrive":
+                self._complete(op[1])
+            elif kind == "tma":
+                self.tma.append(op[1:])
+            elif kind == "mma":
+                self.pipe.append(op)
+            elif kind == "commit":
+                self.pipe.append(op)
+            elif kind == "read":
+                _, r, tag = op
+                if self.res.get(r) != tag:
+                    raise ModelError(f"{name}: reads {r} expecting {tag}, holds {self.res.get(r)}")
+            elif kind == "write":
+                self.res[op[1]] = op[2]
+            else:
+                raise ValueError(op)
+        try:
+            self.pending[name] = next(self.roles[name])
+        except StopIteration:
+            self.pending[name] = None
+            self.done.add(name)
+            return
+        if self.pending[name][0] == "sync":
+            self.sync_waiting.add(name)
+
+    def run(self, max_steps=2_000_000):
+        for name in self.roles:
+            self._step_role_first(name)
+        for _ in range(max_steps):
+            self._check_waits()
+            live = [n for n in self.roles if n not in self.done]
+            if not live and not self.tma and not self.pipe:
+                return
+            # the CTA barrier releases once every live role has reached it
+            if live and self.sync_waiting == set(live):
+                self.sync_waiting.clear()
+                for n in live:
+                    self.pending[n] = ("wait", "__none__", 0)  # released: no-op
+                    self.phases.setdefault("__none__", 0)
+            choices = [("role", n) for n in live if self._runnable(n)]
+            choices += [("tma", i) for i in range(len(self.tma))]
+            if self.pipe:
+                choices.append(("pipe", 0))
+            if not choices:
+                state = {n: self.pending[n] for n in live}
+                raise ModelError(f"deadlock: {state}")
+            kind, i = self.rng.choice(choices)
+            if kind == "role":
+                self._step_role(i)
+            elif kind == "tma":
+                r, tag, bar = self.tma.pop(i)
+                self.res[r] = tag
+                self._complete(bar)
+            else:
+                op = self.pipe.pop(0)
+                if op[0] == "commit":
+                    self._complete(op[1])
+                else:
+                    _, reads, writes = op
+                    for r, tag in reads:
+                        if self.res.get(r) != tag:
+                            raise ModelError(f"MMA reads {r} expecting {tag}, holds {self.res.get(r)}")
+                    for r, tag in writes:
+                        self.res[r] = tag
+        raise ModelError("step limit")
+
+    def _step_role_first(self, name):
+        try:
+            self.pending[name] = next(self.roles[name])
+        except StopIteration:
+            self.pending[name] = None
+            self.done.add(name)
+            return
+        if self.pending[name][0] == "sync":
+            self.sync_waiting.add(name)
+
+
+NS = 3  # K/V (dq) or Q/dO (dk/dv) stages
+
+
+def dq_roles(nblk, skip=()):
+    """The dq kernel for one CTA whose items have nblk[i] key blocks each.
+    `skip` names waits to leave out (to show that the model notices)."""
+    items = list(nblk)
+    seq = [(it, j) for it, n in enumerate(items) for j in range(n)]  # loader order
+    first = [sum(items[:i]) for i in range(len(items))]
+
+    def producer():
+        yield ("tma", "QO", ("QO", 0), "QF")
+        ld = 0
+        while ld < len(seq) and ld < NS:
+            yield ("tma", f"KV{ld % NS}", ("KV", ld), f"KV{ld % NS}")
+            ld += 1
+        n_m2 = 0
+        for it, n in enumerate(items):
+            g0 = first[it]
+            for j in range(n):
+                g = g0 + j
+                if n_m2 > 0 and "producer_mm2" not in skip:
+                    yield ("wait", "MM2", n_m2)  # dQ(g-1): the stage of block g+2 is free
+                while ld < len(seq) and ld <= g + 2:
+                    yield ("tma", f"KV{ld % NS}", ("KV", ld), f"KV{ld % NS}")
+                    ld += 1
+                if j == n - 1 and it + 1 < len(items):
+                    if "producer_mm1" not in skip:
+                        yield ("wait", f"MM1{g & 1}", (g >> 1) + 1)  # last S/dP of the item
+                    yield ("tma", "QO", ("QO", it + 1), "QF")
+                yield ("sync",)
+                n_m2 += 1
+            yield ("sync",)
+
+    def issuer():
+        def issue_sdp(it, g):
+            yield ("wait", f"KV{g % NS}", g // NS + 1)
+            b = g & 1
+            yield ("mma", [("QO", ("QO", it)), (f"KV{g % NS}", ("KV", g))],
+                   [(f"S{b}h0", ("S", g)), (f"S{b}h1", ("S", g))])
+            yield ("commit", f"MM1{b}")
+        for it, n in enumerate(items):
+            g0 = first[it]
+            yield ("wait", "QF", it + 1)
+            yield from issue_sdp(it, g0)
+            for j in range(n):
+                g = g0 + j
+                if j + 1 < n:
+                    yield from issue_sdp(it, g + 1)
+                yield ("sync",)
+                b = g & 1
+                reads = [(f"S{b}h0", ("dS", g)), (f"S{b}h1", ("dS", g)), (f"KV{g % NS}", ("KV", g))]
+                if j > 0:
+                    reads.append(("dQ", ("dQ", it, j - 1)))
+                yield ("mma", reads, [("dQ", ("dQ", it, j))])
+                yield ("commit", "MM2")
+            yield ("sync",)
+
+    def rows(h):
+        def role():
+            n_m2 = 0
+            for it, n in enumerate(items):
+                g0 = first[it]
+                for j in range(n):
+                    g = g0 + j
+                    b = g & 1
+                    yield ("wait", f"MM1{b}", (g >> 1) + 1)
+                    yield ("read", f"S{b}h{h}", ("S", g))
+                    yield ("write", f"S{b}h{h}", ("dS", g))  # dS over this half's S columns
+                    yield ("sync",)
+                    n_m2 += 1
+                if h == 0:  # the epilogue runs on the first half
+                    if "rows_mm2" not in skip:
+                        yield ("wait", "MM2", n_m2)
+                    yield ("read", "dQ", ("dQ", it, n - 1))
+                yield ("sync",)
+        return role()
+
+    return {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}
+
+
+def dkdv_roles(nsub, skip=()):
+    """The dk/dv kernel for one CTA whose items (key blocks) have nsub[i] query
+    sub-tiles each.  `skip` names waits to leave out."""
+    items = list(nsub)
+    seq = [(it, j) for it, n in enumerate(items) for j in range(n)]
+    first = [sum(items[:i]) for i in range(len(items))]
+
+    def producer():
+        yield ("tma", "KVB", ("KVB", 0), "KF")
+        ld = 0
+        while ld < len(seq) and ld < NS:
+            yield ("tma", f"QO{ld % NS}", ("QO", ld), f"QS{ld % NS}")
+            ld += 1
+        n_m1 = 1  # S^T/dP^T of the first sub-tile, issued at the first item's start
+        n_m2 = 0
+        for it, n in enumerate(items):
+            g0 = first[it]
+            if it > 0:
+                n_m1 += 1
+            for s in range(n):
+                g = g0 + s
+                if s == n - 1 and it + 1 < len(items):
+                    yield ("wait", "MM1", n_m1)  # the last S^T/dP^T of the item
+                    yield ("tma", "KVB", ("KVB", it + 1), "KF")
+                if n_m2 > 0 and "producer_mm2" not in skip:
+                    yield ("wait", "MM2", n_m2)  # dV/dK(g-1): the stage of sub-tile g+2 is free
+                while ld < len(seq) and ld <= g + 2:
+                    yield ("tma", f"QO{ld % NS}", ("QO", ld), f"QS{ld % NS}")
+                    ld += 1
+                yield ("sync",)
+                n_m2 += 1
+                if s + 1 < n:
+                    n_m1 += 1
+            yield ("sync",)
+
+    def issuer():
+        def issue_sdp(it, g):
+            yield ("wait", f"QS{g % NS}", g // NS + 1)
+            yield ("mma", [("KVB", ("KVB", it)), (f"QO{g % NS}", ("QO", g))],
+                   [("STh0", ("ST", g)), ("STh1", ("ST", g))])
+            yield ("commit", "MM1")
+        for it, n in enumerate(items):
+            g0 = first[it]
+            yield ("wait", "KF", it + 1)
+            yield from issue_sdp(it, g0)
+            for s in range(n):
+                g = g0 + s
+                yield ("sync",)
+                if s + 1 < n:
+                    yield from issue_sdp(it, g + 1)  # S^T/dP^T(g+1) ahead of dV/dK(g)
+                reads = [("Ph0", ("P", g)), ("Ph1", ("P", g)), (f"QO{g % NS}", ("QO", g))]
+                if s > 0:
+                    reads.append(("acc", ("acc", it, s - 1)))
+                yield ("mma", reads, [("acc", ("acc", it, s))])
+                yield ("commit", "MM2")
+            yield ("sync",)
+
+    def rows(h):
+        def role():
+            n_m1 = n_m2 = 0
+            for it, n in enumerate(items):
+                g0 = first[it]
+                n_m1 += 1
+                for s in range(n):
+                    g = g0 + s
+                    yield ("wait", "MM1", n_m1)
+                    yield ("read", f"STh{h}", ("ST", g))
+                    if n_m2 > 0 and "rows_mm2" not in skip:
+                        yield ("wait", "MM2", n_m2)  # dV/dK(g-1) read P^T/dS^T
+                    yield ("write", f"Ph{h}", ("P", g))
+                    yield ("sync",)
+                    n_m2 += 1
+                    if s + 1 < n:
+                        n_m1 += 1
+                if h == 0:
+                    yield ("wait", "MM2", n_m2)
+                    yield ("read", "acc", ("acc", it, n - 1))
+                yield ("sync",)
+        return role()
+
+    return {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}
+
+
+def run(make_roles, sizes, seed, skip=()):
+    Sim(make_roles(sizes, skip), random.Random(seed)).run()

@@ -1,0 +1,61 @@
+"""The barrier protocols of the backward kernels, checked on a CPU model
+(tests/pipeline_model.py) over many random interleavings: no deadlock, no
+parity wait that its barrier has already passed by two phases, and no MMA or
+thread that reads a shared-memory stage or TMEM region before the data it
+expects has landed or after the next write replaced it.  The model transcribes
+the roles of bwd_dq_kernel and bwd_dkdv_kernel (backward_kernel.cuh); a wait
+left out of it must be caught, which the last tests check."""
+import random
+
+import pytest
+
+from pipeline_model import ModelError, dkdv_roles, dq_roles, run
+
+SIZES = [[1], [2], [3], [1, 1, 1], [1, 2, 1, 3], [3, 3, 3], [5, 1, 4], [2, 7], [1] * 6]
+
+
+def _random_sizes(rng):
+    return [rng.choice([1, 1, 2, 3, 4, 6]) for _ in range(rng.randint(1, 5))]
+
+
+@pytest.mark.parametrize("sizes", SIZES)
+def test_dq_pipeline(sizes):
+    for seed in range(60):
+        run(dq_roles, sizes, seed)
+
+
+@pytest.mark.parametrize("sizes", SIZES)
+def test_dkdv_pipeline(sizes):
+    for seed in range(60):
+        run(dkdv_roles, sizes, seed)
+
+
+def test_random_item_lists():
+    rng = random.Random(7)
+    for seed in range(200):
+        sizes = _random_sizes(rng)
+        run(dq_roles, sizes, seed)
+        run(dkdv_roles, sizes, seed)
+
+
+def _caught(make_roles, skip, sizes=(3, 2, 4)):
+    for seed in range(400):
+        try:
+            run(make_roles, list(sizes), seed, skip=skip)
+        except ModelError:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("skip,sizes", [("producer_mm2", (3, 2, 4)), ("rows_mm2", (3, 2, 4)),
+                                        # with two or more blocks the wait for dQ(g-1) already
+                                        # orders the item's last S/dP before the Q/dO reload;
+                                        # items of one block need the wait on it
+                                        ("producer_mm1", (1, 1, 2, 1))])
+def test_dq_missing_wait_is_caught(skip, sizes):
+    assert _caught(dq_roles, (skip,), sizes)
+
+
+@pytest.mark.parametrize("skip", ["producer_mm2", "rows_mm2"])
+def test_dkdv_missing_wait_is_caught(skip):
+    assert _caught(dkdv_roles, (skip,))
