@@ -1,4 +1,5 @@
-"""CPU model of the mbarrier pipelines of the backward kernels (dq and dk/dv).
+"""CPU model of the mbarrier pipelines of the decode kernel and of the backward
+kernels (dq and dk/dv).
 
 Each kernel role (the copy thread, the MMA thread, the row threads of the two
 column halves) is a generator that yields the operations it performs, in the
@@ -317,3 +318,107 @@ def dkdv_roles(nsub, skip=()):
 
 def run(make_roles, sizes, seed, skip=()):
     Sim(make_roles(sizes, skip), random.Random(seed)).run()
+
+
+def decode_roles(nblk, f8=False, skip=()):
+    """sinkattn_decode_kernel for one CTA whose segments (the cache blocks of a
+    unit in this CTA's range) have nblk[i] 64-key blocks each: the copy thread,
+    the MMA thread, the softmax rows and the RoPE / conversion warps.  bf16
+    cache: four K/V stages the copies fill.  FP8 cache: two staging slots the
+    copies fill and three fp16 stages the conversion warps fill.  QK^T(j) is
+    issued before PV(j-1), which waits for the softmax of block j-1."""
+    segs = list(nblk)
+    S = 3 if f8 else 4
+    S8 = 2
+
+    def producer():
+        gk = 0
+        for q, n in enumerate(segs):
+            yield ("wait", "QEMPTY", q)  # the previous segment's last QK^T read Q
+            yield ("tma", "Q", ("Qraw", q), "QFULL")
+            for _ in range(n):
+                if f8:
+                    s8 = gk % S8
+                    yield ("wait", f"STGEMPTY{s8}", gk // S8)
+                    yield ("tma", f"STG{s8}", ("stg", gk), f"STGFULL{s8}")
+                else:
+                    st = gk % S
+                    if "producer_kvempty" not in skip:
+                        yield ("wait", f"KVEMPTY{st}", gk // S)
+                    yield ("tma", f"K{st}", ("Kraw", gk), f"KVFULL{st}")
+                    yield ("tma", f"V{st}", ("V", gk), f"KVFULL{st}")
+                gk += 1
+
+    def mma():
+        gk = 0
+
+        def issue_pv(q, j, b, first):
+            yield ("wait", f"PFULL{b & 1}", (b >> 1) + 1)
+            if first:
+                yield ("wait", "OEMPTY", q)
+            reads = [(f"P{b & 1}", ("P", b)), (f"V{b % S}", ("V", b))]
+            if not first:
+                reads.append(("O", ("Ors", q, j - 1)))
+            yield ("mma", reads, [("O", ("O", q, j))])
+            yield ("commit", f"KVEMPTY{b % S}")
+            yield ("commit", "PVDONE")
+
+        for q, n in enumerate(segs):
+            yield ("wait", "QREADY", q + 1)
+            for j in range(n):
+                b = gk + j
+                yield ("wait", f"KREADY{b % S}", b // S + 1)
+                yield ("mma", [("Q", ("Q", q)), (f"K{b % S}", ("K", b))], [(f"P{b & 1}", ("S", b))])
+                yield ("commit", f"SFULL{b & 1}")
+                if j == n - 1:
+                    yield ("commit", "QEMPTY")
+                if j > 0:
+                    yield from issue_pv(q, j - 1, b - 1, j == 1)
+            yield from issue_pv(q, n - 1, gk + n - 1, n == 1)
+            gk += n
+
+    def softmax():
+        gs = 0
+        for q, n in enumerate(segs):
+            for j in range(n):
+                b = gs + j
+                yield ("wait", f"SFULL{b & 1}", (b >> 1) + 1)
+                yield ("read", f"P{b & 1}", ("S", b))
+                yield ("write", f"P{b & 1}", ("P", b))  # P over the S columns
+                if j > 0:
+                    if "softmax_pvdone" not in skip:
+                        yield ("wait", "PVDONE", b)  # PV(j-1) complete
+                    yield ("read", "O", ("O", q, j - 1))
+                    yield ("write", "O", ("Ors", q, j - 1))  # rescale before PV(j)
+                yield ("arrive", f"PFULL{b & 1}")
+            yield ("wait", "PVDONE", gs + n)
+            yield ("read", "O", ("O", q, n - 1))
+            yield ("arrive", "OEMPTY")
+            gs += n
+
+    def convert():
+        gk = 0
+        for q, n in enumerate(segs):
+            yield ("wait", "QFULL", q + 1)
+            yield ("read", "Q", ("Qraw", q))
+            yield ("write", "Q", ("Q", q))  # RoPE (and fp16) in place
+            yield ("arrive", "QREADY")
+            for _ in range(n):
+                st = gk % S
+                if f8:
+                    s8 = gk % S8
+                    yield ("wait", f"STGFULL{s8}", gk // S8 + 1)
+                    if "convert_kvempty" not in skip:
+                        yield ("wait", f"KVEMPTY{st}", gk // S)  # PV(gk-S) read the stage
+                    yield ("read", f"STG{s8}", ("stg", gk))
+                    yield ("write", f"K{st}", ("K", gk))
+                    yield ("write", f"V{st}", ("V", gk))
+                    yield ("arrive", f"STGEMPTY{s8}")
+                else:
+                    yield ("wait", f"KVFULL{st}", 2 * (gk // S) + 2)  # K and V copies landed
+                    yield ("read", f"K{st}", ("Kraw", gk))
+                    yield ("write", f"K{st}", ("K", gk))  # RoPE in place
+                yield ("arrive", f"KREADY{st}")
+                gk += 1
+
+    return {"producer": producer(), "mma": mma(), "softmax": softmax(), "convert": convert()}

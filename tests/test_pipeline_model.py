@@ -1,15 +1,16 @@
-"""The barrier protocols of the backward kernels, checked on a CPU model
+"""The barrier protocols of the decode and backward kernels, checked on a CPU model
 (tests/pipeline_model.py) over many random interleavings: no deadlock, no
 parity wait that its barrier has already passed by two phases, and no MMA or
 thread that reads a shared-memory stage or TMEM region before the data it
 expects has landed or after the next write replaced it.  The model transcribes
-the roles of bwd_dq_kernel and bwd_dkdv_kernel (backward_kernel.cuh); a wait
-left out of it must be caught, which the last tests check."""
+the roles of sinkattn_decode_kernel (decode_kernel.cuh) and of bwd_dq_kernel
+and bwd_dkdv_kernel (backward_kernel.cuh); a wait left out of it must be
+caught, which the *_missing_wait_* tests check."""
 import random
 
 import pytest
 
-from pipeline_model import ModelError, dkdv_roles, dq_roles, run
+from pipeline_model import ModelError, decode_roles, dkdv_roles, dq_roles, run
 
 SIZES = [[1], [2], [3], [1, 1, 1], [1, 2, 1, 3], [3, 3, 3], [5, 1, 4], [2, 7], [1] * 6]
 
@@ -59,3 +60,16 @@ def test_dq_missing_wait_is_caught(skip, sizes):
 @pytest.mark.parametrize("skip", ["producer_mm2", "rows_mm2"])
 def test_dkdv_missing_wait_is_caught(skip):
     assert _caught(dkdv_roles, (skip,))
+
+
+@pytest.mark.parametrize("f8", [False, True])
+@pytest.mark.parametrize("sizes", [[1], [2], [5], [1, 1, 1], [3, 1, 4], [2, 6, 1, 2]])
+def test_decode_pipeline(f8, sizes):
+    for seed in range(60):
+        run(lambda s, sk: decode_roles(s, f8, sk), sizes, seed)
+
+
+@pytest.mark.parametrize("f8,skip", [(False, "producer_kvempty"), (True, "convert_kvempty"),
+                                     (False, "softmax_pvdone"), (True, "softmax_pvdone")])
+def test_decode_missing_wait_is_caught(f8, skip):
+    assert _caught(lambda s, sk: decode_roles(s, f8, sk), (skip,), (5, 3, 6))
