@@ -89,20 +89,29 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
     if (a.rope_on) rope_cs(pos, a.rope_turns[lane], c, s);
     const int32_t ia = a.rope_style == 0 ? 2 * lane : lane;
     const int32_t ib = a.rope_style == 0 ? 2 * lane + 1 : lane + 32;
-    // rotated copies: q (Hq heads) then k (Hkv heads)
+    // rotated copies: q (Hq heads) then k (Hkv heads); an interleaved pair is
+    // one 32-bit word
+#pragma unroll 4
     for (int32_t hh = 0; hh < a.Hq + a.Hkv; ++hh) {
       const bool isq = hh < a.Hq;
       const size_t row = isq ? static_cast<size_t>(tok) * a.Hq + hh
                              : static_cast<size_t>(tok) * a.Hkv + (hh - a.Hq);
       const __nv_bfloat16 *src = (isq ? a.q : a.k) + row * kDqk;
       __nv_bfloat16 *dst = (isq ? a.q_rot : a.k_rot) + row * kDqk;
-      const float x = __bfloat162float(src[ia]), y = __bfloat162float(src[ib]);
-      dst[ia] = __float2bfloat16_rn(x * c - y * s);
-      dst[ib] = __float2bfloat16_rn(x * s + y * c);
+      if (a.rope_style == 0) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(src + 2 * lane);
+        const float x = bf16lo(w), y = bf16hi(w);
+        *reinterpret_cast<uint32_t *>(dst + 2 * lane) = pack_bf16x2(x * c - y * s, x * s + y * c);
+      } else {
+        const float x = __bfloat162float(src[ia]), y = __bfloat162float(src[ib]);
+        dst[ia] = __float2bfloat16_rn(x * c - y * s);
+        dst[ib] = __float2bfloat16_rn(x * s + y * c);
+      }
       *reinterpret_cast<uint2 *>(dst + 64 + 4 * lane) =
           *reinterpret_cast<const uint2 *>(src + 64 + 4 * lane);
     }
     // D = dO . o per head (4 dims per lane, warp sum)
+#pragma unroll 4
     for (int32_t h = 0; h < a.Hq; ++h) {
       const size_t row = static_cast<size_t>(tok) * a.Hq + h;
       const uint2 ov = *reinterpret_cast<const uint2 *>(a.out + row * kDv + 4 * lane);
@@ -176,11 +185,13 @@ __device__ __forceinline__ void bwd_unrotate(float (&x)[64], int32_t pos, int32_
 
 // Row epilogue shared by the gradients of q and k: 192 fp32 columns of TMEM at
 // col (this thread's lane) -> * scale, inverse RoPE on dims 0..63, bf16 row.
+// Part 0 writes dims 0..95, part 1 dims 96..191 (the two threads of a row
+// share the epilogue); part -1 writes all of it.
 __device__ __forceinline__ void bwd_store_qk_row(uint32_t t_col, float scale, bool rope_on,
                                                  int32_t style, int32_t pos,
                                                  const unsigned long long *turns,
-                                                 __nv_bfloat16 *dst, bool valid) {
-  {
+                                                 __nv_bfloat16 *dst, bool valid, int32_t part = -1) {
+  if (part != 1) {
     uint32_t r[64];
     tmem_ld32p(t_col, r);
     tmem_ld32p(t_col + 32, r + 32);
@@ -199,8 +210,9 @@ __device__ __forceinline__ void bwd_store_qk_row(uint32_t t_col, float scale, bo
       }
     }
   }
+  const int32_t cb0 = part == 1 ? 96 : 64, cb1 = part == 0 ? 96 : 192;
 #pragma unroll 1
-  for (int32_t cb = 64; cb < 192; cb += 32) {
+  for (int32_t cb = cb0; cb < cb1; cb += 32) {
     uint32_t r[32];
     tmem_ld32p(t_col + cb, r);
     tmem_wait_ld();
@@ -475,11 +487,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++n_m2;
     }
     if (!ok) break;
-    if (compute && half == 0) {
+    if (compute) {
       ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 24);
       tc_fence_after();
       bwd_store_qk_row(lane_t + kDqColAcc, a.scale, a.rope_on, a.rope_style, ti, a.rope_turns,
-                       a.dq + grow * kDqk, rvalid);
+                       a.dq + grow * kDqk, rvalid, half);
     }
     tc_fence_before();
     ok = __syncthreads_and(ok);
@@ -812,9 +824,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++n_m2;
     }
     if (!ok) break;
-    if (compute && half == 0) {
+    if (compute) {
       ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 27);
       tc_fence_after();
+    }
+    if (compute && half == 0) {
       // dV row: 128 fp32 columns -> bf16
       __nv_bfloat16 *dst = a.dv + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDv;
 #pragma unroll 1
@@ -833,6 +847,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
+    }
+    if (compute && half == 1) {
       bwd_store_qk_row(lane_t + kColK, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
                        a.dk + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDqk, kvalid);
     }
