@@ -25,7 +25,7 @@
  * q and k, (3) form every logit of a row, (4) take the max including the sink,
  * (5) the denominator, (6) the weighted sum of values and the log-sum-exp.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - d in eq. (1) is the QK head dim; callers pass scale = 1/sqrt(192).
  *   - one sink per query head, in the units of the scaled logit, with no value
  *     vector (eq. (3) sums over keys only).

@@ -30,7 +30,7 @@ constexpr uint32_t kQBoxBytesHost = 128 * 128;  // one 64-dim box of a 128-row Q
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool pow2_upto_128(int32_t x) { return x >= 1 && x <= 128 && (x & (x - 1)) == 0; }
 
-// ----------------------------------------------------------------- driver entry
+// ----------------------------------------------------------------- CUDA driver entry point
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
