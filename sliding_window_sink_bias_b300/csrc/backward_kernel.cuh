@@ -276,8 +276,9 @@ struct DqLayout {
   static constexpr uint32_t kDoOff = 3 * kQBox;          // dO tile: 2 boxes
   static constexpr uint32_t kStOff = 5 * kQBox;          // stages: K 3 boxes, V 2 boxes
   static constexpr uint32_t kStage = 5 * kKBox;
-  static constexpr uint32_t kBarOff = kStOff + kStages * kStage;  // qf, kv[3], mm1[2], mm2
-  static constexpr uint32_t kMiscOff = kBarOff + 7 * 8;           // tmem slot, abort flag
+  // qf, kv_full[3], kv_empty[3], mm1[2], q_empty, acc_full, ds_ready[2], drain
+  static constexpr uint32_t kBarOff = kStOff + kStages * kStage;
+  static constexpr uint32_t kMiscOff = kBarOff + 14 * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
@@ -286,13 +287,23 @@ static_assert(DqLayout::kDynSmem <= 232448, "dq kernel shared memory");
 // dP at 128 b + 64), the dQ accumulator at 256..447.
 constexpr uint32_t kDqColAcc = 256;
 
-// Pipeline of the dq kernel (thread 128 issues the MMAs, thread 160 the
-// copies; threads 0..127 own one packed query row each):
-//   S(g+1), dP(g+1) are issued before the rows turn S(g), dP(g) into dS(g), so
-//   the tensor core works while they do; one CTA barrier per key block, after
-//   dS(g) is in TMEM, then dQ += dS(g) K(g).  K/V blocks stream through three
-//   stages, loaded two blocks ahead and across item boundaries; the next
-//   item's Q/dO tile is loaded once the last S/dP of the current item is done.
+// Roles of the dq kernel, which meet only on mbarriers (block g is the g-th key
+// block this CTA works on, over all its items):
+//   copy thread (288): the Q/dO tile of an item and the K/V blocks, through
+//     three stages; a stage is refilled once the dQ that read it is done
+//     (KV_EMPTY); the next item's Q/dO once the last S/dP of the item is done
+//     (Q_EMPTY).
+//   MMA thread (256): S(g+1), dP(g+1) go out before dQ(g), so the tensor core
+//     works while the rows turn S(g), dP(g) into dS(g); dQ(g) waits for all
+//     256 row threads to have written dS(g) (DS_READY); after an item's last
+//     dQ it hands the accumulator to the rows (ACC_FULL).
+//   rows (0..255, two threads per packed query row, 32 keys each): dS into
+//     TMEM over their own S columns, then at the end of an item the epilogue.
+//     The first dQ of the next item needs these threads' DS_READY arrivals,
+//     which come after their epilogue, so the accumulator is free by then.
+// Q_EMPTY and ACC_FULL complete once per item: a wait on a barrier that
+// completes per block could find it two phases behind (its parity would then
+// match at once).
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -309,18 +320,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const bool compute = threadIdx.x < 256;
   const bool issuer = threadIdx.x == 256;    // MMAs
   const bool producer = threadIdx.x == 288;  // copies
-  const uint32_t B_QF = sbase + Ly::kBarOff;
-  auto B_KV = [&](uint32_t s) { return B_QF + 8 + 8 * s; };
-  auto B_MM1 = [&](uint32_t b) { return B_QF + 8 + 8 * NS + 8 * b; };
-  const uint32_t B_MM2 = B_QF + 8 + 8 * NS + 16;
+  auto bar = [&](uint32_t i) { return sbase + Ly::kBarOff + 8 * i; };
+  const uint32_t B_QF = bar(0);
+  auto B_KV = [&](uint32_t s) { return bar(1 + s); };
+  auto B_KVE = [&](uint32_t s) { return bar(1 + NS + s); };
+  auto B_MM1 = [&](uint32_t b) { return bar(1 + 2 * NS + b); };
+  const uint32_t B_QE = bar(3 + 2 * NS), B_ACCF = bar(4 + 2 * NS);
+  auto B_DSR = [&](uint32_t b) { return bar(5 + 2 * NS + b); };
+  const uint32_t B_DRAIN = bar(7 + 2 * NS);
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
   if (issuer) {
     mbar_init(B_QF, 1);
-    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s) mbar_init(B_KV(s), 1);
-    mbar_init(B_MM1(0), 1);
-    mbar_init(B_MM1(1), 1);
-    mbar_init(B_MM2, 1);
+    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s) {
+      mbar_init(B_KV(s), 1);
+      mbar_init(B_KVE(s), 1);
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(B_MM1(b), 1);
+      mbar_init(B_DSR(b), 256);
+    }
+    mbar_init(B_QE, 1);
+    mbar_init(B_ACCF, 1);
+    mbar_init(B_DRAIN, 1);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -336,26 +358,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int32_t G = a.G;
-  const int32_t t_row = row / G, g_row = row % G;
-  const uint32_t q_lo = ((sbase + Ly::kQOff) >> 4) | (1u << 16);
-  const uint32_t do_lo = ((sbase + Ly::kDoOff) >> 4) | (1u << 16);
-  constexpr uint32_t kIdS = idesc_f32acc(128, kDqBN, 1, 0, 0);
-  constexpr uint32_t kIdQ = idesc_f32acc(128, kDqk, 1, 0, 1);
-  // issue counts, kept alike by all threads.  Block g is the (g / NS)-th load
-  // of stage g % NS and the (g / 2)-th S/dP of buffer g & 1, so those phases
-  // follow from g.
-  uint32_t n_qf = 0, n_m2 = 0, n_sdp = 0;
-  bool ok = true;
 
-  // ---- K/V loader: walks this CTA's (item, block) sequence ahead of the rows
-  DqItem ld;
-  int32_t ld_it = dq_next_item(a, blockIdx.x, ld), ld_j = 0;
-  uint32_t ld_g = 0;  // global index of the next block to load
-  auto load_next = [&]() {
-    const uint32_t st = ld_g % NS;
-    if (producer) {
+  if (producer) {
+    // ============================================================ copies
+    DqItem ld;
+    int32_t ld_it = dq_next_item(a, blockIdx.x, ld), ld_j = 0;
+    uint32_t ld_g = 0, n_q = 0, n_done = 0;  // n_done: items whose blocks are all loaded
+    auto load_q = [&](const DqItem &d) {
+      mbar_arrive_expect_tx(B_QF, 5 * Ly::kQBox);
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc)
+        tma_load_3d(sbase + Ly::kQOff + cc * Ly::kQBox, &tm_q, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        tma_load_3d(sbase + Ly::kDoOff + cc * Ly::kQBox, &tm_do, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
+      ++n_q;
+    };
+    if (ld.valid) load_q(ld);
+    while (ld.valid) {
+      const uint32_t st = ld_g % NS;
+      // the stage's previous block: its dQ is done
+      if (ld_g >= static_cast<uint32_t>(NS) &&
+          !wait_bar(B_KVE(st), ((ld_g / NS) & 1) ^ 1, abort_flag, 23))
+        break;
       const uint32_t dst = sbase + Ly::kStOff + st * Ly::kStage;
       const int32_t krow = ld.s0 + ld.lo + ld_j * kDqBN;
       mbar_arrive_expect_tx(B_KV(st), Ly::kStage);
@@ -364,32 +390,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, ld.kvh, krow, B_KV(st));
+      ++ld_g;
+      if (++ld_j >= ld.nblk) {
+        ld_j = 0;
+        ld_it = dq_next_item(a, ld_it + gridDim.x, ld);
+        if (ld.valid) {
+          // the item's last S/dP done: the Q/dO tile is free
+          if (!wait_bar(B_QE, n_done & 1, abort_flag, 22)) break;
+          load_q(ld);
+        }
+        ++n_done;
+      }
     }
-    ++ld_g;
-    if (++ld_j >= ld.nblk) {
-      ld_j = 0;
-      ld_it = dq_next_item(a, ld_it + gridDim.x, ld);
-    }
-  };
-  auto load_q = [&](const DqItem &d) {
-    if (producer) {
-      mbar_arrive_expect_tx(B_QF, 5 * Ly::kQBox);
-#pragma unroll
-      for (int cc = 0; cc < 3; ++cc)
-        tma_load_3d(sbase + Ly::kQOff + cc * Ly::kQBox, &tm_q, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-        tma_load_3d(sbase + Ly::kDoOff + cc * Ly::kQBox, &tm_do, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
-    }
-    ++n_qf;
-  };
-  // S(g) = Q K^T and dP(g) = dO V^T into buffer g & 1 (issued only while
-  // `go`; K/V(g) must be the latest load of its stage).  The counts move on
-  // every thread either way.
-  auto issue_sdp = [&](uint32_t g, bool go) -> bool {
-    const uint32_t st = g % NS, buf = g & 1;
-    n_sdp = g + 1;
-    if (issuer && go) {
+    // no copy may still be landing when shared memory goes back
+    if (n_q > 0) drain_wait(B_QF, (n_q - 1) & 1);
+    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
+      if (ld_g > s) drain_wait(B_KV(s), ((ld_g - 1 - s) / NS) & 1);
+  } else if (issuer) {
+    // ============================================================ MMAs
+    const uint32_t q_lo = ((sbase + Ly::kQOff) >> 4) | (1u << 16);
+    const uint32_t do_lo = ((sbase + Ly::kDoOff) >> 4) | (1u << 16);
+    constexpr uint32_t kIdS = idesc_f32acc(128, kDqBN, 1, 0, 0);
+    constexpr uint32_t kIdQ = idesc_f32acc(128, kDqk, 1, 0, 1);
+    // S(g) = Q K^T and dP(g) = dO V^T into buffer g & 1
+    auto issue_sdp = [&](uint32_t g) -> bool {
+      const uint32_t st = g % NS, buf = g & 1;
       if (!wait_bar(B_KV(st), (g / NS) & 1, abort_flag, 21)) return false;
       tc_fence_after();
       const uint32_t k_lo = ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) | (1u << 16);
@@ -407,40 +432,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_ss2(tmem + buf * 128 + 64, do_lo + ao, kBwdDescHi, v_lo + bo, kBwdDescHi, kIdS, ks > 0);
       }
       mma_commit(B_MM1(buf));
-    }
-    return true;
-  };
-
-  DqItem cur;
-  int32_t it = dq_next_item(a, blockIdx.x, cur);
-  if (cur.valid) load_q(cur);
-  while (ld.valid && ld_g < static_cast<uint32_t>(NS)) load_next();
-  uint32_t g0 = 0;  // global index of the current item's first block
-  while (ok && cur.valid) {
-    DqItem nxt;
-    const int32_t it_n = dq_next_item(a, it + gridDim.x, nxt);
-    // this thread's row
-    const int32_t ti = cur.t0 + t_row, h = cur.kvh * G + g_row;
-    const bool rvalid = compute && ti < cur.L;  // both halves of the row
-    const size_t grow = static_cast<size_t>(cur.s0 + ti) * a.Hq + h;
-    const float lse2 = rvalid ? __ldg(a.lse + grow) * kLog2e : 0.f;
-    const float Drow = rvalid ? __ldg(a.D + grow) : 0.f;
-    if (issuer) ok = wait_bar(B_QF, (n_qf - 1) & 1, abort_flag, 20);
-    ok = issue_sdp(g0, ok) && ok;
-    for (int32_t j = 0; j < cur.nblk; ++j) {
-      const uint32_t g = g0 + j;
-      if (j + 1 < cur.nblk) ok = issue_sdp(g + 1, ok) && ok;
-      // the stage of block g+2 was last read by dQ(g-1), the latest dQ
-      if (producer && ok && n_m2 > 0) ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 23);
-      while (ld.valid && ld_g <= g + 2) load_next();
-      // the last S/dP of this item done: the Q/dO tile can take the next item's
-      if (j == cur.nblk - 1 && nxt.valid) {
-        if (producer && ok) ok = wait_bar(B_MM1(g & 1), (g >> 1) & 1, abort_flag, 22);
-        load_q(nxt);
+      return true;
+    };
+    DqItem cur;
+    int32_t it = dq_next_item(a, blockIdx.x, cur);
+    uint32_t g0 = 0, k = 0;
+    bool ok = true, issued = false;
+    while (ok && cur.valid) {
+      if (!(ok = wait_bar(B_QF, k & 1, abort_flag, 20))) break;
+      tc_fence_after();
+      if (!(ok = issue_sdp(g0))) break;
+      issued = true;
+      if (cur.nblk == 1) mma_commit(B_QE);
+      for (int32_t j = 0; j < cur.nblk; ++j) {
+        const uint32_t g = g0 + j;
+        if (j + 1 < cur.nblk) {
+          if (!(ok = issue_sdp(g + 1))) break;
+          if (j + 2 == cur.nblk) mma_commit(B_QE);  // the item's last S/dP
+        }
+        // all 256 row threads wrote dS(g)
+        if (!(ok = wait_bar(B_DSR(g & 1), (g >> 1) & 1, abort_flag, 25))) break;
+        tc_fence_after();
+        const uint32_t st = g % NS;
+        // A = dS: keys 16 ks.. of the block sit at columns 32 (ks / 2) + 8 (ks % 2)
+#pragma unroll
+        for (int ks = 0; ks < kDqBN / 16; ++ks)
+          mma_ts2(tmem + kDqColAcc, tmem + (g & 1) * 128 + (ks >> 1) * 32 + (ks & 1) * 8,
+                  ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) + ks * ((16 * kRowBytes) >> 4) +
+                      ((Ly::kKBox >> 4) << 16),
+                  kBwdDescHi, kIdQ, (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(B_KVE(st));
+        if (j + 1 == cur.nblk) mma_commit(B_ACCF);
       }
-      if (compute) {
-        // S(g), dP(g) complete (and with them every earlier MMA but dQ(g-1))
-        if (!wait_bar(B_MM1(g & 1), (g >> 1) & 1, abort_flag, 22)) ok = false;
+      g0 += cur.nblk;
+      ++k;
+      it = dq_next_item(a, it + gridDim.x, cur);
+    }
+    // every MMA done before TMEM goes back
+    if (issued) {
+      mma_commit(B_DRAIN);
+      drain_wait(B_DRAIN, 0);
+    }
+  } else if (compute) {
+    // ============================================================ rows
+    const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const int32_t t_row = row / G, g_row = row % G;
+    DqItem cur;
+    int32_t it = dq_next_item(a, blockIdx.x, cur);
+    uint32_t g0 = 0, k = 0;
+    bool ok = true;
+    while (ok && cur.valid) {
+      const int32_t ti = cur.t0 + t_row, h = cur.kvh * G + g_row;
+      const bool rvalid = ti < cur.L;  // both halves of the row
+      const size_t grow = static_cast<size_t>(cur.s0 + ti) * a.Hq + h;
+      const float lse2 = rvalid ? __ldg(a.lse + grow) * kLog2e : 0.f;
+      const float Drow = rvalid ? __ldg(a.D + grow) : 0.f;
+      for (int32_t j = 0; j < cur.nblk; ++j) {
+        const uint32_t g = g0 + j;
+        // S(g), dP(g) complete
+        if (!(ok = wait_bar_warp(B_MM1(g & 1), (g >> 1) & 1, abort_flag, 22))) break;
         tc_fence_after();
         const uint32_t cs = lane_t + (g & 1) * 128 + 32 * half;
         uint32_t sv[32], pv[32];
@@ -450,7 +500,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence<32>(sv);
         reg_fence<32>(pv);
         // this row sees keys [max(0, ti - W + 1), ti]: columns c with
-        // c - c_lo < span (unsigned) of this half block
+        // c - c_lo <= span (unsigned) of this half block
         const int32_t kb = cur.lo + j * kDqBN + 32 * half;
         const int32_t c_lo = (a.window > 0 ? ti - a.window + 1 : 0) - kb;
         const uint32_t span = rvalid ? static_cast<uint32_t>(ti - kb - c_lo) : 0u;
@@ -468,45 +518,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // dS of this half (16 bf16 pairs) over the first 16 of its own S columns
         tmem_st16p(cs, sv);
         tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(B_DSR(g & 1));
       }
-      tc_fence_before();
-      ok = __syncthreads_and(ok);
       if (!ok) break;
-      if (issuer) {
-        tc_fence_after();
-        const uint32_t st = g % NS;
-        // A = dS: keys 16 ks.. of the block sit at columns 32 (ks / 2) + 8 (ks % 2)
-#pragma unroll
-        for (int ks = 0; ks < kDqBN / 16; ++ks)
-          mma_ts2(tmem + kDqColAcc, tmem + (g & 1) * 128 + (ks >> 1) * 32 + (ks & 1) * 8,
-                  ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) + ks * ((16 * kRowBytes) >> 4) +
-                      ((Ly::kKBox >> 4) << 16),
-                  kBwdDescHi, kIdQ, (j > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(B_MM2);
-      }
-      ++n_m2;
-    }
-    if (!ok) break;
-    if (compute) {
-      ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 24);
+      // the item's last dQ complete
+      if (!(ok = wait_bar_warp(B_ACCF, k & 1, abort_flag, 24))) break;
       tc_fence_after();
       bwd_store_qk_row(lane_t + kDqColAcc, a.scale, a.rope_on, a.rope_style, ti, a.rope_turns,
                        a.dq + grow * kDqk, rvalid, half);
+      tc_fence_before();
+      g0 += cur.nblk;
+      ++k;
+      it = dq_next_item(a, it + gridDim.x, cur);
     }
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-    g0 += cur.nblk;
-    cur = nxt;
-    it = it_n;
   }
-  // drain: every copy and MMA this CTA issued must land before TMEM and shared
-  // memory go back (only an aborted CTA has any left)
-  if (n_qf > 0) drain_wait(B_QF, (n_qf - 1) & 1);
-  for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
-    if (ld_g > s) drain_wait(B_KV(s), ((ld_g - 1 - s) / NS) & 1);
-  for (uint32_t b = 0; b < 2; ++b)
-    if (n_sdp > b) drain_wait(B_MM1(b), ((n_sdp - 1 - b) >> 1) & 1);
-  if (n_m2 > 0) drain_wait(B_MM2, (n_m2 - 1) & 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

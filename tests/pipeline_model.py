@@ -7,12 +7,15 @@ order the kernel performs them:
 
   ("wait", bar, n)         block until `bar` has completed n phases.  The kernel
                            waits on the parity of phase n-1, which is only
-                           unambiguous while the barrier has completed at most
-                           n phases: the model fails if it ever sees more.
-  ("arrive", bar)          one arrival (every barrier here completes a phase on
-                           one arrival: a commit or a copy's transaction count).
+                           unambiguous while the barrier has completed n-1 or n
+                           phases: with n+1 the wait would miss its phase, with
+                           n-2 or fewer it would pass at once on an older one.
+                           The model fails on either.
+  ("arrive", bar)          one arrival; a barrier completes a phase after
+                           `counts[bar]` arrivals (1 unless the roles say).
   ("tma", res, tag, bar)   an asynchronous copy: later, in any order, `res` gets
-                           `tag` and `bar` completes a phase.
+                           `tag` (res and tag may be lists: one copy of several
+                           boxes) and `bar` completes a phase.
   ("mma", reads, writes)   an MMA joins the tensor pipe, which executes in issue
                            order; on execution every (res, tag) it reads must hold
                            that tag, then every (res, tag) it writes is set.
@@ -37,8 +40,10 @@ class ModelError(AssertionError):
 
 
 class Sim:
-    def __init__(self, roles, rng):
+    def __init__(self, roles, rng, counts=None):
         self.rng = rng
+        self.counts = dict(counts or {})      # barrier -> arrivals per phase
+        self.arrivals = {}
         self.roles = dict(roles)              # name -> generator
         self.pending = {n: None for n in self.roles}  # the op a role is blocked on
         self.done = set()
@@ -51,13 +56,20 @@ class Sim:
     def _complete(self, bar):
         self.phases[bar] = self.phases.get(bar, 0) + 1
 
+    def _arrive(self, bar):
+        self.arrivals[bar] = self.arrivals.get(bar, 0) + 1
+        if self.arrivals[bar] == self.counts.get(bar, 1):
+            self.arrivals[bar] = 0
+            self._complete(bar)
+
     def _check_waits(self):
         for name, op in self.pending.items():
             if op is not None and op[0] == "wait":
                 _, bar, n = op
-                if self.phases.get(bar, 0) > n:
-                    raise ModelError(f"{name}: waits for phase {n} of {bar}, which has "
-                                     f"completed {self.phases[bar]} (parity wait ambiguous)")
+                c = self.phases.get(bar, 0)
+                if c > n or c < n - 1:
+                    raise ModelError(f"{name}: waits for {n} phases of {bar}, which has "
+                                     f"completed {c} (parity wait ambiguous)")
 
     def _runnable(self, name):
         op = self.pending[name]
@@ -76,7 +88,7 @@ class Sim:
             if kind == "wait":
                 pass  # satisfied (checked by _runnable)
             elif kind == "arrive":
-                self._complete(op[1])
+                self._arrive(op[1])
             elif kind == "tma":
                 self.tma.append(op[1:])
             elif kind == "mma":
@@ -126,7 +138,11 @@ class Sim:
                 self._step_role(i)
             elif kind == "tma":
                 r, tag, bar = self.tma.pop(i)
-                self.res[r] = tag
+                if isinstance(r, list):
+                    for rr, tt in zip(r, tag):
+                        self.res[rr] = tt
+                else:
+                    self.res[r] = tag
                 self._complete(bar)
             else:
                 op = self.pipe.pop(0)
@@ -156,7 +172,15 @@ NS = 3  # K/V (dq) or Q/dO (dk/dv) stages
 
 
 def dq_roles(nblk, skip=()):
-    """The dq kernel for one CTA whose items have nblk[i] key blocks each.
+    """The dq kernel for one CTA whose items have nblk[i] key blocks each.  The
+    roles meet only on mbarriers: the rows tell the MMA thread that dS(g) is in
+    TMEM (DSR, per S/dP buffer); the same threads ran the previous item's
+    epilogue before, so the first dQ of an item cannot overwrite what the
+    epilogue still reads.  The MMA thread frees a K/V stage with a commit after
+    the dQ that read it (KVE), the Q/dO tile with a commit after the item's last
+    S/dP (QE) and hands the finished dQ to the rows with a commit after the
+    item's last dQ (ACCF): one phase per item, so neither of the last two waits
+    can find its barrier two phases behind.
     `skip` names waits to leave out (to show that the model notices)."""
     items = list(nblk)
     seq = [(it, j) for it, n in enumerate(items) for j in range(n)]  # loader order
@@ -164,27 +188,18 @@ def dq_roles(nblk, skip=()):
 
     def producer():
         yield ("tma", "QO", ("QO", 0), "QF")
-        ld = 0
-        while ld < len(seq) and ld < NS:
-            yield ("tma", f"KV{ld % NS}", ("KV", ld), f"KV{ld % NS}")
-            ld += 1
-        n_m2 = 0
-        for it, n in enumerate(items):
-            g0 = first[it]
-            for j in range(n):
-                g = g0 + j
-                if n_m2 > 0 and "producer_mm2" not in skip:
-                    yield ("wait", "MM2", n_m2)  # dQ(g-1): the stage of block g+2 is free
-                while ld < len(seq) and ld <= g + 2:
-                    yield ("tma", f"KV{ld % NS}", ("KV", ld), f"KV{ld % NS}")
-                    ld += 1
-                if j == n - 1 and it + 1 < len(items):
-                    if "producer_mm1" not in skip:
-                        yield ("wait", f"MM1{g & 1}", (g >> 1) + 1)  # last S/dP of the item
-                    yield ("tma", "QO", ("QO", it + 1), "QF")
-                yield ("sync",)
-                n_m2 += 1
-            yield ("sync",)
+        for ld in range(len(seq)):
+            st = ld % NS
+            if ld >= NS and "producer_kve" not in skip:
+                yield ("wait", f"KVE{st}", ld // NS)  # dQ(ld - NS) read the stage
+            yield ("tma", f"KV{st}", ("KV", ld), f"KV{st}")
+            it, j = seq[ld]
+            # once block ld is queued, the next item's Q/dO follows the item's
+            # last S/dP (interleaved with the K/V loads as the kernel does)
+            if j == items[it] - 1 and it + 1 < len(items):
+                if "producer_qe" not in skip:
+                    yield ("wait", "QE", it + 1)
+                yield ("tma", "QO", ("QO", it + 1), "QF")
 
     def issuer():
         def issue_sdp(it, g):
@@ -197,22 +212,27 @@ def dq_roles(nblk, skip=()):
             g0 = first[it]
             yield ("wait", "QF", it + 1)
             yield from issue_sdp(it, g0)
+            if n == 1:
+                yield ("commit", "QE")
             for j in range(n):
                 g = g0 + j
                 if j + 1 < n:
                     yield from issue_sdp(it, g + 1)
-                yield ("sync",)
+                    if j + 2 == n:
+                        yield ("commit", "QE")  # the item's last S/dP
                 b = g & 1
+                if "issuer_dsr" not in skip:
+                    yield ("wait", f"DSR{b}", (g >> 1) + 1)  # both row halves wrote dS(g)
                 reads = [(f"S{b}h0", ("dS", g)), (f"S{b}h1", ("dS", g)), (f"KV{g % NS}", ("KV", g))]
                 if j > 0:
                     reads.append(("dQ", ("dQ", it, j - 1)))
                 yield ("mma", reads, [("dQ", ("dQ", it, j))])
-                yield ("commit", "MM2")
-            yield ("sync",)
+                yield ("commit", f"KVE{g % NS}")
+                if j == n - 1:
+                    yield ("commit", "ACCF")
 
     def rows(h):
         def role():
-            n_m2 = 0
             for it, n in enumerate(items):
                 g0 = first[it]
                 for j in range(n):
@@ -221,16 +241,14 @@ def dq_roles(nblk, skip=()):
                     yield ("wait", f"MM1{b}", (g >> 1) + 1)
                     yield ("read", f"S{b}h{h}", ("S", g))
                     yield ("write", f"S{b}h{h}", ("dS", g))  # dS over this half's S columns
-                    yield ("sync",)
-                    n_m2 += 1
-                if h == 0:  # the epilogue runs on the first half
-                    if "rows_mm2" not in skip:
-                        yield ("wait", "MM2", n_m2)
-                    yield ("read", "dQ", ("dQ", it, n - 1))
-                yield ("sync",)
+                    yield ("arrive", f"DSR{b}")
+                if "rows_accf" not in skip:
+                    yield ("wait", "ACCF", it + 1)  # the item's last dQ
+                yield ("read", "dQ", ("dQ", it, n - 1))
         return role()
 
-    return {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}
+    roles = {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}
+    return roles, {"DSR0": 2, "DSR1": 2}
 
 
 def dkdv_roles(nsub, skip=()):
@@ -313,11 +331,12 @@ def dkdv_roles(nsub, skip=()):
                 yield ("sync",)
         return role()
 
-    return {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}
+    return {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}, {}
 
 
 def run(make_roles, sizes, seed, skip=()):
-    Sim(make_roles(sizes, skip), random.Random(seed)).run()
+    roles, counts = make_roles(sizes, skip)
+    Sim(roles, random.Random(seed), counts).run()
 
 
 def decode_roles(nblk, f8=False, skip=()):
@@ -345,8 +364,7 @@ def decode_roles(nblk, f8=False, skip=()):
                     st = gk % S
                     if "producer_kvempty" not in skip:
                         yield ("wait", f"KVEMPTY{st}", gk // S)
-                    yield ("tma", f"K{st}", ("Kraw", gk), f"KVFULL{st}")
-                    yield ("tma", f"V{st}", ("V", gk), f"KVFULL{st}")
+                    yield ("tma", [f"K{st}", f"V{st}"], [("Kraw", gk), ("V", gk)], f"KVFULL{st}")
                 gk += 1
 
     def mma():
@@ -415,10 +433,10 @@ def decode_roles(nblk, f8=False, skip=()):
                     yield ("write", f"V{st}", ("V", gk))
                     yield ("arrive", f"STGEMPTY{s8}")
                 else:
-                    yield ("wait", f"KVFULL{st}", 2 * (gk // S) + 2)  # K and V copies landed
+                    yield ("wait", f"KVFULL{st}", gk // S + 1)  # K and V copies landed
                     yield ("read", f"K{st}", ("Kraw", gk))
                     yield ("write", f"K{st}", ("K", gk))  # RoPE in place
                 yield ("arrive", f"KREADY{st}")
                 gk += 1
 
-    return {"producer": producer(), "mma": mma(), "softmax": softmax(), "convert": convert()}
+    return {"producer": producer(), "mma": mma(), "softmax": softmax(), "convert": convert()}, {}

@@ -48,11 +48,9 @@ def _caught(make_roles, skip, sizes=(3, 2, 4)):
     return False
 
 
-@pytest.mark.parametrize("skip,sizes", [("producer_mm2", (3, 2, 4)), ("rows_mm2", (3, 2, 4)),
-                                        # with two or more blocks the wait for dQ(g-1) already
-                                        # orders the item's last S/dP before the Q/dO reload;
-                                        # items of one block need the wait on it
-                                        ("producer_mm1", (1, 1, 2, 1))])
+@pytest.mark.parametrize("skip,sizes", [("producer_kve", (3, 2, 4)), ("rows_accf", (3, 2, 4)),
+                                        ("issuer_dsr", (1, 2, 1, 3)),
+                                        ("producer_qe", (1, 1, 2, 1))])
 def test_dq_missing_wait_is_caught(skip, sizes):
     assert _caught(dq_roles, (skip,), sizes)
 
