@@ -69,11 +69,13 @@ def barrier(ws):
 
 
 def max_over_ranks(x: float, ws: int) -> float:
+    """The largest of the ranks' values (the slowest rank's time)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
