@@ -1,5 +1,5 @@
-"""CPU model of the mbarrier pipelines of the decode kernel and of the backward
-kernels (dq and dk/dv).
+"""CPU model of the mbarrier pipelines of the GA prefill kernel, the decode
+kernel and the backward kernels (dq and dk/dv).
 
 Each kernel role (the copy thread, the MMA thread, the row threads of the two
 column halves) is a generator that yields the operations it performs, in the
@@ -440,3 +440,123 @@ def decode_roles(nblk, f8=False, skip=()):
                 gk += 1
 
     return {"producer": producer(), "mma": mma(), "softmax": softmax(), "convert": convert()}, {}
+
+
+def causal_roles(nblk, skip=()):
+    """sinkattn_causal_kernel (GA prefill) for one CTA whose items (two query
+    tiles A and B of one KV head) run over nblk[i] 128-key blocks: the Q/K copy
+    warp, the V copy warp, the RoPE warps, the MMA thread and the softmax warps
+    of each tile.  Per block the MMA thread issues PV_A(j), QK_A(j+1), PV_B(j),
+    QK_B(j+1), so each tile's softmax overlaps the other tile's products."""
+    items = list(nblk)
+
+    def producer():
+        gk = 0
+        for i, n in enumerate(items):
+            yield ("wait", "QEMPTY", i)  # the previous item's last QK^T read Q
+            for x in range(2):
+                yield ("tma", f"Q{x}", ("Qraw", i, x), f"QFULL{x}")
+            for _ in range(n):
+                st = gk & 1
+                if "producer_kempty" not in skip:
+                    yield ("wait", f"KEMPTY{st}", gk >> 1)
+                yield ("tma", f"K{st}", ("Kraw", gk), f"KFULL{st}")
+                gk += 1
+
+    def vloader():
+        gv = 0
+        for n in items:
+            for _ in range(n):
+                if "vloader_vempty" not in skip:
+                    yield ("wait", "VEMPTY", gv)
+                yield ("tma", "V", ("V", gv), "VFULL")
+                gv += 1
+
+    def rope():
+        gk = 0
+        for i, n in enumerate(items):
+            for x in range(2):
+                yield ("wait", f"QFULL{x}", i + 1)
+                yield ("read", f"Q{x}", ("Qraw", i, x))
+                yield ("write", f"Q{x}", ("Q", i, x))
+                yield ("arrive", f"QREADY{x}")
+            for _ in range(n):
+                st = gk & 1
+                if "rope_kfull" not in skip:
+                    yield ("wait", f"KFULL{st}", (gk >> 1) + 1)
+                yield ("read", f"K{st}", ("Kraw", gk))
+                yield ("write", f"K{st}", ("K", gk))
+                yield ("arrive", f"KREADY{st}")
+                gk += 1
+
+    def mma():
+        gk = gv = gp = 0
+
+        def qk(i, x, b):
+            yield ("mma", [(f"Q{x}", ("Q", i, x)), (f"K{b & 1}", ("K", b))], [(f"S{x}", ("S", x, b))])
+            yield ("commit", f"SFULL{x}")
+
+        def pv(i, x, j, b, first):
+            if "mma_pfull" not in skip:
+                yield ("wait", f"PFULL{x}", gp + 1)
+            # (the O_EMPTY wait is implied by P_FULL: the softmax threads finish
+            # the previous item's epilogue before they store this item's P)
+            if first:
+                yield ("wait", f"OEMPTY{x}", i)
+            reads = [(f"S{x}", ("P", x, b)), ("V", ("V", gv))]
+            if not first:
+                reads.append((f"O{x}", ("Ors", x, i, j - 1)))
+            yield ("mma", reads, [(f"O{x}", ("O", x, i, j))])
+            yield ("commit", f"PVDONE{x}")
+
+        for i, n in enumerate(items):
+            yield ("wait", "QREADY0", i + 1)
+            yield ("wait", "QREADY1", i + 1)
+            yield ("wait", f"KREADY{gk & 1}", (gk >> 1) + 1)
+            yield from qk(i, 0, gk)
+            yield from qk(i, 1, gk)
+            yield ("commit", f"KEMPTY{gk & 1}")
+            if n == 1:
+                yield ("commit", "QEMPTY")
+            for j in range(n):
+                more = j + 1 < n
+                yield ("wait", "VFULL", gv + 1)
+                yield from pv(i, 0, j, gk, j == 0)
+                if more:
+                    yield ("wait", f"KREADY{(gk + 1) & 1}", ((gk + 1) >> 1) + 1)
+                    yield from qk(i, 0, gk + 1)
+                yield from pv(i, 1, j, gk, j == 0)
+                yield ("commit", "VEMPTY")
+                gv += 1
+                gp += 1
+                if more:
+                    yield from qk(i, 1, gk + 1)
+                    yield ("commit", f"KEMPTY{(gk + 1) & 1}")
+                    if j + 1 == n - 1:
+                        yield ("commit", "QEMPTY")
+                gk += 1
+
+    def softmax(x):
+        def role():
+            gb = 0
+            for i, n in enumerate(items):
+                for j in range(n):
+                    yield ("wait", f"SFULL{x}", gb + 1)
+                    yield ("read", f"S{x}", ("S", x, gb))
+                    yield ("write", f"S{x}", ("P", x, gb))  # P over the S columns
+                    if j > 0:
+                        # (implied by S_FULL(j): QK(j) of this tile was issued
+                        # after PV(j-1); the kernel waits all the same)
+                        yield ("wait", f"PVDONE{x}", gb)
+                        yield ("read", f"O{x}", ("O", x, i, j - 1))
+                        yield ("write", f"O{x}", ("Ors", x, i, j - 1))  # rescale
+                    yield ("arrive", f"PFULL{x}")
+                    gb += 1
+                yield ("wait", f"PVDONE{x}", gb)
+                yield ("read", f"O{x}", ("O", x, i, n - 1))
+                yield ("arrive", f"OEMPTY{x}")
+        return role()
+
+    roles = {"producer": producer(), "vloader": vloader(), "rope": rope(), "mma": mma(),
+             "softmaxA": softmax(0), "softmaxB": softmax(1)}
+    return roles, {}

@@ -1,16 +1,17 @@
-"""The barrier protocols of the decode and backward kernels, checked on a CPU model
+"""The barrier protocols of the GA prefill, decode and backward kernels, checked on a CPU model
 (tests/pipeline_model.py) over many random interleavings: no deadlock, no
 parity wait that its barrier has already passed by two phases, and no MMA or
 thread that reads a shared-memory stage or TMEM region before the data it
 expects has landed or after the next write replaced it.  The model transcribes
-the roles of sinkattn_decode_kernel (decode_kernel.cuh) and of bwd_dq_kernel
+the roles of sinkattn_causal_kernel (causal_kernel.cuh), sinkattn_decode_kernel
+(decode_kernel.cuh) and of bwd_dq_kernel
 and bwd_dkdv_kernel (backward_kernel.cuh); a wait left out of it must be
 caught, which the *_missing_wait_* tests check."""
 import random
 
 import pytest
 
-from pipeline_model import ModelError, decode_roles, dkdv_roles, dq_roles, run
+from pipeline_model import ModelError, causal_roles, decode_roles, dkdv_roles, dq_roles, run
 
 SIZES = [[1], [2], [3], [1, 1, 1], [1, 2, 1, 3], [3, 3, 3], [5, 1, 4], [2, 7], [1] * 6]
 
@@ -71,3 +72,14 @@ def test_decode_pipeline(f8, sizes):
                                      (False, "softmax_pvdone"), (True, "softmax_pvdone")])
 def test_decode_missing_wait_is_caught(f8, skip):
     assert _caught(lambda s, sk: decode_roles(s, f8, sk), (skip,), (5, 3, 6))
+
+
+@pytest.mark.parametrize("sizes", [[1], [2], [4], [1, 1, 1], [3, 1, 2], [2, 5, 1, 3]])
+def test_causal_pipeline(sizes):
+    for seed in range(60):
+        run(causal_roles, sizes, seed)
+
+
+@pytest.mark.parametrize("skip", ["producer_kempty", "vloader_vempty", "mma_pfull", "rope_kfull"])
+def test_causal_missing_wait_is_caught(skip):
+    assert _caught(causal_roles, (skip,), (3, 2, 4))
