@@ -1,5 +1,5 @@
-"""CPU model of the mbarrier pipelines of the GA prefill kernel, the decode
-kernel and the backward kernels (dq and dk/dv).
+"""CPU model of the mbarrier pipelines of the SWA and GA prefill kernels, the
+decode kernel and the backward kernels (dq and dk/dv).
 
 Each kernel role (the copy thread, the MMA thread, the row threads of the two
 column halves) is a generator that yields the operations it performs, in the
@@ -560,3 +560,120 @@ def causal_roles(nblk, skip=()):
     roles = {"producer": producer(), "vloader": vloader(), "rope": rope(), "mma": mma(),
              "softmaxA": softmax(0), "softmaxB": softmax(1)}
     return roles, {}
+
+
+def band_roles(lanes, skip=(), nseg=9, R=12):
+    """sinkattn_band_kernel (SWA prefill) for one CTA whose contiguous range of
+    tiles crosses `lanes`: (first tile index, number of tiles) per (sequence,
+    KV head) lane.  A tile of 16 tokens sees the nwin = min(i + 1, nseg)
+    16-key segments ending at its own; a tile that starts a run (the CTA's
+    first, or the first of a lane) loads its whole window into the 12-slot
+    segment ring, any other tile loads one new segment.  The MMA thread issues
+    PV of the previous tile after this tile's QK^T (before it at a run start,
+    which reloads the ring) and frees the segments leaving the window.  The two
+    threads of a softmax row (modelled as two roles, one per half) swap partial
+    maxima and sums through shared memory, paired by a barrier per parity."""
+    tiles = []  # (tile index within its lane, run)
+    for i0, n in lanes:
+        for k in range(n):
+            tiles.append((i0 + k, k == 0))
+
+    def nwin_of(i):
+        return min(i + 1, nseg)
+
+    def producer():
+        gseg = 0
+        for t, (i, run) in enumerate(tiles):
+            qs = t & 1
+            yield ("wait", f"QEMPTY{qs}", t >> 1)
+            yield ("tma", f"Q{qs}", ("Qraw", t), f"QFULL{qs}")
+            for _ in range(nwin_of(i) if run else 1):
+                slot = gseg % R
+                if "producer_segempty" not in skip:
+                    yield ("wait", f"SEGEMPTY{slot}", gseg // R)
+                yield ("tma", f"SEG{slot}", ("Kraw", gseg), f"SEGFULL{slot}")
+                gseg += 1
+
+    def rope():
+        gseg = 0
+        for t, (i, run) in enumerate(tiles):
+            qs = t & 1
+            yield ("wait", f"QFULL{qs}", (t >> 1) + 1)
+            yield ("read", f"Q{qs}", ("Qraw", t))
+            yield ("write", f"Q{qs}", ("Q", t))
+            yield ("arrive", f"QREADY{qs}")
+            for _ in range(nwin_of(i) if run else 1):
+                slot = gseg % R
+                yield ("wait", f"SEGFULL{slot}", gseg // R + 1)
+                yield ("read", f"SEG{slot}", ("Kraw", gseg))
+                yield ("write", f"SEG{slot}", ("KV", gseg))
+                yield ("arrive", f"SEGREADY{slot}")
+                gseg += 1
+
+    def mma():
+        gseg = 0
+        prev = None  # (tile, nwin, first segment) of the tile whose PV is pending
+
+        def issue_pv(t, nwin, seg0, nfree):
+            b = t & 1
+            yield ("wait", f"PFULL{b}", (t >> 1) + 1)
+            if "mma_oempty" not in skip:
+                yield ("wait", "OEMPTY", t)
+            reads = [(f"S{b}h0", ("P", t)), (f"S{b}h1", ("P", t))]
+            reads += [(f"SEG{(seg0 + k) % R}", ("KV", seg0 + k)) for k in range(nwin)]
+            yield ("mma", reads, [("Oh0", ("O", t)), ("Oh1", ("O", t))])
+            for k in range(nfree):
+                yield ("commit", f"SEGEMPTY{(seg0 + k) % R}")
+            yield ("commit", "PVDONE")
+
+        for t, (i, run) in enumerate(tiles):
+            nwin = nwin_of(i)
+            nload = nwin if run else 1
+            if prev is not None and run:
+                yield from issue_pv(*prev, prev[1])  # the reload needs the whole ring back
+            qs = t & 1
+            yield ("wait", f"QREADY{qs}", (t >> 1) + 1)
+            for j in range(nload):
+                g = gseg + j
+                yield ("wait", f"SEGREADY{g % R}", g // R + 1)
+            gseg += nload
+            seg0 = gseg - nwin
+            b = t & 1
+            reads = [(f"Q{qs}", ("Q", t))] + [(f"SEG{(seg0 + k) % R}", ("KV", seg0 + k))
+                                              for k in range(nwin)]
+            yield ("mma", reads, [(f"S{b}h0", ("S", t)), (f"S{b}h1", ("S", t))])
+            yield ("commit", f"SFULL{b}")
+            yield ("commit", f"QEMPTY{qs}")
+            if prev is not None and not run:
+                yield from issue_pv(*prev, 1 if nwin == prev[1] else 0)
+            prev = (t, nwin, seg0)
+        if prev is not None:
+            yield from issue_pv(*prev, prev[1])
+
+    def softmax(h):
+        def role():
+            for step in range(len(tiles) + 1):
+                have = step < len(tiles)
+                b = step & 1
+                if have:
+                    yield ("wait", f"SFULL{b}", (step >> 1) + 1)
+                    yield ("read", f"S{b}h{h}", ("S", step))
+                par = step & 1  # swap with the other half of the row
+                yield ("write", f"X{par}h{h}", ("X", step))
+                yield ("arrive", f"PAIR{par}")
+                if "softmax_pair" not in skip:
+                    yield ("wait", f"PAIR{par}", (step >> 1) + 1)
+                yield ("read", f"X{par}h{1 - h}", ("X", step))
+                if have:
+                    yield ("write", f"S{b}h{h}", ("P", step))  # P over this half's S columns
+                    yield ("arrive", f"PFULL{b}")
+                if step > 0:
+                    yield ("wait", "PVDONE", step)
+                    yield ("read", f"Oh{h}", ("O", step - 1))
+                    yield ("arrive", "OEMPTY")
+        return role()
+
+    roles = {"producer": producer(), "rope": rope(), "mma": mma(), "half0": softmax(0),
+             "half1": softmax(1)}
+    counts = {"PFULL0": 2, "PFULL1": 2, "OEMPTY": 2, "PAIR0": 2, "PAIR1": 2}
+    return roles, counts

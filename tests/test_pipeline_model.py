@@ -1,9 +1,10 @@
-"""The barrier protocols of the GA prefill, decode and backward kernels, checked on a CPU model
+"""The barrier protocols of the prefill, decode and backward kernels, checked on a CPU model
 (tests/pipeline_model.py) over many random interleavings: no deadlock, no
 parity wait that its barrier has already passed by two phases, and no MMA or
 thread that reads a shared-memory stage or TMEM region before the data it
 expects has landed or after the next write replaced it.  The model transcribes
-the roles of sinkattn_causal_kernel (causal_kernel.cuh), sinkattn_decode_kernel
+the roles of sinkattn_band_kernel (band_kernel.cuh), sinkattn_causal_kernel
+(causal_kernel.cuh), sinkattn_decode_kernel
 (decode_kernel.cuh) and of bwd_dq_kernel
 and bwd_dkdv_kernel (backward_kernel.cuh); a wait left out of it must be
 caught, which the *_missing_wait_* tests check."""
@@ -11,7 +12,7 @@ import random
 
 import pytest
 
-from pipeline_model import ModelError, causal_roles, decode_roles, dkdv_roles, dq_roles, run
+from pipeline_model import ModelError, band_roles, causal_roles, decode_roles, dkdv_roles, dq_roles, run
 
 SIZES = [[1], [2], [3], [1, 1, 1], [1, 2, 1, 3], [3, 3, 3], [5, 1, 4], [2, 7], [1] * 6]
 
@@ -83,3 +84,30 @@ def test_causal_pipeline(sizes):
 @pytest.mark.parametrize("skip", ["producer_kempty", "vloader_vempty", "mma_pfull", "rope_kfull"])
 def test_causal_missing_wait_is_caught(skip):
     assert _caught(causal_roles, (skip,), (3, 2, 4))
+
+
+BAND_RANGES = [[(0, 1)], [(0, 12)], [(5, 3)], [(0, 20)], [(7, 4), (0, 3)],
+               [(30, 2), (0, 12), (0, 1)], [(0, 1), (0, 1), (0, 2)]]
+
+
+@pytest.mark.parametrize("lanes", BAND_RANGES)
+def test_band_pipeline(lanes):
+    for seed in range(60):
+        run(band_roles, lanes, seed)
+
+
+@pytest.mark.parametrize("R", [10, 11])
+def test_band_pipeline_smaller_rings(R):
+    # the kernel's ring is the 9-segment window plus the 3 segments the Q
+    # double buffer lets the copy thread run ahead; smaller rings only wait more
+    for lanes in BAND_RANGES:
+        for seed in range(20):
+            run(lambda s, sk: band_roles(s, sk, R=R), lanes, seed)
+
+
+@pytest.mark.parametrize("skip,R", [("mma_oempty", 12), ("softmax_pair", 12),
+                                    # with 12 slots the segment-empty wait never
+                                    # blocks (see above); with 10 it must
+                                    ("producer_segempty", 10)])
+def test_band_missing_wait_is_caught(skip, R):
+    assert _caught(lambda s, sk: band_roles(s, sk, R=R), (skip,), [(3, 14), (0, 4)])
