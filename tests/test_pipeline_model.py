@@ -1,13 +1,13 @@
-"""The barrier protocols of the prefill, decode and backward kernels, checked on a CPU model
-(tests/pipeline_model.py) over many random interleavings: no deadlock, no
-parity wait that its barrier has already passed by two phases, and no MMA or
-thread that reads a shared-memory stage or TMEM region before the data it
-expects has landed or after the next write replaced it.  The model transcribes
-the roles of sinkattn_band_kernel (band_kernel.cuh), sinkattn_causal_kernel
-(causal_kernel.cuh), sinkattn_decode_kernel
-(decode_kernel.cuh) and of bwd_dq_kernel
-and bwd_dkdv_kernel (backward_kernel.cuh); a wait left out of it must be
-caught, which the *_missing_wait_* tests check."""
+"""The barrier protocols of the prefill, decode and backward kernels, checked
+on a CPU model (tests/pipeline_model.py) over many random interleavings: no
+deadlock, no parity wait whose barrier is two phases past or two phases short
+of the awaited one, and no MMA or thread that reads a shared-memory stage or
+TMEM region before the data it expects has landed or after the next write
+replaced it.  The model transcribes the roles of sinkattn_band_kernel
+(band_kernel.cuh), sinkattn_causal_kernel (causal_kernel.cuh),
+sinkattn_decode_kernel (decode_kernel.cuh), bwd_dq_kernel and bwd_dkdv_kernel
+(backward_kernel.cuh); a wait left out of it must be caught, which the
+*_missing_wait_* tests check."""
 import random
 
 import pytest
