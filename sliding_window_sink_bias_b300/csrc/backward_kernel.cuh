@@ -586,23 +586,35 @@ struct KvLayout {
   static constexpr uint32_t kStOff = 5 * kKBox;          // stages: q_rot rows 3 boxes, dO rows 2
   static constexpr uint32_t kStage = 5 * kQBox;
   static constexpr uint32_t kColOff = kStOff + kStages * kStage;  // lse*log2e, D: 2 sub-tiles
-  static constexpr uint32_t kBarOff = kColOff + 2 * 2 * kKvRows * 4;  // kf, qs[3], mm1, mm2
-  static constexpr uint32_t kMiscOff = kBarOff + 6 * 8;
+  // kv_full, kv_empty, qs_full[3], qs_empty[3], mm1, mm2, p_ready, acc_full, rows_full[2], drain
+  static constexpr uint32_t kBarOff = kColOff + 2 * 2 * kKvRows * 4;
+  static constexpr uint32_t kMiscOff = kBarOff + 15 * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
 static_assert(KvLayout::kDynSmem <= 232448, "dkdv kernel shared memory");
 
-// Pipeline of the dk/dv kernel (thread 128 issues the MMAs, thread 160 the
-// copies; threads 0..127 own one key each).  TMEM: S^T 0..63 and dP^T 64..127 of the current sub-tile, dV
-// 128..255, dK 256..447, and P^T (448..479) and dS^T (480..511) as bf16 pairs.
-// After the one CTA barrier of sub-tile g, S^T/dP^T(g+1) go out first and
-// dV/dK(g) behind them, so the rows work on sub-tile g+1 while dV/dK(g) run;
-// they wait for dV/dK(g) only before writing P^T/dS^T(g+1).  Q/dO sub-tiles
-// (last query rows first) stream through three stages, loaded two ahead and
-// across item boundaries;
-// the next item's K/V block is loaded once the last S^T/dP^T of the current
-// item is done.
+// Roles of the dk/dv kernel, which meet only on mbarriers (sub-tile g is the
+// g-th query sub-tile this CTA works on, over all its items).  TMEM: S^T 0..63
+// and dP^T 64..127 of the current sub-tile, dV 128..255, dK 256..447, and P^T
+// (448..479) and dS^T (480..511) as bf16 pairs.
+//   copy thread (288): the K/V block of an item once the previous item's last
+//     S^T/dP^T is done (KV_EMPTY); Q/dO sub-tiles, last query rows first (so
+//     the CTAs of one KV head stream the same rows together), through three
+//     stages, each refilled once the dV/dK that read it is done (QS_EMPTY).
+//   MMA thread (256): once the rows have P^T/dS^T(g) in TMEM (P_READY, which
+//     also means they have read S^T/dP^T(g)), S^T/dP^T(g+1) go out first and
+//     dV/dK(g) behind them, so the rows work on sub-tile g+1 while dV/dK(g)
+//     run; after an item's last dV/dK it hands the accumulators over
+//     (ACC_FULL).
+//   rows (0..255, two threads per key, 32 query rows each): they wait for
+//     dV/dK(g-1) only before writing P^T/dS^T(g).  Rows 0..63 load lse and D of
+//     the next sub-tile at the top of a sub-tile and put them in a
+//     shared-memory slot after that wait (ROWS_FULL): by then every row has
+//     read the slot's previous contents (dV/dK(g-1) needed all their
+//     P_READY arrivals for sub-tile g-1).
+// KV_EMPTY and ACC_FULL complete once per item, so no wait can find its
+// barrier two phases away from the awaited one.
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -619,18 +631,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const bool compute = threadIdx.x < 256;
   const bool issuer = threadIdx.x == 256;    // MMAs
   const bool producer = threadIdx.x == 288;  // copies
-  const uint32_t B_KF = sbase + Ly::kBarOff;
-  auto B_QS = [&](uint32_t s) { return B_KF + 8 + 8 * s; };
-  const uint32_t B_MM1 = B_KF + 8 + 8 * NS, B_MM2 = B_MM1 + 8;
+  auto bar = [&](uint32_t i) { return sbase + Ly::kBarOff + 8 * i; };
+  const uint32_t B_KF = bar(0), B_KVE = bar(1);
+  auto B_QS = [&](uint32_t s) { return bar(2 + s); };
+  auto B_QSE = [&](uint32_t s) { return bar(2 + NS + s); };
+  const uint32_t B_MM1 = bar(2 + 2 * NS), B_MM2 = bar(3 + 2 * NS);
+  const uint32_t B_PR = bar(4 + 2 * NS), B_ACCF = bar(5 + 2 * NS);
+  auto B_LF = [&](uint32_t p) { return bar(6 + 2 * NS + p); };
+  const uint32_t B_DRAIN = bar(8 + 2 * NS);
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
   float *c_lse = reinterpret_cast<float *>(smem + Ly::kColOff);  // [2][64]
   float *c_D = c_lse + 2 * kKvRows;                                // [2][64]
   if (issuer) {
     mbar_init(B_KF, 1);
-    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s) mbar_init(B_QS(s), 1);
+    mbar_init(B_KVE, 1);
+    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s) {
+      mbar_init(B_QS(s), 1);
+      mbar_init(B_QSE(s), 1);
+    }
     mbar_init(B_MM1, 1);
     mbar_init(B_MM2, 1);
+    mbar_init(B_PR, 256);
+    mbar_init(B_ACCF, 1);
+    mbar_init(B_LF(0), kKvRows);
+    mbar_init(B_LF(1), kKvRows);
+    mbar_init(B_DRAIN, 1);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -646,31 +672,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int32_t G = a.G, TS = kKvRows / G;  // tokens per sub-tile
-  const uint32_t k_lo = ((sbase + Ly::kKOff) >> 4) | (1u << 16);
-  const uint32_t v_lo = ((sbase + Ly::kVOff) >> 4) | (1u << 16);
-  constexpr uint32_t kIdS = idesc_f32acc(128, kKvRows, 1, 0, 0);
-  constexpr uint32_t kIdV = idesc_f32acc(128, kDv, 1, 0, 1);
-  constexpr uint32_t kIdK = idesc_f32acc(128, kDqk, 1, 0, 1);
   constexpr uint32_t kColST = 0, kColPT = 64, kColV = 128, kColK = 256, kColP = 448, kColDS = 480;
-  // issue counts, kept alike by all threads; sub-tile g is the (g / NS)-th
-  // load of stage g % NS
-  uint32_t n_kf = 0, n_m1 = 0, n_m2 = 0;
-  bool ok = true;
-
   // Sub-tile s of an item starts at query token sub0(d, s): the sub-tiles are
   // walked from the last query rows down, so the CTAs working on the blocks of
   // one KV head at the same time stream the same query rows together (L2 then
   // serves the re-reads; walking up, each CTA would start at its own block).
   auto sub0 = [&](const KvItem &d, int32_t sidx) { return d.i_lo + (d.nsub - 1 - sidx) * TS; };
-  // ---- Q/dO loader: walks this CTA's (item, sub-tile) sequence ahead of the keys
-  KvItem ld;
-  int32_t ld_it = kv_next_item(a, blockIdx.x, ld), ld_j = 0;
-  uint32_t ld_g = 0;  // global index of the next sub-tile to load
-  auto load_next = [&]() {
-    const uint32_t st = ld_g % NS;
-    if (producer) {
+
+  if (producer) {
+    // ============================================================ copies
+    KvItem ld;
+    int32_t ld_it = kv_next_item(a, blockIdx.x, ld), ld_j = 0;
+    uint32_t ld_g = 0, n_kv = 0;
+    auto load_kv = [&](const KvItem &d) {
+      mbar_arrive_expect_tx(B_KF, 5 * Ly::kKBox);
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc)
+        tma_load_3d(sbase + Ly::kKOff + cc * Ly::kKBox, &tm_k, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        tma_load_3d(sbase + Ly::kVOff + cc * Ly::kKBox, &tm_v, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
+      ++n_kv;
+    };
+    while (ld.valid) {
+      if (ld_j == 0) {
+        // the previous item's last S^T/dP^T done: the K/V block is free
+        if (n_kv > 0 && !wait_bar(B_KVE, (n_kv - 1) & 1, abort_flag, 24)) break;
+        load_kv(ld);
+      }
+      const uint32_t st = ld_g % NS;
+      // the stage's previous sub-tile: its dV/dK is done
+      if (ld_g >= static_cast<uint32_t>(NS) &&
+          !wait_bar(B_QSE(st), ((ld_g / NS) & 1) ^ 1, abort_flag, 23))
+        break;
       const uint32_t dst = sbase + Ly::kStOff + st * Ly::kStage;
       const int32_t tok = ld.s0 + sub0(ld, ld_j);
       mbar_arrive_expect_tx(B_QS(st), Ly::kStage);
@@ -680,49 +715,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(dst + (3 + cc) * Ly::kQBox, &tm_do, cc * 64, ld.kvh * G, tok, B_QS(st));
+      ++ld_g;
+      if (++ld_j >= ld.nsub) {
+        ld_j = 0;
+        ld_it = kv_next_item(a, ld_it + gridDim.x, ld);
+      }
     }
-    ++ld_g;
-    if (++ld_j >= ld.nsub) {
-      ld_j = 0;
-      ld_it = kv_next_item(a, ld_it + gridDim.x, ld);
-    }
-  };
-  auto load_kv = [&](const KvItem &d) {
-    if (producer) {
-      mbar_arrive_expect_tx(B_KF, 5 * Ly::kKBox);
-#pragma unroll
-      for (int cc = 0; cc < 3; ++cc)
-        tma_load_3d(sbase + Ly::kKOff + cc * Ly::kKBox, &tm_k, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-        tma_load_3d(sbase + Ly::kVOff + cc * Ly::kKBox, &tm_v, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
-    }
-    ++n_kf;
-  };
-  // lse * log2(e) and D of the 64 rows of sub-tile sidx of item d (threads
-  // 0..63 load one row each; stage_rows puts them in slot p)
-  float r_lse = 0.f, r_D = 0.f;
-  auto fetch_rows = [&](const KvItem &d, int32_t sidx) {
-    if (threadIdx.x < kKvRows) {
-      const int32_t ti = sub0(d, sidx) + threadIdx.x / G, h = d.kvh * G + threadIdx.x % G;
-      const bool v = ti < d.L;
-      const size_t grow = static_cast<size_t>(d.s0 + ti) * a.Hq + h;
-      r_lse = v ? __ldg(a.lse + grow) * kLog2e : 0.f;
-      r_D = v ? __ldg(a.D + grow) : 0.f;
-    }
-  };
-  auto stage_rows = [&](uint32_t p) {
-    if (threadIdx.x < kKvRows) {
-      c_lse[p * kKvRows + threadIdx.x] = r_lse;
-      c_D[p * kKvRows + threadIdx.x] = r_D;
-    }
-  };
-  // S^T(g) = K Q^T and dP^T(g) = V dO^T (issued only while `go`; Q/dO(g) must be
-  // the latest load of its stage).  The counts move on every thread either way.
-  auto issue_sdp = [&](uint32_t g, bool go) -> bool {
-    const uint32_t st = g % NS;
-    ++n_m1;
-    if (issuer && go) {
+    // no copy may still be landing when shared memory goes back
+    if (n_kv > 0) drain_wait(B_KF, (n_kv - 1) & 1);
+    for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
+      if (ld_g > s) drain_wait(B_QS(s), ((ld_g - 1 - s) / NS) & 1);
+  } else if (issuer) {
+    // ============================================================ MMAs
+    const uint32_t k_lo = ((sbase + Ly::kKOff) >> 4) | (1u << 16);
+    const uint32_t v_lo = ((sbase + Ly::kVOff) >> 4) | (1u << 16);
+    constexpr uint32_t kIdS = idesc_f32acc(128, kKvRows, 1, 0, 0);
+    constexpr uint32_t kIdV = idesc_f32acc(128, kDv, 1, 0, 1);
+    constexpr uint32_t kIdK = idesc_f32acc(128, kDqk, 1, 0, 1);
+    // S^T(g) = K Q^T and dP^T(g) = V dO^T
+    auto issue_sdp = [&](uint32_t g) -> bool {
+      const uint32_t st = g % NS;
       if (!wait_bar(B_QS(st), (g / NS) & 1, abort_flag, 25)) return false;
       tc_fence_after();
       const uint32_t q_lo = ((sbase + Ly::kStOff + st * Ly::kStage) >> 4) | (1u << 16);
@@ -740,45 +752,94 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_ss2(tmem + kColPT, v_lo + ao, kBwdDescHi, do_lo + bo, kBwdDescHi, kIdS, ks > 0);
       }
       mma_commit(B_MM1);
-    }
-    return true;
-  };
-
-  KvItem cur;
-  int32_t it = kv_next_item(a, blockIdx.x, cur);
-  if (cur.valid) {
-    load_kv(cur);
-    fetch_rows(cur, 0);
-    stage_rows(0);
-  }
-  while (ld.valid && ld_g < static_cast<uint32_t>(NS)) load_next();
-  __syncthreads();  // the first sub-tile's rows
-  uint32_t g0 = 0;  // global index of the current item's first sub-tile
-  while (ok && cur.valid) {
-    KvItem nxt;
-    const int32_t it_n = kv_next_item(a, it + gridDim.x, nxt);
-    const int32_t kj = cur.k0 + lane_row;  // this thread's key (both halves)
-    const bool kvalid = compute && kj < cur.L;
-    if (issuer) ok = wait_bar(B_KF, (n_kf - 1) & 1, abort_flag, 24);
-    ok = issue_sdp(g0, ok) && ok;
-    for (int32_t sidx = 0; sidx < cur.nsub; ++sidx) {
-      const uint32_t g = g0 + sidx;
-      const int32_t i0 = sub0(cur, sidx);
-      // the last S^T/dP^T of this item done: K/V can take the next item's
-      if (sidx == cur.nsub - 1 && nxt.valid) {
-        if (producer && ok) ok = wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 26);
-        load_kv(nxt);
+      return true;
+    };
+    KvItem cur;
+    int32_t it = kv_next_item(a, blockIdx.x, cur);
+    uint32_t g0 = 0, k = 0;
+    bool ok = true, issued = false;
+    while (ok && cur.valid) {
+      if (!(ok = wait_bar(B_KF, k & 1, abort_flag, 24))) break;
+      tc_fence_after();
+      if (!(ok = issue_sdp(g0))) break;
+      issued = true;
+      if (cur.nsub == 1) mma_commit(B_KVE);
+      for (int32_t sidx = 0; sidx < cur.nsub; ++sidx) {
+        const uint32_t g = g0 + sidx;
+        // the rows wrote P^T/dS^T(g) (and so have read S^T/dP^T(g))
+        if (!(ok = wait_bar(B_PR, g & 1, abort_flag, 26))) break;
+        tc_fence_after();
+        // S^T/dP^T of the next sub-tile first, then dV/dK of this one
+        if (sidx + 1 < cur.nsub) {
+          if (!(ok = issue_sdp(g + 1))) break;
+          if (sidx + 2 == cur.nsub) mma_commit(B_KVE);  // the item's last S^T/dP^T
+        }
+        const uint32_t stb = (sbase + Ly::kStOff + (g % NS) * Ly::kStage) >> 4;
+#pragma unroll
+        for (int ks = 0; ks < kKvRows / 16; ++ks) {
+          const uint32_t step = ks * ((16 * kRowBytes) >> 4);
+          // dV += P^T dO: B = the dO rows read N-major (LBO = one box)
+          mma_ts2(tmem + kColV, tmem + kColP + ks * 8,
+                  stb + ((3 * Ly::kQBox) >> 4) + step + ((Ly::kQBox >> 4) << 16), kBwdDescHi, kIdV,
+                  (sidx > 0 || ks > 0) ? 1u : 0u);
+          // dK += dS^T Q: B = the q_rot rows read N-major
+          mma_ts2(tmem + kColK, tmem + kColDS + ks * 8, stb + step + ((Ly::kQBox >> 4) << 16),
+                  kBwdDescHi, kIdK, (sidx > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(B_MM2);
+        mma_commit(B_QSE(g % NS));
+        if (sidx + 1 == cur.nsub) mma_commit(B_ACCF);
       }
-      // the next sub-tile's rows: loads go out now, land in shared memory
-      // before the barrier
-      if (sidx + 1 < cur.nsub)
-        fetch_rows(cur, sidx + 1);
-      else if (nxt.valid)
-        fetch_rows(nxt, 0);
-      uint32_t sv[32], pv[32];
-      if (compute) {
-        // S^T(g), dP^T(g) complete
-        if (!wait_bar(B_MM1, (n_m1 - 1) & 1, abort_flag, 26)) ok = false;
+      g0 += cur.nsub;
+      ++k;
+      it = kv_next_item(a, it + gridDim.x, cur);
+    }
+    // every MMA done before TMEM goes back
+    if (issued) {
+      mma_commit(B_DRAIN);
+      drain_wait(B_DRAIN, 0);
+    }
+  } else if (compute) {
+    // ============================================================ rows
+    const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const bool writer = threadIdx.x < kKvRows;  // stages lse and D of one query row
+    float r_lse = 0.f, r_D = 0.f;
+    auto fetch_rows = [&](const KvItem &d, int32_t sidx) {
+      const int32_t ti = sub0(d, sidx) + threadIdx.x / G, h = d.kvh * G + threadIdx.x % G;
+      const bool v = ti < d.L;
+      const size_t grow = static_cast<size_t>(d.s0 + ti) * a.Hq + h;
+      r_lse = v ? __ldg(a.lse + grow) * kLog2e : 0.f;
+      r_D = v ? __ldg(a.D + grow) : 0.f;
+    };
+    KvItem cur;
+    int32_t it = kv_next_item(a, blockIdx.x, cur);
+    if (cur.valid && writer) {
+      fetch_rows(cur, 0);
+      c_lse[threadIdx.x] = r_lse;
+      c_D[threadIdx.x] = r_D;
+      mbar_arrive(B_LF(0));
+    }
+    uint32_t g0 = 0, k = 0;
+    bool ok = true;
+    while (ok && cur.valid) {
+      KvItem nxt;
+      const int32_t it_n = kv_next_item(a, it + gridDim.x, nxt);
+      const int32_t kj = cur.k0 + lane_row;  // this thread's key (both halves)
+      const bool kvalid = kj < cur.L;
+      for (int32_t sidx = 0; sidx < cur.nsub; ++sidx) {
+        const uint32_t g = g0 + sidx;
+        const int32_t i0 = sub0(cur, sidx);
+        const bool more = sidx + 1 < cur.nsub || nxt.valid;
+        // the next sub-tile's rows: the loads go out now
+        if (writer && more) {
+          if (sidx + 1 < cur.nsub)
+            fetch_rows(cur, sidx + 1);
+          else
+            fetch_rows(nxt, 0);
+        }
+        // S^T(g), dP^T(g) complete; this sub-tile's lse and D in their slot
+        if (!(ok = wait_bar_warp(B_MM1, g & 1, abort_flag, 22))) break;
+        if (!(ok = wait_bar_warp(B_LF(g & 1), (g >> 1) & 1, abort_flag, 21))) break;
         tc_fence_after();
         const float4 *cl4 = reinterpret_cast<const float4 *>(c_lse + (g & 1) * kKvRows + 32 * half);
         const float4 *cd4 = reinterpret_cast<const float4 *>(c_D + (g & 1) * kKvRows + 32 * half);
@@ -792,6 +853,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (a.window > 0) c_hi = min(c_hi, max(0, min(d0 + a.window, kKvRows)) * G);
         c_hi = min(c_hi, kKvRows) - 32 * half;
         const uint32_t span = (kvalid && c_hi > c_lo) ? static_cast<uint32_t>(c_hi - c_lo) : 0u;
+        uint32_t sv[32], pv[32];
         tmem_ld32p(lane_t + kColST + 32 * half, sv);
         tmem_ld32p(lane_t + kColPT + 32 * half, pv);
         tmem_wait_ld();
@@ -813,82 +875,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pv[c >> 1] = pack_bf16x2(ds[0], ds[1]);
           pv[(c >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-      }
-      // dV/dK(g-1) complete: P^T/dS^T and the Q/dO stage of sub-tile g-1 are free
-      if ((compute || producer) && ok && n_m2 > 0)
-        ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 27);
-      while (ld.valid && ld_g <= g + 2) load_next();
-      if (compute) {
+        // dV/dK(g-1) complete: they have read P^T/dS^T(g-1), and every row
+        // has read this CTA's other lse / D slot
+        if (g > 0 && !(ok = wait_bar_warp(B_MM2, (g - 1) & 1, abort_flag, 27))) break;
         tc_fence_after();
         tmem_st16p(lane_t + kColP + 16 * half, sv);   // P^T as bf16 pairs
         tmem_st16p(lane_t + kColDS + 16 * half, pv);  // dS^T as bf16 pairs
         tmem_wait_st();
-      }
-      // slot (g+1) & 1 was last read in sub-tile g-1
-      stage_rows((g + 1) & 1);
-      tc_fence_before();
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
-      if (issuer) tc_fence_after();
-      // S^T/dP^T of the next sub-tile first, then dV/dK of this one
-      if (sidx + 1 < cur.nsub) ok = issue_sdp(g + 1, ok) && ok;
-      if (issuer && ok) {
-        const uint32_t stb = (sbase + Ly::kStOff + (g % NS) * Ly::kStage) >> 4;
-#pragma unroll
-        for (int ks = 0; ks < kKvRows / 16; ++ks) {
-          const uint32_t step = ks * ((16 * kRowBytes) >> 4);
-          // dV += P^T dO: B = the dO rows read N-major (LBO = one box)
-          mma_ts2(tmem + kColV, tmem + kColP + ks * 8,
-                  stb + ((3 * Ly::kQBox) >> 4) + step + ((Ly::kQBox >> 4) << 16), kBwdDescHi, kIdV,
-                  (sidx > 0 || ks > 0) ? 1u : 0u);
-          // dK += dS^T Q: B = the q_rot rows read N-major
-          mma_ts2(tmem + kColK, tmem + kColDS + ks * 8, stb + step + ((Ly::kQBox >> 4) << 16),
-                  kBwdDescHi, kIdK, (sidx > 0 || ks > 0) ? 1u : 0u);
+        tc_fence_before();
+        mbar_arrive(B_PR);
+        if (writer && more) {
+          c_lse[((g + 1) & 1) * kKvRows + threadIdx.x] = r_lse;
+          c_D[((g + 1) & 1) * kKvRows + threadIdx.x] = r_D;
+          mbar_arrive(B_LF((g + 1) & 1));
         }
-        mma_commit(B_MM2);
       }
-      ++n_m2;
-    }
-    if (!ok) break;
-    if (compute) {
-      ok = wait_bar(B_MM2, (n_m2 - 1) & 1, abort_flag, 27);
+      if (!ok) break;
+      // the item's last dV/dK complete
+      if (!(ok = wait_bar_warp(B_ACCF, k & 1, abort_flag, 28))) break;
       tc_fence_after();
-    }
-    if (compute && half == 0) {
-      // dV row: 128 fp32 columns -> bf16
-      __nv_bfloat16 *dst = a.dv + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDv;
+      if (half == 0) {
+        // dV row: 128 fp32 columns -> bf16
+        __nv_bfloat16 *dst = a.dv + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDv;
 #pragma unroll 1
-      for (int32_t cb = 0; cb < kDv; cb += 32) {
-        uint32_t r[32];
-        tmem_ld32p(lane_t + kColV + cb, r);
-        tmem_wait_ld();
-        reg_fence<32>(r);
-        if (kvalid) {
+        for (int32_t cb = 0; cb < kDv; cb += 32) {
+          uint32_t r[32];
+          tmem_ld32p(lane_t + kColV + cb, r);
+          tmem_wait_ld();
+          reg_fence<32>(r);
+          if (kvalid) {
 #pragma unroll
-          for (int32_t e = 0; e < 32; e += 8) {
-            const float *f = reinterpret_cast<const float *>(r + e);
-            *reinterpret_cast<uint4 *>(dst + cb + e) =
-                make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                           pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+            for (int32_t e = 0; e < 32; e += 8) {
+              const float *f = reinterpret_cast<const float *>(r + e);
+              *reinterpret_cast<uint4 *>(dst + cb + e) =
+                  make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                             pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+            }
           }
         }
+      } else {
+        bwd_store_qk_row(lane_t + kColK, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
+                         a.dk + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDqk, kvalid);
       }
+      tc_fence_before();
+      g0 += cur.nsub;
+      ++k;
+      cur = nxt;
+      it = it_n;
     }
-    if (compute && half == 1) {
-      bwd_store_qk_row(lane_t + kColK, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
-                       a.dk + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDqk, kvalid);
-    }
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-    g0 += cur.nsub;
-    cur = nxt;
-    it = it_n;
   }
-  if (n_kf > 0) drain_wait(B_KF, (n_kf - 1) & 1);
-  for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s)
-    if (ld_g > s) drain_wait(B_QS(s), ((ld_g - 1 - s) / NS) & 1);
-  if (n_m1 > 0) drain_wait(B_MM1, (n_m1 - 1) & 1);
-  if (n_m2 > 0) drain_wait(B_MM2, (n_m2 - 1) & 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

@@ -253,38 +253,31 @@ def dq_roles(nblk, skip=()):
 
 def dkdv_roles(nsub, skip=()):
     """The dk/dv kernel for one CTA whose items (key blocks) have nsub[i] query
-    sub-tiles each.  `skip` names waits to leave out."""
+    sub-tiles each.  The roles meet only on mbarriers: the rows tell the MMA
+    thread that P^T/dS^T(g) are in TMEM (PR, 256 arrivals; S^T/dP^T(g+1) and
+    dV/dK(g) follow); rows 0..63 stage lse and D of the next sub-tile in one of
+    two shared-memory slots (LF: written).  They write slot (g+1) & 1 after
+    waiting for dV/dK(g-1), which needed every row's PR for sub-tile g-1, so
+    every read of that slot's previous contents is done.  The MMA thread
+    frees a Q/dO stage after the dV/dK that read it (QSE), the K/V block after
+    the item's last S^T/dP^T (KVE) and hands the finished accumulators to the
+    rows after the item's last dV/dK (ACCF).  `skip` names waits to leave out."""
     items = list(nsub)
     seq = [(it, j) for it, n in enumerate(items) for j in range(n)]
     first = [sum(items[:i]) for i in range(len(items))]
+    total = len(seq)
 
     def producer():
         yield ("tma", "KVB", ("KVB", 0), "KF")
-        ld = 0
-        while ld < len(seq) and ld < NS:
+        for ld in range(total):
+            it, j = seq[ld]
+            if j == 0 and it > 0:
+                if "producer_kve" not in skip:
+                    yield ("wait", "KVE", it)  # the previous item's last S^T/dP^T
+                yield ("tma", "KVB", ("KVB", it), "KF")
+            if ld >= NS and "producer_qse" not in skip:
+                yield ("wait", f"QSE{ld % NS}", ld // NS)  # dV/dK(ld - NS) read the stage
             yield ("tma", f"QO{ld % NS}", ("QO", ld), f"QS{ld % NS}")
-            ld += 1
-        n_m1 = 1  # S^T/dP^T of the first sub-tile, issued at the first item's start
-        n_m2 = 0
-        for it, n in enumerate(items):
-            g0 = first[it]
-            if it > 0:
-                n_m1 += 1
-            for s in range(n):
-                g = g0 + s
-                if s == n - 1 and it + 1 < len(items):
-                    yield ("wait", "MM1", n_m1)  # the last S^T/dP^T of the item
-                    yield ("tma", "KVB", ("KVB", it + 1), "KF")
-                if n_m2 > 0 and "producer_mm2" not in skip:
-                    yield ("wait", "MM2", n_m2)  # dV/dK(g-1): the stage of sub-tile g+2 is free
-                while ld < len(seq) and ld <= g + 2:
-                    yield ("tma", f"QO{ld % NS}", ("QO", ld), f"QS{ld % NS}")
-                    ld += 1
-                yield ("sync",)
-                n_m2 += 1
-                if s + 1 < n:
-                    n_m1 += 1
-            yield ("sync",)
 
     def issuer():
         def issue_sdp(it, g):
@@ -296,42 +289,54 @@ def dkdv_roles(nsub, skip=()):
             g0 = first[it]
             yield ("wait", "KF", it + 1)
             yield from issue_sdp(it, g0)
+            if n == 1:
+                yield ("commit", "KVE")
             for s in range(n):
                 g = g0 + s
-                yield ("sync",)
+                if "issuer_pr" not in skip:
+                    yield ("wait", "PR", g + 1)  # P^T/dS^T(g) written, S^T/dP^T(g) read
                 if s + 1 < n:
-                    yield from issue_sdp(it, g + 1)  # S^T/dP^T(g+1) ahead of dV/dK(g)
+                    yield from issue_sdp(it, g + 1)
+                    if s + 2 == n:
+                        yield ("commit", "KVE")
                 reads = [("Ph0", ("P", g)), ("Ph1", ("P", g)), (f"QO{g % NS}", ("QO", g))]
                 if s > 0:
                     reads.append(("acc", ("acc", it, s - 1)))
                 yield ("mma", reads, [("acc", ("acc", it, s))])
                 yield ("commit", "MM2")
-            yield ("sync",)
+                yield ("commit", f"QSE{g % NS}")
+                if s + 1 == n:
+                    yield ("commit", "ACCF")
 
-    def rows(h):
+    def rows(h, writer):
         def role():
-            n_m1 = n_m2 = 0
+            if writer:  # the first sub-tile's lse / D
+                yield ("write", "L0", ("L", 0))
+                yield ("arrive", "LF0")
             for it, n in enumerate(items):
                 g0 = first[it]
-                n_m1 += 1
                 for s in range(n):
                     g = g0 + s
-                    yield ("wait", "MM1", n_m1)
+                    yield ("wait", "MM1", g + 1)
                     yield ("read", f"STh{h}", ("ST", g))
-                    if n_m2 > 0 and "rows_mm2" not in skip:
-                        yield ("wait", "MM2", n_m2)  # dV/dK(g-1) read P^T/dS^T
+                    if "rows_lf" not in skip:
+                        yield ("wait", f"LF{g & 1}", (g >> 1) + 1)
+                    yield ("read", f"L{g & 1}", ("L", g))
+                    if g > 0 and "rows_mm2" not in skip:
+                        yield ("wait", "MM2", g)  # dV/dK(g-1) read P^T/dS^T
                     yield ("write", f"Ph{h}", ("P", g))
-                    yield ("sync",)
-                    n_m2 += 1
-                    if s + 1 < n:
-                        n_m1 += 1
-                if h == 0:
-                    yield ("wait", "MM2", n_m2)
-                    yield ("read", "acc", ("acc", it, n - 1))
-                yield ("sync",)
+                    yield ("arrive", "PR")
+                    if writer and g + 1 < total:
+                        yield ("write", f"L{(g + 1) & 1}", ("L", g + 1))
+                        yield ("arrive", f"LF{(g + 1) & 1}")
+                yield ("wait", "ACCF", it + 1)
+                yield ("read", "acc", ("acc", it, n - 1))
         return role()
 
-    return {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}, {}
+    roles = {"producer": producer(), "issuer": issuer(), "rows0": rows(0, True),
+             "rows1": rows(1, False)}
+    # PR: both row roles arrive; LF: only the writer
+    return roles, {"PR": 2}
 
 
 def run(make_roles, sizes, seed, skip=()):
