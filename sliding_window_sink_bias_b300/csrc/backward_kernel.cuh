@@ -154,8 +154,6 @@ __global__ void __launch_bounds__(256) bwd_dsink_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ shared pieces
-// TMEM columns: S (or S^T) 0..63, dP (or dP^T) 64..127, accumulators from 128.
-constexpr uint32_t kBwdColS = 0, kBwdColP = 64, kBwdColAcc = 128;
 constexpr uint32_t kBwdDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);  // SW128, SBO 1024
 
 // Inverse RoPE on dims 0..63 held in x[64] (fp32), at position pos.
