@@ -192,3 +192,40 @@ def test_fp8_decode_argument_checks(L):
     assert dec(ks=None) == sa.EINVAL
     assert dec(vs=None) == sa.EINVAL
     assert dec(ring=1, window=128) == sa.EINVAL
+
+
+def test_backward_workspace_size(L):
+    sz = L.sinkattn_prefill_backward_workspace_size
+    assert sz(4096, 64, 8) > sz(1024, 64, 8) > 0
+    assert sz(-1, 64, 8) == 0 and sz(16, 64, 0) == 0 and sz(16, 12, 8) == 0
+
+
+def test_backward_argument_checks(L):
+    """Rejections that happen before any CUDA call (batch and total are
+    non-zero here: an empty batch only clears dsink, on the device)."""
+    import sliding_window_sink_bias_b300 as sa
+    P = ctypes.c_void_p
+    f = lambda x: None if x is None else P(256 * x)
+    ws_ok = L.sinkattn_prefill_backward_workspace_size(16, 64, 8)
+
+    def bwd(q=1, dq=1, total=16, max_seqlen=16, hq=64, hkv=8, scale=0.0, ring=0, ws=1,
+            ws_bytes=None, q_off=0):
+        p = sa.Params(scale, 0, 0, ring)
+        qp = P(256 * q + q_off) if q is not None else None
+        return L.sinkattn_prefill_backward(
+            qp, f(1), f(1), f(1), f(1), 1, total, max_seqlen, hq, hkv, 128, 1e4, ctypes.byref(p),
+            f(1), f(1), f(1), f(ws), ws_ok if ws_bytes is None else ws_bytes, f(dq), f(1), f(1),
+            f(1), None)
+
+    assert bwd(total=-1) == sa.EINVAL
+    assert bwd(hq=64, hkv=7) == sa.EINVAL            # Hq not a multiple of Hkv
+    assert bwd(hq=48, hkv=16) == sa.EUNSUPPORTED     # group of 3
+    assert bwd(hq=128, hkv=1) == sa.EUNSUPPORTED     # group above 64
+    assert bwd(ring=1) == sa.EINVAL                  # no ring cache in prefill
+    assert bwd(max_seqlen=0) == sa.EINVAL
+    assert bwd(scale=-1.0) == sa.EINVAL
+    assert bwd(q=None) == sa.EINVAL
+    assert bwd(dq=None) == sa.EINVAL
+    assert bwd(q_off=8) == sa.EINVAL                 # q not 16-byte aligned
+    assert bwd(ws=None) == sa.EWORKSPACE
+    assert bwd(ws_bytes=ws_ok - 1) == sa.EWORKSPACE
