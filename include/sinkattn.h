@@ -200,8 +200,13 @@ sinkattn_status sinkattn_decode_fp8(const void *q, const void *kcache, const voi
  *     sinkattn_decode_workspace_size) are rejected with SINKATTN_EWORKSPACE
  *     before anything is launched.
  *   - The first call on each device looks up the buffer's device address
- *     (cudaGetSymbolAddress on that device); make that first call before any
- *     stream capture.
+ *     (cudaGetSymbolAddress on that device) and keeps it for the life of the
+ *     process; make that first call before any stream capture.  A
+ *     cudaDeviceReset (or anything else that destroys the device's primary
+ *     context) invalidates the kept address: do not call this entry point on
+ *     that device afterwards.
+ *   - Arguments sinkattn_decode would reject get the same status, before the
+ *     buffer is looked up; an empty batch returns SINKATTN_OK.
  *   - All calls share the one buffer per device: calls that overlap on the GPU
  *     (other streams, other host threads) race and give wrong results.  Calls
  *     on one stream are ordered and safe.

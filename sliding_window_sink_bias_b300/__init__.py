@@ -119,6 +119,24 @@ def _require(t, name, dtype, ndim):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _shape(t, name, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _outputs(out, lse, out_shape, lse_shape, device):
+    """The caller's out/lse (checked: dtype, contiguity, exact shape), or new ones."""
+    if out is None:
+        out = torch.empty(*out_shape, dtype=torch.bfloat16, device=device)
+    if lse is None:
+        lse = torch.empty(*lse_shape, dtype=torch.float32, device=device)
+    _require(out, "out", torch.bfloat16, len(out_shape))
+    _require(lse, "lse", torch.float32, len(lse_shape))
+    _shape(out, "out", out_shape)
+    _shape(lse, "lse", lse_shape)
+    return out, lse
+
+
 def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_base: float,
             out=None, lse=None, scale=None, rope_style: int = 0, rope_off: bool = False,
             stream=None):
@@ -134,14 +152,10 @@ def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_bas
     hkv = k.shape[1]
     if dqk != 192 or k.shape != (total, hkv, 192) or v.shape != (total, hkv, 128):
         raise ValueError("expected q [T,Hq,192], k [T,Hkv,192], v [T,Hkv,128]")
-    if sink.shape[0] != hq:
-        raise ValueError("sink must have one entry per query head")
-    if out is None:
-        out = torch.empty(total, hq, 128, dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty(total, hq, dtype=torch.float32, device=q.device)
-    _require(out, "out", torch.bfloat16, 3)
-    _require(lse, "lse", torch.float32, 2)
+    _shape(sink, "sink", (hq,))
+    if cu_seqlens.shape[0] < 1:
+        raise ValueError("cu_seqlens must have batch + 1 >= 1 entries")
+    out, lse = _outputs(out, lse, (total, hq, 128), (total, hq), q.device)
     p = _params(scale, rope_style, rope_off)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(cu_seqlens), cu_seqlens.shape[0] - 1,
             total, int(max_seqlen), hq, hkv, int(window), float(rope_base))
@@ -179,16 +193,29 @@ def prefill_backward(q, k, v, sink, cu_seqlens, out, lse, dout, *, max_seqlen: i
     _require(dout, "dout", torch.bfloat16, 3)
     total, hq, _ = q.shape
     hkv = k.shape[1]
-    if out.shape != (total, hq, 128) or dout.shape != (total, hq, 128) or lse.shape != (total, hq):
-        raise ValueError("expected out/dout [T, Hq, 128] and lse [T, Hq]")
+    if q.shape[2] != 192 or k.shape != (total, hkv, 192) or v.shape != (total, hkv, 128):
+        raise ValueError("expected q [T,Hq,192], k [T,Hkv,192], v [T,Hkv,128]")
+    _shape(sink, "sink", (hq,))
+    _shape(out, "out", (total, hq, 128))
+    _shape(dout, "dout", (total, hq, 128))
+    _shape(lse, "lse", (total, hq))
+    if cu_seqlens.shape[0] < 1:
+        raise ValueError("cu_seqlens must have batch + 1 >= 1 entries")
     need = prefill_backward_workspace_size(total, hq, hkv)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     dev = q.device
-    dq = torch.empty(total, hq, 192, dtype=torch.bfloat16, device=dev) if dq is None else dq
-    dk = torch.empty(total, hkv, 192, dtype=torch.bfloat16, device=dev) if dk is None else dk
-    dv = torch.empty(total, hkv, 128, dtype=torch.bfloat16, device=dev) if dv is None else dv
-    dsink = torch.empty(hq, dtype=torch.float32, device=dev) if dsink is None else dsink
+    grads = []
+    for name, t, shape, dtype in (("dq", dq, (total, hq, 192), torch.bfloat16),
+                                  ("dk", dk, (total, hkv, 192), torch.bfloat16),
+                                  ("dv", dv, (total, hkv, 128), torch.bfloat16),
+                                  ("dsink", dsink, (hq,), torch.float32)):
+        if t is None:
+            t = torch.empty(*shape, dtype=dtype, device=dev)
+        _require(t, name, dtype, len(shape))
+        _shape(t, name, shape)
+        grads.append(t)
+    dq, dk, dv, dsink = grads
     p = _params(scale, rope_style, rope_off)
     st = lib().sinkattn_prefill_backward(
         _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, total,
@@ -217,13 +244,12 @@ def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, ro
     s_cap, hkv = kcache.shape[1], kcache.shape[2]
     if dqk != 192 or kcache.shape != (b, s_cap, hkv, 192) or vcache.shape != (b, s_cap, hkv, 128):
         raise ValueError("expected q [B,T,Hq,192], kcache [B,S,Hkv,192], vcache [B,S,Hkv,128]")
+    _shape(sink, "sink", (hq,))
+    _shape(seqlens, "seqlens", (b,))
     need = decode_workspace_size(b, t, hq, hkv, max_seqlen, window)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    if out is None:
-        out = torch.empty(b, t, hq, 128, dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty(b, t, hq, dtype=torch.float32, device=q.device)
+    out, lse = _outputs(out, lse, (b, t, hq, 128), (b, t, hq), q.device)
     p = _params(scale, rope_style, rope_off, kv_ring)
     args = (_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(sink), int(window),
             float(rope_base), b, t, s_cap, int(max_seqlen), hq, hkv)
@@ -246,11 +272,9 @@ def decode_fp8(q, kcache, vcache, k_scale, v_scale, seqlens, sink, *, max_seqlen
     and the results as decode()."""
     _require(q, "q", torch.bfloat16, 4)
     for name, t in (("kcache", kcache), ("vcache", vcache)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or \
-                t.dtype not in (torch.float8_e4m3fn, torch.uint8):
-            raise TypeError(f"{name} must be a 4-dim CUDA float8_e4m3fn/uint8 tensor")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
+        if not isinstance(t, torch.Tensor) or t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must be a float8_e4m3fn/uint8 tensor")
+        _require(t, name, t.dtype, 4)
     _require(k_scale, "k_scale", torch.float32, 1)
     _require(v_scale, "v_scale", torch.float32, 1)
     _require(seqlens, "seqlens", torch.int32, 1)
@@ -259,13 +283,14 @@ def decode_fp8(q, kcache, vcache, k_scale, v_scale, seqlens, sink, *, max_seqlen
     s_cap, hkv = kcache.shape[1], kcache.shape[2]
     if dqk != 192 or kcache.shape != (b, s_cap, hkv, 192) or vcache.shape != (b, s_cap, hkv, 128):
         raise ValueError("expected q [B,T,Hq,192], kcache [B,S,Hkv,192], vcache [B,S,Hkv,128]")
+    _shape(k_scale, "k_scale", (hkv,))
+    _shape(v_scale, "v_scale", (hkv,))
+    _shape(sink, "sink", (hq,))
+    _shape(seqlens, "seqlens", (b,))
     need = decode_workspace_size(b, t, hq, hkv, max_seqlen, window)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    if out is None:
-        out = torch.empty(b, t, hq, 128, dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty(b, t, hq, dtype=torch.float32, device=q.device)
+    out, lse = _outputs(out, lse, (b, t, hq, 128), (b, t, hq), q.device)
     p = _params(scale, rope_style, rope_off)
     st = lib().sinkattn_decode_fp8(
         _ptr(q), kcache.data_ptr(), vcache.data_ptr(), _ptr(k_scale), _ptr(v_scale),
@@ -294,12 +319,9 @@ def decode_noalloc(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window:
     s_cap, hkv = kcache.shape[1], kcache.shape[2]
     if dqk != 192 or kcache.shape != (b, s_cap, hkv, 192) or vcache.shape != (b, s_cap, hkv, 128):
         raise ValueError("expected q [B,T,Hq,192], kcache [B,S,Hkv,192], vcache [B,S,Hkv,128]")
-    if out is None:
-        out = torch.empty(b, t, hq, 128, dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty(b, t, hq, dtype=torch.float32, device=q.device)
-    _require(out, "out", torch.bfloat16, 4)
-    _require(lse, "lse", torch.float32, 3)
+    _shape(sink, "sink", (hq,))
+    _shape(seqlens, "seqlens", (b,))
+    out, lse = _outputs(out, lse, (b, t, hq, 128), (b, t, hq), q.device)
     st = lib().sinkattn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens),
                                        _ptr(sink), int(window), float(rope_base), b, t, s_cap,
                                        int(max_seqlen), hq, hkv, _ptr(out), _ptr(lse),

@@ -694,9 +694,12 @@ extern "C" sinkattn_status sinkattn_decode_noalloc(
   const size_t need =
       sinkattn_decode_workspace_size(batch, T, num_q_heads, num_kv_heads, max_seqlen, window);
   if (need > SINKATTN_NOALLOC_SCRATCH_BYTES) return SINKATTN_EWORKSPACE;
-  if (batch == 0) return sinkattn_decode(q, kcache, vcache, seqlens, sink, window, rope_base, batch,
-                                         T, S_cap, max_seqlen, num_q_heads, num_kv_heads, nullptr,
-                                         0, out, lse, stream);
+  // need == 0: an empty batch (nothing to do) or arguments sinkattn_decode
+  // rejects; either way it answers before any CUDA call, and the scratch
+  // buffer is not looked up.
+  if (need == 0) return sinkattn_decode(q, kcache, vcache, seqlens, sink, window, rope_base, batch,
+                                        T, S_cap, max_seqlen, num_q_heads, num_kv_heads, nullptr,
+                                        0, out, lse, stream);
   void *scratch = nullptr;
   if (sinkattn_status st = noalloc_scratch(&scratch)) return st;
   // Every partial the combine step reads is written first by the same call, so
