@@ -37,7 +37,8 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("dqk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("drot", ctypes.c_int32), ("rope_style", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("rope_base", ctypes.c_double), ("scale", ctypes.c_double)]
+                ("rope_base", ctypes.c_double), ("scale", ctypes.c_double),
+                ("k_rotated", ctypes.c_int32)]
 
 
 def _load():
@@ -57,6 +58,8 @@ def _load():
         lib.oracle_prefill_backward.restype = ctypes.c_int
         lib.oracle_rope.argtypes = [P, i32, i32, i32, ctypes.c_double, ctypes.c_double, P]
         lib.oracle_rope.restype = None
+        lib.oracle_rope_rows.argtypes = [P, i64, i32, i32, i32, ctypes.c_double, P, P]
+        lib.oracle_rope_rows.restype = None
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -103,9 +106,9 @@ def _i32(x):
     return np.ascontiguousarray(x, dtype=np.int32)
 
 
-def _cfg(dqk, dv, drot, rope_style, window, dtype, rope_base, scale):
+def _cfg(dqk, dv, drot, rope_style, window, dtype, rope_base, scale, k_rotated=False):
     return _Cfg(int(dqk), int(dv), int(drot), int(rope_style), int(window), int(dtype),
-                float(rope_base), float(scale))
+                float(rope_base), float(scale), int(bool(k_rotated)))
 
 
 def prefill(q, k, v, sink, cu_seqlens, *, window: int, rope_base: float,
@@ -186,10 +189,11 @@ def prefill_backward(q, k, v, sink, cu_seqlens, dout, *, window: int, rope_base:
 
 def decode(q, kcache, vcache, seqlens, sink, *, window: int, rope_base: float,
            scale: float | None = None, drot: int = 64, rope_style: int = 0,
-           rows=None, nthreads: int = 0):
+           rows=None, nthreads: int = 0, k_rotated: bool = False):
     """MTP-verify decode: q [B, T, Hq, dqk] against kcache [B, S_cap, Hkv, dqk] and
     vcache [B, S_cap, Hkv, dv]; seqlens [B] counts cached tokens including the T
-    new ones.  rows: flat indices (b*T + t)*Hq + h (None = all).
+    new ones.  rows: flat indices (b*T + t)*Hq + h (None = all).  k_rotated: the
+    cache holds keys already rotated at their positions (only q is rotated).
     Returns (out [n, dv], lse [n]) or, with rows=None, [B, T, Hq, dv] and [B, T, Hq]."""
     qa, dt_q = _as_input(q)
     ka, dt_k = _as_input(kcache)
@@ -203,7 +207,7 @@ def decode(q, kcache, vcache, seqlens, sink, *, window: int, rope_base: float,
     sl = _i32(seqlens)
     if scale is None:
         scale = 1.0 / math.sqrt(dqk)
-    cfg = _cfg(dqk, dv, drot, rope_style, window, dt_q, rope_base, scale)
+    cfg = _cfg(dqk, dv, drot, rope_style, window, dt_q, rope_base, scale, k_rotated)
     if rows is None:
         ra, n = None, B * T * Hq
     else:
@@ -228,4 +232,17 @@ def rope(x, pos: float, *, base: float, drot: int = 64, rope_style: int = 0):
     y = np.zeros_like(xa)
     _load().oracle_rope(xa.ctypes.data, xa.shape[0], int(drot), int(rope_style),
                         float(base), float(pos), y.ctypes.data)
+    return y
+
+
+def rope_rows(x, pos, *, base: float, drot: int = 64, rope_style: int = 0):
+    """The oracle's rotary embedding of many fp64 rows: x [..., d] with one
+    position per row, pos broadcastable to x.shape[:-1].  Returns fp64 [..., d]."""
+    xa = np.ascontiguousarray(x, dtype=np.float64)
+    d = xa.shape[-1]
+    pa = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.float64), xa.shape[:-1]))
+    y = np.zeros_like(xa)
+    n = int(np.prod(xa.shape[:-1]))
+    _load().oracle_rope_rows(xa.ctypes.data, n, d, int(drot), int(rope_style), float(base),
+                             pa.ctypes.data, y.ctypes.data)
     return y

@@ -33,7 +33,8 @@
  *   - RoPE: theta_t = base^(-2t/drot) for pair t; pair t is dims (2t, 2t+1)
  *     (style 0, RoFormer) or (t, t + drot/2) (style 1); positions are 0-based
  *     per sequence in prefill and the absolute cache index in decode; the
- *     decode K cache holds raw (unrotated) keys.
+ *     decode K cache holds raw (unrotated) keys unless cfg->k_rotated says it
+ *     holds keys already rotated at their positions (then only q is rotated).
  *   - log-sum-exp output: lse_i = m_i + ln(exp(sink - m_i) + sum_j exp(a_ij - m_i)),
  *     natural log, sink included.
  *   - an empty visible set gives o = 0, lse = sink.
@@ -53,6 +54,9 @@ typedef struct {
     int32_t dtype;      /* 0: q/k/v hold bf16 bit patterns; 1: q/k/v hold fp64 */
     double rope_base;   /* <= 0 disables RoPE */
     double scale;       /* the factor applied to q.k (1/sqrt(d) in eq. (1)) */
+    int32_t k_rotated;  /* 1: the keys passed in are already rotated at their own
+                           positions (a cache that stores rotated keys); only q is
+                           rotated here */
 } oracle_cfg;
 
 /* bf16 is the top half of an IEEE binary32; every bf16 value is exact in fp64. */
@@ -88,6 +92,15 @@ void oracle_rope(const double *x, int32_t d, int32_t drot, int32_t style,
         y[ia] = x[ia] * c - x[ib] * s;
         y[ib] = x[ia] * s + x[ib] * c;
     }
+}
+
+/* The rotation above applied to n rows of d values, row r at position pos[r]
+ * (x and y are [n, d] fp64; used to build caches that hold rotated keys). */
+void oracle_rope_rows(const double *x, int64_t n, int32_t d, int32_t drot, int32_t style,
+                      double base, const double *pos, double *y)
+{
+    for (int64_t r = 0; r < n; ++r)
+        oracle_rope(x + r * d, d, drot, style, base, pos[r], y + r * d);
 }
 
 /* One requested output row: which query, which head, which keys it sees. */
@@ -146,8 +159,11 @@ static int run_group(row_t *rows, int64_t n, const void *q, const void *k,
             if (!tmp) continue;
             const int64_t off = ((kv_base + lo + j) * Hkv + g) * (int64_t)dqk;
             for (int32_t e = 0; e < dqk; ++e) tmp[e] = load(k, cfg->dtype, off + e);
-            oracle_rope(tmp, dqk, cfg->drot, cfg->rope_style, cfg->rope_base,
-                        (double)(lo + j), kr + j * dqk);
+            if (cfg->k_rotated)
+                memcpy(kr + j * dqk, tmp, (size_t)dqk * sizeof(double));
+            else
+                oracle_rope(tmp, dqk, cfg->drot, cfg->rope_style, cfg->rope_base,
+                            (double)(lo + j), kr + j * dqk);
         }
         free(tmp);
     }
@@ -361,13 +377,11 @@ int oracle_prefill_backward(const void *q, const void *k, const void *v, const f
     int err = 0;
 #pragma omp parallel num_threads(nthreads)
     {
-        const int64_t maxl = 1 << 20;
         double *qr = (double *)malloc((size_t)dqk * sizeof(double));
         double *tmp = (double *)malloc((size_t)dqk * sizeof(double));
         double *dqr = (double *)malloc((size_t)dqk * sizeof(double));
         double *o = (double *)malloc((size_t)dv * sizeof(double));
         double *dO = (double *)malloc((size_t)dv * sizeof(double));
-        (void)maxl;
         if (!qr || !tmp || !dqr || !o || !dO) {
 #pragma omp atomic write
             err = 1;

@@ -428,3 +428,44 @@ def test_split_merge_counts_sink_once(oracle_mod):
                 o = sum(math.exp(m - M) * O for m, _, O in parts) / Ls
                 np.testing.assert_allclose(o, ref_o[0, t, h], rtol=0, atol=1e-12)
                 assert abs(M + math.log(Ls) - ref_l[0, t, h]) < 1e-12
+
+
+# --------------------------- rotated-cache decode (a cache holding rotated keys)
+@pytest.mark.parametrize("style", [0, 1])
+def test_rope_rows_matches_complex_form(oracle_mod, style):
+    """The oracle's row-wise rotation (used to build rotated caches) against the
+    complex-number form, one position per row."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((50, 3, 192))
+    pos = rng.integers(0, 262144, size=50).astype(np.float64)
+    y = oracle_mod.rope_rows(x, pos[:, None], base=5e6, rope_style=style)
+    np.testing.assert_allclose(y, rope_complex(x, pos, 5e6, 64, style), rtol=0, atol=1e-9)
+
+
+@pytest.mark.parametrize("window,style", [(0, 0), (3, 0), (128, 1)])
+def test_decode_rotated_cache_equals_raw_cache(oracle_mod, window, style):
+    """A cache that stores every key already rotated at its own position (rotated
+    here by the complex-number form, independently of the oracle), decoded with
+    k_rotated, gives the decode of the raw cache: the rotation of a key depends
+    on its position only, so doing it when the key is stored or when it is read
+    is the same arithmetic."""
+    gen = torch.Generator().manual_seed(23)
+    B, T, S_cap, Hq, Hkv, base = 3, 4, 300, 8, 2, 1e4
+    seqlens = [4, 170, 300]
+    kc = to64(bf16_tensor((B, S_cap, Hkv, 192), gen))
+    vc = to64(bf16_tensor((B, S_cap, Hkv, 128), gen))
+    qd = to64(bf16_tensor((B, T, Hq, 192), gen))
+    sink = torch.randn(Hq, generator=gen)
+    sl = torch.tensor(seqlens, dtype=torch.int32)
+    pos = np.arange(S_cap, dtype=np.float64)
+    kr = np.stack([rope_complex(kc[b], pos, base, 64, style) for b in range(B)])
+    o0, l0 = oracle_mod.decode(qd, kc, vc, sl, sink, window=window, rope_base=base,
+                               rope_style=style)
+    o1, l1 = oracle_mod.decode(qd, kr, vc, sl, sink, window=window, rope_base=base,
+                               rope_style=style, k_rotated=True)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l0, rtol=0, atol=1e-12)
+    # without the switch the keys would be rotated twice: a different result
+    o2, _ = oracle_mod.decode(qd, kr, vc, sl, sink, window=window, rope_base=base,
+                              rope_style=style)
+    assert np.abs(o2 - o0).max() > 1e-3
