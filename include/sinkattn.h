@@ -28,6 +28,15 @@
  *   - Keys are passed UNROTATED; the kernels rotate q and k on chip.  RoPE pairs
  *     dims (2t, 2t+1) for t < 32 with angle pos * base^(-2t/64) (RoFormer), unless
  *     a params struct selects pairs (t, t+32).
+ *   - Input range of the rotated dims.  The forward kernels keep dims 0..63 of
+ *     q and k, after the rotation, as fp16 (11 significant bits instead of
+ *     bf16's 8).  A rotation keeps the length of each pair, so every rotated
+ *     pair (x, y) of q and k must have sqrt(x^2 + y^2) <= 65504 (guaranteed when
+ *     |x|, |y| <= 46000); a longer pair overflows to inf and its rows come out
+ *     NaN, with no status.  Values below 2^-14 (about 6.1e-5) are kept as fp16
+ *     subnormals, with an absolute step of 2^-24 (about 6e-8).  The FP8-cache
+ *     decode also rounds dims 64..191 of q to fp16 (|q| <= 65504 there).  The
+ *     backward pass keeps bf16 copies and has no such limit.
  *   - lse is the natural-log log-sum-exp of the row INCLUDING the sink:
  *     lse_i = ln(exp(sink_h) + sum_{j visible} exp(a_ij)).
  *   - out is bf16 (round to nearest even of the fp32 result), lse fp32.
@@ -70,6 +79,11 @@ typedef struct {
     int32_t kv_ring;    /* decode only (prefill rejects it): 1 -> kcache/vcache are rings of
                            S_cap slots holding the latest keys, position j at slot j % S_cap
                            (the KV cache of a sliding-window layer keeps only its window) */
+    int32_t k_rotated;  /* decode only (prefill and backward reject it): 1 -> kcache holds
+                           every key already rotated at its own absolute position (a
+                           serving cache that stores keys after RoPE), so the decode
+                           rotates only q.  With a bf16 cache the rotated dims of q are
+                           then kept in bf16 (the cache's type) instead of fp16 */
 } sinkattn_params;
 
 /*
@@ -265,7 +279,8 @@ const char *sinkattn_status_string(sinkattn_status status);
  */
 sinkattn_status sinkattn_get_device_status(uint32_t *detail);
 
-/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH.  0.2.0 added
+ * sinkattn_params.k_rotated (the struct grew by one int32). */
 int32_t sinkattn_version(void);
 
 #ifdef __cplusplus

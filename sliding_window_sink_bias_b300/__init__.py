@@ -40,9 +40,10 @@ class SinkAttnError(RuntimeError):
 
 
 class Params(ctypes.Structure):
-    """sinkattn_params: scale (0 = 1/sqrt(192)), rope_off, rope_style."""
+    """sinkattn_params: scale (0 = 1/sqrt(192)), rope_off, rope_style, kv_ring, k_rotated."""
     _fields_ = [("scale", ctypes.c_float), ("rope_off", ctypes.c_int32),
-                ("rope_style", ctypes.c_int32), ("kv_ring", ctypes.c_int32)]
+                ("rope_style", ctypes.c_int32), ("kv_ring", ctypes.c_int32),
+                ("k_rotated", ctypes.c_int32)]
 
 
 _lib = None
@@ -102,10 +103,11 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _params(scale, rope_style, rope_off, kv_ring=False):
-    if scale is None and rope_style == 0 and not rope_off and not kv_ring:
+def _params(scale, rope_style, rope_off, kv_ring=False, k_rotated=False):
+    if scale is None and rope_style == 0 and not rope_off and not kv_ring and not k_rotated:
         return None
-    return Params(float(scale or 0.0), int(bool(rope_off)), int(rope_style), int(bool(kv_ring)))
+    return Params(float(scale or 0.0), int(bool(rope_off)), int(rope_style), int(bool(kv_ring)),
+                  int(bool(k_rotated)))
 
 
 def _require(t, name, dtype, ndim):
@@ -229,12 +231,13 @@ def prefill_backward(q, k, v, sink, cu_seqlens, out, lse, dout, *, max_seqlen: i
 
 def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, rope_base: float,
            workspace=None, out=None, lse=None, scale=None, rope_style: int = 0,
-           rope_off: bool = False, kv_ring: bool = False, stream=None):
+           rope_off: bool = False, kv_ring: bool = False, k_rotated: bool = False, stream=None):
     """MTP-verify decode.  q [B, T, Hq, 192]; kcache [B, S_cap, Hkv, 192];
     vcache [B, S_cap, Hkv, 128] bf16; seqlens int32 [B] (cached tokens including
     the T new ones); sink fp32 [Hq].  Returns (out [B, T, Hq, 128], lse [B, T, Hq]).
     kv_ring=True: the caches are rings of S_cap slots, position j at slot
-    j % S_cap (sliding-window layers; seqlens may exceed S_cap)."""
+    j % S_cap (sliding-window layers; seqlens may exceed S_cap).
+    k_rotated=True: kcache holds keys already rotated at their positions."""
     _require(q, "q", torch.bfloat16, 4)
     _require(kcache, "kcache", torch.bfloat16, 4)
     _require(vcache, "vcache", torch.bfloat16, 4)
@@ -250,7 +253,7 @@ def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, ro
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     out, lse = _outputs(out, lse, (b, t, hq, 128), (b, t, hq), q.device)
-    p = _params(scale, rope_style, rope_off, kv_ring)
+    p = _params(scale, rope_style, rope_off, kv_ring, k_rotated)
     args = (_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(sink), int(window),
             float(rope_base), b, t, s_cap, int(max_seqlen), hq, hkv)
     tail = (_ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
@@ -265,11 +268,12 @@ def decode(q, kcache, vcache, seqlens, sink, *, max_seqlen: int, window: int, ro
 
 def decode_fp8(q, kcache, vcache, k_scale, v_scale, seqlens, sink, *, max_seqlen: int,
                window: int, rope_base: float, workspace=None, out=None, lse=None, scale=None,
-               rope_style: int = 0, rope_off: bool = False, stream=None):
+               rope_style: int = 0, rope_off: bool = False, k_rotated: bool = False,
+               stream=None):
     """MTP-verify decode over an FP8 (E4M3) cache: kcache [B, S_cap, Hkv, 192] and
     vcache [B, S_cap, Hkv, 128] as torch.float8_e4m3fn (or uint8 bit patterns),
     k_scale / v_scale fp32 [Hkv] (key = e4m3 * k_scale[kv head]).  Other arguments
-    and the results as decode()."""
+    and the results as decode() (k_rotated: the E4M3 keys are already rotated)."""
     _require(q, "q", torch.bfloat16, 4)
     for name, t in (("kcache", kcache), ("vcache", vcache)):
         if not isinstance(t, torch.Tensor) or t.dtype not in (torch.float8_e4m3fn, torch.uint8):
@@ -291,7 +295,7 @@ def decode_fp8(q, kcache, vcache, k_scale, v_scale, seqlens, sink, *, max_seqlen
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     out, lse = _outputs(out, lse, (b, t, hq, 128), (b, t, hq), q.device)
-    p = _params(scale, rope_style, rope_off)
+    p = _params(scale, rope_style, rope_off, k_rotated=k_rotated)
     st = lib().sinkattn_decode_fp8(
         _ptr(q), kcache.data_ptr(), vcache.data_ptr(), _ptr(k_scale), _ptr(v_scale),
         _ptr(seqlens), _ptr(sink), int(window), float(rope_base), b, t, s_cap, int(max_seqlen),

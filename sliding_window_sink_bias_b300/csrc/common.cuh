@@ -92,8 +92,17 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 // The rotated dims 0..63 are written back as fp16, not bf16: the 64-dim part of
 // q.k then runs as its own fp16 x fp16 MMA k-steps (fp32 accumulate), and the
-// rotation's re-rounding error drops 8-fold (11 vs 8 significant bits).
+// rotation's re-rounding error drops 8-fold (11 vs 8 significant bits).  The
+// one exception is a query tile multiplied with keys a cache already holds
+// rotated in bf16 (the two operands of one MMA share a type): kBf16 = true.
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack_rot(float lo, float hi) {
+  if constexpr (kBf16) return pack_bf16x2(lo, hi);
+  else return pack_f16x2(lo, hi);
+}
+
 // Rotate the four (2t, 2t+1) pairs stored in one 16-byte chunk (pairs 4c..4c+3).
+template <bool kBf16 = false>
 __device__ __forceinline__ void rot_chunk_interleaved(uint4 *p, const float (&cs)[4],
                                                       const float (&sn)[4]) {
   uint4 v = *p;
@@ -101,13 +110,14 @@ __device__ __forceinline__ void rot_chunk_interleaved(uint4 *p, const float (&cs
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float x = bf16lo(w[e]), y = bf16hi(w[e]);
-    w[e] = pack_f16x2(x * cs[e] - y * sn[e], x * sn[e] + y * cs[e]);
+    w[e] = pack_rot<kBf16>(x * cs[e] - y * sn[e], x * sn[e] + y * cs[e]);
   }
   *p = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Rotate the eight (t, t+32) pairs held by chunk c (dims 8c..8c+7) and chunk
 // c+4 (dims 32+8c..32+8c+7).
+template <bool kBf16 = false>
 __device__ __forceinline__ void rot_chunks_half(uint4 *pa, uint4 *pb, const float (&cs)[8],
                                                 const float (&sn)[8]) {
   uint4 va = *pa, vb = *pb;
@@ -118,8 +128,8 @@ __device__ __forceinline__ void rot_chunks_half(uint4 *pa, uint4 *pb, const floa
     const float x0 = bf16lo(a[e]), y0 = bf16lo(b[e]);
     const float x1 = bf16hi(a[e]), y1 = bf16hi(b[e]);
     const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
-    a[e] = pack_f16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
-    b[e] = pack_f16x2(x0 * s0 + y0 * c0, x1 * s1 + y1 * c1);
+    a[e] = pack_rot<kBf16>(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
+    b[e] = pack_rot<kBf16>(x0 * s0 + y0 * c0, x1 * s1 + y1 * c1);
   }
   *pa = make_uint4(a[0], a[1], a[2], a[3]);
   *pb = make_uint4(b[0], b[1], b[2], b[3]);
@@ -133,6 +143,8 @@ __device__ __forceinline__ uint4 *swz_chunk(uint8_t *box, int32_t r, int32_t c) 
 // RoPE on dims 0..63 (box 0) of a Q tile of packed rows r = t * G + g: the
 // n_tok tokens at positions pos0 + t share their angles, so each (token, chunk)
 // unit computes its angles once and rotates all G heads.  128 threads.
+// kBf16: store the rotated dims as bf16 instead of fp16.
+template <bool kBf16 = false>
 __device__ void rope_q_tile(uint8_t *box0, int32_t G, int32_t n_tok, int32_t pos0,
                             int32_t rope_style, const unsigned long long *turns, int32_t tid) {
   if (n_tok <= 0) return;
@@ -149,14 +161,15 @@ __device__ void rope_q_tile(uint8_t *box0, int32_t G, int32_t n_tok, int32_t pos
       float cs[4], sn[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) rope_cs(pos, turns[4 * c + e], cs[e], sn[e]);
-      for (int32_t g = g0; g < g1; ++g) rot_chunk_interleaved(swz_chunk(box0, t * G + g, c), cs, sn);
+      for (int32_t g = g0; g < g1; ++g)
+        rot_chunk_interleaved<kBf16>(swz_chunk(box0, t * G + g, c), cs, sn);
     } else {
       float cs[8], sn[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) rope_cs(pos, turns[8 * c + e], cs[e], sn[e]);
       for (int32_t g = g0; g < g1; ++g) {
         const int32_t r = t * G + g;
-        rot_chunks_half(swz_chunk(box0, r, c), swz_chunk(box0, r, c + 4), cs, sn);
+        rot_chunks_half<kBf16>(swz_chunk(box0, r, c), swz_chunk(box0, r, c + 4), cs, sn);
       }
     }
   }

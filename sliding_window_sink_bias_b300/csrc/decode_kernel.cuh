@@ -55,6 +55,7 @@ struct DecArgs {
   // is u = k * n_sub + s; CTA c works on list c % n_sub.
   int32_t n_sub, n_k;
   int32_t kv_ring;        // 1: the cache is a ring of S_cap slots, position j at slot j % S_cap
+  int32_t k_rotated;      // 1: the cached keys are already rotated at their positions
   int32_t rope_on, rope_style;
   const float *k_scale, *v_scale;  // FP8 cache: per-KV-head dequantisation scales
   uint32_t q_tx_bytes;
@@ -490,7 +491,9 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      const uint32_t rot = args.rope_on ? 0u : 1u;  // rotated dims are fp16
+      // dims 0..63 of Q and K are fp16 once rotated here; keys a bf16 cache
+      // already holds rotated stay bf16, and Q's rotated dims are bf16 to match
+      const uint32_t rot = (args.rope_on && !args.k_rotated) ? 0u : 1u;
       // FP8 cache: every operand (Q, the converted K and V, P) is fp16
       const uint32_t kIdQK = idesc_f32acc(128, BN, F8 ? 0 : 1, 0, 0);
       const uint32_t kIdQKRot = idesc_f32acc(128, BN, F8 ? 0 : rot, 0, 0);
@@ -742,8 +745,12 @@ __global__ void __launch_bounds__(512, 1)
     DecSeg sg;
     while (ok && dec_next(c, args, sg)) {
       if (!(ok = wait_bar_warp(B_QFULL, gq & 1, abort_flag, 10))) break;
-      if (args.rope_on && tid < 128)
-        rope_q_tile(smem + Ly::kQOff, G, args.T, sg.L - args.T, args.rope_style, turns, tid);
+      if (args.rope_on && tid < 128) {
+        if (!F8 && args.k_rotated)
+          rope_q_tile<true>(smem + Ly::kQOff, G, args.T, sg.L - args.T, args.rope_style, turns, tid);
+        else
+          rope_q_tile(smem + Ly::kQOff, G, args.T, sg.L - args.T, args.rope_style, turns, tid);
+      }
       if constexpr (F8) {
         // every MMA operand is fp16 with an FP8 cache (the rotation above
         // already wrote box 0 as fp16; the conversion touches the other boxes)
@@ -765,7 +772,8 @@ __global__ void __launch_bounds__(512, 1)
           const int32_t kp = kpos0 + j * BN;
           const int32_t r0 = min(BN, max(0, vis_lo - kp)), r1 = max(r0, min(BN, sg.L - kp));
           dec_convert_fp8(smem + Ly::kStgOff + s8 * Ly::kStg, smem + Ly::kKVOff + st * Ly::kKVStage, kp,
-                          r0, r1, args.rope_on, args.rope_style, turns, tid, DecThreads<F8>::kConv);
+                          r0, r1, args.rope_on && !args.k_rotated, args.rope_style, turns, tid,
+                          DecThreads<F8>::kConv);
           fence_proxy_async_smem();
           mbar_arrive(B_STGEMPTY(s8));
           mbar_arrive(B_KREADY(st));
@@ -775,7 +783,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!(ok = wait_bar_warp(B_KVFULL(st), (gk / S) & 1, abort_flag, 11))) break;
         uint8_t *kv = smem + Ly::kKVOff + st * Ly::kKVStage;
         const int32_t kp = kpos0 + j * BN;
-        if (args.rope_on) rope_k_rows(kv, BN, kp, args.rope_style, turns, tid);
+        if (args.rope_on && !args.k_rotated) rope_k_rows(kv, BN, kp, args.rope_style, turns, tid);
         // Their scores are masked, but P = 0 times a NaN value is NaN: zero
         // the value rows of keys outside [vis_lo, L), whose cache rows (past
         // the sequence, or old ring slots) may hold anything.

@@ -22,7 +22,7 @@ namespace {
 using sa::AttnArgs;
 using sa::Layout;
 
-constexpr int32_t kVersion = 100;  // 0.1.0
+constexpr int32_t kVersion = 200;  // 0.2.0: sinkattn_params gained k_rotated
 constexpr int32_t kBNWide = 144;   // one key block covers a 128-key window + 16-token tile
 constexpr int32_t kBN = 128;
 constexpr uint32_t kQBoxBytesHost = 128 * 128;  // one 64-dim box of a 128-row Q tile
@@ -267,7 +267,7 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
   const int32_t G = num_q_heads / num_kv_heads;
   if (!pow2_upto_128(G) || G > 64) return SINKATTN_EUNSUPPORTED;
   if (num_q_heads > 65535 || num_kv_heads > 65535) return SINKATTN_EUNSUPPORTED;
-  if (params && params->kv_ring) return SINKATTN_EINVAL;
+  if (params && (params->kv_ring || params->k_rotated)) return SINKATTN_EINVAL;
   if (total > 0 && max_seqlen == 0) return SINKATTN_EINVAL;
   AttnArgs a;
   if (sinkattn_status st = fill_common(a, params, rope_base, num_q_heads, num_kv_heads, window))
@@ -414,7 +414,8 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
       !aligned(lse, 4) || !aligned(sink, 4) || !aligned(cu_seqlens, 4))
     return SINKATTN_EINVAL;
   AttnArgs a;
-  if (params && params->kv_ring) return SINKATTN_EINVAL;  // a prefill reads no cache
+  // a prefill reads no cache: neither a ring nor pre-rotated keys
+  if (params && (params->kv_ring || params->k_rotated)) return SINKATTN_EINVAL;
   if (sinkattn_status st = fill_common(a, params, rope_base, num_q_heads, num_kv_heads, window))
     return st;
 
@@ -507,7 +508,9 @@ static sinkattn_status decode_impl(const void *q, const void *kcache, const void
   const bool fp8 = k_scale != nullptr;
   if (batch < 0 || T <= 0 || S_cap <= 0 || max_seqlen < 0 || window < 0) return SINKATTN_EINVAL;
   const bool ring = params && params->kv_ring;
+  const bool k_rotated = params && params->k_rotated;
   if (params && params->kv_ring != 0 && params->kv_ring != 1) return SINKATTN_EINVAL;
+  if (params && params->k_rotated != 0 && params->k_rotated != 1) return SINKATTN_EINVAL;
   if (ring) {
     // the visible positions [L - T - W + 1, L) must sit in distinct slots, read
     // in 16-key pieces that never straddle the ring's end
@@ -548,6 +551,7 @@ static sinkattn_status decode_impl(const void *q, const void *kcache, const void
   d.S_cap = S_cap;
   d.n_units = batch * num_kv_heads;
   d.kv_ring = ring ? 1 : 0;
+  d.k_rotated = k_rotated ? 1 : 0;
   d.k_scale = k_scale;
   d.v_scale = v_scale;
   d.rope_on = a.rope_on;

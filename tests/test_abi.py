@@ -229,3 +229,26 @@ def test_backward_argument_checks(L):
     assert bwd(q_off=8) == sa.EINVAL                 # q not 16-byte aligned
     assert bwd(ws=None) == sa.EWORKSPACE
     assert bwd(ws_bytes=ws_ok - 1) == sa.EWORKSPACE
+
+
+def test_rotated_cache_argument_checks(L):
+    """params k_rotated (a cache of keys already rotated at their positions) is a
+    decode-only option taking 0 or 1; the prefill and the backward take raw keys
+    and refuse it.  All refused on the host, before any launch."""
+    import sliding_window_sink_bias_b300 as sa
+    P = ctypes.c_void_p
+    f = lambda x: P(256 * x)
+    ws = L.sinkattn_decode_workspace_size(2, 4, 64, 4, 100, 0)
+    p = sa.Params(0.0, 0, 0, 0, 2)
+    assert L.sinkattn_decode_ex(f(1), f(1), f(1), f(1), f(1), 0, 5e6, 2, 4, 100, 100, 64, 4,
+                                ctypes.byref(p), f(1), ws, f(1), f(1), None) == sa.EINVAL
+    assert L.sinkattn_decode_fp8(f(1), f(1), f(1), f(1), f(1), f(1), f(1), 0, 5e6, 2, 4, 256,
+                                 100, 64, 4, ctypes.byref(p), f(1), ws, f(1), f(1),
+                                 None) == sa.EINVAL
+    p = sa.Params(0.0, 0, 0, 0, 1)
+    assert L.sinkattn_prefill_ex(f(1), f(1), f(1), f(1), f(1), 1, 16, 16, 64, 8, 128, 1e4,
+                                 ctypes.byref(p), f(1), f(1), None) == sa.EINVAL
+    wsb = L.sinkattn_prefill_backward_workspace_size(16, 64, 8)
+    assert L.sinkattn_prefill_backward(
+        f(1), f(1), f(1), f(1), f(1), 1, 16, 16, 64, 8, 128, 1e4, ctypes.byref(p), f(1), f(1),
+        f(1), f(1), wsb, f(1), f(1), f(1), f(1), None) == sa.EINVAL

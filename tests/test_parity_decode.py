@@ -179,3 +179,57 @@ def test_ring_cache_matches_full_cache(oracle_mod, cap, window, t):
     ro, rl = oracle_mod.decode(full.q, full.kcache, full.vcache, full.seqlens, full.sink,
                                window=window, rope_base=1e4)
     assert_parity(out, lse, ro, rl, f"ring cap={cap} W={window} T={t}")
+
+
+# ------------------------------------------------ cache of keys already rotated
+def rotated_cache(oracle_mod, kcache, base, rope_style=0):
+    """The cache a serving layer would keep if it stored keys after RoPE: every
+    key rotated at its own position (slot j = position j) by the oracle's fp64
+    rotation, then rounded to bf16."""
+    pos = np.arange(kcache.shape[1], dtype=np.float64)[None, :, None]
+    kr = oracle_mod.rope_rows(kcache.to(torch.float64).numpy(), pos, base=base,
+                              rope_style=rope_style)
+    return torch.from_numpy(kr).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("window,hkv,base,style", [(0, 4, 5e6, 0), (128, 8, 1e4, 0),
+                                                   (0, 4, 1e4, 1)])
+def test_rotated_cache(oracle_mod, window, hkv, base, style):
+    """k_rotated: the kernel reads keys a cache already holds rotated (in bf16)
+    and rotates only q; compared with the oracle on that same rotated cache."""
+    import sliding_window_sink_bias_b300 as sa
+    seqlens = [4, 5, 63, 64, 65, 1000, 2999, 3000, 131]
+    inp = synth.decode_inputs(seqlens, 4, 3000, 64, hkv, window=window, rope_base=base, seed=31,
+                              device="cpu")
+    kc = rotated_cache(oracle_mod, inp.kcache, base, style)
+    _nan_past_end(kc, seqlens)
+    out, lse = sa.decode(inp.q.to(DEV), kc.to(DEV), inp.vcache.to(DEV), inp.seqlens.to(DEV),
+                         inp.sink.to(DEV), max_seqlen=max(seqlens), window=window,
+                         rope_base=base, rope_style=style, k_rotated=True)
+    torch.cuda.synchronize()
+    assert sa.device_status()[0] == sa.OK
+    ro, rl = oracle_mod.decode(inp.q, kc, inp.vcache, inp.seqlens, inp.sink, window=window,
+                               rope_base=base, rope_style=style, k_rotated=True)
+    assert_parity(out, lse, ro, rl, f"rotated cache W={window} style={style}")
+
+
+@pytest.mark.parametrize("cap,t", [(144, 4), (32, 1)])
+def test_rotated_ring_cache(oracle_mod, cap, t):
+    """A ring cache of keys rotated at their absolute positions (slot j % cap
+    holds position j, rotated at j)."""
+    import sliding_window_sink_bias_b300 as sa
+    window = 128 if cap >= 131 else 16
+    seqlens = [t, 100, cap - 1, cap, cap + 1, 1000, 4099 + t]
+    full = synth.decode_inputs(seqlens, t, max(seqlens), 64, 8, window=window, rope_base=1e4,
+                               seed=33 + t, device="cpu")
+    kfull = rotated_cache(oracle_mod, full.kcache, 1e4)
+    keep = window + t - 1
+    kr, vr = _ring_of(kfull, seqlens, cap, keep), _ring_of(full.vcache, seqlens, cap, keep)
+    out, lse = sa.decode(full.q.to(DEV), kr.to(DEV), vr.to(DEV), full.seqlens.to(DEV),
+                         full.sink.to(DEV), max_seqlen=max(seqlens), window=window,
+                         rope_base=1e4, kv_ring=True, k_rotated=True)
+    torch.cuda.synchronize()
+    assert sa.device_status()[0] == sa.OK
+    ro, rl = oracle_mod.decode(full.q, kfull, full.vcache, full.seqlens, full.sink,
+                               window=window, rope_base=1e4, k_rotated=True)
+    assert_parity(out, lse, ro, rl, f"rotated ring cap={cap} T={t}")

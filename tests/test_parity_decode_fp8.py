@@ -70,3 +70,30 @@ def test_fp8_half_split_rope_and_tokens(oracle_mod):
 def test_fp8_long_cache_many_splits(oracle_mod):
     o, l, ro, rl = _run(oracle_mod, [20000, 9000], 4, 20000, 4, 0, 5e6, seed=24)
     assert_parity(o, l, ro, rl, "fp8 long cache")
+
+
+@pytest.mark.parametrize("window,hkv,base", [(0, 4, 5e6), (128, 8, 1e4)])
+def test_fp8_rotated_cache(oracle_mod, window, hkv, base):
+    """An E4M3 cache of keys already rotated at their positions (rotated in fp64
+    by the oracle, then quantised): the kernel converts them without rotating;
+    the oracle decodes the exactly dequantised cache with k_rotated."""
+    import numpy as np
+
+    import sliding_window_sink_bias_b300 as sa
+    seqlens = [4, 64, 65, 1000, 2999, 3000, 131]
+    inp = synth.decode_inputs(seqlens, 4, 3000, 64, hkv, window=window, rope_base=base, seed=25,
+                              device="cpu")
+    pos = np.arange(3000, dtype=np.float64)[None, :, None]
+    krot = torch.from_numpy(oracle_mod.rope_rows(inp.kcache.to(torch.float64).numpy(), pos,
+                                                 base=base))
+    k8, ks = _quantize(krot, 25)
+    v8, vs = _quantize(inp.vcache, 26)
+    out, lse = sa.decode_fp8(inp.q.to(DEV), k8.to(DEV), v8.to(DEV), ks.to(DEV), vs.to(DEV),
+                             inp.seqlens.to(DEV), inp.sink.to(DEV), max_seqlen=max(seqlens),
+                             window=window, rope_base=base, k_rotated=True)
+    torch.cuda.synchronize()
+    assert sa.device_status()[0] == sa.OK
+    ro, rl = oracle_mod.decode(inp.q.to(torch.float64), _dequant(k8, ks), _dequant(v8, vs),
+                               inp.seqlens, inp.sink, window=window, rope_base=base,
+                               k_rotated=True)
+    assert_parity(out, lse, ro, rl, f"fp8 rotated cache W={window}")
