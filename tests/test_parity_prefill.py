@@ -161,3 +161,42 @@ def test_ga_prefill_long_sampled(oracle_mod):
     tok = torch.as_tensor(rows // 64).to(DEV)
     hd = torch.as_tensor(rows % 64).to(DEV)
     assert_parity(out[tok, hd], lse[tok, hd], ro, rl, "ga long")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("layer", ["swa", "ga"])
+def test_hybrid_block_ragged_sampled(oracle_mod, layer):
+    """The ragged hybrid block at full size (8 sequences of log-uniform lengths in
+    [4096, 131072], seed 0, packed through cu_seqlens): one SWA layer (64/8, W=128,
+    base 1e4) and the GA layer (64/4, global, base 5e6), each with its own sink,
+    the inputs and sinks the benchmark draws.  Every sequence is sampled: its
+    first and last rows, rows 127 and 128 (the window's edge), and 16 more, all
+    64 heads.  This reaches the band kernel's ring refill at every sequence
+    boundary and the causal kernel's longest-first schedule across sequences."""
+    import sliding_window_sink_bias_b300 as sa
+    wl = synth.WORKLOADS["hybrid_block_ragged_8seq"]
+    lens = synth.log_uniform_lengths(wl["n_seq"], wl["len_lo"], wl["len_hi"], seed=0)
+    hq = wl["hq"]
+    if layer == "swa":
+        hkv, window, base, seed, sink_seed = wl["swa_hkv"], wl["window"], wl["swa_base"], 0, 10
+    else:
+        hkv, window, base, seed, sink_seed = wl["ga_hkv"], 0, wl["ga_base"], 1, 10 + wl["swa_layers"]
+    inp = synth.prefill_inputs(lens, hq, hkv, window=window, rope_base=base, seed=seed,
+                               device=DEV)
+    sink = synth.sink_vector(hq, seed=sink_seed, device=DEV)
+    out, lse = sa.prefill(inp.q, inp.k, inp.v, sink, inp.cu_seqlens, max_seqlen=max(lens),
+                          window=window, rope_base=base)
+    torch.cuda.synchronize()
+    assert sa.device_status()[0] == sa.OK
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    for b, L in enumerate(lens):
+        s0 = int(cu[b])
+        toks, rows = sample_rows(L, hq, 20, seed=30 + b, must=(0, 127, 128, L - 1))
+        hi = int(toks.max()) + 1  # keys past the last sampled row are never seen
+        sl = slice(s0, s0 + hi)
+        ro, rl = oracle_mod.prefill(inp.q[sl].cpu(), inp.k[sl].cpu(), inp.v[sl].cpu(),
+                                    sink.cpu(), np.array([0, hi], dtype=np.int32),
+                                    window=window, rope_base=base, rows=rows)
+        tok = (torch.as_tensor(rows // hq) + s0).to(DEV)
+        hd = torch.as_tensor(rows % hq).to(DEV)
+        assert_parity(out[tok, hd], lse[tok, hd], ro, rl, f"hybrid {layer} seq {b} (L={L})")
