@@ -93,8 +93,9 @@ def load_peaks():
 
 class ClockSampler:
     """Samples the SM clock and the clock-event (throttle) reasons of this
-    process's GPU while the timed region runs: through NVML every 5 ms when the
-    pynvml module imports, else through `nvidia-smi -lms 50` in a subprocess."""
+    process's GPU while the timed region runs: through NVML every 5 ms (pynvml,
+    or the driver's NVML library by ctypes), else through `nvidia-smi -lms 50`
+    in a subprocess."""
 
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
                0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
@@ -113,28 +114,69 @@ class ClockSampler:
         p = torch.cuda.get_device_properties(self.cuda_index)
         return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
 
+    def _nvml(self):
+        """(get_clock, get_reasons, max_clock) through pynvml if it imports, else
+        through the driver's libnvidia-ml.so.1 by ctypes (same NVML calls)."""
+        import torch
+        uuid = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            try:
+                h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            except Exception:
+                h = pynvml.nvmlDeviceGetHandleByPciBusId(self._bus_id())
+            return (lambda: pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM),
+                    lambda: pynvml.nvmlDeviceGetCurrentClocksEventReasons(h),
+                    pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM), "nvml")
+        except ImportError:
+            pass
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0 and \
+                nv.nvmlDeviceGetHandleByPciBusId_v2(self._bus_id().encode(), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle for this GPU")
+        sm = 1  # NVML_CLOCK_SM
+        mx = ctypes.c_uint(0)
+        nv.nvmlDeviceGetMaxClockInfo(h, sm, ctypes.byref(mx))
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+
+        def clock():
+            v = ctypes.c_uint(0)
+            if nv.nvmlDeviceGetClockInfo(h, sm, ctypes.byref(v)) != 0:
+                raise RuntimeError("nvmlDeviceGetClockInfo failed")
+            return v.value
+
+        def reasons():
+            v = ctypes.c_ulonglong(0)
+            if reasons_fn(h, ctypes.byref(v)) != 0:
+                raise RuntimeError("clock event reasons query failed")
+            return v.value
+
+        return clock, reasons, mx.value, "nvml-ctypes"
+
     def _start_nvml(self):
         import threading
-
-        import pynvml
-        pynvml.nvmlInit()
-        h = pynvml.nvmlDeviceGetHandleByPciBusId(self._bus_id().encode())
-        self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+        clock, reasons, self.max_mhz, source = self._nvml()
+        clock(), reasons()  # fail here, not in the sampling thread
         self._stop = threading.Event()
 
         def loop():
             while not self._stop.is_set():
                 try:
-                    mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
-                    rs = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-                    self.samples.append((mhz, rs))
+                    self.samples.append((clock(), reasons()))
                 except Exception as e:
                     self.error = f"{type(e).__name__}: {e}"
                 time.sleep(0.005)
 
         self._t = threading.Thread(target=loop, daemon=True)
         self._t.start()
-        self.source = "nvml"
+        self.source = source
 
     def _start_smi(self):
         import subprocess
@@ -193,8 +235,11 @@ class ClockSampler:
         mhz = [s[0] for s in self.samples]
         reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items()
                           if r & bit})
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(mhz), "source": self.source}
+        out = {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+               "reasons": reasons, "samples": len(mhz), "source": self.source}
+        if self.source == "nvidia-smi" and self.error:
+            out["nvml_error"] = self.error[:200]
+        return out
 
 
 # ------------------------------------------------------------------ workloads
@@ -502,9 +547,12 @@ def bench_decode(name, steps, warmup, ws, local):
     torch.cuda.synchronize()
     barrier(ws)
     stream = torch.cuda.current_stream()
-    # every step is enqueued without waiting for the previous one (the flush
-    # kernel keeps the GPU busy while the host prepares the next call)
+    # every step is enqueued without waiting for the previous one; a GPU sleep
+    # ahead of the first step (outside the timed steps) lets the host enqueue
+    # all of them before the GPU reaches them, so the host's per-call latency
+    # never shows in a step's events
     with ClockSampler(local) as clk:
+        torch.cuda._sleep(int(2e6) * max(20, steps))  # about 1 ms per step at 2 GHz
         evs = []
         for _ in range(steps):
             flush.zero_()
@@ -554,6 +602,18 @@ def oracle_sample_prefill(wl, n_tokens, seed=0):
     return dt, pairs * wl["hq"] * FLOP_PER_PAIR_HEAD, oracle.max_threads()
 
 
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
 def cpu_baseline(target_s=12.0):
     from sliding_window_sink_bias_b300 import synth
     wl = synth.WORKLOADS[MAIN]
@@ -561,6 +621,7 @@ def cpu_baseline(target_s=12.0):
     n = int(min(32768, max(256, 256 * target_s / max(dt, 1e-3))))
     dt, fl, thr = oracle_sample_prefill(wl, n)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"first {n} tokens of sequence 0 of {MAIN}, all 64 heads "
                       f"({fl / 1e9:.1f} GFLOP, {dt:.1f} s)"}
 
@@ -591,6 +652,7 @@ def run_reference(args):
         "config": {"workload": MAIN, "sample_tokens_per_step": n, "window": 128,
                    "heads": "64q/8kv", "head_dims": "192/128"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"first {n} tokens of sequence 0 of {MAIN}, all 64 heads, "
                                    "per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -672,6 +734,39 @@ def traffic_for(key, tokens):
 def roofline_obj(bound, achieved, peak, unit, traffic=None):
     return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak if peak else None, "traffic": traffic}
+
+
+def _r(x, n=4):
+    return None if x is None else round(float(x), n)
+
+
+def summary_of(line):
+    """One compact entry per workload (time per step, value, roofline fraction,
+    median SM clock), placed last on the line so that a reader keeping only the
+    end of the output still has every workload's numbers."""
+    def entry(ms, value, unit, roof, clocks):
+        e = {"ms": _r(ms, 4), "value": _r(value, 1), "unit": unit}
+        if roof:
+            e["frac"] = _r(roof.get("frac"), 4)
+            e["bound"] = roof.get("bound")
+        if clocks:
+            e["sm_mhz"] = clocks.get("sm_mhz")
+            e["clk_samples"] = clocks.get("samples")
+        return e
+    out = {line["config"]["workload"]: entry(line["ms_per_step"], line["value"], line["unit"],
+                                             line.get("roofline"), line.get("clocks"))}
+    for name, w in line.get("other_workloads", {}).items():
+        if name == "hybrid_vs_all_ga":
+            out[name] = {f"{r['seq_len']}": _r(r["block_ratio"], 3) for r in w["rows"]}
+            continue
+        e = entry(w.get("ms_per_step"), w.get("value"), w.get("unit"), w.get("roofline"),
+                  w.get("clocks"))
+        if "per_layer" in w:
+            pl = w["per_layer"]
+            e["swa_frac_hbm"] = _r(pl["swa_frac_hbm"])
+            e["ga_frac_tensor"] = _r(pl["ga_frac_tensor"])
+        out[name] = e
+    return out
 
 
 def main():
@@ -757,6 +852,7 @@ def main():
         line["other_workloads"] = extra
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+    line["summary"] = summary_of(line)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
