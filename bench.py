@@ -531,7 +531,7 @@ def bench_decode(name, steps, warmup, ws, local):
         if fp8:
             sa.decode_fp8(inp.q, k8, v8, ks, vs, inp.seqlens, inp.sink, max_seqlen=max(lens),
                           window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
-                          lse=lse)
+                          lse=lse, k_rotated=wl.get("k_rotated", False))
         else:
             sa.decode(inp.q, inp.kcache, inp.vcache, inp.seqlens, inp.sink, max_seqlen=max(lens),
                       window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
@@ -818,7 +818,8 @@ def main():
             "frac_of_sustained_peak": (g_tf / peaks["bf16_tflops_sustained"]
                                        if peaks.get("bf16_tflops_sustained") else None),
             "clocks": g["clocks"]}
-        for name in ("mtp_decode_ga_b64_t4", "mtp_decode_ga_fp8_b64_t4", "mtp_decode_swa_b64_t4",
+        for name in ("mtp_decode_ga_b64_t4", "mtp_decode_ga_fp8_b64_t4",
+                     "mtp_decode_ga_fp8_rot_b64_t4", "mtp_decode_swa_b64_t4",
                      "mtp_decode_swa_ring_b64_t4"):
             d = bench_decode(name, args.steps, args.warmup, ws, local)
             d_gbs = d["bytes"] / (d["ms"] / 1e3) / 1e9

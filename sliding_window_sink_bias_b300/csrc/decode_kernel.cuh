@@ -21,11 +21,13 @@
 //
 // Warp roles (384 threads, one CTA per SM):
 //   warp 0       TMA producer: Q tile once per chunk, K/V blocks.
-//   warp 1       MMA issuer: S = Q K^T (12 k-steps), then O += P V.
-//   warp 2       TMEM allocator (S0, S1, O: 256 columns).
+//   warp 1       MMA issuer: S = Q K^T (12 k-steps, Q from TMEM), then O += P V.
+//   warp 2       TMEM allocator (S0, S1, O, Q: 512 columns).
 //   warp 3       set-up: this CTA's block range and first unit (CTA 0 also writes
 //                the per-unit block offsets the combine step reads).
-//   warps 4-7    online softmax, one row per thread: the block's masked max
+//   warps 4-7    at the start of a unit, its Q tile from shared memory into
+//                TMEM (one row per thread); then the online softmax, one row
+//                per thread: the block's masked max
 //                (3-input max), lazy running max (moves only when a block
 //                exceeds it by more than 2^8), P = 2^(s * scale * log2e - m) as
 //                bf16 pairs into TMEM, l, and the rescale of this row's O when
@@ -39,8 +41,12 @@ namespace sa {
 
 constexpr int32_t kDecBN = 64;      // keys per block
 constexpr int32_t kDecStages = 4;   // K/V blocks in flight
-constexpr uint32_t kDecTmemCols = 256;
+constexpr uint32_t kDecTmemCols = 512;
 constexpr uint32_t kDecTmemO = 128;
+// The unit's query tile (128 rows x 192 dims, 16-bit pairs): QK^T reads its A
+// operand from TMEM, so the tile is not re-read from shared memory for every
+// cache block (with N = 64 keys, 48 KB of Q against 24 KB of K per block).
+constexpr uint32_t kDecTmemQ = 256;
 constexpr int32_t kDecMaxGrid = 160;  // CTAs at most (2 partial slots each)
 
 struct DecArgs {
@@ -208,8 +214,8 @@ struct DecLayoutT {
   static constexpr uint32_t kStgOff = kKVOff + S * kKVStage;
   static constexpr uint32_t kBarOff = kStgOff + S8 * kStg;
   // q_full q_ready q_empty | kv_full[S] k_ready[S] kv_empty[S] | s_full[2] p_full[2] pv_done
-  // o_empty drain | stg_full[S8] stg_empty[S8]
-  static constexpr uint32_t kNumBars = 3 + 3 * S + 7 + 2 * S8;
+  // o_empty drain | stg_full[S8] stg_empty[S8] | q_tmem
+  static constexpr uint32_t kNumBars = 3 + 3 * S + 7 + 2 * S8 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag, cursor
   static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;  // + cursor[4]
   static constexpr uint32_t kBytes = kTurnsOff + 32 * 8;
@@ -311,6 +317,107 @@ __device__ void dec_convert_fp8(const uint8_t *stg, uint8_t *kv, int32_t kp, int
   }
 }
 
+// The raw E4M3 block of a staging slot, held in registers between the two
+// halves of the conversion: 64 keys x (192 + 128) bytes = 1280 16-byte units,
+// kFp8Per per thread for NTHR threads.  Unit order: K dims 0..63 (box 0, the
+// rotated ones) first, then K dims 64..191, then V, so that each of a thread's
+// units is of one kind across the whole warp.
+constexpr int32_t kFp8UnitsK0 = kDecBN * 4;    // K dims 0..63: 4 units of 16 a row
+constexpr int32_t kFp8UnitsK = kDecBN * 12;    // all of K
+constexpr int32_t kFp8Units = kDecBN * 20;     // K and V
+template <int32_t NTHR>
+struct Fp8Regs {
+  static constexpr int32_t kPer = kFp8Units / NTHR;
+  static_assert(kFp8Units % NTHR == 0 && kFp8UnitsK0 % NTHR == 0 && kFp8UnitsK % NTHR == 0,
+                "each unit index of a thread has one kind");
+  uint4 raw[kPer];
+};
+
+// Row, first dim and staging offset of unit u.
+__device__ __forceinline__ void fp8_unit(int32_t u, int32_t &r, int32_t &c16, uint32_t &off) {
+  constexpr uint32_t kK8 = kDecBN * kDqk;
+  if (u < kFp8UnitsK0) {
+    r = u >> 2;
+    c16 = u & 3;
+    off = r * kDqk + c16 * 16;
+  } else if (u < kFp8UnitsK) {
+    const int32_t v = u - kFp8UnitsK0;
+    r = v >> 3;
+    c16 = 4 + (v & 7);
+    off = r * kDqk + c16 * 16;
+  } else {
+    const int32_t v = u - kFp8UnitsK;
+    r = v >> 3;
+    c16 = v & 7;
+    off = kK8 + r * kDv + c16 * 16;
+  }
+}
+
+// First half: the staging slot's bytes into registers (all loads in flight
+// together).  The slot may be refilled as soon as this returns.
+template <int32_t NTHR>
+__device__ __forceinline__ void fp8_load(const uint8_t *stg, Fp8Regs<NTHR> &x, int32_t tid) {
+#pragma unroll
+  for (int32_t i = 0; i < Fp8Regs<NTHR>::kPer; ++i) {
+    int32_t r, c16;
+    uint32_t off;
+    fp8_unit(tid + i * NTHR, r, c16, off);
+    x.raw[i] = *reinterpret_cast<const uint4 *>(stg + off);
+  }
+}
+
+// Second half: convert to fp16 (exact) into the stage the MMA reads, in the
+// layout the TMA gives a bf16 block (K in 3 boxes, V in 2, 128-byte rows,
+// 128-byte swizzle); with rotate, K dims 0..63 are rotated at positions kp + row
+// (pairs (2t, 2t+1)); V rows outside [r0, r1) (keys no query sees) become zeros.
+template <int32_t NTHR>
+__device__ __forceinline__ void fp8_store(uint8_t *kv, const Fp8Regs<NTHR> &x, int32_t kp, int32_t r0,
+                                          int32_t r1, bool rotate, const unsigned long long *turns,
+                                          int32_t tid) {
+  constexpr uint32_t kBox = kDecBN * kRowBytes;
+#pragma unroll
+  for (int32_t i = 0; i < Fp8Regs<NTHR>::kPer; ++i) {
+    const int32_t u = tid + i * NTHR;
+    int32_t r, c16;
+    uint32_t off;
+    fp8_unit(u, r, c16, off);
+    const uint4 v = x.raw[i];
+    uint4 lo = e4m3x8_to_f16(make_uint2(v.x, v.y));
+    uint4 hi = e4m3x8_to_f16(make_uint2(v.z, v.w));
+    int32_t bi;  // box index in the stage
+    if (i * NTHR < kFp8UnitsK) {
+      bi = c16 >> 2;
+      if (i * NTHR < kFp8UnitsK0 && rotate) {
+        // pairs 8 c16 .. 8 c16 + 7, one per 32-bit word
+        uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int32_t e = 0; e < 8; ++e) {
+          float cs, sn;
+          rope_cs(kp + r, turns[8 * c16 + e], cs, sn);
+          const float a = f16lo(w[e]), b = f16hi(w[e]);
+          w[e] = pack_f16x2(a * cs - b * sn, a * sn + b * cs);
+        }
+        lo = make_uint4(w[0], w[1], w[2], w[3]);
+        hi = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    } else {
+      bi = 3 + (c16 >> 2);
+      if (r < r0 || r >= r1) lo = hi = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // The eight threads of a quarter warp store one row into two boxes (K dims
+    // 64..191, V) or two rows into one box (K dims 0..63).  Boxes are 8 KB apart
+    // and so share banks: threads of an odd box store their two 16-byte halves
+    // in the other order, so one store instruction writes the even chunks of one
+    // box and the odd chunks of the other (rows next to each other already
+    // differ in their swizzle parity).
+    uint8_t *box = kv + bi * kBox;
+    const int32_t ch = (c16 & 3) * 2;
+    const bool swap = bi & 1;
+    *swz_chunk(box, r, ch + (swap ? 1 : 0)) = swap ? hi : lo;
+    *swz_chunk(box, r, ch + (swap ? 0 : 1)) = swap ? lo : hi;
+  }
+}
+
 // The Q tile's rows [0, R) to fp16 in place: boxes 1 and 2, and box 0 unless
 // the RoPE pass has already written it as fp16.  nthr threads.
 __device__ void dec_q_to_f16(uint8_t *q, int32_t R, bool box0, int32_t tid, int32_t nthr) {
@@ -362,6 +469,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t B_DRAIN = bar(3 + 3 * S + 6);
   auto B_STGFULL = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + s8); };
   auto B_STGEMPTY = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + S8 + s8); };
+  const uint32_t B_QTMEM = bar(3 + 3 * S + 7 + 2 * S8);
 
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
@@ -372,7 +480,8 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 0) {
     mbar_init(B_QFULL, 1);
     mbar_init(B_QREADY, DecThreads<F8>::kConv);
-    mbar_init(B_QEMPTY, 1);
+    mbar_init(B_QEMPTY, 128);  // the softmax threads, once Q is in TMEM
+    mbar_init(B_QTMEM, 128);
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(B_KVFULL(s), 1);
       mbar_init(B_KREADY(s), DecThreads<F8>::kConv);
@@ -499,7 +608,6 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t kIdQKRot = idesc_f32acc(128, BN, F8 ? 0 : rot, 0, 0);
       constexpr uint32_t kIdPV = idesc_f32acc(128, kDv, F8 ? 0 : 1, 0, 1);
       constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
-      const uint32_t q_lo = ((sbase + Ly::kQOff) >> 4) | (1u << 16);
       const uint32_t kv_lo = ((sbase + Ly::kKVOff) >> 4) | (1u << 16);
       // V is MN-major: LBO = one box (the two 64-column halves of dv)
       const uint32_t v_lo = ((sbase + Ly::kKVOff + 3 * Ly::kKBox) >> 4) | ((Ly::kKBox >> 4) << 16);
@@ -525,7 +633,7 @@ __global__ void __launch_bounds__(512, 1)
       DecCursor c = c0;
       DecSeg sg;
       while (ok && dec_next(c, args, sg)) {
-        if (!(ok = wait_bar(B_QREADY, gq & 1, abort_flag, 3))) break;
+        if (!(ok = wait_bar(B_QTMEM, gq & 1, abort_flag, 3))) break;
         tc_fence_after();
         for (int32_t j = 0; ok && j < sg.nblk; ++j) {
           const uint32_t st = (gk + j) % S;
@@ -538,13 +646,12 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int kstep = 0; kstep < kDqk / 16; ++kstep) {
             const uint32_t box = kstep >> 2, off = (kstep & 3) * 32;
-            mma_ss2(s_t, q_lo + ((box * kQBoxBytes + off) >> 4), kDescHi,
+            mma_ts2(s_t, tmem + kDecTmemQ + kstep * 8,
                     kv_lo + st * kStageLo + ((box * Ly::kKBox + off) >> 4), kDescHi,
                     box == 0 ? kIdQKRot : kIdQK, kstep > 0 ? 1u : 0u);
           }
           issued = true;
           mma_commit(B_SFULL((gs + j) & 1));
-          if (j == sg.nblk - 1) mma_commit(B_QEMPTY);
           if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
         }
         if (ok) ok = issue_pv(gs + sg.nblk - 1, (gk + sg.nblk - 1) % S, sg.nblk == 1);
@@ -565,11 +672,37 @@ __global__ void __launch_bounds__(512, 1)
     const bool warp_active = (warp & 3) * 32 < R;  // the warp holds at least one real row
     const int32_t t = row / G, g = row % G;
     const int32_t W = args.window;
-    uint32_t gs = 0, gpv = 0;
+    uint32_t gs = 0, gpv = 0, gq = 0;
     bool ok = true;
     DecCursor c = c0;
     DecSeg sg;
     while (ok && dec_next(c, args, sg)) {
+      // The unit's Q tile (rotated; fp16 with an FP8 cache) into TMEM, one row
+      // per thread, then the shared-memory tile back to the copy thread.  Every
+      // QK^T that read the previous unit's rows has completed: this thread
+      // waited for that unit's last PV, issued after them.
+      if (!(ok = wait_bar_warp(B_QREADY, gq & 1, abort_flag, 13))) break;
+      if (warp_active) {
+        uint8_t *qs = smem + Ly::kQOff;
+#pragma unroll 1
+        for (int32_t b = 0; b < 3; ++b) {
+          uint32_t w[32];
+#pragma unroll
+          for (int32_t ch = 0; ch < 8; ++ch) {
+            const uint4 v = *swz_chunk(qs + b * kQBoxBytes, row, ch);
+            w[4 * ch] = v.x;
+            w[4 * ch + 1] = v.y;
+            w[4 * ch + 2] = v.z;
+            w[4 * ch + 3] = v.w;
+          }
+          tmem_st32p(tmem + lane_off + kDecTmemQ + b * 32, w);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(B_QTMEM);
+      mbar_arrive(B_QEMPTY);
+      ++gq;
       // query t sits at position L - T + t and sees cache keys
       // [max(0, pos - W + 1), pos], here limited to this segment's keys
       const int32_t pos = sg.L - args.T + t;
@@ -767,15 +900,26 @@ __global__ void __launch_bounds__(512, 1)
         if constexpr (F8) {
           const uint32_t s8 = gk % S8;
           if (!(ok = wait_bar_warp(B_STGFULL(s8), (gk / S8) & 1, abort_flag, 11))) break;
-          // the fp16 stage is free once the PV that last read it completed
-          if (!(ok = wait_bar_warp(B_KVEMPTY(st), ((gk / S) & 1) ^ 1, abort_flag, 12))) break;
           const int32_t kp = kpos0 + j * BN;
           const int32_t r0 = min(BN, max(0, vis_lo - kp)), r1 = max(r0, min(BN, sg.L - kp));
-          dec_convert_fp8(smem + Ly::kStgOff + s8 * Ly::kStg, smem + Ly::kKVOff + st * Ly::kKVStage, kp,
-                          r0, r1, args.rope_on && !args.k_rotated, args.rope_style, turns, tid,
-                          DecThreads<F8>::kConv);
+          const bool rotate = args.rope_on && !args.k_rotated;
+          uint8_t *stage = smem + Ly::kKVOff + st * Ly::kKVStage;
+          if (!rotate || args.rope_style == 0) {
+            // the raw block into registers, the staging slot back to the TMA
+            // at once, then the wait for the fp16 stage
+            Fp8Regs<DecThreads<F8>::kConv> x;
+            fp8_load(smem + Ly::kStgOff + s8 * Ly::kStg, x, tid);
+            mbar_arrive(B_STGEMPTY(s8));
+            // the fp16 stage is free once the PV that last read it completed
+            if (!(ok = wait_bar_warp(B_KVEMPTY(st), ((gk / S) & 1) ^ 1, abort_flag, 12))) break;
+            fp8_store(stage, x, kp, r0, r1, rotate, turns, tid);
+          } else {
+            if (!(ok = wait_bar_warp(B_KVEMPTY(st), ((gk / S) & 1) ^ 1, abort_flag, 12))) break;
+            dec_convert_fp8(smem + Ly::kStgOff + s8 * Ly::kStg, stage, kp, r0, r1, true,
+                            args.rope_style, turns, tid, DecThreads<F8>::kConv);
+            mbar_arrive(B_STGEMPTY(s8));
+          }
           fence_proxy_async_smem();
-          mbar_arrive(B_STGEMPTY(s8));
           mbar_arrive(B_KREADY(st));
           ++gk;
           continue;

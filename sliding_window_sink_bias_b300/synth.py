@@ -134,6 +134,10 @@ WORKLOADS = {
     # the GA decode batch over an FP8 (E4M3) cache, one scale per KV head
     "mtp_decode_ga_fp8_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=262144, fp8=True,
                                      len_lo=65536, len_hi=262144, **GA),
+    # the same FP8 batch with the keys stored after RoPE (an FP8 cache is
+    # quantised when a key is stored, after its rotation): the kernel rotates q only
+    "mtp_decode_ga_fp8_rot_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=262144, fp8=True,
+                                         k_rotated=True, len_lo=65536, len_hi=262144, **GA),
     # the same SWA layer with the KV cache an SWA layer needs: a ring of 144
     # slots (>= W + T - 1 = 131, a multiple of 16) per sequence
     "mtp_decode_swa_ring_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=144, kv_ring=True,
@@ -160,6 +164,8 @@ WORKLOADS = {
                                 len_lo=65536, len_hi=131072, **GA),
     "mtp_decode_ga_fp8_b8_t4": dict(kind="decode", batch=8, t=4, s_cap=131072, fp8=True,
                                     len_lo=65536, len_hi=131072, **GA),
+    "mtp_decode_ga_fp8_rot_b8_t4": dict(kind="decode", batch=8, t=4, s_cap=131072, fp8=True,
+                                        k_rotated=True, len_lo=65536, len_hi=131072, **GA),
     "swa_backward_1x32768": dict(kind="backward", seqlens=[32768], **SWA),
     "ga_backward_1x8192": dict(kind="backward", seqlens=[8192], **GA),
 }

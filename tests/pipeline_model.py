@@ -350,7 +350,9 @@ def decode_roles(nblk, f8=False, skip=()):
     the MMA thread, the softmax rows and the RoPE / conversion warps.  bf16
     cache: four K/V stages the copies fill.  FP8 cache: two staging slots the
     copies fill and three fp16 stages the conversion warps fill.  QK^T(j) is
-    issued before PV(j-1), which waits for the softmax of block j-1."""
+    issued before PV(j-1), which waits for the softmax of block j-1.  The
+    softmax rows copy each unit's rotated Q tile from shared memory into TMEM
+    (QK^T reads it there) and then free the shared-memory tile."""
     segs = list(nblk)
     S = 3 if f8 else 4
     S8 = 2
@@ -358,7 +360,7 @@ def decode_roles(nblk, f8=False, skip=()):
     def producer():
         gk = 0
         for q, n in enumerate(segs):
-            yield ("wait", "QEMPTY", q)  # the previous segment's last QK^T read Q
+            yield ("wait", "QEMPTY", q)  # the rows copied the previous tile to TMEM
             yield ("tma", "Q", ("Qraw", q), "QFULL")
             for _ in range(n):
                 if f8:
@@ -387,14 +389,12 @@ def decode_roles(nblk, f8=False, skip=()):
             yield ("commit", "PVDONE")
 
         for q, n in enumerate(segs):
-            yield ("wait", "QREADY", q + 1)
+            yield ("wait", "QTMEM", q + 1)
             for j in range(n):
                 b = gk + j
                 yield ("wait", f"KREADY{b % S}", b // S + 1)
-                yield ("mma", [("Q", ("Q", q)), (f"K{b % S}", ("K", b))], [(f"P{b & 1}", ("S", b))])
+                yield ("mma", [("QT", ("Q", q)), (f"K{b % S}", ("K", b))], [(f"P{b & 1}", ("S", b))])
                 yield ("commit", f"SFULL{b & 1}")
-                if j == n - 1:
-                    yield ("commit", "QEMPTY")
                 if j > 0:
                     yield from issue_pv(q, j - 1, b - 1, j == 1)
             yield from issue_pv(q, n - 1, gk + n - 1, n == 1)
@@ -403,6 +403,12 @@ def decode_roles(nblk, f8=False, skip=()):
     def softmax():
         gs = 0
         for q, n in enumerate(segs):
+            if "softmax_qready" not in skip:
+                yield ("wait", "QREADY", q + 1)  # rotated (and converted) tile in place
+            yield ("read", "Q", ("Q", q))
+            yield ("write", "QT", ("Q", q))  # into TMEM
+            yield ("arrive", "QTMEM")
+            yield ("arrive", "QEMPTY")
             for j in range(n):
                 b = gs + j
                 yield ("wait", f"SFULL{b & 1}", (b >> 1) + 1)
@@ -429,14 +435,16 @@ def decode_roles(nblk, f8=False, skip=()):
             for _ in range(n):
                 st = gk % S
                 if f8:
+                    # the staging slot's bytes go to registers and the slot back
+                    # to the copies before the wait for the fp16 stage
                     s8 = gk % S8
                     yield ("wait", f"STGFULL{s8}", gk // S8 + 1)
+                    yield ("read", f"STG{s8}", ("stg", gk))
+                    yield ("arrive", f"STGEMPTY{s8}")
                     if "convert_kvempty" not in skip:
                         yield ("wait", f"KVEMPTY{st}", gk // S)  # PV(gk-S) read the stage
-                    yield ("read", f"STG{s8}", ("stg", gk))
                     yield ("write", f"K{st}", ("K", gk))
                     yield ("write", f"V{st}", ("V", gk))
-                    yield ("arrive", f"STGEMPTY{s8}")
                 else:
                     yield ("wait", f"KVFULL{st}", gk // S + 1)  # K and V copies landed
                     yield ("read", f"K{st}", ("Kraw", gk))

@@ -71,7 +71,8 @@ def test_decode_pipeline(f8, sizes):
 
 
 @pytest.mark.parametrize("f8,skip", [(False, "producer_kvempty"), (True, "convert_kvempty"),
-                                     (False, "softmax_pvdone"), (True, "softmax_pvdone")])
+                                     (False, "softmax_pvdone"), (True, "softmax_pvdone"),
+                                     (False, "softmax_qready"), (True, "softmax_qready")])
 def test_decode_missing_wait_is_caught(f8, skip):
     assert _caught(lambda s, sk: decode_roles(s, f8, sk), (skip,), (5, 3, 6))
 
