@@ -9,6 +9,9 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libsinkattn.so")
+# the same sources with -DSINKATTN_TEST_HOOKS: the library the timeout-path
+# test loads (it can stall one wait on purpose); the product never loads it
+TEST_LIB = os.path.join(HERE, "libsinkattn_test.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 NVCC_FLAGS = [
@@ -28,17 +31,25 @@ def deps():
         [os.path.join(ROOT, "include", "sinkattn.h")]
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ into one shared library (skipped when up to date)."""
-    if not force and os.path.exists(LIB):
-        t = os.path.getmtime(LIB)
+def _build_one(out: str, extra, force: bool, verbose: bool) -> None:
+    if not force and os.path.exists(out):
+        t = os.path.getmtime(out)
         if all(os.path.getmtime(d) <= t for d in deps()):
-            return LIB
-    cmd = [NVCC, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include")]
+            return
+    cmd = [NVCC, *NVCC_FLAGS, *extra, "-I", os.path.join(ROOT, "include")]
     if verbose:
         cmd += ["-Xptxas", "-v"]
-    cmd += ["-o", LIB, *sources()]
+    cmd += ["-o", out, *sources()]
     subprocess.run(cmd, check=True)
+
+
+def build(force: bool = False, verbose: bool = False, test_lib: bool = True) -> str:
+    """Compile every .cu under csrc/ into the shared library (and, unless told
+    not to, the test build of the same sources); each is skipped when up to
+    date.  Returns the product library's path."""
+    _build_one(LIB, [], force, verbose)
+    if test_lib:
+        _build_one(TEST_LIB, ["-DSINKATTN_TEST_HOOKS"], force, verbose)
     return LIB
 
 

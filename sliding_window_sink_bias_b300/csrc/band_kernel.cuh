@@ -555,6 +555,11 @@ __global__ void __launch_bounds__(kBandThreads, 1)
       const uint32_t rot = args.rope_on ? 0u : 1u;  // rotated dims are fp16
       uint32_t gt = 0, gseg = 0;
       bool ok = true;
+#ifdef SINKATTN_TEST_HOOKS
+      // B_DRAIN completes only after a commit issued when every MMA is out,
+      // which has not happened yet: this wait can only run out
+      if (g_test_stall_ns) ok = wait_bar_slow(B_DRAIN, 0, abort_flag, 0x7E, g_test_stall_ns);
+#endif
       // the previous tile, whose PV is issued after the next tile's QK^T
       int32_t p_nwin = 0;
       uint32_t p_slot = 0;

@@ -29,16 +29,19 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;        // 0.2 s to drain after 
 __device__ uint32_t g_status_word;
 
 // Bounded mbarrier wait, slow path: the timed loop.  Returns false if this CTA
-// is aborting.
+// is aborting (another wait gave up) or this wait runs past limit_ns, which
+// then records SINKATTN_ETIMEOUT and the site in the status word and sets the
+// CTA's abort flag.
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity,
-                                           volatile uint32_t *abort_flag, uint32_t site) {
+                                           volatile uint32_t *abort_flag, uint32_t site,
+                                           uint64_t limit_ns = kWaitLimitNs) {
   // each try_wait sleeps up to its suspend hint (1 ms), so checking the clock
   // and the abort flag once per round costs nothing
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
       atomicOr(&g_status_word, 1u | (site << 8));
       return false;
@@ -63,6 +66,14 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
   const bool ok = wait_bar(bar, parity, abort_flag, site);
   return __all_sync(0xffffffffu, ok);
 }
+
+#ifdef SINKATTN_TEST_HOOKS
+// Test builds only (never in the product library): when the host sets it, the
+// MMA thread of the next band-kernel launches first waits, for at most this
+// many nanoseconds, on a barrier that nothing can complete yet, so that the
+// timeout, abort and drain path runs without any fault.
+__device__ uint64_t g_test_stall_ns;
+#endif
 
 // Wait used only while draining: ignores the abort flag, short limit.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {

@@ -712,3 +712,10 @@ extern "C" sinkattn_status sinkattn_decode_noalloc(
                          max_seqlen, num_q_heads, num_kv_heads, scratch,
                          SINKATTN_NOALLOC_SCRATCH_BYTES, out, lse, stream);
 }
+
+#ifdef SINKATTN_TEST_HOOKS
+// Test builds only: see sa::g_test_stall_ns.  0 turns the stall off.
+extern "C" int sinkattn_test_set_stall_ns(uint64_t ns) {
+  return cudaMemcpyToSymbol(sa::g_test_stall_ns, &ns, sizeof ns) == cudaSuccess ? 0 : 1;
+}
+#endif

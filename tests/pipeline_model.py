@@ -25,6 +25,17 @@ order the kernel performs them:
                            hold `tag` (written and complete, not overwritten yet).
   ("write", res, tag)      a thread writes `res`.
   ("sync",)                the CTA barrier: every role must arrive.
+  ("await", bar, n)        a bounded wait (the kernels' wait_bar): like "wait",
+                           but once the CTA is aborting it may return False (the
+                           value the generator receives) instead of blocking.
+  ("drain", bar, n)        the wait of the drain after an abort: blocks until
+                           `bar` has completed n phases, whatever the abort flag.
+
+With `aborts=True` a blocked "await" may time out at any moment (rarely, at
+random): the CTA's abort flag is set, that await returns False, and so may
+every later await that is not already satisfied.  Roles then run their drain
+code.  When every role has finished, no copy may still be in flight and the
+tensor pipe must be empty: the kernel frees shared memory and TMEM there.
 
 A scheduler picks at random among the runnable roles, the copies in flight and
 the head of the tensor pipe, so one run is one interleaving; many runs with
@@ -39,10 +50,18 @@ class ModelError(AssertionError):
     pass
 
 
+# A roles factory that models its kernel's drain puts this key in its counts:
+# then, also without aborts, nothing may be in flight when every role is done.
+EXIT_CHECK = "__exit_check__"
+
+
 class Sim:
-    def __init__(self, roles, rng, counts=None):
+    def __init__(self, roles, rng, counts=None, aborts=False):
         self.rng = rng
+        self.aborts = aborts                  # random timeouts enabled
+        self.aborted = False                  # the CTA's abort flag
         self.counts = dict(counts or {})      # barrier -> arrivals per phase
+        self.exit_checked = aborts or bool(self.counts.pop(EXIT_CHECK, False))
         self.arrivals = {}
         self.roles = dict(roles)              # name -> generator
         self.pending = {n: None for n in self.roles}  # the op a role is blocked on
@@ -64,29 +83,37 @@ class Sim:
 
     def _check_waits(self):
         for name, op in self.pending.items():
-            if op is not None and op[0] == "wait":
+            if op is not None and op[0] in ("wait", "await", "drain"):
                 _, bar, n = op
                 c = self.phases.get(bar, 0)
                 if c > n or c < n - 1:
                     raise ModelError(f"{name}: waits for {n} phases of {bar}, which has "
                                      f"completed {c} (parity wait ambiguous)")
 
+    def _satisfied(self, op):
+        return self.phases.get(op[1], 0) >= op[2]
+
     def _runnable(self, name):
         op = self.pending[name]
         if op is None:
             return True
-        if op[0] == "wait":
-            return self.phases.get(op[1], 0) >= op[2]
+        if op[0] in ("wait", "drain"):
+            return self._satisfied(op)
+        if op[0] == "await":
+            return self._satisfied(op) or self.aborted
         if op[0] == "sync":
             return False
         return True
 
     def _step_role(self, name):
         op = self.pending[name]
+        result = None
         if op is not None:
             kind = op[0]
-            if kind == "wait":
+            if kind in ("wait", "drain"):
                 pass  # satisfied (checked by _runnable)
+            elif kind == "await":
+                result = self._satisfied(op)  # False: the CTA is aborting
             elif kind == "arrive":
                 self._arrive(op[1])
             elif kind == "tma":
@@ -104,7 +131,7 @@ class Sim:
             else:
                 raise ValueError(op)
         try:
-            self.pending[name] = next(self.roles[name])
+            self.pending[name] = self.roles[name].send(result)
         except StopIteration:
             self.pending[name] = None
             self.done.add(name)
@@ -118,6 +145,9 @@ class Sim:
         for _ in range(max_steps):
             self._check_waits()
             live = [n for n in self.roles if n not in self.done]
+            if not live and self.exit_checked and (self.tma or self.pipe):
+                raise ModelError(f"every role finished with copies {self.tma} or tensor-pipe "
+                                 f"work {self.pipe} still in flight")
             if not live and not self.tma and not self.pipe:
                 return
             # the CTA barrier releases once every live role has reached it
@@ -127,9 +157,22 @@ class Sim:
                     self.pending[n] = ("wait", "__none__", 0)  # released: no-op
                     self.phases.setdefault("__none__", 0)
             choices = [("role", n) for n in live if self._runnable(n)]
+            if self.aborts and not self.aborted and self.rng.random() < 0.01:
+                blocked = [n for n in live if self.pending[n] is not None
+                           and self.pending[n][0] == "await" and not self._satisfied(self.pending[n])]
+                if blocked:
+                    self.aborted = True  # a wait ran out: the CTA aborts
+                    choices = [("role", self.rng.choice(blocked))]
             choices += [("tma", i) for i in range(len(self.tma))]
             if self.pipe:
                 choices.append(("pipe", 0))
+            if not choices and self.aborts and not self.aborted:
+                # nothing can move: a bounded wait is the next thing to run out
+                blocked = [n for n in live if self.pending[n] is not None
+                           and self.pending[n][0] == "await"]
+                if blocked:
+                    self.aborted = True
+                    choices = [("role", self.rng.choice(blocked))]
             if not choices:
                 state = {n: self.pending[n] for n in live}
                 raise ModelError(f"deadlock: {state}")
@@ -339,9 +382,11 @@ def dkdv_roles(nsub, skip=()):
     return roles, {"PR": 2}
 
 
-def run(make_roles, sizes, seed, skip=()):
+def run(make_roles, sizes, seed, skip=(), aborts=False):
     roles, counts = make_roles(sizes, skip)
-    Sim(roles, random.Random(seed), counts).run()
+    sim = Sim(roles, random.Random(seed), counts, aborts=aborts)
+    sim.run()
+    return sim
 
 
 def decode_roles(nblk, f8=False, skip=()):
@@ -575,7 +620,7 @@ def causal_roles(nblk, skip=()):
     return roles, {}
 
 
-def band_roles(lanes, skip=(), nseg=9, R=12):
+def band_roles(lanes, skip=(), nseg=9, R=12, stall=False):
     """sinkattn_band_kernel (SWA prefill) for one CTA whose contiguous range of
     tiles crosses `lanes`: (first tile index, number of tiles) per (sequence,
     KV head) lane.  A tile of 16 tokens sees the nwin = min(i + 1, nseg)
@@ -585,7 +630,13 @@ def band_roles(lanes, skip=(), nseg=9, R=12):
     PV of the previous tile after this tile's QK^T (before it at a run start,
     which reloads the ring) and frees the segments leaving the window.  The two
     threads of a softmax row (modelled as two roles, one per half) swap partial
-    maxima and sums through shared memory, paired by a barrier per parity."""
+    maxima and sums through shared memory, paired by a barrier per parity.
+    Every wait is bounded ("await"): a role whose wait returns False (the CTA
+    is aborting) leaves its loop, and the copy and MMA threads then drain what
+    they issued (the last copy into each Q stage and segment slot; a commit
+    behind every MMA), as the kernel does before its final barrier.  With
+    `stall`, the MMA thread first waits on a barrier nothing completes (the
+    test build's stall), which can only end by running out."""
     tiles = []  # (tile index within its lane, run)
     for i0, n in lanes:
         for k in range(n):
@@ -595,29 +646,47 @@ def band_roles(lanes, skip=(), nseg=9, R=12):
         return min(i + 1, nseg)
 
     def producer():
-        gseg = 0
+        gq = gseg = 0
+        ok = True
         for t, (i, run) in enumerate(tiles):
             qs = t & 1
-            yield ("wait", f"QEMPTY{qs}", t >> 1)
+            ok = yield ("await", f"QEMPTY{qs}", t >> 1)
+            if not ok:
+                break
             yield ("tma", f"Q{qs}", ("Qraw", t), f"QFULL{qs}")
+            gq += 1
             for _ in range(nwin_of(i) if run else 1):
                 slot = gseg % R
                 if "producer_segempty" not in skip:
-                    yield ("wait", f"SEGEMPTY{slot}", gseg // R)
+                    ok = yield ("await", f"SEGEMPTY{slot}", gseg // R)
+                    if not ok:
+                        break
                 yield ("tma", f"SEG{slot}", ("Kraw", gseg), f"SEGFULL{slot}")
                 gseg += 1
+            if not ok:
+                break
+        # drain: the last copy into each stage and slot lands before the exit
+        if "producer_drain" not in skip:
+            for st in range(2):
+                if gq > st:
+                    yield ("drain", f"QFULL{st}", (gq - 1 - st) // 2 + 1)
+            for st in range(R):
+                if gseg > st:
+                    yield ("drain", f"SEGFULL{st}", (gseg - 1 - st) // R + 1)
 
     def rope():
         gseg = 0
         for t, (i, run) in enumerate(tiles):
             qs = t & 1
-            yield ("wait", f"QFULL{qs}", (t >> 1) + 1)
+            if not (yield ("await", f"QFULL{qs}", (t >> 1) + 1)):
+                return
             yield ("read", f"Q{qs}", ("Qraw", t))
             yield ("write", f"Q{qs}", ("Q", t))
             yield ("arrive", f"QREADY{qs}")
             for _ in range(nwin_of(i) if run else 1):
                 slot = gseg % R
-                yield ("wait", f"SEGFULL{slot}", gseg // R + 1)
+                if not (yield ("await", f"SEGFULL{slot}", gseg // R + 1)):
+                    return
                 yield ("read", f"SEG{slot}", ("Kraw", gseg))
                 yield ("write", f"SEG{slot}", ("KV", gseg))
                 yield ("arrive", f"SEGREADY{slot}")
@@ -626,42 +695,62 @@ def band_roles(lanes, skip=(), nseg=9, R=12):
     def mma():
         gseg = 0
         prev = None  # (tile, nwin, first segment) of the tile whose PV is pending
+        issued = False
 
         def issue_pv(t, nwin, seg0, nfree):
             b = t & 1
-            yield ("wait", f"PFULL{b}", (t >> 1) + 1)
+            if not (yield ("await", f"PFULL{b}", (t >> 1) + 1)):
+                return False
             if "mma_oempty" not in skip:
-                yield ("wait", "OEMPTY", t)
+                if not (yield ("await", "OEMPTY", t)):
+                    return False
             reads = [(f"S{b}h0", ("P", t)), (f"S{b}h1", ("P", t))]
             reads += [(f"SEG{(seg0 + k) % R}", ("KV", seg0 + k)) for k in range(nwin)]
             yield ("mma", reads, [("Oh0", ("O", t)), ("Oh1", ("O", t))])
             for k in range(nfree):
                 yield ("commit", f"SEGEMPTY{(seg0 + k) % R}")
             yield ("commit", "PVDONE")
+            return True
 
-        for t, (i, run) in enumerate(tiles):
+        ok = True
+        if stall:
+            ok = yield ("await", "STALL", 1)
+        for t, (i, run) in enumerate(tiles if ok else ()):
             nwin = nwin_of(i)
             nload = nwin if run else 1
             if prev is not None and run:
-                yield from issue_pv(*prev, prev[1])  # the reload needs the whole ring back
+                ok = yield from issue_pv(*prev, prev[1])  # the reload needs the whole ring back
+                if not ok:
+                    break
             qs = t & 1
-            yield ("wait", f"QREADY{qs}", (t >> 1) + 1)
+            ok = yield ("await", f"QREADY{qs}", (t >> 1) + 1)
             for j in range(nload):
+                if not ok:
+                    break
                 g = gseg + j
-                yield ("wait", f"SEGREADY{g % R}", g // R + 1)
+                ok = yield ("await", f"SEGREADY{g % R}", g // R + 1)
+            if not ok:
+                break
             gseg += nload
             seg0 = gseg - nwin
             b = t & 1
             reads = [(f"Q{qs}", ("Q", t))] + [(f"SEG{(seg0 + k) % R}", ("KV", seg0 + k))
                                               for k in range(nwin)]
             yield ("mma", reads, [(f"S{b}h0", ("S", t)), (f"S{b}h1", ("S", t))])
+            issued = True
             yield ("commit", f"SFULL{b}")
             yield ("commit", f"QEMPTY{qs}")
             if prev is not None and not run:
-                yield from issue_pv(*prev, 1 if nwin == prev[1] else 0)
+                ok = yield from issue_pv(*prev, 1 if nwin == prev[1] else 0)
+                if not ok:
+                    break
             prev = (t, nwin, seg0)
-        if prev is not None:
+        if ok and prev is not None:
             yield from issue_pv(*prev, prev[1])
+        # drain: every MMA done before TMEM goes back
+        if issued and "mma_drain" not in skip:
+            yield ("commit", "DRAIN")
+            yield ("drain", "DRAIN", 1)
 
     def softmax(h):
         def role():
@@ -669,24 +758,28 @@ def band_roles(lanes, skip=(), nseg=9, R=12):
                 have = step < len(tiles)
                 b = step & 1
                 if have:
-                    yield ("wait", f"SFULL{b}", (step >> 1) + 1)
+                    if not (yield ("await", f"SFULL{b}", (step >> 1) + 1)):
+                        return
                     yield ("read", f"S{b}h{h}", ("S", step))
                 par = step & 1  # swap with the other half of the row
                 yield ("write", f"X{par}h{h}", ("X", step))
                 yield ("arrive", f"PAIR{par}")
                 if "softmax_pair" not in skip:
-                    yield ("wait", f"PAIR{par}", (step >> 1) + 1)
+                    if not (yield ("await", f"PAIR{par}", (step >> 1) + 1)):
+                        return
                 yield ("read", f"X{par}h{1 - h}", ("X", step))
                 if have:
                     yield ("write", f"S{b}h{h}", ("P", step))  # P over this half's S columns
                     yield ("arrive", f"PFULL{b}")
                 if step > 0:
-                    yield ("wait", "PVDONE", step)
+                    if not (yield ("await", "PVDONE", step)):
+                        return
                     yield ("read", f"Oh{h}", ("O", step - 1))
                     yield ("arrive", "OEMPTY")
         return role()
 
     roles = {"producer": producer(), "rope": rope(), "mma": mma(), "half0": softmax(0),
              "half1": softmax(1)}
-    counts = {"PFULL0": 2, "PFULL1": 2, "OEMPTY": 2, "PAIR0": 2, "PAIR1": 2}
+    counts = {"PFULL0": 2, "PFULL1": 2, "OEMPTY": 2, "PAIR0": 2, "PAIR1": 2,
+              EXIT_CHECK: True}
     return roles, counts

@@ -113,3 +113,42 @@ def test_band_pipeline_smaller_rings(R):
                                     ("producer_segempty", 10)])
 def test_band_missing_wait_is_caught(skip, R):
     assert _caught(lambda s, sk: band_roles(s, sk, R=R), (skip,), [(3, 14), (0, 4)])
+
+
+# ------------------------------------------------ abort and drain (band kernel)
+@pytest.mark.parametrize("lanes", [[(0, 1)], [(0, 5)], [(3, 14), (0, 4)], [(0, 1), (0, 1), (2, 3)]])
+def test_band_abort_drains_everything(lanes):
+    """A bounded wait runs out at a random moment: the CTA's abort flag is set
+    and every later unsatisfied wait gives up.  No role may then wait forever,
+    no read may see the wrong data, and when every role is done no copy may
+    still be landing and no MMA still running (the kernel frees its shared
+    memory and TMEM there)."""
+    aborted = 0
+    for seed in range(300):
+        sim = run(band_roles, lanes, seed, aborts=True)
+        aborted += sim.aborted
+    assert aborted > 50  # most runs took the abort path somewhere
+
+
+@pytest.mark.parametrize("skip", ["producer_drain", "mma_drain"])
+def test_band_missing_drain_is_caught(skip):
+    """Leaving out the copy thread's or the MMA thread's drain lets the CTA
+    finish with work in flight: the model notices."""
+    caught = False
+    for seed in range(400):
+        try:
+            run(band_roles, [(3, 14), (0, 4)], seed, skip=(skip,), aborts=True)
+        except ModelError:
+            caught = True
+            break
+    assert caught
+
+
+@pytest.mark.parametrize("lanes", [[(0, 1)], [(0, 5)], [(3, 14), (0, 4)]])
+def test_band_stalled_mma_thread_drains(lanes):
+    """The test build's stall: the MMA thread's first wait can only run out.
+    The CTA must abort, every role must leave, and the copies already issued
+    must land before the exit, whatever the interleaving."""
+    for seed in range(200):
+        sim = run(lambda s, sk: band_roles(s, sk, stall=True), lanes, seed, aborts=True)
+        assert sim.aborted
