@@ -576,7 +576,7 @@ def bench_decode(name, steps, warmup, ws, local):
     pairs = synth.algorithmic_pairs_decode(lens, t, W)
     res = {"name": name, "ms": ms, "kv_bytes": kv_bytes, "bytes": kv_bytes + io_bytes,
            "flops": pairs * hq * FLOP_PER_PAIR_HEAD, "clocks": clk.summary(),
-           "launches": 2 * steps, "tokens": wl["batch"] * t, "vis_keys": sum(keys)}
+           "launches": steps, "tokens": wl["batch"] * t, "vis_keys": sum(keys)}
     del inp, work, out, lse, flush
     torch.cuda.empty_cache()
     return res

@@ -121,13 +121,15 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
 /*
  * Bytes of device workspace sinkattn_decode needs for these sizes.  The decode
  * cuts every unit's (sequence, KV head) visible keys into 64-key blocks and
- * splits the list of all blocks evenly over at most 160 CTAs; the workspace
- * holds the per-unit block offsets (batch * num_kv_heads + 1 int32, padded to
- * 256 bytes) and, per CTA, two partial slots of T * (num_q_heads / num_kv_heads)
- * rows x 132 fp32 for the units a CTA boundary cuts (their running max, sum and
- * unnormalised output; §2.3.1's multi-token verify split over the cache).  It
- * does not depend on the cache lengths or the window.  Returns 0 for arguments
- * sinkattn_decode would reject.
+ * splits the list of all blocks evenly over at most 160 CTAs, in one launch.
+ * A unit a CTA boundary cuts leaves, per CTA, its running max, sum and
+ * unnormalised output without the sink; the CTA that finishes the unit last
+ * (told by the unit's ticket) merges them and adds the sink once.  The
+ * workspace holds one 64-bit ticket per unit (batch * num_kv_heads, padded to
+ * 256 bytes) and, per CTA, two partial slots of T * (num_q_heads /
+ * num_kv_heads) rows x 132 fp32 (§2.3.1's multi-token verify split over the
+ * cache).  It does not depend on the cache lengths or the window.  Returns 0
+ * for arguments sinkattn_decode would reject.
  */
 size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_heads,
                                       int32_t num_kv_heads, int32_t max_seqlen, int32_t window);
@@ -149,7 +151,9 @@ size_t sinkattn_decode_workspace_size(int32_t batch, int32_t T, int32_t num_q_he
  *   T        1 <= T and T * (num_q_heads / num_kv_heads) <= 128.
  *   workspace, workspace_bytes  device scratch of at least
  *            sinkattn_decode_workspace_size(...) bytes, 256-byte aligned; it
- *            needs no clearing and its contents are rewritten by every call.
+ *            needs no clearing (each call's tickets carry a number of their
+ *            own) and its contents are rewritten by every call.  Calls that
+ *            share one workspace must not overlap on the GPU.
  *   The logit scale must be positive (sinkattn_decode_ex with a scale <= 0
  *   returns SINKATTN_EINVAL).
  *   Ring cache (sinkattn_decode_ex with params->kv_ring = 1; the KV cache of an

@@ -12,8 +12,9 @@
 // different times fetches those bursts twice).  A unit that lies entirely inside one CTA's range is finished there
 // (eqs. (1)-(3) of §2.2, the sink added once); a unit cut by a range boundary
 // leaves, per CTA, its running max m, the sum l of 2^(a - m) and the
-// unnormalised O = sum 2^(a - m) v without the sink, and
-// sinkattn_decode_combine_kernel merges those and adds the sink once.
+// unnormalised O = sum 2^(a - m) v without the sink; the CTA whose arrival
+// completes the unit's ticket (the last of its CTAs to finish it) merges the
+// partials in a fixed order and adds the sink once, in the same launch.
 //
 // The cache is streamed in 64-key blocks, four in flight (TMA into a shared
 // memory ring); S = Q K^T and O += P V run on tcgen05 with S, P and O in TMEM.
@@ -23,8 +24,8 @@
 //   warp 0       TMA producer: Q tile once per chunk, K/V blocks.
 //   warp 1       MMA issuer: S = Q K^T (12 k-steps, Q from TMEM), then O += P V.
 //   warp 2       TMEM allocator (S0, S1, O, Q: 512 columns).
-//   warp 3       set-up: this CTA's block range and first unit (CTA 0 also writes
-//                the per-unit block offsets the combine step reads).
+//   warp 3       set-up: this CTA's block range and first unit; the rows of
+//                its share of the units with no key at all.
 //   warps 4-7    at the start of a unit, its Q tile from shared memory into
 //                TMEM (one row per thread); then the online softmax, one row
 //                per thread: the block's masked max
@@ -70,7 +71,11 @@ struct DecArgs {
   const float *sink;
   __nv_bfloat16 *out;
   float *lse;
-  int32_t *unit_blk;      // [n_k + 1] block offsets of the units of a list (written by CTA 0)
+  // per-unit tickets of the units CTA ranges cut: (epoch << 16) | arrivals;
+  // epoch is this call's number (48 bits), so a word another call left behind
+  // just starts over and the workspace needs no clearing
+  unsigned long long *tickets;
+  unsigned long long epoch;
   float *part_o;          // [gridDim.x * 2, R, 128] unnormalised O
   float *part_ml;         // [gridDim.x * 2, R, 4] (m, l, 0, 0), log2 domain
   unsigned long long rope_turns[32];
@@ -130,17 +135,30 @@ __device__ __forceinline__ bool dec_next(DecCursor &c, const DecArgs &a, DecSeg 
   return false;
 }
 
-// Set-up (one warp): block offsets of the units of this CTA's list (a warp
+// Rows of unit u with no key at all (an empty cache): o = 0, lse = sink (the
+// empty sum of eqs. (2)-(3)).  One warp.
+__device__ void dec_write_empty_unit(const DecArgs &a, int32_t u, int32_t lane) {
+  const int32_t b = u / a.Hkv, kvh = u % a.Hkv;
+  for (int32_t r = 0; r < a.R; ++r) {
+    const int32_t head = kvh * a.G + r % a.G;
+    const size_t orow = (static_cast<size_t>(b) * a.T + r / a.G) * a.Hq + head;
+    reinterpret_cast<uint2 *>(a.out + orow * kDv)[lane] = make_uint2(0u, 0u);
+    if (lane == 0) a.lse[orow] = __ldg(a.sink + head);
+  }
+}
+
+// Set-up (one warp): the block counts of the units of this CTA's list (a warp
 // scan), this CTA's range [f0, f1) of the list's blocks (the list's G =
 // gridDim.x / n_sub CTAs split it evenly) and the unit/block it starts at.
-// Every list has the same block counts (a unit's keys depend on its sequence
-// only when n_sub = Hkv), so CTA 0 stores one offset table for the combine.
+// Units without keys are written here, unit k of the list by the list's CTA
+// k % G.  cur: first unit, its first block, blocks of the range, list, the
+// list's total blocks, f0.
 __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
   const int32_t sl = static_cast<int32_t>(blockIdx.x) % a.n_sub;
   const int32_t g = static_cast<int32_t>(blockIdx.x) / a.n_sub;
   const int32_t G = static_cast<int32_t>(gridDim.x) / a.n_sub;
   int64_t run = 0;
-  // pass 1: total blocks of the list (and, for CTA 0, the offset table)
+  // pass 1: total blocks of the list; this CTA's share of the empty units
   for (int32_t base = 0; base < a.n_k; base += 32) {
     const int32_t k = base + lane;
     int32_t nb = 0;
@@ -148,16 +166,20 @@ __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
       int32_t L, lo;
       dec_unit_keys(a, k * a.n_sub + sl, L, lo, nb);
     }
+    uint32_t empty = __ballot_sync(0xffffffffu, k < a.n_k && nb == 0 && k % G == g);
+    while (empty) {
+      const int32_t j = __ffs(empty) - 1;
+      empty &= empty - 1;
+      dec_write_empty_unit(a, (base + j) * a.n_sub + sl, lane);
+    }
     int32_t incl = nb;
 #pragma unroll
     for (int32_t o = 1; o < 32; o <<= 1) {
       const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    if (blockIdx.x == 0 && k < a.n_k) a.unit_blk[k] = static_cast<int32_t>(run + incl - nb);
     run += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (blockIdx.x == 0 && lane == 0) a.unit_blk[a.n_k] = static_cast<int32_t>(run);
   const int64_t T = run;
   const int64_t f0 = T * g / G;
   const int64_t f1 = T * (g + 1) / G;
@@ -194,7 +216,27 @@ __device__ void dec_locate(const DecArgs &a, int32_t lane, int32_t *cur) {
     cur[1] = sblk;
     cur[2] = found ? static_cast<int32_t>(f1 - f0) : 0;
     cur[3] = sl;
+    cur[4] = static_cast<int32_t>(T);
+    cur[5] = static_cast<int32_t>(f0);
   }
+}
+
+// One arrival on a cut unit's ticket for this call; true for the arrival that
+// completes n (this CTA is then the last to finish the unit).  A word left by
+// another call starts over at 1.  The compare-and-swap retries only when
+// another CTA of the unit arrived in between, so n - 1 retries at most; the
+// bound is a safeguard.
+__device__ __forceinline__ bool dec_ticket_arrive(unsigned long long *t, unsigned long long epoch,
+                                                  uint32_t n) {
+  unsigned long long cur = atomicAdd(t, 0ull);
+  for (int32_t i = 0; i < 1024; ++i) {
+    const unsigned long long want = (cur >> 16) == epoch ? cur + 1ull : (epoch << 16) | 1ull;
+    const unsigned long long prev = atomicCAS(t, cur, want);
+    if (prev == cur) return static_cast<uint32_t>(want & 0xFFFFull) == n;
+    cur = prev;
+  }
+  atomicOr(&g_status_word, 1u | (0xFDu << 8));
+  return false;
 }
 
 // Shared memory of the decode kernel.  bf16 cache: four K/V stages the TMA
@@ -214,10 +256,11 @@ struct DecLayoutT {
   static constexpr uint32_t kStgOff = kKVOff + S * kKVStage;
   static constexpr uint32_t kBarOff = kStgOff + S8 * kStg;
   // q_full q_ready q_empty | kv_full[S] k_ready[S] kv_empty[S] | s_full[2] p_full[2] pv_done
-  // o_empty drain | stg_full[S8] stg_empty[S8] | q_tmem
-  static constexpr uint32_t kNumBars = 3 + 3 * S + 7 + 2 * S8 + 1;
-  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag, cursor
-  static constexpr uint32_t kTurnsOff = (kMiscOff + 32 + 7) & ~7u;  // + cursor[4]
+  // o_empty drain | stg_full[S8] stg_empty[S8] | q_tmem part_out last_known
+  static constexpr uint32_t kNumBars = 3 + 3 * S + 7 + 2 * S8 + 3;
+  // tmem slot, abort flag, cursor[6], the "last to finish a cut unit" flag
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kTurnsOff = (kMiscOff + 40 + 7) & ~7u;
   static constexpr uint32_t kBytes = kTurnsOff + 32 * 8;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
@@ -441,7 +484,7 @@ struct DecThreads {
 };
 
 template <bool F8>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
     sinkattn_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
@@ -470,10 +513,14 @@ __global__ void __launch_bounds__(512, 1)
   auto B_STGFULL = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + s8); };
   auto B_STGEMPTY = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + S8 + s8); };
   const uint32_t B_QTMEM = bar(3 + 3 * S + 7 + 2 * S8);
+  // a cut unit's partial is out (128 softmax threads), the ticket's answer is known (1)
+  const uint32_t B_PARTOUT = bar(3 + 3 * S + 7 + 2 * S8 + 1);
+  const uint32_t B_LASTKNOWN = bar(3 + 3 * S + 7 + 2 * S8 + 2);
 
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
   int32_t *cur_smem = reinterpret_cast<int32_t *>(smem + Ly::kMiscOff + 8);
+  volatile int32_t *last_flag = reinterpret_cast<volatile int32_t *>(smem + Ly::kMiscOff + 32);
   unsigned long long *turns = reinterpret_cast<unsigned long long *>(smem + Ly::kTurnsOff);
 
   // ---------------------------------------------------------------- set-up
@@ -482,6 +529,8 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(B_QREADY, DecThreads<F8>::kConv);
     mbar_init(B_QEMPTY, 128);  // the softmax threads, once Q is in TMEM
     mbar_init(B_QTMEM, 128);
+    mbar_init(B_PARTOUT, 128);
+    mbar_init(B_LASTKNOWN, 1);
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(B_KVFULL(s), 1);
       mbar_init(B_KREADY(s), DecThreads<F8>::kConv);
@@ -672,11 +721,17 @@ __global__ void __launch_bounds__(512, 1)
     const bool warp_active = (warp & 3) * 32 < R;  // the warp holds at least one real row
     const int32_t t = row / G, g = row % G;
     const int32_t W = args.window;
-    uint32_t gs = 0, gpv = 0, gq = 0;
+    uint32_t gs = 0, gpv = 0, gq = 0, gcut = 0;
     bool ok = true;
     DecCursor c = c0;
     DecSeg sg;
+    // the list's CTAs, its total blocks, and the flat index of this CTA's next block
+    const int32_t n_grp = static_cast<int32_t>(gridDim.x) / args.n_sub;
+    const int64_t Tb = cur_smem[4];
+    int64_t flat = cur_smem[5];
     while (ok && dec_next(c, args, sg)) {
+      const int64_t F0 = flat - sg.blk0;  // the unit's blocks are [F0, F0 + nblk_u) of the list
+      flat += sg.nblk;
       // The unit's Q tile (rotated; fp16 with an FP8 cache) into TMEM, one row
       // per thread, then the shared-memory tile back to the copy thread.  Every
       // QK^T that read the previous unit's rows has completed: this thread
@@ -810,7 +865,7 @@ __global__ void __launch_bounds__(512, 1)
         const int32_t head = sg.kvh * G + g;
         // whole unit: eqs. (2)-(3) with the sink added once,
         //   M = max(m, sink), L = l 2^(m - M) + 2^(sink - M), o = O 2^(m - M) / L;
-        // else the unnormalised partial (m, l, O) for the combine step
+        // else the unnormalised partial (m, l, O) for the merge
         float scale_o = 1.f, lse_v = 0.f;
         if (whole_unit) {
           const float sk2 = __ldg(args.sink + head) * kLog2e;
@@ -827,7 +882,7 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         // FP8 cache: the values' scale multiplies O (partials included: the
-        // combine is linear in O)
+        // merge is linear in O)
         const float vs = F8 ? __ldg(args.v_scale + sg.kvh) : 1.f;
         scale_o *= vs;
         const size_t orow = (static_cast<size_t>(sg.b) * args.T + t) * args.Hq + head;
@@ -868,6 +923,89 @@ __global__ void __launch_bounds__(512, 1)
       }
       tc_fence_before();
       mbar_arrive(B_OEMPTY);
+      if (!whole_unit) {
+        // A cut unit: this CTA's partial is out; the CTA that completes the
+        // unit's ticket merges every partial of the unit (they are written
+        // before their CTA's arrival, which the fences order device-wide).
+        // Group i of the list holds blocks [Tb i / n_grp, Tb (i + 1) / n_grp).
+        const int64_t F1 = F0 + sg.nblk_u;
+        auto grp_of = [&](int64_t f) { return static_cast<int32_t>(((f + 1) * n_grp - 1) / Tb); };
+        auto has_part = [&](int32_t i) { return Tb * i / n_grp != Tb * (i + 1) / n_grp; };
+        const int32_t c_first = grp_of(F0), c_last = grp_of(F1 - 1);
+        uint32_t n_part = 0;
+        for (int32_t i = c_first; i <= c_last; ++i) n_part += has_part(i) ? 1u : 0u;
+        __threadfence();
+        mbar_arrive(B_PARTOUT);
+        if (threadIdx.x == 128) {
+          // (no early exit here: the whole warp meets again in the wait below;
+          // an aborted CTA merges nothing)
+          const bool all_out = wait_bar(B_PARTOUT, gcut & 1, abort_flag, 14);
+          *last_flag = all_out && dec_ticket_arrive(args.tickets + sg.u, args.epoch, n_part) ? 1 : 0;
+          mbar_arrive(B_LASTKNOWN);
+        }
+        if (!(ok = wait_bar_warp(B_LASTKNOWN, gcut & 1, abort_flag, 15))) break;
+        ++gcut;
+        if (*last_flag && warp_active && row < R) {
+          __threadfence();
+          // M = max(sink, m_i), L = 2^(sink - M) + sum_i l_i 2^(m_i - M),
+          // o = sum_i 2^(m_i - M) O_i / L, in group order (eq. (2) over the
+          // partition of the unit's keys, the sink once)
+          const int32_t sl = static_cast<int32_t>(blockIdx.x) % args.n_sub;
+          const int32_t head = sg.kvh * G + g;
+          const size_t orow = (static_cast<size_t>(sg.b) * args.T + t) * args.Hq + head;
+          const float4 *ml = reinterpret_cast<const float4 *>(args.part_ml);
+          auto prow_of = [&](int32_t i) {
+            const size_t cta = static_cast<size_t>(i) * args.n_sub + sl;
+            return (cta * 2 + ((i == c_first && Tb * i / n_grp < F0) ? 1 : 0)) * R + row;
+          };
+          const float sk_raw = __ldg(args.sink + head);
+          const float sk2 = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
+          float M = sk2;
+          for (int32_t i = c_first; i <= c_last; ++i)
+            if (has_part(i)) M = fmaxf(M, __ldcg(ml + prow_of(i)).x);
+          if (M == -INFINITY) {
+            uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv);
+            for (int32_t q4 = 0; q4 < kDv / 8; ++q4) dst[q4] = make_uint4(0u, 0u, 0u, 0u);
+            args.lse[orow] = -INFINITY;
+          } else {
+            float Ls = sk2 == -INFINITY ? 0.f : ex2(sk2 - M);
+            for (int32_t i = c_first; i <= c_last; ++i) {
+              if (!has_part(i)) continue;
+              const float4 v = __ldcg(ml + prow_of(i));
+              Ls += v.y * (v.x == -INFINITY ? 0.f : ex2(v.x - M));
+            }
+#pragma unroll 1
+            for (int32_t cb = 0; cb < kDv; cb += 32) {
+              float acc[32];
+#pragma unroll
+              for (int32_t e = 0; e < 32; ++e) acc[e] = 0.f;
+              for (int32_t i = c_first; i <= c_last; ++i) {
+                if (!has_part(i)) continue;
+                const size_t pr = prow_of(i);
+                const float4 v = __ldcg(ml + pr);
+                const float w = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+                const float4 *src = reinterpret_cast<const float4 *>(args.part_o + pr * kDv + cb);
+#pragma unroll
+                for (int32_t q4 = 0; q4 < 8; ++q4) {
+                  const float4 o4 = __ldcg(src + q4);
+                  acc[4 * q4] += w * o4.x;
+                  acc[4 * q4 + 1] += w * o4.y;
+                  acc[4 * q4 + 2] += w * o4.z;
+                  acc[4 * q4 + 3] += w * o4.w;
+                }
+              }
+              uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv + cb);
+#pragma unroll
+              for (int32_t q4 = 0; q4 < 4; ++q4)
+                dst[q4] = make_uint4(pack_bf16x2(acc[8 * q4] / Ls, acc[8 * q4 + 1] / Ls),
+                                     pack_bf16x2(acc[8 * q4 + 2] / Ls, acc[8 * q4 + 3] / Ls),
+                                     pack_bf16x2(acc[8 * q4 + 4] / Ls, acc[8 * q4 + 5] / Ls),
+                                     pack_bf16x2(acc[8 * q4 + 6] / Ls, acc[8 * q4 + 7] / Ls));
+            }
+            args.lse[orow] = (M + __log2f(Ls)) * kLn2;
+          }
+        }
+      }
     }
   } else if (warp >= 8) {
     // ============================================================ RoPE
@@ -953,77 +1091,6 @@ __global__ void __launch_bounds__(512, 1)
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kDecTmemCols);
-  }
-}
-
-// Combine step: for each output row of a unit that a CTA-range boundary cut,
-// merge the per-CTA partials (m_c, l_c, O_c), computed without the sink, and
-// add the sink exactly once (eq. (2) over a partition of the keys):
-//   M = max(sink, max_c m_c),  L = 2^(sink - M) + sum_c l_c 2^(m_c - M),
-//   o = sum_c 2^(m_c - M) O_c / L,  lse = (M + log2 L) ln 2   (log2 domain).
-// Units the decode kernel finished return at once; rows of units with no
-// visible key get o = 0 and lse = sink.  Grid (units, kCombParts), 512 threads:
-// thread (w, e) takes value dim e of rows part * 4 + w, + 16, + 32, ...; the
-// partials are visited in a fixed order.
-constexpr int32_t kCombParts = 4;
-constexpr int32_t kCombThreads = 512;
-
-__global__ void __launch_bounds__(kCombThreads)
-    sinkattn_decode_combine_kernel(const __grid_constant__ DecArgs a, int32_t grid) {
-  const int32_t u = blockIdx.x;
-  const int32_t k = u / a.n_sub, sl = u % a.n_sub;  // unit k of list sl
-  const int32_t G = grid / a.n_sub;                // CTAs of a list; CTA of group g: g * n_sub + sl
-  const int32_t F0 = a.unit_blk[k], F1 = a.unit_blk[k + 1];
-  const int64_t Tb = a.unit_blk[a.n_k];
-  auto grp_of = [&](int64_t f) { return static_cast<int32_t>(((f + 1) * G - 1) / Tb); };
-  const bool empty_unit = F1 == F0;
-  int32_t c_first = 0, c_last = 0;  // groups
-  if (!empty_unit) {
-    c_first = grp_of(F0);
-    c_last = grp_of(F1 - 1);
-    if (c_first == c_last) return;  // finished by the decode kernel
-  }
-  const int32_t b = u / a.Hkv, kvh = u % a.Hkv;
-  const int32_t e = threadIdx.x & (kDv - 1);
-  const float4 *ml = reinterpret_cast<const float4 *>(a.part_ml);
-  // groups whose range is empty (fewer blocks than CTAs) hold no partial
-  auto has_part = [&](int32_t c) { return Tb * c / G != Tb * (c + 1) / G; };
-  auto slot = [&](int32_t c, int32_t r) {
-    const int64_t bnd = Tb * c / G;  // first block of group c
-    const size_t cta = static_cast<size_t>(c) * a.n_sub + sl;
-    return (cta * 2 + ((c == c_first && bnd < F0) ? 1 : 0)) * a.R + r;
-  };
-  constexpr int32_t kStride = kCombParts * (kCombThreads / kDv);
-  for (int32_t r = blockIdx.y * (kCombThreads / kDv) + (threadIdx.x >> 7); r < a.R; r += kStride) {
-    const int32_t t = r / a.G, h = kvh * a.G + r % a.G;
-    const size_t rowid = (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
-    const float sk_raw = __ldg(a.sink + h);
-    const float sk = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
-    if (empty_unit) {  // no visible key at all: the empty sum
-      a.out[rowid * kDv + e] = __float2bfloat16_rn(0.f);
-      if (e == 0) a.lse[rowid] = sk_raw;
-      continue;
-    }
-    float M = sk;
-    for (int32_t c = c_first; c <= c_last; ++c)
-      if (has_part(c)) M = fmaxf(M, ml[slot(c, r)].x);
-    if (M == -INFINITY) {
-      a.out[rowid * kDv + e] = __float2bfloat16_rn(0.f);
-      if (e == 0) a.lse[rowid] = -INFINITY;
-      continue;
-    }
-    float Ls = sk == -INFINITY ? 0.f : ex2(sk - M);
-    float acc = 0.f;
-    for (int32_t c = c_first; c <= c_last; ++c) {
-      if (!has_part(c)) continue;
-      const size_t pr = slot(c, r);
-      const float4 v = ml[pr];
-      const float wgt = v.x == -INFINITY ? 0.f : ex2(v.x - M);
-      Ls += v.y * wgt;
-      acc += wgt * a.part_o[pr * kDv + e];
-    }
-    a.out[rowid * kDv + e] = __float2bfloat16_rn(acc / Ls);
-    if (e == 0) a.lse[rowid] = (M + __log2f(Ls)) * kLn2;
   }
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -162,9 +164,6 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
-// Decode workspace: the per-unit block offsets (n_units + 1 int32, padded to
-// 256 bytes), then 2 partial slots per CTA of R rows x (128 + 4) fp32, for at
-// most sa::kDecMaxGrid CTAs.
 // Global causal prefill with G >= 4 query heads per KV head: pairs of query
 // tiles per CTA, longest first.
 sinkattn_status launch_causal(const void *q, const void *k, const void *v, const AttnArgs &a,
@@ -211,13 +210,30 @@ struct DecodePlan {
   size_t tab_bytes = 0, bytes = 0;
 };
 
+// Decode workspace: one 64-bit ticket per unit (batch x KV heads, padded to
+// 256 bytes), then 2 partial slots per CTA of R rows x (128 + 4) fp32, for at
+// most sa::kDecMaxGrid CTAs.
 DecodePlan decode_plan(int32_t batch, int32_t T, int32_t hq, int32_t hkv) {
   DecodePlan p;
   p.rows = T * (hq / hkv);
-  p.tab_bytes = ((static_cast<size_t>(batch) * hkv + 1) * sizeof(int32_t) + 255) & ~size_t(255);
+  p.tab_bytes = (static_cast<size_t>(batch) * hkv * sizeof(uint64_t) + 255) & ~size_t(255);
   p.bytes = p.tab_bytes +
             static_cast<size_t>(sa::kDecMaxGrid) * 2 * p.rows * (sa::kDv + 4) * sizeof(float);
   return p;
+}
+
+// A number for each decode call, different from every other call of this
+// process (48 bits): the tickets of a call are told from the words earlier
+// calls left in the workspace by it.  It starts at a value drawn from the
+// clock and the address space, so another process that used the same memory
+// is unlikely (2^-48 per ticket) to have left this call's number behind.
+unsigned long long next_decode_epoch() {
+  static std::atomic<unsigned long long> counter{
+      (static_cast<unsigned long long>(
+           std::chrono::steady_clock::now().time_since_epoch().count()) ^
+       (reinterpret_cast<uintptr_t>(&counter) << 7)) & 0xFFFFFFFFFFFFull};
+  unsigned long long e = counter.fetch_add(1) & 0xFFFFFFFFFFFFull;
+  return e == 0 ? 1ull : e;
 }
 
 }  // namespace
@@ -562,7 +578,8 @@ static sinkattn_status decode_impl(const void *q, const void *kcache, const void
   d.sink = sink;
   d.out = static_cast<__nv_bfloat16 *>(out);
   d.lse = lse;
-  d.unit_blk = static_cast<int32_t *>(workspace);
+  d.tickets = static_cast<unsigned long long *>(workspace);
+  d.epoch = next_decode_epoch();
   d.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.tab_bytes);
   d.part_ml = d.part_o + static_cast<size_t>(sa::kDecMaxGrid) * 2 * plan.rows * sa::kDv;
   std::memcpy(d.rope_turns, a.rope_turns, sizeof d.rope_turns);
@@ -608,10 +625,6 @@ static sinkattn_status decode_impl(const void *q, const void *kcache, const void
       return SINKATTN_ECUDA;
     kern<<<grid, sa::kThreads, smem, s>>>(mq, mk, mv, d);
   }
-  if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
-
-  sa::sinkattn_decode_combine_kernel<<<dim3(static_cast<unsigned>(d.n_units), sa::kCombParts),
-                                       sa::kCombThreads, 0, s>>>(d, grid);
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
@@ -706,8 +719,8 @@ extern "C" sinkattn_status sinkattn_decode_noalloc(
                                         0, out, lse, stream);
   void *scratch = nullptr;
   if (sinkattn_status st = noalloc_scratch(&scratch)) return st;
-  // Every partial the combine step reads is written first by the same call, so
-  // the buffer needs no clearing between calls.
+  // Every partial a merge reads is written first by the same call, and the
+  // tickets carry the call's own number, so the buffer needs no clearing.
   return sinkattn_decode(q, kcache, vcache, seqlens, sink, window, rope_base, batch, T, S_cap,
                          max_seqlen, num_q_heads, num_kv_heads, scratch,
                          SINKATTN_NOALLOC_SCRATCH_BYTES, out, lse, stream);

@@ -101,14 +101,14 @@ def test_decode_workspace_size(L):
     assert ws(2, 4, 64, 5, 1000, 0) == 0
     a = ws(64, 4, 64, 4, 262144, 0)
     b = ws(64, 4, 64, 4, 65536, 0)
-    # the layout does not depend on the cache lengths or the window: the block
-    # offsets of the batch*Hkv units (int32, padded to 256 bytes), then two
-    # partial slots of T*G rows x 132 fp32 (128 values, max, sum, pad) per CTA
-    # for at most 160 CTAs
+    # the layout does not depend on the cache lengths or the window: one 64-bit
+    # ticket per unit (batch*Hkv, padded to 256 bytes), then two partial slots
+    # of T*G rows x 132 fp32 (128 values, max, sum, pad) per CTA for at most
+    # 160 CTAs
     assert a == b == ws(64, 4, 64, 4, 262144, 128)
-    tab = ((64 * 4 + 1) * 4 + 255) // 256 * 256
+    tab = (64 * 4 * 8 + 255) // 256 * 256
     assert a == tab + 160 * 2 * (4 * 16) * 132 * 4
-    tab8 = ((64 * 8 + 1) * 4 + 255) // 256 * 256
+    tab8 = (64 * 8 * 8 + 255) // 256 * 256
     assert ws(64, 4, 64, 8, 262144, 128) == tab8 + 160 * 2 * (4 * 8) * 132 * 4
 
 

@@ -1,4 +1,4 @@
-"""GPU parity: sinkattn_decode (MTP verify, split-KV + combine) against the oracle."""
+"""GPU parity: sinkattn_decode (MTP verify, split-KV with the merge of cut units) against the oracle."""
 import math
 
 import numpy as np
@@ -58,7 +58,7 @@ def test_token_counts(oracle_mod, t):
 
 
 def test_many_splits_long_cache(oracle_mod):
-    # 20000 keys -> many chunks per (sequence, kv head): the combine must count the sink once
+    # 20000 keys -> many chunks per (sequence, kv head): the merge must count the sink once
     o, l, ro, rl = run_decode(oracle_mod, [20000, 9000], 4, 20000, 64, 4, 0, 5e6, seed=2)
     assert_parity(o, l, ro, rl, "long cache")
 
