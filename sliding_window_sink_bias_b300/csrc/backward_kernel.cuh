@@ -25,7 +25,8 @@
 //                     P^T and dS^T in registers, back to TMEM as bf16,
 //                     dV += P^T dO and dK += dS^T Q (A from TMEM, B = the same
 //                     shared-memory tiles read N-major); epilogue as above.
-//   bwd_dsink_kernel  the per-chunk partials summed in chunk order.
+//   bwd_dsink_kernel  the per-chunk partials summed in a fixed order, one CTA
+//                     per head.
 //
 // The MMA kernels run 8 warps that own half a row each (TMEM lane; warps w and
 // w + 4 share the lanes of w % 4), a ninth warp whose first thread issues the
@@ -89,39 +90,80 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
     if (a.rope_on) rope_cs(pos, a.rope_turns[lane], c, s);
     const int32_t ia = a.rope_style == 0 ? 2 * lane : lane;
     const int32_t ib = a.rope_style == 0 ? 2 * lane + 1 : lane + 32;
-    // rotated copies: q (Hq heads) then k (Hkv heads); an interleaved pair is
-    // one 32-bit word
+    // rotated copies: q (Hq heads) then k (Hkv heads), in 16-byte units (24 a
+    // row).  Pairs (2t, 2t+1): unit c < 8 of a row holds pairs 4c..4c+3,
+    // whose angles this warp's lanes 4c..4c+3 computed above.
+    if (a.rope_style == 0) {
+      const int32_t nunit = (a.Hq + a.Hkv) * 24;
+      // the trip count is the same for every lane (the shuffles need all 32)
+#pragma unroll 2
+      for (int32_t j0 = 0; j0 < nunit; j0 += 32) {
+        const int32_t j = j0 + lane;
+        const bool act = j < nunit;
+        const int32_t hh = j / 24, cc = j % 24;
+        const bool isq = hh < a.Hq;
+        const size_t row = isq ? static_cast<size_t>(tok) * a.Hq + hh
+                               : static_cast<size_t>(tok) * a.Hkv + (hh - a.Hq);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (act) v = *reinterpret_cast<const uint4 *>((isq ? a.q : a.k) + row * kDqk + 8 * cc);
+        // every lane takes part in the shuffles; only units of box 0 rotate
+        const int32_t src_lane = cc < 8 ? 4 * cc : 0;
+        const float c0 = __shfl_sync(0xffffffffu, c, src_lane & 31);
+        const float s0 = __shfl_sync(0xffffffffu, s, src_lane & 31);
+        const float c1 = __shfl_sync(0xffffffffu, c, (src_lane + 1) & 31);
+        const float s1 = __shfl_sync(0xffffffffu, s, (src_lane + 1) & 31);
+        const float c2 = __shfl_sync(0xffffffffu, c, (src_lane + 2) & 31);
+        const float s2 = __shfl_sync(0xffffffffu, s, (src_lane + 2) & 31);
+        const float c3 = __shfl_sync(0xffffffffu, c, (src_lane + 3) & 31);
+        const float s3 = __shfl_sync(0xffffffffu, s, (src_lane + 3) & 31);
+        if (cc < 8) {
+          v.x = pack_bf16x2(bf16lo(v.x) * c0 - bf16hi(v.x) * s0, bf16lo(v.x) * s0 + bf16hi(v.x) * c0);
+          v.y = pack_bf16x2(bf16lo(v.y) * c1 - bf16hi(v.y) * s1, bf16lo(v.y) * s1 + bf16hi(v.y) * c1);
+          v.z = pack_bf16x2(bf16lo(v.z) * c2 - bf16hi(v.z) * s2, bf16lo(v.z) * s2 + bf16hi(v.z) * c2);
+          v.w = pack_bf16x2(bf16lo(v.w) * c3 - bf16hi(v.w) * s3, bf16lo(v.w) * s3 + bf16hi(v.w) * c3);
+        }
+        if (act) *reinterpret_cast<uint4 *>((isq ? a.q_rot : a.k_rot) + row * kDqk + 8 * cc) = v;
+      }
+    } else {
+      // pairs (t, t + 32): lane t holds pair t of every row
 #pragma unroll 4
-    for (int32_t hh = 0; hh < a.Hq + a.Hkv; ++hh) {
-      const bool isq = hh < a.Hq;
-      const size_t row = isq ? static_cast<size_t>(tok) * a.Hq + hh
-                             : static_cast<size_t>(tok) * a.Hkv + (hh - a.Hq);
-      const __nv_bfloat16 *src = (isq ? a.q : a.k) + row * kDqk;
-      __nv_bfloat16 *dst = (isq ? a.q_rot : a.k_rot) + row * kDqk;
-      if (a.rope_style == 0) {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(src + 2 * lane);
-        const float x = bf16lo(w), y = bf16hi(w);
-        *reinterpret_cast<uint32_t *>(dst + 2 * lane) = pack_bf16x2(x * c - y * s, x * s + y * c);
-      } else {
+      for (int32_t hh = 0; hh < a.Hq + a.Hkv; ++hh) {
+        const bool isq = hh < a.Hq;
+        const size_t row = isq ? static_cast<size_t>(tok) * a.Hq + hh
+                               : static_cast<size_t>(tok) * a.Hkv + (hh - a.Hq);
+        const __nv_bfloat16 *src = (isq ? a.q : a.k) + row * kDqk;
+        __nv_bfloat16 *dst = (isq ? a.q_rot : a.k_rot) + row * kDqk;
         const float x = __bfloat162float(src[ia]), y = __bfloat162float(src[ib]);
         dst[ia] = __float2bfloat16_rn(x * c - y * s);
         dst[ib] = __float2bfloat16_rn(x * s + y * c);
+        *reinterpret_cast<uint2 *>(dst + 64 + 4 * lane) =
+            *reinterpret_cast<const uint2 *>(src + 64 + 4 * lane);
       }
-      *reinterpret_cast<uint2 *>(dst + 64 + 4 * lane) =
-          *reinterpret_cast<const uint2 *>(src + 64 + 4 * lane);
     }
-    // D = dO . o per head (4 dims per lane, warp sum)
-#pragma unroll 4
-    for (int32_t h = 0; h < a.Hq; ++h) {
-      const size_t row = static_cast<size_t>(tok) * a.Hq + h;
-      const uint2 ov = *reinterpret_cast<const uint2 *>(a.out + row * kDv + 4 * lane);
-      const uint2 dv = *reinterpret_cast<const uint2 *>(a.dout + row * kDv + 4 * lane);
-      float acc = bf16lo(ov.x) * bf16lo(dv.x) + bf16hi(ov.x) * bf16hi(dv.x) +
-                  bf16lo(ov.y) * bf16lo(dv.y) + bf16hi(ov.y) * bf16hi(dv.y);
+    // D = dO . o per head: four lanes a head (32 dims each, 16-byte loads),
+    // eight heads per round
+    const int32_t quarter = lane & 3;
+#pragma unroll 2
+    for (int32_t h0 = 0; h0 < a.Hq; h0 += 8) {
+      const int32_t h = h0 + (lane >> 2);
+      float acc = 0.f;
+      if (h < a.Hq) {
+        const size_t row = static_cast<size_t>(tok) * a.Hq + h;
+        const uint4 *op = reinterpret_cast<const uint4 *>(a.out + row * kDv + 32 * quarter);
+        const uint4 *dp = reinterpret_cast<const uint4 *>(a.dout + row * kDv + 32 * quarter);
 #pragma unroll
-      for (int32_t o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) {
-        a.D[row] = acc;
+        for (int32_t u = 0; u < 4; ++u) {
+          const uint4 ov = op[u], dv = dp[u];
+          acc += bf16lo(ov.x) * bf16lo(dv.x) + bf16hi(ov.x) * bf16hi(dv.x);
+          acc += bf16lo(ov.y) * bf16lo(dv.y) + bf16hi(ov.y) * bf16hi(dv.y);
+          acc += bf16lo(ov.z) * bf16lo(dv.z) + bf16hi(ov.z) * bf16hi(dv.z);
+          acc += bf16lo(ov.w) * bf16lo(dv.w) + bf16hi(ov.w) * bf16hi(dv.w);
+        }
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (quarter == 0 && h < a.Hq) {
+        a.D[static_cast<size_t>(tok) * a.Hq + h] = acc;
         if (h < 64) sD[tt][h] = acc;
       }
     }
@@ -145,12 +187,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
   }
 }
 
+// One CTA per head: thread i sums the chunks i, i + 256, ... in order, then a
+// fixed tree adds the 256 sums (the same bits every run).
 __global__ void __launch_bounds__(256) bwd_dsink_kernel(const __grid_constant__ BwdArgs a) {
-  for (int32_t h = threadIdx.x; h < a.Hq; h += blockDim.x) {
-    float acc = 0.f;
-    for (int32_t c = 0; c < a.n_chunks; ++c) acc += a.dsink_part[static_cast<size_t>(c) * a.Hq + h];
-    a.dsink[h] = acc;
+  __shared__ float part[256];
+  const int32_t h = blockIdx.x;
+  float acc = 0.f;
+  for (int32_t c = threadIdx.x; c < a.n_chunks; c += 256)
+    acc += a.dsink_part[static_cast<size_t>(c) * a.Hq + h];
+  part[threadIdx.x] = acc;
+  __syncthreads();
+#pragma unroll
+  for (int32_t w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
   }
+  if (threadIdx.x == 0) a.dsink[h] = part[0];
 }
 
 // ------------------------------------------------------------------ shared pieces

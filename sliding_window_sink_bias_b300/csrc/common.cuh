@@ -153,17 +153,18 @@ __device__ __forceinline__ uint4 *swz_chunk(uint8_t *box, int32_t r, int32_t c) 
 
 // RoPE on dims 0..63 (box 0) of a Q tile of packed rows r = t * G + g: the
 // n_tok tokens at positions pos0 + t share their angles, so each (token, chunk)
-// unit computes its angles once and rotates all G heads.  128 threads.
-// kBf16: store the rotated dims as bf16 instead of fp16.
+// unit computes its angles once and rotates all G heads.  nthr threads (128
+// unless given).  kBf16: store the rotated dims as bf16 instead of fp16.
 template <bool kBf16 = false>
 __device__ void rope_q_tile(uint8_t *box0, int32_t G, int32_t n_tok, int32_t pos0,
-                            int32_t rope_style, const unsigned long long *turns, int32_t tid) {
+                            int32_t rope_style, const unsigned long long *turns, int32_t tid,
+                            int32_t nthr = 128) {
   if (n_tok <= 0) return;
   const int32_t nch = rope_style == 0 ? 8 : 4;
   const int32_t units = n_tok * nch;
-  const int32_t hsplit = units >= 128 ? 1 : min(G, 128 / units);
+  const int32_t hsplit = units >= nthr ? 1 : min(G, nthr / units);
   const int32_t hper = (G + hsplit - 1) / hsplit;
-  for (int32_t u = tid; u < units * hsplit; u += 128) {
+  for (int32_t u = tid; u < units * hsplit; u += nthr) {
     const int32_t hs = u / units, tc = u % units;
     const int32_t t = tc / nch, c = tc % nch;
     const int32_t pos = pos0 + t;

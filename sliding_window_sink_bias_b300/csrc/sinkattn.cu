@@ -352,7 +352,7 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
 
   sa::bwd_pre_kernel<<<static_cast<unsigned>(plan.chunks), 256, 0, s>>>(b);
   if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
-  sa::bwd_dsink_kernel<<<1, 256, 0, s>>>(b);
+  sa::bwd_dsink_kernel<<<static_cast<unsigned>(num_q_heads), 256, 0, s>>>(b);
   if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
 
   CUtensorMap mq, mdo, mk, mv;
