@@ -6,8 +6,17 @@ accumulation, where P and dS are rounded to bf16 (relative 2^-9 each), the
 rotated q and k are rounded to bf16 (2^-9), D = dO . o comes from the bf16
 forward output (2^-9), and the result is rounded to bf16 (2^-9).  Those five
 roundings give a worst-case relative error near 5 * 2^-9 = 1e-2 of the
-gradient's scale; the test allows 2e-2 of the largest reference magnitude per
-tensor.  dsink is an fp32 sum over tokens of exp(sink - lse) D: 1e-2 relative.
+gradient's scale.  The bounds are per row (one token and head):
+  dk, dv: |error| <= 2e-2 (|row| + 0.05 |tensor|), where |row| is the row's
+          largest reference magnitude and |tensor| the tensor's: every row is
+          held to its own scale down to 5% of the tensor's (measured: within
+          0.7% of that sum);
+  dq:     |error| <= 2e-2 |row| + 1e-2 |tensor|.  A row of dq whose rotated
+          keys cancel (dP close to D for every key it sees) is a small
+          difference of large bf16-rounded terms, so its error follows the
+          terms, i.e. the tensor's scale (measured: up to 4.5e-3 of it), not
+          its own magnitude.
+dsink is an fp32 sum over tokens of exp(sink - lse) D: 1e-2 relative.
 """
 import numpy as np
 import pytest
@@ -49,10 +58,15 @@ def _check(got, ref, what):
     names = ("dq", "dk", "dv")
     for name, g, r in zip(names, got[:3], ref[:3]):
         g = g.float().cpu().numpy().astype(np.float64)
-        scale = max(np.max(np.abs(r)), 1e-30)
-        err = np.max(np.abs(g - r))
         assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
-        assert err <= REL * scale, f"{what} {name}: max err {err:.3e} vs scale {scale:.3e}"
+        tmax = max(np.max(np.abs(r)), 1e-30)
+        err_row = np.max(np.abs(g - r), axis=-1)
+        row = np.max(np.abs(r), axis=-1)
+        bound = REL * row + (1e-2 * tmax if name == "dq" else REL * 0.05 * tmax)
+        worst = np.unravel_index(np.argmax(err_row - bound), err_row.shape)
+        assert np.all(err_row <= bound), (
+            f"{what} {name}: row {worst} err {err_row[worst]:.3e} > bound {bound[worst]:.3e} "
+            f"(row scale {row[worst]:.3e}, tensor scale {tmax:.3e})")
     gs = got[3].cpu().numpy().astype(np.float64)
     rs = ref[3]
     err = np.max(np.abs(gs - rs))
