@@ -26,15 +26,14 @@
 //   warp 2       TMEM allocator (S0, S1, O, Q: 512 columns).
 //   warp 3       set-up: this CTA's block range and first unit; the rows of
 //                its share of the units with no key at all.
-//   warps 4-7    at the start of a unit, its Q tile from shared memory into
-//                TMEM (one row per thread); then the online softmax, one row
-//                per thread: the block's masked max
+//   warps 4-7    online softmax, one row per thread: the block's masked max
 //                (3-input max), lazy running max (moves only when a block
 //                exceeds it by more than 2^8), P = 2^(s * scale * log2e - m) as
 //                bf16 pairs into TMEM, l, and the rescale of this row's O when
 //                m moves; at the end of a unit's segment the row is finished
 //                (with the sink) or its partial is written.
-//   warps 8-11   RoPE on dims 0..63 of the Q tile and of every K block.
+//   warps 8-11   RoPE on dims 0..63 of the Q tile, the tile into one of two
+//                TMEM buffers (one row per thread), RoPE on every K block.
 #pragma once
 #include "common.cuh"
 
@@ -44,10 +43,12 @@ constexpr int32_t kDecBN = 64;      // keys per block
 constexpr int32_t kDecStages = 4;   // K/V blocks in flight
 constexpr uint32_t kDecTmemCols = 512;
 constexpr uint32_t kDecTmemO = 128;
-// The unit's query tile (128 rows x 192 dims, 16-bit pairs): QK^T reads its A
-// operand from TMEM, so the tile is not re-read from shared memory for every
-// cache block (with N = 64 keys, 48 KB of Q against 24 KB of K per block).
-constexpr uint32_t kDecTmemQ = 256;
+// The units' query tiles (128 rows x 192 dims, 16-bit pairs: 96 columns), two
+// buffers: QK^T reads its A operand from TMEM, so a tile is not re-read from
+// shared memory for every cache block (with N = 64 keys, 48 KB of Q against
+// 24 KB of K per block), and the next unit's tile goes in while QK^T still
+// reads the current one.
+__host__ __device__ constexpr uint32_t dec_tmem_q(uint32_t b) { return 256u + 96u * b; }
 constexpr int32_t kDecMaxGrid = 160;  // CTAs at most (2 partial slots each)
 
 struct DecArgs {
@@ -256,8 +257,9 @@ struct DecLayoutT {
   static constexpr uint32_t kStgOff = kKVOff + S * kKVStage;
   static constexpr uint32_t kBarOff = kStgOff + S8 * kStg;
   // q_full q_ready q_empty | kv_full[S] k_ready[S] kv_empty[S] | s_full[2] p_full[2] pv_done
-  // o_empty drain | stg_full[S8] stg_empty[S8] | q_tmem part_out last_known
-  static constexpr uint32_t kNumBars = 3 + 3 * S + 7 + 2 * S8 + 3;
+  // o_empty drain | stg_full[S8] stg_empty[S8] | q_tmem1 part_out last_known q_tfree[2]
+  // (bar 1 is q_tmem0: a query tile rotated and in TMEM buffer 0)
+  static constexpr uint32_t kNumBars = 3 + 3 * S + 7 + 2 * S8 + 6;  // + q_rot
   // tmem slot, abort flag, cursor[6], the "last to finish a cut unit" flag
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kTurnsOff = (kMiscOff + 40 + 7) & ~7u;
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
   const int32_t lane = threadIdx.x & 31;
 
   auto bar = [&](uint32_t i) { return sbase + Ly::kBarOff + i * 8; };
-  const uint32_t B_QFULL = bar(0), B_QREADY = bar(1), B_QEMPTY = bar(2);
+  const uint32_t B_QFULL = bar(0), B_QEMPTY = bar(2);
   auto B_KVFULL = [&](uint32_t s) { return bar(3 + s); };
   auto B_KREADY = [&](uint32_t s) { return bar(3 + S + s); };
   auto B_KVEMPTY = [&](uint32_t s) { return bar(3 + 2 * S + s); };
@@ -512,7 +514,11 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
   const uint32_t B_DRAIN = bar(3 + 3 * S + 6);
   auto B_STGFULL = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + s8); };
   auto B_STGEMPTY = [&](uint32_t s8) { return bar(3 + 3 * S + 7 + S8 + s8); };
-  const uint32_t B_QTMEM = bar(3 + 3 * S + 7 + 2 * S8);
+  // a query tile rotated and in TMEM buffer b (the conversion threads); buffer
+  // b free again (a commit after the last QK^T that read it)
+  auto B_QTMEM = [&](uint32_t b) { return b ? bar(3 + 3 * S + 7 + 2 * S8) : bar(1); };
+  auto B_QTFREE = [&](uint32_t b) { return bar(3 + 3 * S + 7 + 2 * S8 + 3 + b); };
+  const uint32_t B_QROT = bar(3 + 3 * S + 7 + 2 * S8 + 5);  // the tile rotated (all conversion threads)
   // a cut unit's partial is out (128 softmax threads), the ticket's answer is known (1)
   const uint32_t B_PARTOUT = bar(3 + 3 * S + 7 + 2 * S8 + 1);
   const uint32_t B_LASTKNOWN = bar(3 + 3 * S + 7 + 2 * S8 + 2);
@@ -526,9 +532,12 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     mbar_init(B_QFULL, 1);
-    mbar_init(B_QREADY, DecThreads<F8>::kConv);
-    mbar_init(B_QEMPTY, 128);  // the softmax threads, once Q is in TMEM
-    mbar_init(B_QTMEM, 128);
+    mbar_init(B_QEMPTY, DecThreads<F8>::kConv);  // the conversion threads, once Q is in TMEM
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(B_QTMEM(b), DecThreads<F8>::kConv);
+      mbar_init(B_QTFREE(b), 1);
+    }
+    mbar_init(B_QROT, DecThreads<F8>::kConv);
     mbar_init(B_PARTOUT, 128);
     mbar_init(B_LASTKNOWN, 1);
     for (uint32_t s = 0; s < S; ++s) {
@@ -682,7 +691,8 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
       DecCursor c = c0;
       DecSeg sg;
       while (ok && dec_next(c, args, sg)) {
-        if (!(ok = wait_bar(B_QTMEM, gq & 1, abort_flag, 3))) break;
+        const uint32_t qb = gq & 1;
+        if (!(ok = wait_bar(B_QTMEM(qb), (gq >> 1) & 1, abort_flag, 3))) break;
         tc_fence_after();
         for (int32_t j = 0; ok && j < sg.nblk; ++j) {
           const uint32_t st = (gk + j) % S;
@@ -695,12 +705,13 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
 #pragma unroll
           for (int kstep = 0; kstep < kDqk / 16; ++kstep) {
             const uint32_t box = kstep >> 2, off = (kstep & 3) * 32;
-            mma_ts2(s_t, tmem + kDecTmemQ + kstep * 8,
+            mma_ts2(s_t, tmem + dec_tmem_q(qb) + kstep * 8,
                     kv_lo + st * kStageLo + ((box * Ly::kKBox + off) >> 4), kDescHi,
                     box == 0 ? kIdQKRot : kIdQK, kstep > 0 ? 1u : 0u);
           }
           issued = true;
           mma_commit(B_SFULL((gs + j) & 1));
+          if (j == sg.nblk - 1) mma_commit(B_QTFREE(qb));  // the unit's last read of its tile
           if (j > 0 && !(ok = issue_pv(gs + j - 1, (gk + j - 1) % S, j == 1))) break;
         }
         if (ok) ok = issue_pv(gs + sg.nblk - 1, (gk + sg.nblk - 1) % S, sg.nblk == 1);
@@ -721,7 +732,7 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
     const bool warp_active = (warp & 3) * 32 < R;  // the warp holds at least one real row
     const int32_t t = row / G, g = row % G;
     const int32_t W = args.window;
-    uint32_t gs = 0, gpv = 0, gq = 0, gcut = 0;
+    uint32_t gs = 0, gpv = 0, gcut = 0;
     bool ok = true;
     DecCursor c = c0;
     DecSeg sg;
@@ -732,32 +743,6 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
     while (ok && dec_next(c, args, sg)) {
       const int64_t F0 = flat - sg.blk0;  // the unit's blocks are [F0, F0 + nblk_u) of the list
       flat += sg.nblk;
-      // The unit's Q tile (rotated; fp16 with an FP8 cache) into TMEM, one row
-      // per thread, then the shared-memory tile back to the copy thread.  Every
-      // QK^T that read the previous unit's rows has completed: this thread
-      // waited for that unit's last PV, issued after them.
-      if (!(ok = wait_bar_warp(B_QREADY, gq & 1, abort_flag, 13))) break;
-      if (warp_active) {
-        uint8_t *qs = smem + Ly::kQOff;
-#pragma unroll 1
-        for (int32_t b = 0; b < 3; ++b) {
-          uint32_t w[32];
-#pragma unroll
-          for (int32_t ch = 0; ch < 8; ++ch) {
-            const uint4 v = *swz_chunk(qs + b * kQBoxBytes, row, ch);
-            w[4 * ch] = v.x;
-            w[4 * ch + 1] = v.y;
-            w[4 * ch + 2] = v.z;
-            w[4 * ch + 3] = v.w;
-          }
-          tmem_st32p(tmem + lane_off + kDecTmemQ + b * 32, w);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      mbar_arrive(B_QTMEM);
-      mbar_arrive(B_QEMPTY);
-      ++gq;
       // query t sits at position L - T + t and sees cache keys
       // [max(0, pos - W + 1), pos], here limited to this segment's keys
       const int32_t pos = sg.L - args.T + t;
@@ -945,64 +930,66 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
         }
         if (!(ok = wait_bar_warp(B_LASTKNOWN, gcut & 1, abort_flag, 15))) break;
         ++gcut;
-        if (*last_flag && warp_active && row < R) {
+        if (*last_flag) {
           __threadfence();
           // M = max(sink, m_i), L = 2^(sink - M) + sum_i l_i 2^(m_i - M),
           // o = sum_i 2^(m_i - M) O_i / L, in group order (eq. (2) over the
-          // partition of the unit's keys, the sink once)
+          // partition of the unit's keys, the sink once).  All 128 threads:
+          // item (row r, 32 dims), four a row; each item's loads go out
+          // together.
           const int32_t sl = static_cast<int32_t>(blockIdx.x) % args.n_sub;
-          const int32_t head = sg.kvh * G + g;
-          const size_t orow = (static_cast<size_t>(sg.b) * args.T + t) * args.Hq + head;
           const float4 *ml = reinterpret_cast<const float4 *>(args.part_ml);
-          auto prow_of = [&](int32_t i) {
-            const size_t cta = static_cast<size_t>(i) * args.n_sub + sl;
-            return (cta * 2 + ((i == c_first && Tb * i / n_grp < F0) ? 1 : 0)) * R + row;
-          };
-          const float sk_raw = __ldg(args.sink + head);
-          const float sk2 = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
-          float M = sk2;
-          for (int32_t i = c_first; i <= c_last; ++i)
-            if (has_part(i)) M = fmaxf(M, __ldcg(ml + prow_of(i)).x);
-          if (M == -INFINITY) {
-            uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv);
-            for (int32_t q4 = 0; q4 < kDv / 8; ++q4) dst[q4] = make_uint4(0u, 0u, 0u, 0u);
-            args.lse[orow] = -INFINITY;
-          } else {
+          for (int32_t wi = row; wi < R * 4; wi += 128) {
+            const int32_t r = wi >> 2, cb = (wi & 3) * 32;
+            const int32_t head = sg.kvh * G + r % G;
+            const size_t orow = (static_cast<size_t>(sg.b) * args.T + r / G) * args.Hq + head;
+            auto prow_of = [&](int32_t i) {
+              const size_t cta = static_cast<size_t>(i) * args.n_sub + sl;
+              return (cta * 2 + ((i == c_first && Tb * i / n_grp < F0) ? 1 : 0)) * R + r;
+            };
+            const float sk_raw = __ldg(args.sink + head);
+            const float sk2 = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
+            float M = sk2;
+#pragma unroll 4
+            for (int32_t i = c_first; i <= c_last; ++i)
+              if (has_part(i)) M = fmaxf(M, __ldcg(ml + prow_of(i)).x);
+            uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv + cb);
+            if (M == -INFINITY) {
+#pragma unroll
+              for (int32_t q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(0u, 0u, 0u, 0u);
+              if (cb == 0) args.lse[orow] = -INFINITY;
+              continue;
+            }
             float Ls = sk2 == -INFINITY ? 0.f : ex2(sk2 - M);
+            float acc[32];
+#pragma unroll
+            for (int32_t e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll 2
             for (int32_t i = c_first; i <= c_last; ++i) {
               if (!has_part(i)) continue;
-              const float4 v = __ldcg(ml + prow_of(i));
-              Ls += v.y * (v.x == -INFINITY ? 0.f : ex2(v.x - M));
-            }
-#pragma unroll 1
-            for (int32_t cb = 0; cb < kDv; cb += 32) {
-              float acc[32];
+              const size_t pr = prow_of(i);
+              const float4 *src = reinterpret_cast<const float4 *>(args.part_o + pr * kDv + cb);
+              float4 o4[8];
 #pragma unroll
-              for (int32_t e = 0; e < 32; ++e) acc[e] = 0.f;
-              for (int32_t i = c_first; i <= c_last; ++i) {
-                if (!has_part(i)) continue;
-                const size_t pr = prow_of(i);
-                const float4 v = __ldcg(ml + pr);
-                const float w = v.x == -INFINITY ? 0.f : ex2(v.x - M);
-                const float4 *src = reinterpret_cast<const float4 *>(args.part_o + pr * kDv + cb);
+              for (int32_t q4 = 0; q4 < 8; ++q4) o4[q4] = __ldcg(src + q4);
+              const float4 v = __ldcg(ml + pr);
+              const float w = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+              Ls += v.y * w;
 #pragma unroll
-                for (int32_t q4 = 0; q4 < 8; ++q4) {
-                  const float4 o4 = __ldcg(src + q4);
-                  acc[4 * q4] += w * o4.x;
-                  acc[4 * q4 + 1] += w * o4.y;
-                  acc[4 * q4 + 2] += w * o4.z;
-                  acc[4 * q4 + 3] += w * o4.w;
-                }
+              for (int32_t q4 = 0; q4 < 8; ++q4) {
+                acc[4 * q4] += w * o4[q4].x;
+                acc[4 * q4 + 1] += w * o4[q4].y;
+                acc[4 * q4 + 2] += w * o4[q4].z;
+                acc[4 * q4 + 3] += w * o4[q4].w;
               }
-              uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv + cb);
-#pragma unroll
-              for (int32_t q4 = 0; q4 < 4; ++q4)
-                dst[q4] = make_uint4(pack_bf16x2(acc[8 * q4] / Ls, acc[8 * q4 + 1] / Ls),
-                                     pack_bf16x2(acc[8 * q4 + 2] / Ls, acc[8 * q4 + 3] / Ls),
-                                     pack_bf16x2(acc[8 * q4 + 4] / Ls, acc[8 * q4 + 5] / Ls),
-                                     pack_bf16x2(acc[8 * q4 + 6] / Ls, acc[8 * q4 + 7] / Ls));
             }
-            args.lse[orow] = (M + __log2f(Ls)) * kLn2;
+#pragma unroll
+            for (int32_t q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_uint4(pack_bf16x2(acc[8 * q4] / Ls, acc[8 * q4 + 1] / Ls),
+                                   pack_bf16x2(acc[8 * q4 + 2] / Ls, acc[8 * q4 + 3] / Ls),
+                                   pack_bf16x2(acc[8 * q4 + 4] / Ls, acc[8 * q4 + 5] / Ls),
+                                   pack_bf16x2(acc[8 * q4 + 6] / Ls, acc[8 * q4 + 7] / Ls));
+            if (cb == 0) args.lse[orow] = (M + __log2f(Ls)) * kLn2;
           }
         }
       }
@@ -1027,8 +1014,40 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
         // already wrote box 0 as fp16; the conversion touches the other boxes)
         dec_q_to_f16(smem + Ly::kQOff, R, !args.rope_on, tid, DecThreads<F8>::kConv);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(B_QREADY);
+      // every conversion thread's rotation / conversion of the tile is done
+      // before any thread copies rows of it
+      mbar_arrive(B_QROT);
+      if (!(ok = wait_bar_warp(B_QROT, gq & 1, abort_flag, 13))) break;
+      // TMEM buffer qb is free once the last QK^T of the unit two back read it
+      const uint32_t qb = gq & 1;
+      if (!(ok = wait_bar_warp(B_QTFREE(qb), ((gq >> 1) & 1) ^ 1, abort_flag, 14))) break;
+      tc_fence_after();
+      {
+        // one row a thread (lane quarter warp % 4); with an FP8 cache warps
+        // 8-11 copy boxes 0 and 1 and warps 12-15 box 2
+        const int32_t q4 = warp & 3, row = q4 * 32 + lane;
+        const int32_t b0 = (F8 && warp >= 12) ? 2 : 0, b1 = (F8 && warp < 12) ? 2 : 3;
+        if (q4 * 32 < R) {
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + dec_tmem_q(qb);
+#pragma unroll 1
+          for (int32_t b = b0; b < b1; ++b) {
+            uint32_t w[32];
+#pragma unroll
+            for (int32_t ch = 0; ch < 8; ++ch) {
+              const uint4 v = *swz_chunk(smem + Ly::kQOff + b * kQBoxBytes, row, ch);
+              w[4 * ch] = v.x;
+              w[4 * ch + 1] = v.y;
+              w[4 * ch + 2] = v.z;
+              w[4 * ch + 3] = v.w;
+            }
+            tmem_st32p(taddr + b * 32, w);
+          }
+          tmem_wait_st();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(B_QTMEM(qb));
+      mbar_arrive(B_QEMPTY);
       ++gq;
       const int32_t kpos0 = sg.lo + sg.blk0 * BN;
       // keys no query of the unit can see: below the window or past the cache

@@ -396,8 +396,10 @@ def decode_roles(nblk, f8=False, skip=()):
     cache: four K/V stages the copies fill.  FP8 cache: two staging slots the
     copies fill and three fp16 stages the conversion warps fill.  QK^T(j) is
     issued before PV(j-1), which waits for the softmax of block j-1.  The
-    softmax rows copy each unit's rotated Q tile from shared memory into TMEM
-    (QK^T reads it there) and then free the shared-memory tile."""
+    conversion warps rotate each unit's Q tile in shared memory, copy it into
+    one of two TMEM buffers (QK^T reads it there) once the last QK^T of the
+    unit two back has freed that buffer (QTFREE, a commit), and then free the
+    shared-memory tile."""
     segs = list(nblk)
     S = 3 if f8 else 4
     S8 = 2
@@ -434,12 +436,15 @@ def decode_roles(nblk, f8=False, skip=()):
             yield ("commit", "PVDONE")
 
         for q, n in enumerate(segs):
-            yield ("wait", "QTMEM", q + 1)
+            qb = q & 1
+            yield ("wait", f"QTMEM{qb}", q // 2 + 1)
             for j in range(n):
                 b = gk + j
                 yield ("wait", f"KREADY{b % S}", b // S + 1)
-                yield ("mma", [("QT", ("Q", q)), (f"K{b % S}", ("K", b))], [(f"P{b & 1}", ("S", b))])
+                yield ("mma", [(f"QT{qb}", ("Q", q)), (f"K{b % S}", ("K", b))], [(f"P{b & 1}", ("S", b))])
                 yield ("commit", f"SFULL{b & 1}")
+                if j == n - 1:
+                    yield ("commit", f"QTFREE{qb}")
                 if j > 0:
                     yield from issue_pv(q, j - 1, b - 1, j == 1)
             yield from issue_pv(q, n - 1, gk + n - 1, n == 1)
@@ -448,12 +453,6 @@ def decode_roles(nblk, f8=False, skip=()):
     def softmax():
         gs = 0
         for q, n in enumerate(segs):
-            if "softmax_qready" not in skip:
-                yield ("wait", "QREADY", q + 1)  # rotated (and converted) tile in place
-            yield ("read", "Q", ("Q", q))
-            yield ("write", "QT", ("Q", q))  # into TMEM
-            yield ("arrive", "QTMEM")
-            yield ("arrive", "QEMPTY")
             for j in range(n):
                 b = gs + j
                 yield ("wait", f"SFULL{b & 1}", (b >> 1) + 1)
@@ -476,7 +475,13 @@ def decode_roles(nblk, f8=False, skip=()):
             yield ("wait", "QFULL", q + 1)
             yield ("read", "Q", ("Qraw", q))
             yield ("write", "Q", ("Q", q))  # RoPE (and fp16) in place
-            yield ("arrive", "QREADY")
+            qb = q & 1
+            if q >= 2 and "convert_qtfree" not in skip:
+                yield ("wait", f"QTFREE{qb}", q // 2)  # the unit two back read the buffer
+            yield ("read", "Q", ("Q", q))
+            yield ("write", f"QT{qb}", ("Q", q))  # into TMEM buffer qb
+            yield ("arrive", f"QTMEM{qb}")
+            yield ("arrive", "QEMPTY")
             for _ in range(n):
                 st = gk % S
                 if f8:

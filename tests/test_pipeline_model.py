@@ -71,10 +71,16 @@ def test_decode_pipeline(f8, sizes):
 
 
 @pytest.mark.parametrize("f8,skip", [(False, "producer_kvempty"), (True, "convert_kvempty"),
-                                     (False, "softmax_pvdone"), (True, "softmax_pvdone"),
-                                     (False, "softmax_qready"), (True, "softmax_qready")])
+                                     (False, "softmax_pvdone"), (True, "softmax_pvdone")])
 def test_decode_missing_wait_is_caught(f8, skip):
     assert _caught(lambda s, sk: decode_roles(s, f8, sk), (skip,), (5, 3, 6))
+
+
+@pytest.mark.parametrize("f8", [False, True])
+def test_decode_missing_qtfree_is_caught(f8):
+    # with one-block units the K stages do not order a unit's QK^T before the
+    # Q copy of the unit two later: only the buffer-free commit does
+    assert _caught(lambda s, sk: decode_roles(s, f8, sk), ("convert_qtfree",), (1, 1, 1, 1, 1, 1))
 
 
 @pytest.mark.parametrize("sizes", [[1], [2], [4], [1, 1, 1], [3, 1, 2], [2, 5, 1, 3]])
