@@ -358,6 +358,10 @@ def bench_hybrid(name, steps, warmup, ws, local):
         swa_layers()
         ga_layers()
 
+    # the SWA layers alone first, before any GA layer has run the GPU into its
+    # power cap (the split below times them right after a GA layer)
+    with ClockSampler(local) as clk_swa:
+        swa_alone_ms, _ = time_calls(swa_layers, max(3, steps), warmup, ws)
     with ClockSampler(local) as clk:
         ms, _ = time_calls(call, steps, warmup, ws)
     # the split of one pass between the SWA layers and the GA layer (events
@@ -381,6 +385,8 @@ def bench_hybrid(name, steps, warmup, ws, local):
     flops = hq * FLOP_PER_PAIR_HEAD * (wl["swa_layers"] * swa_pairs + wl["ga_layers"] * ga_pairs)
     hkv = wl["swa_hkv"]
     per_layer = {"swa_ms": swa_ms, "ga_ms": ga_ms,
+                 "swa_ms_alone": swa_alone_ms / wl["swa_layers"],
+                 "swa_alone_clocks": clk_swa.summary(),
                  "swa_bytes": total * (hq * 192 * 2 + hkv * 192 * 2 + hkv * 128 * 2 + hq * 128 * 2
                                        + hq * 4),
                  "ga_flops": hq * FLOP_PER_PAIR_HEAD * ga_pairs}
@@ -396,8 +402,13 @@ def per_layer_roofline(pl, peaks):
     (tensor-bound) of a hybrid block pass."""
     swa_gbs = pl["swa_bytes"] / (pl["swa_ms"] / 1e3) / 1e9
     ga_tf = pl["ga_flops"] / (pl["ga_ms"] / 1e3) / 1e12
-    return {"swa_ms": pl["swa_ms"], "swa_gbs": swa_gbs, "swa_frac_hbm": swa_gbs / peaks["hbm_gbs"],
-            "ga_ms": pl["ga_ms"], "ga_tflops": ga_tf, "ga_frac_tensor": ga_tf / peaks["bf16_tflops"]}
+    out = {"swa_ms": pl["swa_ms"], "swa_gbs": swa_gbs, "swa_frac_hbm": swa_gbs / peaks["hbm_gbs"],
+           "ga_ms": pl["ga_ms"], "ga_tflops": ga_tf, "ga_frac_tensor": ga_tf / peaks["bf16_tflops"]}
+    if "swa_ms_alone" in pl:
+        a_gbs = pl["swa_bytes"] / (pl["swa_ms_alone"] / 1e3) / 1e9
+        out.update({"swa_ms_alone": pl["swa_ms_alone"], "swa_frac_hbm_alone": a_gbs / peaks["hbm_gbs"],
+                    "swa_alone_sm_mhz": pl["swa_alone_clocks"].get("sm_mhz")})
+    return out
 
 
 def bench_ratio(name, warmup, ws, local):
@@ -764,6 +775,7 @@ def summary_of(line):
         if "per_layer" in w:
             pl = w["per_layer"]
             e["swa_frac_hbm"] = _r(pl["swa_frac_hbm"])
+            e["swa_frac_hbm_alone"] = _r(pl.get("swa_frac_hbm_alone"))
             e["ga_frac_tensor"] = _r(pl["ga_frac_tensor"])
         out[name] = e
     return out
