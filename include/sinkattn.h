@@ -47,6 +47,11 @@
  *     SINKATTN_ECUDA reports a CUDA error from a launch; kernels that hit an
  *     internal wait limit record SINKATTN_ETIMEOUT in a device status word
  *     that sinkattn_get_device_status reads.  Kernels never trap.
+ *   - A build with -DSINKATTN_CHECKS (the test library) also checks, inside
+ *     the kernels, every TMA copy's x coordinate and shared-memory
+ *     destination, every TMEM access and MMA operand, and every global store
+ *     index against its tensor's extent; a failed check skips that access and
+ *     records SINKATTN_ECHECK.  The product library carries no checks.
  *   - Results are deterministic: the same inputs give the same bits.
  */
 #ifndef SINKATTN_H
@@ -65,7 +70,8 @@ typedef enum {
     SINKATTN_EUNSUPPORTED = 2, /* head dims, group size or device not supported */
     SINKATTN_EWORKSPACE = 3,   /* decode workspace missing or too small */
     SINKATTN_ECUDA = 4,        /* a CUDA runtime call failed */
-    SINKATTN_ETIMEOUT = 5      /* a kernel gave up on an internal wait */
+    SINKATTN_ETIMEOUT = 5,     /* a kernel gave up on an internal wait */
+    SINKATTN_ECHECK = 6        /* a bounds check failed (checking builds only) */
 } sinkattn_status;
 
 /* cudaStream_t, passed as an opaque pointer so that this header needs no CUDA include. */
@@ -278,8 +284,11 @@ const char *sinkattn_status_string(sinkattn_status status);
 /*
  * Synchronises the current device, then reads and clears the library's device
  * status word.  Returns SINKATTN_OK, SINKATTN_ETIMEOUT (a kernel gave up on a
- * wait and wrote no trustworthy output) or SINKATTN_ECUDA.  `detail`, if not
- * NULL, receives the raw word (bit 0: timeout; bits 8..15: the wait site).
+ * wait and wrote no trustworthy output), SINKATTN_ECHECK (only a library built
+ * with SINKATTN_CHECKS: an in-kernel bounds check failed and its access was
+ * skipped) or SINKATTN_ECUDA.  `detail`, if not NULL, receives the raw word
+ * (bit 0: timeout, bits 8..15: the wait site; bit 1: a failed check, bits
+ * 16..23: the check site).
  */
 sinkattn_status sinkattn_get_device_status(uint32_t *detail);
 

@@ -16,10 +16,12 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libsinkattn.so")
+# SINKATTN_LIBRARY may name another build of the same sources (the checking
+# test build, to run a test suite with every in-kernel bounds check on)
+LIB_PATH = os.environ.get("SINKATTN_LIBRARY") or os.path.join(_HERE, "libsinkattn.so")
 
 # status codes of include/sinkattn.h
-OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA, ETIMEOUT = range(6)
+OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA, ETIMEOUT, ECHECK = range(7)
 
 EXPORTED = (
     "sinkattn_prefill", "sinkattn_prefill_ex", "sinkattn_decode_workspace_size",

@@ -9,8 +9,9 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libsinkattn.so")
-# the same sources with -DSINKATTN_TEST_HOOKS: the library the timeout-path
-# test loads (it can stall one wait on purpose); the product never loads it
+# the same sources with -DSINKATTN_TEST_HOOKS -DSINKATTN_CHECKS: the library the
+# timeout-path and bounds-check tests load (it can stall one wait on purpose
+# and checks every access in the kernels); the product never loads it
 TEST_LIB = os.path.join(HERE, "libsinkattn_test.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
@@ -49,7 +50,7 @@ def build(force: bool = False, verbose: bool = False, test_lib: bool = True) -> 
     date.  Returns the product library's path."""
     _build_one(LIB, [], force, verbose)
     if test_lib:
-        _build_one(TEST_LIB, ["-DSINKATTN_TEST_HOOKS"], force, verbose)
+        _build_one(TEST_LIB, ["-DSINKATTN_TEST_HOOKS", "-DSINKATTN_CHECKS"], force, verbose)
     return LIB
 
 

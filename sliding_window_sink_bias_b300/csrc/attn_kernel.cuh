@@ -54,6 +54,7 @@ struct AttnArgs {
   const float *sink;
   __nv_bfloat16 *out;
   float *lse;
+  int64_t n_rows;          // rows of out and lse: tokens x Hq (checked stores)
   unsigned long long rope_turns[32];  // round(theta_t / (2 pi) * 2^64), t = 0..31
 };
 
@@ -423,13 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
       const size_t orow = static_cast<size_t>(it.q_row + t) * args.Hq + head;
       uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv);
+      const bool st_ok = rvalid && SA_OUT(orow, args.n_rows, 0x10);
 #pragma unroll
       for (int32_t c0 = 0; c0 < kDv; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(o_t + c0, r);
         tmem_wait_ld();
         reg_fence<32>(r);
-        if (rvalid) {
+        if (st_ok) {
 #pragma unroll
           for (int32_t q4 = 0; q4 < 4; ++q4) {
             uint32_t w4[4];
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (rvalid) args.lse[orow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if (st_ok) args.lse[orow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(B_OEMPTY);
     }

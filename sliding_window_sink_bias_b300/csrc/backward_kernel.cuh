@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
           v.z = pack_bf16x2(bf16lo(v.z) * c2 - bf16hi(v.z) * s2, bf16lo(v.z) * s2 + bf16hi(v.z) * c2);
           v.w = pack_bf16x2(bf16lo(v.w) * c3 - bf16hi(v.w) * s3, bf16lo(v.w) * s3 + bf16hi(v.w) * c3);
         }
-        if (act) *reinterpret_cast<uint4 *>((isq ? a.q_rot : a.k_rot) + row * kDqk + 8 * cc) = v;
+        if (act && SA_IN(row, static_cast<int64_t>(a.total) * (isq ? a.Hq : a.Hkv), 0x30))
+          *reinterpret_cast<uint4 *>((isq ? a.q_rot : a.k_rot) + row * kDqk + 8 * cc) = v;
       }
     } else {
       // pairs (t, t + 32): lane t holds pair t of every row
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
         const bool isq = hh < a.Hq;
         const size_t row = isq ? static_cast<size_t>(tok) * a.Hq + hh
                                : static_cast<size_t>(tok) * a.Hkv + (hh - a.Hq);
+        if (!SA_IN(row, static_cast<int64_t>(a.total) * (isq ? a.Hq : a.Hkv), 0x30)) continue;
         const __nv_bfloat16 *src = (isq ? a.q : a.k) + row * kDqk;
         __nv_bfloat16 *dst = (isq ? a.q_rot : a.k_rot) + row * kDqk;
         const float x = __bfloat162float(src[ia]), y = __bfloat162float(src[ib]);
@@ -162,7 +164,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
       }
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (quarter == 0 && h < a.Hq) {
+      if (quarter == 0 && h < a.Hq &&
+          SA_IN(static_cast<size_t>(tok) * a.Hq + h, static_cast<int64_t>(a.total) * a.Hq, 0x31)) {
         a.D[static_cast<size_t>(tok) * a.Hq + h] = acc;
         if (h < 64) sD[tt][h] = acc;
       }
@@ -183,7 +186,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
         if (l != -INFINITY) acc -= ex2((sk - l) * kLog2e) * d;
       }
     }
-    a.dsink_part[static_cast<size_t>(blockIdx.x) * a.Hq + h] = acc;
+    if (SA_IN(static_cast<size_t>(blockIdx.x) * a.Hq + h, static_cast<int64_t>(a.n_chunks) * a.Hq,
+              0x32))
+      a.dsink_part[static_cast<size_t>(blockIdx.x) * a.Hq + h] = acc;
   }
 }
 
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(256) bwd_dsink_kernel(const __grid_constant__ 
     if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
     __syncthreads();
   }
-  if (threadIdx.x == 0) a.dsink[h] = part[0];
+  if (threadIdx.x == 0 && SA_OUT(h, a.Hq, 0x33)) a.dsink[h] = part[0];
 }
 
 // ------------------------------------------------------------------ shared pieces
@@ -576,7 +581,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!(ok = wait_bar_warp(B_ACCF, k & 1, abort_flag, 24))) break;
       tc_fence_after();
       bwd_store_qk_row(lane_t + kDqColAcc, a.scale, a.rope_on, a.rope_style, ti, a.rope_turns,
-                       a.dq + grow * kDqk, rvalid, half);
+                       a.dq + grow * kDqk,
+                       rvalid && SA_OUT(grow, static_cast<int64_t>(a.total) * a.Hq, 0x34), half);
       tc_fence_before();
       g0 += cur.nblk;
       ++k;
@@ -946,14 +952,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       if (half == 0) {
         // dV row: 128 fp32 columns -> bf16
-        __nv_bfloat16 *dst = a.dv + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDv;
+        const size_t vrow = static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh;
+        __nv_bfloat16 *dst = a.dv + vrow * kDv;
+        const bool st_ok = kvalid && SA_OUT(vrow, static_cast<int64_t>(a.total) * a.Hkv, 0x35);
 #pragma unroll 1
         for (int32_t cb = 0; cb < kDv; cb += 32) {
           uint32_t r[32];
           tmem_ld32p(lane_t + kColV + cb, r);
           tmem_wait_ld();
           reg_fence<32>(r);
-          if (kvalid) {
+          if (st_ok) {
 #pragma unroll
             for (int32_t e = 0; e < 32; e += 8) {
               const float *f = reinterpret_cast<const float *>(r + e);
@@ -964,8 +972,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       } else {
+        const size_t krow = static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh;
         bwd_store_qk_row(lane_t + kColK, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
-                         a.dk + (static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh) * kDqk, kvalid);
+                         a.dk + krow * kDqk,
+                         kvalid && SA_OUT(krow, static_cast<int64_t>(a.total) * a.Hkv, 0x36));
       }
       tc_fence_before();
       g0 += cur.nsub;

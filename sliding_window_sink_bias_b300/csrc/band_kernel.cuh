@@ -54,6 +54,7 @@ struct BandArgs {
   const float *sink;
   __nv_bfloat16 *out;
   float *lse;
+  int64_t n_rows;       // rows of out and lse: tokens x Hq (checked stores)
   unsigned long long rope_turns[32];
 };
 
@@ -402,6 +403,7 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
 #pragma unroll
         for (int32_t pq = 0; pq < 4; ++pq) {
           uint32_t (&sec)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8 * pq);
+          if (!SA_OUT(p_orow - q + pq, args.n_rows, 0x11)) continue;
           if (args.out_v8) {
             st_global_v8(row0 + pq * kDv, sec);
           } else {
@@ -411,7 +413,8 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
           }
         }
       }
-      if (p_valid && half == 0) args.lse[p_orow] = l > 0.f ? (p_m + __log2f(l)) * kLn2 : -INFINITY;
+      if (p_valid && half == 0 && SA_OUT(p_orow, args.n_rows, 0x12))
+        args.lse[p_orow] = l > 0.f ? (p_m + __log2f(l)) * kLn2 : -INFINITY;
     }
     if (!have) break;
     p_valid = rvalid;

@@ -53,6 +53,7 @@ struct CausalArgs {
   const float *sink;
   __nv_bfloat16 *out;
   float *lse;
+  int64_t n_rows;       // rows of out and lse: tokens x Hq (checked stores)
   unsigned long long rope_turns[32];
 };
 
@@ -276,6 +277,7 @@ __device__ __forceinline__ void cau_softmax(const CausalArgs &args, int32_t X, u
 #pragma unroll
         for (int32_t pq = 0; pq < 4; ++pq) {
           uint32_t (&sec)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8 * pq);
+          if (!SA_OUT(orow - q + pq, args.n_rows, 0x13)) continue;
           if (args.out_v8) {
             st_global_v8(row0 + pq * kDv, sec);
           } else {
@@ -286,7 +288,7 @@ __device__ __forceinline__ void cau_softmax(const CausalArgs &args, int32_t X, u
         }
       }
     }
-    if (rvalid) args.lse[orow] = lse_v;
+    if (rvalid && SA_OUT(orow, args.n_rows, 0x14)) args.lse[orow] = lse_v;
     ++gi;
   }
 }

@@ -25,9 +25,6 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;        // 4 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;        // 0.2 s to drain after an abort
 
-// Device status word: bit 0 = a wait timed out; bits 8..15 = the wait site.
-__device__ uint32_t g_status_word;
-
 // Bounded mbarrier wait, slow path: the timed loop.  Returns false if this CTA
 // is aborting (another wait gave up) or this wait runs past limit_ns, which
 // then records SINKATTN_ETIMEOUT and the site in the status word and sets the
@@ -43,7 +40,7 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity,
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
-      atomicOr(&g_status_word, 1u | (site << 8));
+      status_record(1u, site, 8);
       return false;
     }
   }
@@ -80,7 +77,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kDrainLimitNs) {
-      atomicOr(&g_status_word, 1u | (0xFFu << 8));
+      status_record(1u, 0xFFu, 8);
       return;
     }
   }

@@ -79,6 +79,8 @@ struct DecArgs {
   unsigned long long epoch;
   float *part_o;          // [gridDim.x * 2, R, 128] unnormalised O
   float *part_ml;         // [gridDim.x * 2, R, 4] (m, l, 0, 0), log2 domain
+  int64_t n_rows;         // rows of out and lse: B x T x Hq (checked stores)
+  int64_t n_part_rows;    // rows the partial buffers hold (checked accesses)
   unsigned long long rope_turns[32];
 };
 
@@ -143,6 +145,7 @@ __device__ void dec_write_empty_unit(const DecArgs &a, int32_t u, int32_t lane) 
   for (int32_t r = 0; r < a.R; ++r) {
     const int32_t head = kvh * a.G + r % a.G;
     const size_t orow = (static_cast<size_t>(b) * a.T + r / a.G) * a.Hq + head;
+    if (!SA_OUT(orow, a.n_rows, 0x20)) continue;
     reinterpret_cast<uint2 *>(a.out + orow * kDv)[lane] = make_uint2(0u, 0u);
     if (lane == 0) a.lse[orow] = __ldg(a.sink + head);
   }
@@ -236,7 +239,7 @@ __device__ __forceinline__ bool dec_ticket_arrive(unsigned long long *t, unsigne
     if (prev == cur) return static_cast<uint32_t>(want & 0xFFFFull) == n;
     cur = prev;
   }
-  atomicOr(&g_status_word, 1u | (0xFDu << 8));
+  status_record(1u, 0xFDu, 8);
   return false;
 }
 
@@ -872,13 +875,15 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
         scale_o *= vs;
         const size_t orow = (static_cast<size_t>(sg.b) * args.T + t) * args.Hq + head;
         const size_t prow = (static_cast<size_t>(blockIdx.x) * 2 + (sg.first ? 0 : 1)) * R + row;
+        const bool st_ok = row < R && (whole_unit ? SA_OUT(orow, args.n_rows, 0x21)
+                                                  : SA_IN(prow, args.n_part_rows, 0x22));
 #pragma unroll 1
         for (int32_t cb = 0; cb < kDv; cb += 32) {
           uint32_t o[32];
           tmem_ld32p(o_t + cb, o);
           tmem_wait_ld();
           reg_fence<32>(o);
-          if (row < R) {
+          if (st_ok) {
             if (whole_unit) {
               uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv + cb);
 #pragma unroll
@@ -899,7 +904,7 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
             }
           }
         }
-        if (row < R) {
+        if (st_ok) {
           if (whole_unit)
             args.lse[orow] = lse_v;
           else
@@ -925,7 +930,9 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
           // (no early exit here: the whole warp meets again in the wait below;
           // an aborted CTA merges nothing)
           const bool all_out = wait_bar(B_PARTOUT, gcut & 1, abort_flag, 14);
-          *last_flag = all_out && dec_ticket_arrive(args.tickets + sg.u, args.epoch, n_part) ? 1 : 0;
+          *last_flag = all_out && SA_IN(sg.u, args.n_units, 0x23) &&
+                               dec_ticket_arrive(args.tickets + sg.u, args.epoch, n_part)
+                           ? 1 : 0;
           mbar_arrive(B_LASTKNOWN);
         }
         if (!(ok = wait_bar_warp(B_LASTKNOWN, gcut & 1, abort_flag, 15))) break;
@@ -947,6 +954,11 @@ __global__ void __launch_bounds__(DecThreads<F8>::kAll, 1)
               const size_t cta = static_cast<size_t>(i) * args.n_sub + sl;
               return (cta * 2 + ((i == c_first && Tb * i / n_grp < F0) ? 1 : 0)) * R + r;
             };
+            if (!SA_OUT(orow, args.n_rows, 0x24)) continue;
+            // (checking builds: every partial row the merge reads is in the buffer)
+            if (!(SA_IN(prow_of(c_first), args.n_part_rows, 0x25) &&
+                  SA_IN(prow_of(c_last), args.n_part_rows, 0x25)))
+              continue;
             const float sk_raw = __ldg(args.sink + head);
             const float sk2 = sk_raw == -INFINITY ? -INFINITY : sk_raw * kLog2e;
             float M = sk2;

@@ -146,6 +146,7 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
   b.sink = a.sink;
   b.out = a.out;
   b.lse = a.lse;
+  b.n_rows = a.n_rows;
   std::memcpy(b.rope_turns, a.rope_turns, sizeof b.rope_turns);
   // upper bound of the tile count: sum_b ceil(L_b / 16) <= (total + 15 * batch) / 16
   const int64_t tiles = int64_t(a.Hkv) * ((int64_t(total) + 15 * int64_t(batch)) / sa::kBandSeg);
@@ -190,6 +191,7 @@ sinkattn_status launch_causal(const void *q, const void *k, const void *v, const
   c.sink = a.sink;
   c.out = a.out;
   c.lse = a.lse;
+  c.n_rows = a.n_rows;
   std::memcpy(c.rope_turns, a.rope_turns, sizeof c.rope_turns);
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, a.Hq, total, a.G, c.T) ||
@@ -397,6 +399,7 @@ const char *sinkattn_status_string(sinkattn_status s) {
     case SINKATTN_EWORKSPACE: return "workspace missing or too small";
     case SINKATTN_ECUDA: return "CUDA error";
     case SINKATTN_ETIMEOUT: return "kernel wait timed out";
+    case SINKATTN_ECHECK: return "bounds check failed (checking build)";
   }
   return "unknown status";
 }
@@ -410,7 +413,8 @@ sinkattn_status sinkattn_get_device_status(uint32_t *detail) {
   if (cudaMemcpyToSymbol(sa::g_status_word, &zero, sizeof zero) != cudaSuccess)
     return SINKATTN_ECUDA;
   if (detail) *detail = word;
-  return (word & 1u) ? SINKATTN_ETIMEOUT : SINKATTN_OK;
+  if (word & 1u) return SINKATTN_ETIMEOUT;
+  return (word & 2u) ? SINKATTN_ECHECK : SINKATTN_OK;
 }
 
 sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v, const float *sink,
@@ -454,6 +458,7 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
   a.sink = sink;
   a.out = static_cast<__nv_bfloat16 *>(out);
   a.lse = lse;
+  a.n_rows = int64_t(total) * num_q_heads;
 
   DeviceInfo dev;
   if (!device_info(dev)) return SINKATTN_ECUDA;
@@ -582,6 +587,8 @@ static sinkattn_status decode_impl(const void *q, const void *kcache, const void
   d.epoch = next_decode_epoch();
   d.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.tab_bytes);
   d.part_ml = d.part_o + static_cast<size_t>(sa::kDecMaxGrid) * 2 * plan.rows * sa::kDv;
+  d.n_rows = int64_t(batch) * T * num_q_heads;
+  d.n_part_rows = int64_t(sa::kDecMaxGrid) * 2 * plan.rows;
   std::memcpy(d.rope_turns, a.rope_turns, sizeof d.rope_turns);
 
   DeviceInfo dev;
@@ -730,5 +737,19 @@ extern "C" sinkattn_status sinkattn_decode_noalloc(
 // Test builds only: see sa::g_test_stall_ns.  0 turns the stall off.
 extern "C" int sinkattn_test_set_stall_ns(uint64_t ns) {
   return cudaMemcpyToSymbol(sa::g_test_stall_ns, &ns, sizeof ns) == cudaSuccess ? 0 : 1;
+}
+#endif
+
+#ifdef SINKATTN_CHECKS
+// Checking builds only: make the checks see every tensor as `row_shrink` rows
+// (or elements) shorter and admit only `tmem_cols` TMEM columns, so a test can
+// see them fire without any access actually out of bounds.  (0, 512) restores
+// the true limits.
+extern "C" int sinkattn_test_set_check_limits(int64_t row_shrink, uint32_t tmem_cols) {
+  if (row_shrink < 0 || tmem_cols > 512) return 1;
+  if (cudaMemcpyToSymbol(sa::g_check_row_shrink, &row_shrink, sizeof row_shrink) != cudaSuccess)
+    return 1;
+  return cudaMemcpyToSymbol(sa::g_check_tmem_cols, &tmem_cols, sizeof tmem_cols) == cudaSuccess
+             ? 0 : 1;
 }
 #endif
