@@ -54,13 +54,14 @@ struct BwdArgs {
   const float *sink;
   const __nv_bfloat16 *q, *k, *out, *dout;
   const float *lse;
-  __nv_bfloat16 *q_rot, *k_rot;
+  __nv_bfloat16 *q_rot, *k_rot;  // rotated dims 0..63: [total, Hq, 64], [total, Hkv, 64]
   float *D, *dsink_part;
   int32_t n_chunks;
   __nv_bfloat16 *dq, *dk, *dv;
   float *dsink;
   int32_t dq_tiles, dq_items;   // tiles per sequence (virtual, of 128/G tokens), items
   int32_t kv_blocks, kv_items;  // key blocks per sequence (virtual), items
+  int32_t grad_v8;              // dq, dk, dv 32-byte aligned (whole-sector stores)
   unsigned long long rope_turns[32];
 };
 
@@ -76,7 +77,9 @@ __device__ __forceinline__ int32_t bwd_seq_of(const BwdArgs &a, int32_t tok) {
 
 // ------------------------------------------------------------------ pre-pass
 // One warp per token (chunk of kBwdChunk tokens per CTA, 256 threads).  Lane l
-// owns rotary pair l (dims (2l, 2l+1) or (l, l+32)) and dims 64+4l..64+4l+3.
+// owns rotary pair l (dims (2l, 2l+1) or (l, l+32)).  Only the 64 rotated dims
+// of q and k are written out (the MMA kernels read dims 64..191 from q and k
+// themselves); without RoPE nothing is.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
   __shared__ float sD[kBwdChunk][64];  // D of the chunk's tokens (heads < 64 cached here)
   const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,47 +89,37 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
     if (tok >= a.total) break;
     const int32_t b = bwd_seq_of(a, tok);
     const int32_t pos = tok - __ldg(a.cu_seqlens + b);
-    float c = 1.f, s = 0.f;
-    if (a.rope_on) rope_cs(pos, a.rope_turns[lane], c, s);
-    const int32_t ia = a.rope_style == 0 ? 2 * lane : lane;
-    const int32_t ib = a.rope_style == 0 ? 2 * lane + 1 : lane + 32;
-    // rotated copies: q (Hq heads) then k (Hkv heads), in 16-byte units (24 a
-    // row).  Pairs (2t, 2t+1): unit c < 8 of a row holds pairs 4c..4c+3,
-    // whose angles this warp's lanes 4c..4c+3 computed above.
-    if (a.rope_style == 0) {
-      const int32_t nunit = (a.Hq + a.Hkv) * 24;
-      // the trip count is the same for every lane (the shuffles need all 32)
-#pragma unroll 2
-      for (int32_t j0 = 0; j0 < nunit; j0 += 32) {
-        const int32_t j = j0 + lane;
-        const bool act = j < nunit;
-        const int32_t hh = j / 24, cc = j % 24;
+    if (a.rope_on && a.rope_style == 0) {
+      float c, s;
+      rope_cs(pos, a.rope_turns[lane], c, s);
+      // rotated rows: q (Hq heads) then k (Hkv heads), in 16-byte units (8 a
+      // row).  Pairs (2t, 2t+1): unit c of a row holds pairs 4c..4c+3, whose
+      // angles lanes 4c..4c+3 computed above; lane l works on unit l % 8, so
+      // it fetches the same four angles in every round.
+      const int32_t cc = lane & 7;
+      const float c0 = __shfl_sync(0xffffffffu, c, 4 * cc), s0 = __shfl_sync(0xffffffffu, s, 4 * cc);
+      const float c1 = __shfl_sync(0xffffffffu, c, 4 * cc + 1), s1 = __shfl_sync(0xffffffffu, s, 4 * cc + 1);
+      const float c2 = __shfl_sync(0xffffffffu, c, 4 * cc + 2), s2 = __shfl_sync(0xffffffffu, s, 4 * cc + 2);
+      const float c3 = __shfl_sync(0xffffffffu, c, 4 * cc + 3), s3 = __shfl_sync(0xffffffffu, s, 4 * cc + 3);
+      const int32_t nunit = (a.Hq + a.Hkv) * 8;
+#pragma unroll 4
+      for (int32_t j = lane; j < nunit; j += 32) {
+        const int32_t hh = j >> 3;
         const bool isq = hh < a.Hq;
         const size_t row = isq ? static_cast<size_t>(tok) * a.Hq + hh
                                : static_cast<size_t>(tok) * a.Hkv + (hh - a.Hq);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (act) v = *reinterpret_cast<const uint4 *>((isq ? a.q : a.k) + row * kDqk + 8 * cc);
-        // every lane takes part in the shuffles; only units of box 0 rotate
-        const int32_t src_lane = cc < 8 ? 4 * cc : 0;
-        const float c0 = __shfl_sync(0xffffffffu, c, src_lane & 31);
-        const float s0 = __shfl_sync(0xffffffffu, s, src_lane & 31);
-        const float c1 = __shfl_sync(0xffffffffu, c, (src_lane + 1) & 31);
-        const float s1 = __shfl_sync(0xffffffffu, s, (src_lane + 1) & 31);
-        const float c2 = __shfl_sync(0xffffffffu, c, (src_lane + 2) & 31);
-        const float s2 = __shfl_sync(0xffffffffu, s, (src_lane + 2) & 31);
-        const float c3 = __shfl_sync(0xffffffffu, c, (src_lane + 3) & 31);
-        const float s3 = __shfl_sync(0xffffffffu, s, (src_lane + 3) & 31);
-        if (cc < 8) {
-          v.x = pack_bf16x2(bf16lo(v.x) * c0 - bf16hi(v.x) * s0, bf16lo(v.x) * s0 + bf16hi(v.x) * c0);
-          v.y = pack_bf16x2(bf16lo(v.y) * c1 - bf16hi(v.y) * s1, bf16lo(v.y) * s1 + bf16hi(v.y) * c1);
-          v.z = pack_bf16x2(bf16lo(v.z) * c2 - bf16hi(v.z) * s2, bf16lo(v.z) * s2 + bf16hi(v.z) * c2);
-          v.w = pack_bf16x2(bf16lo(v.w) * c3 - bf16hi(v.w) * s3, bf16lo(v.w) * s3 + bf16hi(v.w) * c3);
-        }
-        if (act && SA_IN(row, static_cast<int64_t>(a.total) * (isq ? a.Hq : a.Hkv), 0x30))
-          *reinterpret_cast<uint4 *>((isq ? a.q_rot : a.k_rot) + row * kDqk + 8 * cc) = v;
+        uint4 v = *reinterpret_cast<const uint4 *>((isq ? a.q : a.k) + row * kDqk + 8 * cc);
+        v.x = pack_bf16x2(bf16lo(v.x) * c0 - bf16hi(v.x) * s0, bf16lo(v.x) * s0 + bf16hi(v.x) * c0);
+        v.y = pack_bf16x2(bf16lo(v.y) * c1 - bf16hi(v.y) * s1, bf16lo(v.y) * s1 + bf16hi(v.y) * c1);
+        v.z = pack_bf16x2(bf16lo(v.z) * c2 - bf16hi(v.z) * s2, bf16lo(v.z) * s2 + bf16hi(v.z) * c2);
+        v.w = pack_bf16x2(bf16lo(v.w) * c3 - bf16hi(v.w) * s3, bf16lo(v.w) * s3 + bf16hi(v.w) * c3);
+        if (SA_IN(row, static_cast<int64_t>(a.total) * (isq ? a.Hq : a.Hkv), 0x30))
+          *reinterpret_cast<uint4 *>((isq ? a.q_rot : a.k_rot) + row * 64 + 8 * cc) = v;
       }
-    } else {
+    } else if (a.rope_on) {
       // pairs (t, t + 32): lane t holds pair t of every row
+      float c, s;
+      rope_cs(pos, a.rope_turns[lane], c, s);
 #pragma unroll 4
       for (int32_t hh = 0; hh < a.Hq + a.Hkv; ++hh) {
         const bool isq = hh < a.Hq;
@@ -134,12 +127,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
                                : static_cast<size_t>(tok) * a.Hkv + (hh - a.Hq);
         if (!SA_IN(row, static_cast<int64_t>(a.total) * (isq ? a.Hq : a.Hkv), 0x30)) continue;
         const __nv_bfloat16 *src = (isq ? a.q : a.k) + row * kDqk;
-        __nv_bfloat16 *dst = (isq ? a.q_rot : a.k_rot) + row * kDqk;
-        const float x = __bfloat162float(src[ia]), y = __bfloat162float(src[ib]);
-        dst[ia] = __float2bfloat16_rn(x * c - y * s);
-        dst[ib] = __float2bfloat16_rn(x * s + y * c);
-        *reinterpret_cast<uint2 *>(dst + 64 + 4 * lane) =
-            *reinterpret_cast<const uint2 *>(src + 64 + 4 * lane);
+        __nv_bfloat16 *dst = (isq ? a.q_rot : a.k_rot) + row * 64;
+        const float x = __bfloat162float(src[lane]), y = __bfloat162float(src[lane + 32]);
+        dst[lane] = __float2bfloat16_rn(x * c - y * s);
+        dst[lane + 32] = __float2bfloat16_rn(x * s + y * c);
       }
     }
     // D = dO . o per head: four lanes a head (32 dims each, 16-byte loads),
@@ -238,49 +229,73 @@ __device__ __forceinline__ void bwd_unrotate(float (&x)[64], int32_t pos, int32_
   }
 }
 
-// Row epilogue shared by the gradients of q and k: 192 fp32 columns of TMEM at
-// col (this thread's lane) -> * scale, inverse RoPE on dims 0..63, bf16 row.
-// Part 0 writes dims 0..95, part 1 dims 96..191 (the two threads of a row
-// share the epilogue); part -1 writes all of it.
-__device__ __forceinline__ void bwd_store_qk_row(uint32_t t_col, float scale, bool rope_on,
-                                                 int32_t style, int32_t pos,
-                                                 const unsigned long long *turns,
-                                                 __nv_bfloat16 *dst, bool valid, int32_t part = -1) {
-  if (part != 1) {
+// Gradient epilogues write 64-dim lines (128 bytes) of rows.  The four threads
+// of a lane quad hold the same line of four rows, as 32 packed bf16 pairs each
+// (w[8 s .. 8 s + 7] = sector s, 16 dims).  A 4 x 4 exchange of sectors inside
+// the quad leaves in thread q sector q of rows 0..3 of the quad, so store j of
+// the quad writes the whole line of row j: every store instruction moves whole
+// 128-byte lines instead of a 16-byte piece of 32 lines.  All 32 lanes take
+// part (the exchange is a warp shuffle); `line(j)` gives where row j's line
+// starts, or null for a row that is not written.
+template <class LineOf>
+__device__ __forceinline__ void bwd_store_line_quad(uint32_t (&w)[32], LineOf line, bool v8) {
+  const int32_t q = threadIdx.x & 3;
+#pragma unroll
+  for (int32_t j = 0; j < 2; ++j) {  // partner q ^ 2: sectors {0,1} <-> {2,3}
+#pragma unroll
+    for (int32_t e = 0; e < 8; ++e) {
+      const uint32_t send = (q & 2) ? w[8 * j + e] : w[8 * (j + 2) + e];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+      if (q & 2) w[8 * j + e] = recv; else w[8 * (j + 2) + e] = recv;
+    }
+  }
+#pragma unroll
+  for (int32_t j = 0; j < 4; j += 2) {  // partner q ^ 1: positions j <-> j + 1
+#pragma unroll
+    for (int32_t e = 0; e < 8; ++e) {
+      const uint32_t send = (q & 1) ? w[8 * j + e] : w[8 * (j + 1) + e];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+      if (q & 1) w[8 * j + e] = recv; else w[8 * (j + 1) + e] = recv;
+    }
+  }
+#pragma unroll
+  for (int32_t j = 0; j < 4; ++j) {
+    __nv_bfloat16 *dst = line(j);
+    if (dst == nullptr) continue;
+    uint32_t (&sec)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8 * j);
+    if (v8) {
+      st_global_v8(dst + 16 * q, sec);
+    } else {
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + 16 * q);
+      d4[0] = make_uint4(sec[0], sec[1], sec[2], sec[3]);
+      d4[1] = make_uint4(sec[4], sec[5], sec[6], sec[7]);
+    }
+  }
+}
+
+// Lines [l0, l0 + nl) of a gradient row held in TMEM from column t_col (fp32,
+// this thread's lane): * scale, inverse RoPE on line 0 (dims 0..63, at
+// position pos) when rope_on, bf16, stored through bwd_store_line_quad.
+template <class LineOf>
+__device__ __forceinline__ void bwd_store_lines(uint32_t t_col, int32_t l0, int32_t nl, float scale,
+                                                bool rope_on, int32_t style, int32_t pos,
+                                                const unsigned long long *turns, LineOf line,
+                                                bool v8) {
+#pragma unroll 1
+  for (int32_t l = l0; l < l0 + nl; ++l) {
     uint32_t r[64];
-    tmem_ld32p(t_col, r);
-    tmem_ld32p(t_col + 32, r + 32);
+    tmem_ld32p(t_col + 64 * l, r);
+    tmem_ld32p(t_col + 64 * l + 32, r + 32);
     tmem_wait_ld();
     reg_fence<64>(r);
     float x[64];
 #pragma unroll
     for (int32_t e = 0; e < 64; ++e) x[e] = __uint_as_float(r[e]) * scale;
-    if (rope_on) bwd_unrotate(x, pos, style, turns);
-    if (valid) {
+    if (l == 0 && rope_on) bwd_unrotate(x, pos, style, turns);
+    uint32_t w[32];
 #pragma unroll
-      for (int32_t e = 0; e < 64; e += 8) {
-        *reinterpret_cast<uint4 *>(dst + e) =
-            make_uint4(pack_bf16x2(x[e], x[e + 1]), pack_bf16x2(x[e + 2], x[e + 3]),
-                       pack_bf16x2(x[e + 4], x[e + 5]), pack_bf16x2(x[e + 6], x[e + 7]));
-      }
-    }
-  }
-  const int32_t cb0 = part == 1 ? 96 : 64, cb1 = part == 0 ? 96 : 192;
-#pragma unroll 1
-  for (int32_t cb = cb0; cb < cb1; cb += 32) {
-    uint32_t r[32];
-    tmem_ld32p(t_col + cb, r);
-    tmem_wait_ld();
-    reg_fence<32>(r);
-    if (valid) {
-#pragma unroll
-      for (int32_t e = 0; e < 32; e += 8) {
-        const float *f = reinterpret_cast<const float *>(r + e);
-        *reinterpret_cast<uint4 *>(dst + cb + e) =
-            make_uint4(pack_bf16x2(f[0] * scale, f[1] * scale), pack_bf16x2(f[2] * scale, f[3] * scale),
-                       pack_bf16x2(f[4] * scale, f[5] * scale), pack_bf16x2(f[6] * scale, f[7] * scale));
-      }
-    }
+    for (int32_t e = 0; e < 32; ++e) w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+    bwd_store_line_quad(w, [&](int32_t j) { return line(j, l); }, v8);
   }
 }
 
@@ -360,8 +375,9 @@ constexpr uint32_t kDqColAcc = 256;
 // completes per block could find it two phases behind (its parity would then
 // match at once).
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q0,
+                  const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_k0, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ BwdArgs a) {
   using Ly = DqLayout;
   constexpr int32_t NS = Ly::kStages;
@@ -401,8 +417,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_q0);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_k0);
     tma_prefetch_desc(&tm_v);
   }
   if (warp == 0) {
@@ -424,7 +442,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(B_QF, 5 * Ly::kQBox);
 #pragma unroll
       for (int cc = 0; cc < 3; ++cc)
-        tma_load_3d(sbase + Ly::kQOff + cc * Ly::kQBox, &tm_q, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
+        tma_load_3d(sbase + Ly::kQOff + cc * Ly::kQBox, cc ? &tm_q : &tm_q0, cc * 64, d.kvh * G,
+                    d.s0 + d.t0, B_QF);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(sbase + Ly::kDoOff + cc * Ly::kQBox, &tm_do, cc * 64, d.kvh * G, d.s0 + d.t0, B_QF);
@@ -441,7 +460,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int32_t krow = ld.s0 + ld.lo + ld_j * kDqBN;
       mbar_arrive_expect_tx(B_KV(st), Ly::kStage);
 #pragma unroll
-      for (int cc = 0; cc < 3; ++cc) tma_load_3d(dst + cc * Ly::kKBox, &tm_k, cc * 64, ld.kvh, krow, B_KV(st));
+      for (int cc = 0; cc < 3; ++cc)
+        tma_load_3d(dst + cc * Ly::kKBox, cc ? &tm_k : &tm_k0, cc * 64, ld.kvh, krow, B_KV(st));
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(dst + (3 + cc) * Ly::kKBox, &tm_v, cc * 64, ld.kvh, krow, B_KV(st));
@@ -532,16 +552,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ============================================================ rows
     const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const int32_t t_row = row / G, g_row = row % G;
+    // this row's lse (log2 domain) and D in an item; loaded one item ahead,
+    // before the epilogue, so they are in by the next item's first dS
+    auto fetch_rows = [&](const DqItem &d, float &l2, float &dd) {
+      const int32_t ti = d.t0 + t_row;
+      const size_t grow = static_cast<size_t>(d.s0 + ti) * a.Hq + d.kvh * G + g_row;
+      l2 = ti < d.L ? __ldg(a.lse + grow) * kLog2e : 0.f;
+      dd = ti < d.L ? __ldg(a.D + grow) : 0.f;
+    };
     DqItem cur;
     int32_t it = dq_next_item(a, blockIdx.x, cur);
+    float lse2 = 0.f, Drow = 0.f;
+    if (cur.valid) fetch_rows(cur, lse2, Drow);
     uint32_t g0 = 0, k = 0;
     bool ok = true;
     while (ok && cur.valid) {
-      const int32_t ti = cur.t0 + t_row, h = cur.kvh * G + g_row;
+      const int32_t ti = cur.t0 + t_row;
       const bool rvalid = ti < cur.L;  // both halves of the row
-      const size_t grow = static_cast<size_t>(cur.s0 + ti) * a.Hq + h;
-      const float lse2 = rvalid ? __ldg(a.lse + grow) * kLog2e : 0.f;
-      const float Drow = rvalid ? __ldg(a.D + grow) : 0.f;
       for (int32_t j = 0; j < cur.nblk; ++j) {
         const uint32_t g = g0 + j;
         // S(g), dP(g) complete
@@ -577,16 +604,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(B_DSR(g & 1));
       }
       if (!ok) break;
+      DqItem nxt;
+      const int32_t it_n = dq_next_item(a, it + gridDim.x, nxt);
+      float lse2_n = 0.f, D_n = 0.f;
+      if (nxt.valid) fetch_rows(nxt, lse2_n, D_n);
       // the item's last dQ complete
       if (!(ok = wait_bar_warp(B_ACCF, k & 1, abort_flag, 24))) break;
       tc_fence_after();
-      bwd_store_qk_row(lane_t + kDqColAcc, a.scale, a.rope_on, a.rope_style, ti, a.rope_turns,
-                       a.dq + grow * kDqk,
-                       rvalid && SA_OUT(grow, static_cast<int64_t>(a.total) * a.Hq, 0x34), half);
+      // dQ rows: line 0 (inverse RoPE) by the first thread of a row, lines 1
+      // and 2 by the second
+      const int32_t quad0 = row & ~3;
+      auto line = [&](int32_t j, int32_t l) -> __nv_bfloat16 * {
+        const int32_t r = quad0 + j, tj = cur.t0 + r / G;
+        const size_t gr = static_cast<size_t>(cur.s0 + tj) * a.Hq + cur.kvh * G + r % G;
+        if (tj >= cur.L || !SA_OUT(gr, static_cast<int64_t>(a.total) * a.Hq, 0x34)) return nullptr;
+        return a.dq + gr * kDqk + 64 * l;
+      };
+      bwd_store_lines(lane_t + kDqColAcc, half == 0 ? 0 : 1, half == 0 ? 1 : 2, a.scale, a.rope_on,
+                      a.rope_style, ti, a.rope_turns, line, a.grad_v8 != 0);
       tc_fence_before();
       g0 += cur.nblk;
       ++k;
-      it = dq_next_item(a, it + gridDim.x, cur);
+      cur = nxt;
+      it = it_n;
+      lse2 = lse2_n;
+      Drow = D_n;
     }
   }
   tc_fence_before();
@@ -672,8 +714,9 @@ static_assert(KvLayout::kDynSmem <= 232448, "dkdv kernel shared memory");
 // KV_EMPTY and ACC_FULL complete once per item, so no wait can find its
 // barrier two phases away from the awaited one.
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q0,
+                    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_k0, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ BwdArgs a) {
   using Ly = KvLayout;
   constexpr int32_t NS = Ly::kStages;
@@ -716,8 +759,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_q0);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_k0);
     tma_prefetch_desc(&tm_v);
   }
   if (warp == 0) {
@@ -745,7 +790,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(B_KF, 5 * Ly::kKBox);
 #pragma unroll
       for (int cc = 0; cc < 3; ++cc)
-        tma_load_3d(sbase + Ly::kKOff + cc * Ly::kKBox, &tm_k, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
+        tma_load_3d(sbase + Ly::kKOff + cc * Ly::kKBox, cc ? &tm_k : &tm_k0, cc * 64, d.kvh,
+                    d.s0 + d.k0, B_KF);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(sbase + Ly::kVOff + cc * Ly::kKBox, &tm_v, cc * 64, d.kvh, d.s0 + d.k0, B_KF);
@@ -767,7 +813,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(B_QS(st), Ly::kStage);
 #pragma unroll
       for (int cc = 0; cc < 3; ++cc)
-        tma_load_3d(dst + cc * Ly::kQBox, &tm_q, cc * 64, ld.kvh * G, tok, B_QS(st));
+        tma_load_3d(dst + cc * Ly::kQBox, cc ? &tm_q : &tm_q0, cc * 64, ld.kvh * G, tok, B_QS(st));
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
         tma_load_3d(dst + (3 + cc) * Ly::kQBox, &tm_do, cc * 64, ld.kvh * G, tok, B_QS(st));
@@ -950,32 +996,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // the item's last dV/dK complete
       if (!(ok = wait_bar_warp(B_ACCF, k & 1, abort_flag, 28))) break;
       tc_fence_after();
+      // dV rows (lines 0, 1) and line 2 of the dK rows by the first thread of
+      // a key, dK lines 0 (inverse RoPE) and 1 by the second
+      const int32_t quad0 = lane_row & ~3;
+      auto kv_row = [&](int32_t j, int64_t &r) {
+        const int32_t kk = cur.k0 + quad0 + j;
+        r = static_cast<int64_t>(cur.s0 + kk) * a.Hkv + cur.kvh;
+        return kk < cur.L;
+      };
+      auto dv_line = [&](int32_t j, int32_t l) -> __nv_bfloat16 * {
+        int64_t r;
+        if (!kv_row(j, r) || !SA_OUT(r, static_cast<int64_t>(a.total) * a.Hkv, 0x35)) return nullptr;
+        return a.dv + r * kDv + 64 * l;
+      };
+      auto dk_line = [&](int32_t j, int32_t l) -> __nv_bfloat16 * {
+        int64_t r;
+        if (!kv_row(j, r) || !SA_OUT(r, static_cast<int64_t>(a.total) * a.Hkv, 0x36)) return nullptr;
+        return a.dk + r * kDqk + 64 * l;
+      };
       if (half == 0) {
-        // dV row: 128 fp32 columns -> bf16
-        const size_t vrow = static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh;
-        __nv_bfloat16 *dst = a.dv + vrow * kDv;
-        const bool st_ok = kvalid && SA_OUT(vrow, static_cast<int64_t>(a.total) * a.Hkv, 0x35);
-#pragma unroll 1
-        for (int32_t cb = 0; cb < kDv; cb += 32) {
-          uint32_t r[32];
-          tmem_ld32p(lane_t + kColV + cb, r);
-          tmem_wait_ld();
-          reg_fence<32>(r);
-          if (st_ok) {
-#pragma unroll
-            for (int32_t e = 0; e < 32; e += 8) {
-              const float *f = reinterpret_cast<const float *>(r + e);
-              *reinterpret_cast<uint4 *>(dst + cb + e) =
-                  make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                             pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-            }
-          }
-        }
+        bwd_store_lines(lane_t + kColV, 0, 2, 1.f, false, 0, 0, a.rope_turns, dv_line,
+                        a.grad_v8 != 0);
+        bwd_store_lines(lane_t + kColK, 2, 1, a.scale, false, 0, 0, a.rope_turns, dk_line,
+                        a.grad_v8 != 0);
       } else {
-        const size_t krow = static_cast<size_t>(cur.s0 + kj) * a.Hkv + cur.kvh;
-        bwd_store_qk_row(lane_t + kColK, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
-                         a.dk + krow * kDqk,
-                         kvalid && SA_OUT(krow, static_cast<int64_t>(a.total) * a.Hkv, 0x36));
+        bwd_store_lines(lane_t + kColK, 0, 2, a.scale, a.rope_on, a.rope_style, kj, a.rope_turns,
+                        dk_line, a.grad_v8 != 0);
       }
       tc_fence_before();
       g0 += cur.nsub;

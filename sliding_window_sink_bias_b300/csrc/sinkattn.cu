@@ -245,7 +245,8 @@ extern "C" {
 int32_t sinkattn_version(void) { return kVersion; }
 
 // ----------------------------------------------------------------- backward
-// Workspace: q_rot bf16 [total, Hq, 192], k_rot bf16 [total, Hkv, 192],
+// Workspace: the rotated dims 0..63 of q and k, bf16 [total, Hq, 64] and
+// [total, Hkv, 64],
 // D fp32 [total, Hq], per-chunk sink-gradient partials fp32 [chunks, Hq];
 // each region starts on 256 bytes.
 struct BwdPlan {
@@ -258,8 +259,8 @@ BwdPlan bwd_plan(int64_t total, int32_t hq, int32_t hkv) {
   BwdPlan p;
   p.chunks = static_cast<int32_t>((total + sa::kBwdChunk - 1) / sa::kBwdChunk);
   p.q_rot = 0;
-  p.k_rot = p.q_rot + up(static_cast<size_t>(total) * hq * 192 * 2);
-  p.D = p.k_rot + up(static_cast<size_t>(total) * hkv * 192 * 2);
+  p.k_rot = p.q_rot + up(static_cast<size_t>(total) * hq * 64 * 2);
+  p.D = p.k_rot + up(static_cast<size_t>(total) * hkv * 64 * 2);
   p.part = p.D + up(static_cast<size_t>(total) * hq * 4);
   p.bytes = p.part + up(static_cast<size_t>(p.chunks > 0 ? p.chunks : 1) * hq * 4);
   return p;
@@ -345,6 +346,7 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
   b.dq_items = static_cast<int32_t>(int64_t(batch) * num_kv_heads * dq_tiles);
   b.kv_blocks = static_cast<int32_t>(kv_blocks);
   b.kv_items = static_cast<int32_t>(int64_t(batch) * num_kv_heads * kv_blocks);
+  b.grad_v8 = aligned(dq, 32) && aligned(dk, 32) && aligned(dv, 32) ? 1 : 0;
   std::memcpy(b.rope_turns, a.rope_turns, sizeof b.rope_turns);
 
   DeviceInfo dev;
@@ -357,11 +359,24 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
   sa::bwd_dsink_kernel<<<static_cast<unsigned>(num_q_heads), 256, 0, s>>>(b);
   if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
 
-  CUtensorMap mq, mdo, mk, mv;
+  // Q and K tiles: dims 0..63 from the rotated copies (from q and k as they
+  // are without RoPE), dims 64..191 from q and k.
+  CUtensorMap mq, mq0, mdo, mk, mk0, mv;
+  auto qk_maps = [&](uint32_t q_rows, uint32_t k_rows) {
+    if (!make_map(&mq, q, 192, num_q_heads, total, G, q_rows) ||
+        !make_map(&mk, k, 192, num_kv_heads, total, 1, k_rows))
+      return false;
+    if (!a.rope_on) {
+      mq0 = mq;
+      mk0 = mk;
+      return true;
+    }
+    return make_map(&mq0, b.q_rot, 64, num_q_heads, total, G, q_rows) &&
+           make_map(&mk0, b.k_rot, 64, num_kv_heads, total, 1, k_rows);
+  };
   // dq kernel: 128 packed rows (G heads x 128/G tokens) and 64-key blocks
-  if (!make_map(&mq, b.q_rot, 192, num_q_heads, total, G, static_cast<uint32_t>(T)) ||
+  if (!qk_maps(static_cast<uint32_t>(T), sa::kDqBN) ||
       !make_map(&mdo, dout, 128, num_q_heads, total, G, static_cast<uint32_t>(T)) ||
-      !make_map(&mk, b.k_rot, 192, num_kv_heads, total, 1, sa::kDqBN) ||
       !make_map(&mv, v, 128, num_kv_heads, total, 1, sa::kDqBN))
     return SINKATTN_ECUDA;
   {
@@ -370,13 +385,12 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
                              static_cast<int>(sa::DqLayout::kDynSmem)) != cudaSuccess)
       return SINKATTN_ECUDA;
     const int grid = static_cast<int>(std::min<int64_t>(b.dq_items, dev.sms));
-    kern<<<grid, sa::kBwdThreads, sa::DqLayout::kDynSmem, s>>>(mq, mdo, mk, mv, b);
+    kern<<<grid, sa::kBwdThreads, sa::DqLayout::kDynSmem, s>>>(mq, mq0, mdo, mk, mk0, mv, b);
     if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
   }
   // dkdv kernel: 64 packed rows (G heads x 64/G tokens) and 128-key blocks
-  if (!make_map(&mq, b.q_rot, 192, num_q_heads, total, G, static_cast<uint32_t>(sa::kKvRows / G)) ||
+  if (!qk_maps(static_cast<uint32_t>(sa::kKvRows / G), sa::kKvBN) ||
       !make_map(&mdo, dout, 128, num_q_heads, total, G, static_cast<uint32_t>(sa::kKvRows / G)) ||
-      !make_map(&mk, b.k_rot, 192, num_kv_heads, total, 1, sa::kKvBN) ||
       !make_map(&mv, v, 128, num_kv_heads, total, 1, sa::kKvBN))
     return SINKATTN_ECUDA;
   {
@@ -385,7 +399,7 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
                              static_cast<int>(sa::KvLayout::kDynSmem)) != cudaSuccess)
       return SINKATTN_ECUDA;
     const int grid = static_cast<int>(std::min<int64_t>(b.kv_items, dev.sms));
-    kern<<<grid, sa::kBwdThreads, sa::KvLayout::kDynSmem, s>>>(mq, mdo, mk, mv, b);
+    kern<<<grid, sa::kBwdThreads, sa::KvLayout::kDynSmem, s>>>(mq, mq0, mdo, mk, mk0, mv, b);
     if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
   }
   return SINKATTN_OK;
