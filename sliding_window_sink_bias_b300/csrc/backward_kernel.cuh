@@ -684,9 +684,10 @@ struct KvLayout {
   static constexpr uint32_t kStOff = 5 * kKBox;          // stages: q_rot rows 3 boxes, dO rows 2
   static constexpr uint32_t kStage = 5 * kQBox;
   static constexpr uint32_t kColOff = kStOff + kStages * kStage;  // lse*log2e, D: 2 sub-tiles
-  // kv_full, kv_empty, qs_full[3], qs_empty[3], mm1, mm2, p_ready, acc_full, rows_full[2], drain
+  // kv_full, kv_empty, qs_full[3], qs_empty[3], mm1, mm2, p_ready, acc_full, rows_full[2],
+  // drain, s_read
   static constexpr uint32_t kBarOff = kColOff + 2 * 2 * kKvRows * 4;
-  static constexpr uint32_t kMiscOff = kBarOff + 15 * 8;
+  static constexpr uint32_t kMiscOff = kBarOff + 16 * 8;
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
@@ -700,11 +701,12 @@ static_assert(KvLayout::kDynSmem <= 232448, "dkdv kernel shared memory");
 //     S^T/dP^T is done (KV_EMPTY); Q/dO sub-tiles, last query rows first (so
 //     the CTAs of one KV head stream the same rows together), through three
 //     stages, each refilled once the dV/dK that read it is done (QS_EMPTY).
-//   MMA thread (256): once the rows have P^T/dS^T(g) in TMEM (P_READY, which
-//     also means they have read S^T/dP^T(g)), S^T/dP^T(g+1) go out first and
-//     dV/dK(g) behind them, so the rows work on sub-tile g+1 while dV/dK(g)
-//     run; after an item's last dV/dK it hands the accumulators over
-//     (ACC_FULL).
+//   MMA thread (256): once every row has S^T/dP^T(g) in registers (S_READ),
+//     S^T/dP^T(g+1) go out, so the tensor core computes them while the rows
+//     turn sub-tile g into P^T/dS^T; once those are in TMEM (P_READY),
+//     dV/dK(g) follow; after an item's last dV/dK it hands the accumulators
+//     over (ACC_FULL).  The first S^T/dP^T of an item goes out after the
+//     previous item's last P_READY, which also means its S^T/dP^T were read.
 //   rows (0..255, two threads per key, 32 query rows each): they wait for
 //     dV/dK(g-1) only before writing P^T/dS^T(g).  Rows 0..63 load lse and D of
 //     the next sub-tile at the top of a sub-tile and put them in a
@@ -737,7 +739,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t B_MM1 = bar(2 + 2 * NS), B_MM2 = bar(3 + 2 * NS);
   const uint32_t B_PR = bar(4 + 2 * NS), B_ACCF = bar(5 + 2 * NS);
   auto B_LF = [&](uint32_t p) { return bar(6 + 2 * NS + p); };
-  const uint32_t B_DRAIN = bar(8 + 2 * NS);
+  const uint32_t B_DRAIN = bar(8 + 2 * NS), B_SR = bar(9 + 2 * NS);
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Ly::kMiscOff + 4);
   float *c_lse = reinterpret_cast<float *>(smem + Ly::kColOff);  // [2][64]
@@ -756,6 +758,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(B_LF(0), kKvRows);
     mbar_init(B_LF(1), kKvRows);
     mbar_init(B_DRAIN, 1);
+    mbar_init(B_SR, 256);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -868,14 +871,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (cur.nsub == 1) mma_commit(B_KVE);
       for (int32_t sidx = 0; sidx < cur.nsub; ++sidx) {
         const uint32_t g = g0 + sidx;
-        // the rows wrote P^T/dS^T(g) (and so have read S^T/dP^T(g))
-        if (!(ok = wait_bar(B_PR, g & 1, abort_flag, 26))) break;
-        tc_fence_after();
-        // S^T/dP^T of the next sub-tile first, then dV/dK of this one
+        // S^T/dP^T of the next sub-tile as soon as every row has S^T/dP^T(g)
+        // in registers, so they run while the rows compute P^T/dS^T(g)
         if (sidx + 1 < cur.nsub) {
+          if (!(ok = wait_bar(B_SR, g & 1, abort_flag, 29))) break;
+          tc_fence_after();
           if (!(ok = issue_sdp(g + 1))) break;
           if (sidx + 2 == cur.nsub) mma_commit(B_KVE);  // the item's last S^T/dP^T
         }
+        // the rows wrote P^T/dS^T(g): dV/dK(g)
+        if (!(ok = wait_bar(B_PR, g & 1, abort_flag, 26))) break;
+        tc_fence_after();
         const uint32_t stb = (sbase + Ly::kStOff + (g % NS) * Ly::kStage) >> 4;
 #pragma unroll
         for (int ks = 0; ks < kKvRows / 16; ++ks) {
@@ -961,6 +967,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_ld();
         reg_fence<32>(sv);
         reg_fence<32>(pv);
+        // S^T/dP^T(g) are in registers: their columns may take the next sub-tile's
+        tc_fence_before();
+        mbar_arrive(B_SR);
 #pragma unroll
         for (int32_t c = 0; c < 32; c += 4) {
           const float4 l4 = cl4[c >> 2], d4 = cd4[c >> 2];

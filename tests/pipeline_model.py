@@ -297,8 +297,9 @@ def dq_roles(nblk, skip=()):
 def dkdv_roles(nsub, skip=()):
     """The dk/dv kernel for one CTA whose items (key blocks) have nsub[i] query
     sub-tiles each.  The roles meet only on mbarriers: the rows tell the MMA
-    thread that P^T/dS^T(g) are in TMEM (PR, 256 arrivals; S^T/dP^T(g+1) and
-    dV/dK(g) follow); rows 0..63 stage lse and D of the next sub-tile in one of
+    thread that they have read S^T/dP^T(g) into registers (SR, 256 arrivals;
+    S^T/dP^T(g+1) follow into the same columns) and that P^T/dS^T(g) are in
+    TMEM (PR, 256 arrivals; dV/dK(g) follow); rows 0..63 stage lse and D of the next sub-tile in one of
     two shared-memory slots (LF: written).  They write slot (g+1) & 1 after
     waiting for dV/dK(g-1), which needed every row's PR for sub-tile g-1, so
     every read of that slot's previous contents is done.  The MMA thread
@@ -336,12 +337,14 @@ def dkdv_roles(nsub, skip=()):
                 yield ("commit", "KVE")
             for s in range(n):
                 g = g0 + s
-                if "issuer_pr" not in skip:
-                    yield ("wait", "PR", g + 1)  # P^T/dS^T(g) written, S^T/dP^T(g) read
                 if s + 1 < n:
+                    if "issuer_sr" not in skip:
+                        yield ("wait", "SR", g + 1)  # S^T/dP^T(g) read by every row
                     yield from issue_sdp(it, g + 1)
                     if s + 2 == n:
                         yield ("commit", "KVE")
+                if "issuer_pr" not in skip:
+                    yield ("wait", "PR", g + 1)  # P^T/dS^T(g) written
                 reads = [("Ph0", ("P", g)), ("Ph1", ("P", g)), (f"QO{g % NS}", ("QO", g))]
                 if s > 0:
                     reads.append(("acc", ("acc", it, s - 1)))
@@ -362,6 +365,7 @@ def dkdv_roles(nsub, skip=()):
                     g = g0 + s
                     yield ("wait", "MM1", g + 1)
                     yield ("read", f"STh{h}", ("ST", g))
+                    yield ("arrive", "SR")
                     if "rows_lf" not in skip:
                         yield ("wait", f"LF{g & 1}", (g >> 1) + 1)
                     yield ("read", f"L{g & 1}", ("L", g))
@@ -378,8 +382,8 @@ def dkdv_roles(nsub, skip=()):
 
     roles = {"producer": producer(), "issuer": issuer(), "rows0": rows(0, True),
              "rows1": rows(1, False)}
-    # PR: both row roles arrive; LF: only the writer
-    return roles, {"PR": 2}
+    # PR, SR: both row roles arrive; LF: only the writer
+    return roles, {"PR": 2, "SR": 2}
 
 
 def run(make_roles, sizes, seed, skip=(), aborts=False):

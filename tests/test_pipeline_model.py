@@ -57,8 +57,8 @@ def test_dq_missing_wait_is_caught(skip, sizes):
     assert _caught(dq_roles, (skip,), sizes)
 
 
-@pytest.mark.parametrize("skip", ["producer_kve", "producer_qse", "issuer_pr", "rows_lf",
-                                  "rows_mm2"])
+@pytest.mark.parametrize("skip", ["producer_kve", "producer_qse", "issuer_pr", "issuer_sr",
+                                  "rows_lf", "rows_mm2"])
 def test_dkdv_missing_wait_is_caught(skip):
     assert _caught(dkdv_roles, (skip,))
 
