@@ -552,23 +552,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ============================================================ rows
     const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const int32_t t_row = row / G, g_row = row % G;
-    // this row's lse (log2 domain) and D in an item; loaded one item ahead,
-    // before the epilogue, so they are in by the next item's first dS
-    auto fetch_rows = [&](const DqItem &d, float &l2, float &dd) {
+    // this row's lse and D in an item, loaded one item ahead (before the
+    // epilogue) as they are, from a row that exists (row 0 for a row past the
+    // end): nothing uses the loaded values before the next item starts, so
+    // the loads never hold a thread up
+    auto fetch_rows = [&](const DqItem &d, float &l_raw, float &d_raw) {
       const int32_t ti = d.t0 + t_row;
-      const size_t grow = static_cast<size_t>(d.s0 + ti) * a.Hq + d.kvh * G + g_row;
-      l2 = ti < d.L ? __ldg(a.lse + grow) * kLog2e : 0.f;
-      dd = ti < d.L ? __ldg(a.D + grow) : 0.f;
+      const size_t grow =
+          ti < d.L ? static_cast<size_t>(d.s0 + ti) * a.Hq + d.kvh * G + g_row : 0;
+      l_raw = __ldg(a.lse + grow);
+      d_raw = __ldg(a.D + grow);
     };
     DqItem cur;
     int32_t it = dq_next_item(a, blockIdx.x, cur);
-    float lse2 = 0.f, Drow = 0.f;
-    if (cur.valid) fetch_rows(cur, lse2, Drow);
+    float l_raw = 0.f, d_raw = 0.f;
+    if (cur.valid) fetch_rows(cur, l_raw, d_raw);
     uint32_t g0 = 0, k = 0;
     bool ok = true;
     while (ok && cur.valid) {
       const int32_t ti = cur.t0 + t_row;
       const bool rvalid = ti < cur.L;  // both halves of the row
+      const float lse2 = rvalid ? l_raw * kLog2e : 0.f;
+      const float Drow = rvalid ? d_raw : 0.f;
       for (int32_t j = 0; j < cur.nblk; ++j) {
         const uint32_t g = g0 + j;
         // S(g), dP(g) complete
@@ -606,8 +611,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       DqItem nxt;
       const int32_t it_n = dq_next_item(a, it + gridDim.x, nxt);
-      float lse2_n = 0.f, D_n = 0.f;
-      if (nxt.valid) fetch_rows(nxt, lse2_n, D_n);
+      if (nxt.valid) fetch_rows(nxt, l_raw, d_raw);
       // the item's last dQ complete
       if (!(ok = wait_bar_warp(B_ACCF, k & 1, abort_flag, 24))) break;
       tc_fence_after();
@@ -627,8 +631,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++k;
       cur = nxt;
       it = it_n;
-      lse2 = lse2_n;
-      Drow = D_n;
     }
   }
   tc_fence_before();
@@ -911,20 +913,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ============================================================ rows
     const uint32_t lane_t = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const bool writer = threadIdx.x < kKvRows;  // stages lse and D of one query row
+    // the values as loaded (from row 0 for a row past the end) and whether
+    // the row exists: nothing uses a loaded value until it is staged, after
+    // the sub-tile's work, so the loads never hold the writer up
     float r_lse = 0.f, r_D = 0.f;
+    bool r_v = false;
     auto fetch_rows = [&](const KvItem &d, int32_t sidx) {
       const int32_t ti = sub0(d, sidx) + threadIdx.x / G, h = d.kvh * G + threadIdx.x % G;
-      const bool v = ti < d.L;
-      const size_t grow = static_cast<size_t>(d.s0 + ti) * a.Hq + h;
-      r_lse = v ? __ldg(a.lse + grow) * kLog2e : 0.f;
-      r_D = v ? __ldg(a.D + grow) : 0.f;
+      r_v = ti < d.L;
+      const size_t grow = r_v ? static_cast<size_t>(d.s0 + ti) * a.Hq + h : 0;
+      r_lse = __ldg(a.lse + grow);
+      r_D = __ldg(a.D + grow);
     };
     KvItem cur;
     int32_t it = kv_next_item(a, blockIdx.x, cur);
     if (cur.valid && writer) {
       fetch_rows(cur, 0);
-      c_lse[threadIdx.x] = r_lse;
-      c_D[threadIdx.x] = r_D;
+      c_lse[threadIdx.x] = r_v ? r_lse * kLog2e : 0.f;
+      c_D[threadIdx.x] = r_v ? r_D : 0.f;
       mbar_arrive(B_LF(0));
     }
     uint32_t g0 = 0, k = 0;
@@ -996,8 +1002,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         mbar_arrive(B_PR);
         if (writer && more) {
-          c_lse[((g + 1) & 1) * kKvRows + threadIdx.x] = r_lse;
-          c_D[((g + 1) & 1) * kKvRows + threadIdx.x] = r_D;
+          c_lse[((g + 1) & 1) * kKvRows + threadIdx.x] = r_v ? r_lse * kLog2e : 0.f;
+          c_D[((g + 1) & 1) * kKvRows + threadIdx.x] = r_v ? r_D : 0.f;
           mbar_arrive(B_LF((g + 1) & 1));
         }
       }
