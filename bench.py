@@ -830,6 +830,14 @@ def main():
             "frac_of_sustained_peak": (g_tf / peaks["bf16_tflops_sustained"]
                                        if peaks.get("bf16_tflops_sustained") else None),
             "clocks": g["clocks"]}
+        w = bench_prefill("swa_w512_prefill_1x32768", args.steps, args.warmup, ws, local,
+                          with_e2e=False)
+        w_tf = w["flops"] / (w["ms"] / 1e3) / 1e12
+        extra["swa_w512_prefill_1x32768"] = {
+            "value": ws * w_tf, "unit": "TFLOP/s", "ms_per_step": w["ms"],
+            "kernel": "general prefill kernel (window 512 > 128)",
+            "roofline": roofline_obj("tensor", w_tf, peaks["bf16_tflops"], "TFLOP/s", None),
+            "clocks": w["clocks"]}
         for name in ("mtp_decode_ga_b64_t4", "mtp_decode_ga_fp8_b64_t4",
                      "mtp_decode_ga_fp8_rot_b64_t4", "mtp_decode_swa_b64_t4",
                      "mtp_decode_swa_ring_b64_t4"):

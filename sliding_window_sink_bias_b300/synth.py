@@ -157,6 +157,10 @@ WORKLOADS = {
     # a GA layer at 32K tokens
     "swa_backward_4x32768": dict(kind="backward", seqlens=[32768] * 4, **SWA),
     "ga_backward_1x32768": dict(kind="backward", seqlens=[32768], **GA),
+    # the same SWA layer with a 512-token window (outside the band kernel's
+    # W <= 128): the general prefill kernel over 128-key blocks
+    "swa_w512_prefill_1x32768": dict(kind="prefill", seqlens=[32768], hq=64, hkv=8, window=512,
+                                     rope_base=1e4),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)
     "swa_prefill_1x32768": dict(kind="prefill", seqlens=[32768], **SWA),
     "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),
