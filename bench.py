@@ -835,7 +835,7 @@ def main():
         w_tf = w["flops"] / (w["ms"] / 1e3) / 1e12
         extra["swa_w512_prefill_1x32768"] = {
             "value": ws * w_tf, "unit": "TFLOP/s", "ms_per_step": w["ms"],
-            "kernel": "general prefill kernel (window 512 > 128)",
+            "kernel": "causal prefill kernel with a window (512 > 128)",
             "roofline": roofline_obj("tensor", w_tf, peaks["bf16_tflops"], "TFLOP/s", None),
             "clocks": w["clocks"]}
         for name in ("mtp_decode_ga_b64_t4", "mtp_decode_ga_fp8_b64_t4",

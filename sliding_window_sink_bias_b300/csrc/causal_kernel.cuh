@@ -3,7 +3,10 @@
 // Computes the attention layer of the MiMo-V2-Flash Technical Report (§2.2
 // eqs. (1)-(3), shapes of §2.1 Table 1) for the global layers: every query
 // attends to all keys at or before its position, with the per-head sink in the
-// softmax denominator.
+// softmax denominator.  The same kernel runs sliding windows the band kernel
+// does not take (window > 128, or 4, 16, 32 or 64 query heads per KV head):
+// an item then visits only the 128-key blocks its window reaches, and the low
+// edge of the window is masked like the diagonal.
 //
 // A query tile is T = 128 / G consecutive tokens x the G query heads of one KV
 // head (128 MMA rows, row r = token * G + head).  Each work item is a pair of
@@ -40,6 +43,7 @@ constexpr int32_t kCauThreads = 512;
 
 struct CausalArgs {
   int32_t Hq, Hkv, G;
+  int32_t window;       // 0: global causal; W > 0: keys (pos - W, pos]
   int32_t T;            // tokens per tile = 128 / G
   int32_t batch;
   int32_t max_seqlen;
@@ -80,7 +84,8 @@ struct CauItem {
   int32_t b, kvh;
   int32_t s0, L;   // first packed row and length of the sequence
   int32_t t0;      // position of tile A's first token
-  int32_t nblk;    // key blocks: keys [0, min(L, t0 + 2T))
+  int32_t kb0;     // first key block: the one holding key max(0, t0 - W + 1) (0 if global)
+  int32_t nblk;    // key blocks kb0 .. kb0 + nblk - 1: keys up to min(L, t0 + 2T) - 1
 };
 
 // Items longest first: pair index descending, then (sequence, KV head).
@@ -96,7 +101,8 @@ __device__ __forceinline__ CauItem cau_item(const CausalArgs &a, int32_t w) {
   it.t0 = n * 2 * a.T;
   it.valid = it.t0 < it.L;
   const int32_t kend = min(it.L, it.t0 + 2 * a.T);
-  it.nblk = (kend + kCauBN - 1) / kCauBN;
+  it.kb0 = a.window > 0 ? max(0, it.t0 - a.window + 1) / kCauBN : 0;
+  it.nblk = (kend + kCauBN - 1) / kCauBN - it.kb0;
   return it;
 }
 
@@ -131,9 +137,12 @@ __device__ __forceinline__ void cau_softmax(const CausalArgs &args, int32_t X, u
     for (int32_t j = 0; ok && j < it.nblk; ++j) {
       if (!(ok = wait_bar_warp(B_SFULL, gb & 1, abort_flag, 7))) break;
       tc_fence_after();
-      // visible columns of block j: k <= pos - 128 j (none for a padding row)
-      const int32_t hi = rvalid ? pos - j * kCauBN : -1;
-      const bool whole = __all_sync(0xffffffffu, hi >= kCauBN - 1);
+      // visible columns of block j (keys from 128 (kb0 + j)): lo <= k <= hi,
+      // lo from the window (none for a padding row)
+      const int32_t kbase = (it.kb0 + j) * kCauBN;
+      const int32_t hi = rvalid ? pos - kbase : -1;
+      const int32_t lo = args.window > 0 ? pos - args.window + 1 - kbase : INT32_MIN;
+      const bool whole = __all_sync(0xffffffffu, hi >= kCauBN - 1 && lo <= 0);
       float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll 1
       for (int32_t ch = 0; ch < 2; ++ch) {
@@ -146,7 +155,7 @@ __device__ __forceinline__ void cau_softmax(const CausalArgs &args, int32_t X, u
           // masked columns become -inf in TMEM too, so the exp pass needs no mask
 #pragma unroll
           for (int32_t k = 0; k < 64; ++k)
-            if (ch * 64 + k > hi) r[k] = kNegInf;
+            if (ch * 64 + k > hi || ch * 64 + k < lo) r[k] = kNegInf;
           tmem_st32p(s_t + ch * 64, r);
           tmem_st32p(s_t + ch * 64 + 32, r + 32);
         }
@@ -382,7 +391,7 @@ __global__ void __launch_bounds__(kCauThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 3; ++cc)
             tma_load_3d(sbase + Ly::kKOff + st * Ly::kKStage + cc * Ly::kKBox, &tm_k, cc * 64,
-                        it.kvh, it.s0 + j * kCauBN, B_KFULL(st));
+                        it.kvh, it.s0 + (it.kb0 + j) * kCauBN, B_KFULL(st));
           ++gk;
         }
       }
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(kCauThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
             tma_load_3d(sbase + Ly::kVOff + cc * Ly::kKBox, &tm_v, cc * 64, it.kvh,
-                        it.s0 + j * kCauBN, B_VFULL);
+                        it.s0 + (it.kb0 + j) * kCauBN, B_VFULL);
           ++gv;
         }
       }
@@ -522,8 +531,8 @@ __global__ void __launch_bounds__(kCauThreads, 1)
         const uint32_t st = gk & 1;
         if (!(ok = wait_bar_warp(B_KFULL(st), (gk >> 1) & 1, abort_flag, 11))) break;
         if (args.rope_on)
-          rope_k_rows(smem + Ly::kKOff + st * Ly::kKStage, kCauBN, j * kCauBN, args.rope_style,
-                      turns, tid);
+          rope_k_rows(smem + Ly::kKOff + st * Ly::kKStage, kCauBN, (it.kb0 + j) * kCauBN,
+                      args.rope_style, turns, tid);
         fence_proxy_async_smem();
         mbar_arrive(B_KREADY(st));
         ++gk;

@@ -158,7 +158,7 @@ WORKLOADS = {
     "swa_backward_4x32768": dict(kind="backward", seqlens=[32768] * 4, **SWA),
     "ga_backward_1x32768": dict(kind="backward", seqlens=[32768], **GA),
     # the same SWA layer with a 512-token window (outside the band kernel's
-    # W <= 128): the general prefill kernel over 128-key blocks
+    # W <= 128): the causal kernel, visiting only the key blocks the window reaches
     "swa_w512_prefill_1x32768": dict(kind="prefill", seqlens=[32768], hq=64, hkv=8, window=512,
                                      rope_base=1e4),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)

@@ -132,8 +132,9 @@ CASES = {
     # general kernel: 2 heads a KV head with a window, 1 head a KV head global
     "general_g2_window": lambda: _prefill_case(16, 8, [150, 33], 64, 1e4, 62),
     "general_g1_global": lambda: _prefill_case(8, 8, [140, 9], 0, 5e6, 63),
-    # global causal kernel, several sequences
+    # causal kernel: global, several sequences; and with a window past one block
     "ga_causal": lambda: _prefill_case(64, 4, [300, 129, 5], 0, 5e6, 64),
+    "causal_window": lambda: _prefill_case(64, 8, [700, 129, 1], 256, 1e4, 70),
     # decode: long caches cut over many CTAs (partials merged in the launch)
     "decode_ga_split": lambda: _decode_case(4, [20000, 9000, 0, 3], 4, 20000, 0, 5e6, 65),
     "decode_swa_ring": lambda: _decode_case(8, [5000, 131, 2], 4, 144, 128, 1e4, 66, ring=True),

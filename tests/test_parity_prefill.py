@@ -58,6 +58,16 @@ def test_window_sweep(oracle_mod, window):
     assert_parity(o, l, ro, rl, f"window {window}")
 
 
+@pytest.mark.parametrize("hq,hkv,window", [(64, 16, 129), (64, 8, 256), (64, 4, 300),
+                                           (32, 2, 150), (64, 1, 513), (64, 8, 700)])
+def test_causal_kernel_windows(oracle_mod, hq, hkv, window):
+    """Windows too wide for one 144-key block with G >= 4 run on the causal
+    kernel: an item's first key block is the one its window reaches and the
+    window's low edge is masked; ragged sequences, windows across block edges."""
+    o, l, ro, rl = run_case(oracle_mod, [700, 129, 1, 300], hq, hkv, window, 1e4, seed=window)
+    assert_parity(o, l, ro, rl, f"Hq={hq} Hkv={hkv} W={window}")
+
+
 @pytest.mark.parametrize("L", [1, 2, 15, 16, 17, 127, 128, 129, 255, 300])
 @pytest.mark.parametrize("window", [0, 128])
 def test_ragged_lengths(oracle_mod, L, window):
@@ -145,9 +155,9 @@ def test_swa_prefill_bulk_sampled(oracle_mod):
 
 @pytest.mark.slow
 def test_swa_w512_prefill_sampled(oracle_mod):
-    """1 x 32768 tokens, 64/8 heads, W=512 (the general kernel over 128-key
-    blocks, as the benchmark runs it): sampled rows, including both sides of
-    the window's edge and of block boundaries."""
+    """1 x 32768 tokens, 64/8 heads, W=512 (the causal kernel with a window, as
+    the benchmark runs it): sampled rows, including both sides of the window's
+    edge and of block boundaries."""
     import sliding_window_sink_bias_b300 as sa
     wl = synth.WORKLOADS["swa_w512_prefill_1x32768"]
     inp = synth.prefill_inputs(wl["seqlens"], wl["hq"], wl["hkv"], window=wl["window"],
