@@ -838,6 +838,16 @@ def main():
             "kernel": "causal prefill kernel with a window (512 > 128)",
             "roofline": roofline_obj("tensor", w_tf, peaks["bf16_tflops"], "TFLOP/s", None),
             "clocks": w["clocks"]}
+        w = bench_prefill("swa_g2_prefill_1x32768", args.steps, args.warmup, ws, local,
+                          with_e2e=False)
+        w_tf = w["flops"] / (w["ms"] / 1e3) / 1e12
+        w_gbs = w["bytes"] / (w["ms"] / 1e3) / 1e9
+        extra["swa_g2_prefill_1x32768"] = {
+            "value": ws * w_tf, "unit": "TFLOP/s", "ms_per_step": w["ms"],
+            "kernel": "general prefill kernel (2 query heads per KV head, W = 128)",
+            "gbs": w_gbs,
+            "roofline": roofline_obj("hbm", w_gbs, peaks["hbm_gbs"], "GB/s", None),
+            "clocks": w["clocks"]}
         for name in ("mtp_decode_ga_b64_t4", "mtp_decode_ga_fp8_b64_t4",
                      "mtp_decode_ga_fp8_rot_b64_t4", "mtp_decode_swa_b64_t4",
                      "mtp_decode_swa_ring_b64_t4"):

@@ -3,10 +3,10 @@
 // Computes the attention layer of the MiMo-V2-Flash Technical Report (§2.2
 // eqs. (1)-(3), shapes of §2.1 Table 1) for the global layers: every query
 // attends to all keys at or before its position, with the per-head sink in the
-// softmax denominator.  The same kernel runs sliding windows the band kernel
-// does not take (window > 128, or 4, 16, 32 or 64 query heads per KV head):
-// an item then visits only the 128-key blocks its window reaches, and the low
-// edge of the window is masked like the diagonal.
+// softmax denominator.  The same kernel runs the sliding windows the band
+// kernel does not take (window > 128, or 4, 16, 32, 64 or 128 query heads per
+// KV head): an item then visits only the 128-key blocks its window reaches,
+// and the low edge of the window is masked like the diagonal.
 //
 // A query tile is T = 128 / G consecutive tokens x the G query heads of one KV
 // head (128 MMA rows, row r = token * G + head).  Each work item is a pair of

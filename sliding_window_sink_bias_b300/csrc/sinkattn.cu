@@ -165,8 +165,8 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
   return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
-// Causal prefill with G >= 4 query heads per KV head, global or with a window
-// wider than one 144-key block: pairs of query tiles per CTA, longest first.
+// Causal prefill with G >= 4 query heads per KV head, global or windowed
+// (except the band kernel's shapes): pairs of query tiles per CTA, longest first.
 sinkattn_status launch_causal(const void *q, const void *k, const void *v, const AttnArgs &a,
                               const int32_t *cu_seqlens, int32_t batch, int32_t total,
                               int32_t max_seqlen, const DeviceInfo &dev, cudaStream_t stream) {
@@ -483,9 +483,9 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
   if (G == sa::kBandG && window >= 1 && window <= sa::kBandMaxWin * sa::kBandSeg - sa::kBandSeg &&
       a.scale_log2 > 0.f)
     return launch_band(q, k, v, a, cu_seqlens, batch, total, dev, s);
-  // global causal, and windows too wide for one 144-key block, with G >= 4:
-  // the two-tile causal kernel (a window only trims its key blocks)
-  if (G >= 4 && (window == 0 || !wide) && a.scale_log2 > 0.f)
+  // every other shape with G >= 4, global or windowed: the two-tile causal
+  // kernel (a window only trims the key blocks of an item)
+  if (G >= 4 && a.scale_log2 > 0.f)
     return launch_causal(q, k, v, a, cu_seqlens, batch, total, max_seqlen, dev, s);
 
   CUtensorMap mq, mk, mv;

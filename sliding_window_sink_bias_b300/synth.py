@@ -161,6 +161,10 @@ WORKLOADS = {
     # W <= 128): the causal kernel, visiting only the key blocks the window reaches
     "swa_w512_prefill_1x32768": dict(kind="prefill", seqlens=[32768], hq=64, hkv=8, window=512,
                                      rope_base=1e4),
+    # a 128-token window over 64 query heads in pairs (2 per KV head, tiles of
+    # 64 tokens): the general prefill kernel
+    "swa_g2_prefill_1x32768": dict(kind="prefill", seqlens=[32768], hq=64, hkv=32, window=128,
+                                   rope_base=1e4),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)
     "swa_prefill_1x32768": dict(kind="prefill", seqlens=[32768], **SWA),
     "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),

@@ -179,6 +179,29 @@ def test_swa_w512_prefill_sampled(oracle_mod):
 
 
 @pytest.mark.slow
+def test_swa_g2_prefill_sampled(oracle_mod):
+    """1 x 32768 tokens, 64/32 heads, W=128 (the general kernel, tiles of 64
+    tokens x 2 heads): sampled rows."""
+    import sliding_window_sink_bias_b300 as sa
+    wl = synth.WORKLOADS["swa_g2_prefill_1x32768"]
+    inp = synth.prefill_inputs(wl["seqlens"], wl["hq"], wl["hkv"], window=wl["window"],
+                               rope_base=wl["rope_base"], seed=0, device=DEV)
+    out, lse = sa.prefill(inp.q, inp.k, inp.v, inp.sink, inp.cu_seqlens,
+                          max_seqlen=inp.max_seqlen, window=wl["window"],
+                          rope_base=wl["rope_base"])
+    torch.cuda.synchronize()
+    assert sa.device_status()[0] == sa.OK
+    L = 32768
+    toks, rows = sample_rows(L, 64, 24, seed=31, must=(0, 63, 64, 127, 128, 191, 192, L - 1))
+    ro, rl = oracle_mod.prefill(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sink.cpu(),
+                                np.array([0, L], dtype=np.int32), window=128,
+                                rope_base=wl["rope_base"], rows=rows)
+    tok = torch.as_tensor(rows // 64).to(DEV)
+    hd = torch.as_tensor(rows % 64).to(DEV)
+    assert_parity(out[tok, hd], lse[tok, hd], ro, rl, "swa g2")
+
+
+@pytest.mark.slow
 def test_ga_prefill_long_sampled(oracle_mod):
     """1 x 131072 tokens, 64/4 heads, global, base 5e6: sampled rows."""
     import sliding_window_sink_bias_b300 as sa

@@ -38,8 +38,8 @@ def _edge(x, mag):
 
 @pytest.mark.parametrize("q_mag,k_mag", MAGS, ids=MAG_IDS)
 @pytest.mark.parametrize("hq,hkv,window,base", [(64, 8, 128, 1e4), (64, 4, 0, 5e6),
-                                                (8, 4, 32, 1e4)],
-                         ids=["band", "causal", "generic"])
+                                                (64, 16, 64, 1e4), (8, 4, 32, 1e4)],
+                         ids=["band", "causal", "causal_window", "generic"])
 def test_prefill_rotated_dims_at_fp16_edges(oracle_mod, q_mag, k_mag, hq, hkv, window, base):
     import sliding_window_sink_bias_b300 as sa
     lens = [300, 77]
