@@ -58,6 +58,67 @@ struct BandArgs {
   unsigned long long rope_turns[32];
 };
 
+// RoPE on dims 0..63 of a band Q tile (16 tokens x 8 heads, rows t * 8 + g),
+// 128 threads.  A thread takes one (token, 16-byte chunk) unit and its angles
+// once, then all the heads of that token: the loads of the heads' chunks go
+// out together before any rotation (the RoPE warps share their schedulers
+// with the softmax warps, so a chain of dependent load-rotate-store steps
+// per head would run at a fraction of their issue rate).
+__device__ __forceinline__ void band_rope_q(uint8_t *box0, int32_t n_tok, int32_t pos0,
+                                            int32_t style, const unsigned long long *turns,
+                                            int32_t tid) {
+  if (style == 0) {
+    // interleaved pairs: 16 tokens x 8 chunks (4 pairs each) = 128 units
+    const int32_t t = tid >> 3, c = tid & 7;
+    if (t >= n_tok) return;
+    float cs[4], sn[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) rope_cs(pos0 + t, turns[4 * c + e], cs[e], sn[e]);
+    uint4 v[kBandG];
+#pragma unroll
+    for (int32_t g = 0; g < kBandG; ++g) v[g] = *swz_chunk(box0, t * kBandG + g, c);
+#pragma unroll
+    for (int32_t g = 0; g < kBandG; ++g) {
+      uint32_t w[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = bf16lo(w[e]), y = bf16hi(w[e]);
+        w[e] = pack_f16x2(x * cs[e] - y * sn[e], x * sn[e] + y * cs[e]);
+      }
+      *swz_chunk(box0, t * kBandG + g, c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    // half-split pairs (p, p + 32): 16 tokens x 4 chunk pairs = 64 units, each
+    // taken by two threads (4 heads each)
+    const int32_t u = tid >> 1, t = u >> 2, c = u & 3, g0 = (tid & 1) * (kBandG / 2);
+    if (t >= n_tok) return;
+    float cs[8], sn[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rope_cs(pos0 + t, turns[8 * c + e], cs[e], sn[e]);
+    uint4 va[kBandG / 2], vb[kBandG / 2];
+#pragma unroll
+    for (int32_t g = 0; g < kBandG / 2; ++g) {
+      va[g] = *swz_chunk(box0, t * kBandG + g0 + g, c);
+      vb[g] = *swz_chunk(box0, t * kBandG + g0 + g, c + 4);
+    }
+#pragma unroll
+    for (int32_t g = 0; g < kBandG / 2; ++g) {
+      uint32_t a[4] = {va[g].x, va[g].y, va[g].z, va[g].w};
+      uint32_t b[4] = {vb[g].x, vb[g].y, vb[g].z, vb[g].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = bf16lo(a[e]), y0 = bf16lo(b[e]);
+        const float x1 = bf16hi(a[e]), y1 = bf16hi(b[e]);
+        const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
+        a[e] = pack_f16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
+        b[e] = pack_f16x2(x0 * s0 + y0 * c0, x1 * s1 + y1 * c1);
+      }
+      *swz_chunk(box0, t * kBandG + g0 + g, c) = make_uint4(a[0], a[1], a[2], a[3]);
+      *swz_chunk(box0, t * kBandG + g0 + g, c + 4) = make_uint4(b[0], b[1], b[2], b[3]);
+    }
+  }
+}
+
 struct BandLayout {
   static constexpr uint32_t kSegBox = kBandSeg * kRowBytes;   // 16 keys x 64 dims: 2 KB
   static constexpr uint32_t kRingBox = kBandRing * kSegBox;   // 24 KB
@@ -661,7 +722,7 @@ __global__ void __launch_bounds__(kBandThreads, 1)
       const uint32_t qs = gq & 1;
       if (!(ok = wait_bar_warp(B_QFULL(qs), (gq >> 1) & 1, abort_flag, 10))) break;
       if (args.rope_on)
-        rope_q_tile(smem + Ly::kQOff + qs * kQStageBytes, kBandG, min(kBandSeg, c.L - c.i * kBandSeg),
+        band_rope_q(smem + Ly::kQOff + qs * kQStageBytes, min(kBandSeg, c.L - c.i * kBandSeg),
                     c.i * kBandSeg, args.rope_style, turns, tid);
       fence_proxy_async_smem();
       mbar_arrive(B_QREADY(qs));
