@@ -434,41 +434,18 @@ __device__ __forceinline__ void band_softmax(const BandArgs &args, const BandCur
           w[e] = pack_bf16x2(v.x, v.y);
         }
       }
-      // Each half-row is one 128-byte line of out.  Transpose the 4 x 4 sectors
-      // within each quad of lanes (rows 4k..4k+3, consecutive heads of one
-      // token): afterwards lane q holds sector q of rows 4k..4k+3, so each of
-      // the four stores below writes 8 whole lines per warp instead of 32
-      // partial ones.
-      const int32_t q = threadIdx.x & 3;
-#pragma unroll
-      for (int32_t j = 0; j < 2; ++j) {  // partner q ^ 2: sectors {0,1} <-> {2,3}
-#pragma unroll
-        for (int32_t e = 0; e < 8; ++e) {
-          const uint32_t send = (q & 2) ? w[8 * j + e] : w[8 * (j + 2) + e];
-          const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
-          if (q & 2) w[8 * j + e] = recv; else w[8 * (j + 2) + e] = recv;
-        }
-      }
-#pragma unroll
-      for (int32_t j = 0; j < 4; j += 2) {  // partner q ^ 1: positions j <-> j + 1
-#pragma unroll
-        for (int32_t e = 0; e < 8; ++e) {
-          const uint32_t send = (q & 1) ? w[8 * j + e] : w[8 * (j + 1) + e];
-          const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
-          if (q & 1) w[8 * j + e] = recv; else w[8 * (j + 1) + e] = recv;
-        }
-      }
-      if (p_valid) {
-        // rows of a quad share the token; row 4k+p is head (g & ~3) + p
-        __nv_bfloat16 *row0 = args.out + (p_orow - q) * kDv + half * 64 + q * 16;
+      // Each half-row is one 128-byte line of out, stored as its four 32-byte
+      // sectors.  (Exchanging sectors within lane quads so that each store
+      // writes whole lines cost the softmax warps more time than it saved.)
+      if (p_valid && SA_OUT(p_orow, args.n_rows, 0x11)) {
+        __nv_bfloat16 *line = args.out + p_orow * kDv + half * 64;
 #pragma unroll
         for (int32_t pq = 0; pq < 4; ++pq) {
           uint32_t (&sec)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8 * pq);
-          if (!SA_OUT(p_orow - q + pq, args.n_rows, 0x11)) continue;
           if (args.out_v8) {
-            st_global_v8(row0 + pq * kDv, sec);
+            st_global_v8(line + pq * 16, sec);
           } else {
-            uint4 *d4 = reinterpret_cast<uint4 *>(row0 + pq * kDv);
+            uint4 *d4 = reinterpret_cast<uint4 *>(line + pq * 16);
             d4[0] = make_uint4(sec[0], sec[1], sec[2], sec[3]);
             d4[1] = make_uint4(sec[4], sec[5], sec[6], sec[7]);
           }
