@@ -92,7 +92,8 @@ def test_group_sizes(oracle_mod, hq, hkv):
 
 def test_rope_variants_and_scale(oracle_mod):
     for kw in (dict(rope_style=1), dict(rope_off=True), dict(scale=0.11)):
-        for window, hkv in ((128, 8), (0, 4)):
+        # band, causal, causal with a window, general
+        for window, hkv in ((128, 8), (0, 4), (300, 16), (64, 32)):
             o, l, ro, rl = run_case(oracle_mod, [150], 64, hkv, window, 1e4, seed=4, **kw)
             assert_parity(o, l, ro, rl, f"{kw} W={window}")
 
