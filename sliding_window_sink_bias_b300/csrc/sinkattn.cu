@@ -11,6 +11,8 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "attn_kernel.cuh"
 #include "band_kernel.cuh"
@@ -20,6 +22,56 @@
 #include "sinkattn.h"
 
 namespace {
+
+// Raise a kernel's dynamic shared-memory limit on the current device once: the
+// attribute stays with the context, and setting it before every launch costs a
+// driver call per launch.  A failed launch forgets the kernel, so the next call
+// sets it again (a device reset clears it).
+std::mutex g_smem_attr_mu;
+std::vector<std::pair<const void *, uint64_t>> g_smem_attr_done;  // kernel, devices set (bit)
+
+bool smem_attr_set(const void *kern, uint64_t bit) {
+  std::lock_guard<std::mutex> lock(g_smem_attr_mu);
+  for (auto &e : g_smem_attr_done)
+    if (e.first == kern) return (e.second & bit) != 0;
+  return false;
+}
+
+void smem_attr_mark(const void *kern, uint64_t bit, bool set) {
+  std::lock_guard<std::mutex> lock(g_smem_attr_mu);
+  for (auto &e : g_smem_attr_done)
+    if (e.first == kern) {
+      e.second = set ? (e.second | bit) : (e.second & ~bit);
+      return;
+    }
+  if (set) g_smem_attr_done.emplace_back(kern, bit);
+}
+
+template <typename Kernel>
+sinkattn_status smem_attr_once(Kernel kern, uint32_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SINKATTN_ECUDA;
+  const void *key = reinterpret_cast<const void *>(kern);
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (bit != 0 && smem_attr_set(key, bit)) return SINKATTN_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return SINKATTN_ECUDA;
+  if (bit != 0) smem_attr_mark(key, bit, true);
+  return SINKATTN_OK;
+}
+
+// The status of a launch just made; on failure the kernel's attribute is set
+// again at its next launch.
+template <typename Kernel>
+sinkattn_status launched(Kernel kern) {
+  if (cudaGetLastError() == cudaSuccess) return SINKATTN_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev < 64)
+    smem_attr_mark(reinterpret_cast<const void *>(kern), 1ull << dev, false);
+  return SINKATTN_ECUDA;
+}
+
 
 using sa::AttnArgs;
 using sa::Layout;
@@ -119,11 +171,9 @@ sinkattn_status launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
                        const AttnArgs &a, int grid, cudaStream_t stream) {
   using Ly = Layout<BN, NQ, NKV>;
   auto kern = sa::sinkattn_fwd_kernel<BN, NQ, NKV>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(Ly::kDynSmem)) != cudaSuccess)
-    return SINKATTN_ECUDA;
+  if (sinkattn_status st = smem_attr_once(kern, Ly::kDynSmem)) return st;
   kern<<<grid, sa::kThreads, Ly::kDynSmem, stream>>>(mq, mk, mv, a);
-  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+  return launched(kern);
 }
 
 // Sliding-window prefill with 8 query heads per KV head and W <= 128: the
@@ -158,11 +208,9 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
     return SINKATTN_ECUDA;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, dev.sms)));
   auto kern = sa::sinkattn_band_kernel;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sa::BandLayout::kDynSmem)) != cudaSuccess)
-    return SINKATTN_ECUDA;
+  if (sinkattn_status st = smem_attr_once(kern, sa::BandLayout::kDynSmem)) return st;
   kern<<<grid, sa::kBandThreads, sa::BandLayout::kDynSmem, stream>>>(mq, mk, mv, b);
-  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+  return launched(kern);
 }
 
 // Causal prefill with G >= 4 query heads per KV head, global or windowed
@@ -201,11 +249,9 @@ sinkattn_status launch_causal(const void *q, const void *k, const void *v, const
     return SINKATTN_ECUDA;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n_items, dev.sms)));
   auto kern = sa::sinkattn_causal_kernel;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sa::CauLayout::kDynSmem)) != cudaSuccess)
-    return SINKATTN_ECUDA;
+  if (sinkattn_status st = smem_attr_once(kern, sa::CauLayout::kDynSmem)) return st;
   kern<<<grid, sa::kCauThreads, sa::CauLayout::kDynSmem, stream>>>(mq, mk, mv, c);
-  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
+  return launched(kern);
 }
 
 struct DecodePlan {
@@ -382,12 +428,10 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
     return SINKATTN_ECUDA;
   {
     auto kern = sa::bwd_dq_kernel;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sa::DqLayout::kDynSmem)) != cudaSuccess)
-      return SINKATTN_ECUDA;
+    if (sinkattn_status st = smem_attr_once(kern, sa::DqLayout::kDynSmem)) return st;
     const int grid = static_cast<int>(std::min<int64_t>(b.dq_items, dev.sms));
     kern<<<grid, sa::kBwdThreads, sa::DqLayout::kDynSmem, s>>>(mq, mq0, mdo, mk, mk0, mv, b);
-    if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
+    if (sinkattn_status st = launched(kern)) return st;
   }
   // dkdv kernel: 64 packed rows (G heads x 64/G tokens) and 128-key blocks
   if (!qk_maps(static_cast<uint32_t>(sa::kKvRows / G), sa::kKvBN) ||
@@ -396,12 +440,10 @@ sinkattn_status sinkattn_prefill_backward(const void *q, const void *k, const vo
     return SINKATTN_ECUDA;
   {
     auto kern = sa::bwd_dkdv_kernel;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sa::KvLayout::kDynSmem)) != cudaSuccess)
-      return SINKATTN_ECUDA;
+    if (sinkattn_status st = smem_attr_once(kern, sa::KvLayout::kDynSmem)) return st;
     const int grid = static_cast<int>(std::min<int64_t>(b.kv_items, dev.sms));
     kern<<<grid, sa::kBwdThreads, sa::KvLayout::kDynSmem, s>>>(mq, mq0, mdo, mk, mk0, mv, b);
-    if (cudaGetLastError() != cudaSuccess) return SINKATTN_ECUDA;
+    if (sinkattn_status st = launched(kern)) return st;
   }
   return SINKATTN_OK;
 }
@@ -637,19 +679,16 @@ static sinkattn_status decode_impl(const void *q, const void *kcache, const void
   if (fp8) {
     auto kern = sa::sinkattn_decode_kernel<true>;
     constexpr uint32_t smem = sa::DecLayoutT<true>::kDynSmem;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return SINKATTN_ECUDA;
+    if (sinkattn_status st = smem_attr_once(kern, smem)) return st;
     kern<<<grid, sa::DecThreads<true>::kAll, smem, s>>>(mq, mk, mv, d);
+    return launched(kern);
   } else {
     auto kern = sa::sinkattn_decode_kernel<false>;
     constexpr uint32_t smem = sa::DecLayoutT<false>::kDynSmem;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return SINKATTN_ECUDA;
+    if (sinkattn_status st = smem_attr_once(kern, smem)) return st;
     kern<<<grid, sa::kThreads, smem, s>>>(mq, mk, mv, d);
+    return launched(kern);
   }
-  return cudaGetLastError() == cudaSuccess ? SINKATTN_OK : SINKATTN_ECUDA;
 }
 
 sinkattn_status sinkattn_decode_ex(const void *q, const void *kcache, const void *vcache,
