@@ -62,6 +62,14 @@ def test_fp8_block_edges_and_nan_tail(oracle_mod, window, hkv):
     assert_parity(o, l, ro, rl, f"fp8 edges W={window}")
 
 
+@pytest.mark.parametrize("t,hkv", [(5, 4), (8, 4), (8, 8), (16, 8)])
+def test_fp8_tile_sizes(oracle_mod, t, hkv):
+    """Query tiles of T * G = 80 and 128 rows as well as 64: more MTP tokens
+    than the verify step's four, over the same caches."""
+    o, l, ro, rl = _run(oracle_mod, [1, 64, 700, 1500, 1501], t, 1501, hkv, 0, 5e6, seed=26)
+    assert_parity(o, l, ro, rl, f"fp8 T={t} G={64 // hkv}")
+
+
 def test_fp8_half_split_rope_and_tokens(oracle_mod):
     o, l, ro, rl = _run(oracle_mod, [333, 1000, 2], 2, 1000, 4, 0, 5e6, seed=23, rope_style=1)
     assert_parity(o, l, ro, rl, "fp8 half-split")
