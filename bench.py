@@ -836,7 +836,7 @@ def main():
         w_gbs = w["bytes"] / (w["ms"] / 1e3) / 1e9
         extra["swa_g2_prefill_1x32768"] = {
             "value": ws * w_tf, "unit": "TFLOP/s", "ms_per_step": w["ms"],
-            "kernel": "general prefill kernel (2 query heads per KV head, W = 128)",
+            "kernel": "causal prefill kernel (2 query heads per KV head, W = 128)",
             "gbs": w_gbs,
             "roofline": roofline_obj("hbm", w_gbs, peaks["hbm_gbs"], "GB/s", None),
             "clocks": w["clocks"]}

@@ -1,9 +1,10 @@
 // attn_kernel.cuh -- the general sink-bias GQA prefill kernel for sm_103a.
 //
-// The shapes of the model run on specialised kernels (band_kernel.cuh: sliding
-// window, 8 heads per KV head, W <= 128; causal_kernel.cuh: every other shape
-// with >= 4 heads per KV head, global or windowed).  This kernel covers the
-// rest: 1 or 2 query heads per KV head, and non-positive logit scales.
+// Prefill with a positive logit scale runs on specialised kernels
+// (band_kernel.cuh: sliding window, 8 heads per KV head, W <= 128;
+// causal_kernel.cuh: every other shape, global or windowed).  This kernel
+// covers the rest: logit scales <= 0, whose running maximum it takes over the
+// scaled logits.
 //
 // Computes, for one tile of 128 packed query rows at a time, the attention of
 // the MiMo-V2-Flash Technical Report (§2.2 eqs. (1)-(3); shapes from §2.1

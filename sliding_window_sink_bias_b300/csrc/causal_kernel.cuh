@@ -4,9 +4,9 @@
 // eqs. (1)-(3), shapes of §2.1 Table 1) for the global layers: every query
 // attends to all keys at or before its position, with the per-head sink in the
 // softmax denominator.  The same kernel runs the sliding windows the band
-// kernel does not take (window > 128, or 4, 16, 32, 64 or 128 query heads per
-// KV head): an item then visits only the 128-key blocks its window reaches,
-// and the low edge of the window is masked like the diagonal.
+// kernel does not take (window > 128, or other than 8 query heads per KV
+// head): an item then visits only the 128-key blocks its window reaches, and
+// the low edge of the window is masked like the diagonal.
 //
 // A query tile is T = 128 / G consecutive tokens x the G query heads of one KV
 // head (128 MMA rows, row r = token * G + head).  Each work item is a pair of
@@ -261,8 +261,8 @@ __device__ __forceinline__ void cau_softmax(const CausalArgs &args, int32_t X, u
           w[e] = pack_bf16x2(v.x, v.y);
         }
       }
-      // Rows 4k..4k+3 are 4 consecutive heads of one token (G >= 4): transpose
-      // the 4 x 4 sectors within each lane quad so each store writes whole lines.
+      // Transpose the 4 x 4 sectors within each lane quad so each store writes
+      // the whole 128-byte line of one of the quad's rows.
 #pragma unroll
       for (int32_t jj = 0; jj < 2; ++jj) {
 #pragma unroll
@@ -281,19 +281,23 @@ __device__ __forceinline__ void cau_softmax(const CausalArgs &args, int32_t X, u
           if (q & 1) w[8 * jj + e] = recv; else w[8 * (jj + 1) + e] = recv;
         }
       }
-      if (rvalid) {
-        __nv_bfloat16 *row0 = args.out + (orow - q) * kDv + hf * 64 + q * 16;
+      // The quad's rows are four heads of one token when G >= 4 (consecutive
+      // rows of out), else the heads of two (G = 2) or four (G = 1) tokens.
 #pragma unroll
-        for (int32_t pq = 0; pq < 4; ++pq) {
-          uint32_t (&sec)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8 * pq);
-          if (!SA_OUT(orow - q + pq, args.n_rows, 0x13)) continue;
-          if (args.out_v8) {
-            st_global_v8(row0 + pq * kDv, sec);
-          } else {
-            uint4 *d4 = reinterpret_cast<uint4 *>(row0 + pq * kDv);
-            d4[0] = make_uint4(sec[0], sec[1], sec[2], sec[3]);
-            d4[1] = make_uint4(sec[4], sec[5], sec[6], sec[7]);
-          }
+      for (int32_t pq = 0; pq < 4; ++pq) {
+        uint32_t (&sec)[8] = *reinterpret_cast<uint32_t(*)[8]>(w + 8 * pq);
+        const int32_t rq = (row & ~3) + pq;
+        const int32_t pos_q = it.t0 + X * args.T + rq / G;
+        if (pos_q >= it.L) continue;
+        const size_t orq = static_cast<size_t>(it.s0 + pos_q) * args.Hq + it.kvh * G + rq % G;
+        if (!SA_OUT(orq, args.n_rows, 0x13)) continue;
+        __nv_bfloat16 *dst = args.out + orq * kDv + hf * 64 + q * 16;
+        if (args.out_v8) {
+          st_global_v8(dst, sec);
+        } else {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+          d4[0] = make_uint4(sec[0], sec[1], sec[2], sec[3]);
+          d4[1] = make_uint4(sec[4], sec[5], sec[6], sec[7]);
         }
       }
     }

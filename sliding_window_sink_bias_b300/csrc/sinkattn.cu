@@ -213,8 +213,8 @@ sinkattn_status launch_band(const void *q, const void *k, const void *v, const A
   return launched(kern);
 }
 
-// Causal prefill with G >= 4 query heads per KV head, global or windowed
-// (except the band kernel's shapes): pairs of query tiles per CTA, longest first.
+// Causal prefill, global or windowed, positive logit scale (except the band
+// kernel's shapes): pairs of query tiles per CTA, longest first.
 sinkattn_status launch_causal(const void *q, const void *k, const void *v, const AttnArgs &a,
                               const int32_t *cu_seqlens, int32_t batch, int32_t total,
                               int32_t max_seqlen, const DeviceInfo &dev, cudaStream_t stream) {
@@ -525,10 +525,13 @@ sinkattn_status sinkattn_prefill_ex(const void *q, const void *k, const void *v,
   if (G == sa::kBandG && window >= 1 && window <= sa::kBandMaxWin * sa::kBandSeg - sa::kBandSeg &&
       a.scale_log2 > 0.f)
     return launch_band(q, k, v, a, cu_seqlens, batch, total, dev, s);
-  // every other shape with G >= 4, global or windowed: the two-tile causal
-  // kernel (a window only trims the key blocks of an item)
-  if (G >= 4 && a.scale_log2 > 0.f)
+  // every other shape, global or windowed: the two-tile causal kernel (a
+  // window only trims the key blocks of an item)
+  if (a.scale_log2 > 0.f)
     return launch_causal(q, k, v, a, cu_seqlens, batch, total, max_seqlen, dev, s);
+  // a logit scale <= 0: the general kernel (the band and causal kernels take
+  // the maximum of the raw logits and scale it, which is the maximum of the
+  // scaled logits only for a positive scale)
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, 192, num_q_heads, total, G, tile_tokens) ||

@@ -162,7 +162,7 @@ WORKLOADS = {
     "swa_w512_prefill_1x32768": dict(kind="prefill", seqlens=[32768], hq=64, hkv=8, window=512,
                                      rope_base=1e4),
     # a 128-token window over 64 query heads in pairs (2 per KV head, tiles of
-    # 64 tokens): the general prefill kernel
+    # 64 tokens): the causal kernel
     "swa_g2_prefill_1x32768": dict(kind="prefill", seqlens=[32768], hq=64, hkv=32, window=128,
                                    rope_base=1e4),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)

@@ -59,17 +59,17 @@ def _set_limits(L, shrink, cols):
 
 
 # ---------------------------------------------------------------- the cases
-def _prefill_case(hq, hkv, lens, window, base, seed):
+def _prefill_case(hq, hkv, lens, window, base, seed, scale=None):
     inp = synth.prefill_inputs(lens, hq, hkv, window=window, rope_base=base, seed=seed, device="cpu")
 
     def run(sa, out=None, lse=None):
         return sa.prefill(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.sink.to(DEV),
                           inp.cu_seqlens.to(DEV), max_seqlen=max(lens), window=window,
-                          rope_base=base, out=out, lse=lse)
+                          rope_base=base, out=out, lse=lse, scale=scale)
 
     def oracle(om):
         return om.prefill(inp.q, inp.k, inp.v, inp.sink, inp.cu_seqlens, window=window,
-                          rope_base=base)
+                          rope_base=base, scale=scale)
     return run, oracle
 
 
@@ -129,9 +129,11 @@ def _fp8_case(lens, seed):
 CASES = {
     # band kernel (8 heads a KV head, W <= 128), ragged lengths
     "swa_band": lambda: _prefill_case(64, 8, [200, 57, 1, 300], 128, 1e4, 61),
-    # general kernel: 2 heads a KV head with a window, 1 head a KV head global
-    "general_g2_window": lambda: _prefill_case(16, 8, [150, 33], 64, 1e4, 62),
-    "general_g1_global": lambda: _prefill_case(8, 8, [140, 9], 0, 5e6, 63),
+    # causal kernel with 2 heads a KV head and a window, 1 head a KV head global
+    "causal_g2_window": lambda: _prefill_case(16, 8, [150, 33], 64, 1e4, 62),
+    "causal_g1_global": lambda: _prefill_case(8, 8, [140, 9], 0, 5e6, 63),
+    # general kernel: a negative logit scale
+    "general_neg_scale": lambda: _prefill_case(64, 8, [150, 33], 128, 1e4, 71, scale=-0.05),
     # causal kernel: global, several sequences; and with a window past one block
     "ga_causal": lambda: _prefill_case(64, 4, [300, 129, 5], 0, 5e6, 64),
     "causal_window": lambda: _prefill_case(64, 8, [700, 129, 1], 256, 1e4, 70),

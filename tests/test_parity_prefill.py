@@ -98,6 +98,17 @@ def test_rope_variants_and_scale(oracle_mod):
             assert_parity(o, l, ro, rl, f"{kw} W={window}")
 
 
+@pytest.mark.parametrize("window,hkv", [(128, 8), (0, 4), (64, 32), (0, 64), (300, 16)])
+def test_negative_scale(oracle_mod, window, hkv):
+    """A logit scale < 0 (the general kernel: the running max over the scaled
+    logits) on the band's, the causal kernel's and 1-2 heads a KV head's
+    shapes."""
+    for scale in (-0.05, -1.0 / 192 ** 0.5):
+        o, l, ro, rl = run_case(oracle_mod, [150, 1, 70], 64, hkv, window, 1e4, seed=8,
+                                scale=scale)
+        assert_parity(o, l, ro, rl, f"scale={scale:.3f} W={window} Hkv={hkv}")
+
+
 def test_long_positions_rope(oracle_mod):
     # large positions stress the RoPE angle: GA base 5e6, rows near the end of 20000 tokens
     L = 20000
@@ -181,8 +192,8 @@ def test_swa_w512_prefill_sampled(oracle_mod):
 
 @pytest.mark.slow
 def test_swa_g2_prefill_sampled(oracle_mod):
-    """1 x 32768 tokens, 64/32 heads, W=128 (the general kernel, tiles of 64
-    tokens x 2 heads): sampled rows."""
+    """1 x 32768 tokens, 64/32 heads, W=128 (the causal kernel with tiles of
+    64 tokens x 2 heads, a lane quad's rows two tokens apart): sampled rows."""
     import sliding_window_sink_bias_b300 as sa
     wl = synth.WORKLOADS["swa_g2_prefill_1x32768"]
     inp = synth.prefill_inputs(wl["seqlens"], wl["hq"], wl["hkv"], window=wl["window"],
