@@ -287,7 +287,8 @@ def bench_prefill(name, steps, warmup, ws, local, with_e2e):
 
     def call():
         sa.prefill(inp.q, inp.k, inp.v, inp.sink, inp.cu_seqlens, max_seqlen=inp.max_seqlen,
-                   window=wl["window"], rope_base=wl["rope_base"], out=out, lse=lse)
+                   window=wl["window"], rope_base=wl["rope_base"], out=out, lse=lse,
+                   scale=wl.get("scale"))
 
     with ClockSampler(local) as clk:
         ms, per = time_calls(call, steps, warmup, ws)

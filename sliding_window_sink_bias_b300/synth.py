@@ -167,6 +167,9 @@ WORKLOADS = {
                                    rope_base=1e4),
     # reduced shapes of the same kernels, for profiler captures (a few GB on the device)
     "swa_prefill_1x32768": dict(kind="prefill", seqlens=[32768], **SWA),
+    # the SWA layer with a negative logit scale: the general prefill kernel
+    "swa_negscale_prefill_1x32768": dict(kind="prefill", seqlens=[32768], scale=-0.0721,
+                                         **SWA),
     "ga_prefill_1x16384": dict(kind="prefill", seqlens=[16384], **GA),
     "mtp_decode_ga_b8_t4": dict(kind="decode", batch=8, t=4, s_cap=131072,
                                 len_lo=65536, len_hi=131072, **GA),
