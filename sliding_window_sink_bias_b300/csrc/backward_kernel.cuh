@@ -229,6 +229,32 @@ __device__ __forceinline__ void bwd_unrotate(float (&x)[64], int32_t pos, int32_
   }
 }
 
+// The same with the 32 angles of this row's position given, (cos, sin) of
+// pair t at cs[t] (shared memory: the rows of one token share them).
+template <int32_t kStyle>
+__device__ __forceinline__ void bwd_unrotate_cs_t(float (&x)[64], const float2 *cs) {
+  const float4 *cs4 = reinterpret_cast<const float4 *>(cs);
+#pragma unroll
+  for (int32_t t2 = 0; t2 < 16; ++t2) {
+    const float4 a = cs4[t2];  // pairs 2 t2 and 2 t2 + 1
+#pragma unroll
+    for (int32_t e = 0; e < 2; ++e) {
+      const int32_t t = 2 * t2 + e;
+      const float c = e ? a.z : a.x, sn = e ? a.w : a.y;
+      constexpr bool kInter = kStyle == 0;
+      const int32_t i0 = kInter ? 2 * t : t, i1 = kInter ? 2 * t + 1 : t + 32;
+      const float u = x[i0], w = x[i1];
+      x[i0] = u * c + w * sn;
+      x[i1] = w * c - u * sn;
+    }
+  }
+}
+// (the pairing is a compile-time index pattern in each instance, so x stays in registers)
+__device__ __forceinline__ void bwd_unrotate_cs(float (&x)[64], int32_t style, const float2 *cs) {
+  if (style == 0) bwd_unrotate_cs_t<0>(x, cs);
+  else bwd_unrotate_cs_t<1>(x, cs);
+}
+
 // Gradient epilogues write 64-dim lines (128 bytes) of rows.  The four threads
 // of a lane quad hold the same line of four rows, as 32 packed bf16 pairs each
 // (w[8 s .. 8 s + 7] = sector s, 16 dims).  A 4 x 4 exchange of sectors inside
@@ -275,12 +301,13 @@ __device__ __forceinline__ void bwd_store_line_quad(uint32_t (&w)[32], LineOf li
 
 // Lines [l0, l0 + nl) of a gradient row held in TMEM from column t_col (fp32,
 // this thread's lane): * scale, inverse RoPE on line 0 (dims 0..63, at
-// position pos) when rope_on, bf16, stored through bwd_store_line_quad.
+// position pos; angles from cs when given) when rope_on, bf16, stored through
+// bwd_store_line_quad.
 template <class LineOf>
 __device__ __forceinline__ void bwd_store_lines(uint32_t t_col, int32_t l0, int32_t nl, float scale,
                                                 bool rope_on, int32_t style, int32_t pos,
                                                 const unsigned long long *turns, LineOf line,
-                                                bool v8) {
+                                                bool v8, const float2 *cs = nullptr) {
 #pragma unroll 1
   for (int32_t l = l0; l < l0 + nl; ++l) {
     uint32_t r[64];
@@ -291,7 +318,10 @@ __device__ __forceinline__ void bwd_store_lines(uint32_t t_col, int32_t l0, int3
     float x[64];
 #pragma unroll
     for (int32_t e = 0; e < 64; ++e) x[e] = __uint_as_float(r[e]) * scale;
-    if (l == 0 && rope_on) bwd_unrotate(x, pos, style, turns);
+    if (l == 0 && rope_on) {
+      if (cs != nullptr) bwd_unrotate_cs(x, style, cs);
+      else bwd_unrotate(x, pos, style, turns);
+    }
     uint32_t w[32];
 #pragma unroll
     for (int32_t e = 0; e < 32; ++e) w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
@@ -349,7 +379,9 @@ struct DqLayout {
   // qf, kv_full[3], kv_empty[3], mm1[2], q_empty, acc_full, ds_ready[2], drain
   static constexpr uint32_t kBarOff = kStOff + kStages * kStage;
   static constexpr uint32_t kMiscOff = kBarOff + 14 * 8;  // tmem slot, abort flag
-  static constexpr uint32_t kBytes = kMiscOff + 16;
+  // RoPE angles of the epilogue: 4 warps x 4 tokens x 32 pairs of (cos, sin)
+  static constexpr uint32_t kAngOff = kMiscOff + 16;
+  static constexpr uint32_t kBytes = kAngOff + 4 * 4 * 32 * 8;
   static constexpr uint32_t kDynSmem = kBytes + 1024;
 };
 static_assert(DqLayout::kDynSmem <= 232448, "dq kernel shared memory");
@@ -624,8 +656,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (tj >= cur.L || !SA_OUT(gr, static_cast<int64_t>(a.total) * a.Hq, 0x34)) return nullptr;
         return a.dq + gr * kDqk + 64 * l;
       };
+      // line 0's inverse rotation: the G >= 8 rows of a token share its 32
+      // angles, so its lanes compute 32 / min(G, 32) of them each and the warp
+      // reads them back from shared memory
+      const float2 *cs = nullptr;
+      if (half == 0 && a.rope_on && G >= 8) {
+        const int32_t lane = threadIdx.x & 31, Gw = min(G, 32);
+        float2 *ang = reinterpret_cast<float2 *>(smem + Ly::kAngOff) + (warp * 4 + lane / Gw) * 32;
+        __syncwarp();  // the previous item's angles are read
+        for (int32_t p = lane % Gw; p < 32; p += Gw) {
+          float c, sn;
+          rope_cs(ti, a.rope_turns[p], c, sn);
+          ang[p] = make_float2(c, sn);
+        }
+        __syncwarp();
+        cs = ang;
+      }
       bwd_store_lines(lane_t + kDqColAcc, half == 0 ? 0 : 1, half == 0 ? 1 : 2, a.scale, a.rope_on,
-                      a.rope_style, ti, a.rope_turns, line, a.grad_v8 != 0);
+                      a.rope_style, ti, a.rope_turns, line, a.grad_v8 != 0, cs);
       tc_fence_before();
       g0 += cur.nblk;
       ++k;
