@@ -839,7 +839,8 @@ def main():
             "value": ws * w_tf, "unit": "TFLOP/s", "ms_per_step": w["ms"],
             "kernel": "causal prefill kernel (2 query heads per KV head, W = 128)",
             "gbs": w_gbs,
-            "roofline": roofline_obj("hbm", w_gbs, peaks["hbm_gbs"], "GB/s", None),
+            "roofline": roofline_obj("hbm", w_gbs, peaks["hbm_gbs"], "GB/s",
+                                     traffic_for("causal_swa_g2_prefill_1x32768", w["tokens"])),
             "clocks": w["clocks"]}
         for name in ("mtp_decode_ga_b64_t4", "mtp_decode_ga_fp8_b64_t4",
                      "mtp_decode_ga_fp8_rot_b64_t4", "mtp_decode_swa_b64_t4",
