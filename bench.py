@@ -547,7 +547,8 @@ def bench_decode(name, steps, warmup, ws, local):
         else:
             sa.decode(inp.q, inp.kcache, inp.vcache, inp.seqlens, inp.sink, max_seqlen=max(lens),
                       window=wl["window"], rope_base=wl["rope_base"], workspace=work, out=out,
-                      lse=lse, kv_ring=wl.get("kv_ring", False))
+                      lse=lse, kv_ring=wl.get("kv_ring", False),
+                      k_rotated=wl.get("k_rotated", False))
 
     # the decode working set can sit in L2 for the SWA layer: flush between steps
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)

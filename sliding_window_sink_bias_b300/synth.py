@@ -142,6 +142,9 @@ WORKLOADS = {
     # slots (>= W + T - 1 = 131, a multiple of 16) per sequence
     "mtp_decode_swa_ring_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=144, kv_ring=True,
                                        len_lo=65536, len_hi=262144, **SWA),
+    # the same ring holding keys stored after RoPE: the kernel rotates q only
+    "mtp_decode_swa_ring_rot_b64_t4": dict(kind="decode", batch=64, t=4, s_cap=144, kv_ring=True,
+                                           k_rotated=True, len_lo=65536, len_hi=262144, **SWA),
     # one hybrid block of the model (§2.1: 5 SWA layers then 1 GA layer) over a
     # varlen batch of 8 sequences, lengths log-uniform in [4096, 131072]
     "hybrid_block_ragged_8seq": dict(kind="hybrid", n_seq=8, len_lo=4096, len_hi=131072,
