@@ -23,7 +23,7 @@ DV = 128
 DROT = 64
 
 # tensor stream ids, so each tensor of a workload has its own seed
-_STREAM = {"q": 1, "k": 2, "v": 3, "sink": 4, "lens": 5, "kcache": 6, "vcache": 7}
+_STREAM = {"q": 1, "k": 2, "v": 3, "sink": 4, "lens": 5, "kcache": 6, "vcache": 7, "dout": 8}
 
 
 def _gen(seed: int, stream: str, device) -> torch.Generator:
