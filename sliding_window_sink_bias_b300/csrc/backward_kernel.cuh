@@ -623,16 +623,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int32_t kb = cur.lo + j * kDqBN + 32 * half;
         const int32_t c_lo = (a.window > 0 ? ti - a.window + 1 : 0) - kb;
         const uint32_t span = rvalid ? static_cast<uint32_t>(ti - kb - c_lo) : 0u;
+        // every row of the warp sees all 32 columns: no per-element mask
+        const bool whole = __all_sync(0xffffffffu, rvalid && c_lo <= 0 && ti - kb >= 31);
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nl2 = make_float2(-lse2, -lse2), nd2 = make_float2(-Drow, -Drow);
 #pragma unroll
         for (int32_t c = 0; c < 32; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int32_t e = 0; e < 2; ++e) {
-            const bool vis = static_cast<uint32_t>(c + e - c_lo) <= span && rvalid;
-            const float p = vis ? ex2(__uint_as_float(sv[c + e]) * a.scale_log2 - lse2) : 0.f;
-            ds[e] = p * (__uint_as_float(pv[c + e]) - Drow);
+          const float2 y =
+              ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl2);
+          float2 p = make_float2(ex2(y.x), ex2(y.y));
+          if (!whole) {
+            if (!(static_cast<uint32_t>(c - c_lo) <= span && rvalid)) p.x = 0.f;
+            if (!(static_cast<uint32_t>(c + 1 - c_lo) <= span && rvalid)) p.y = 0.f;
           }
-          sv[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+          const float2 ds = fmul2(
+              p, fadd2(make_float2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), nd2));
+          sv[c >> 1] = pack_bf16x2(ds.x, ds.y);
         }
         // dS of this half (16 bf16 pairs) over the first 16 of its own S columns
         tmem_st16p(cs, sv);
