@@ -1035,21 +1035,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // S^T/dP^T(g) are in registers: their columns may take the next sub-tile's
         tc_fence_before();
         mbar_arrive(B_SR);
+        // every key of the warp sees all 32 columns: no per-element mask
+        const bool whole = __all_sync(
+            0xffffffffu, kvalid && c_lo <= 0 && static_cast<int64_t>(span) > 31 - c_lo);
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int32_t c = 0; c < 32; c += 4) {
           const float4 l4 = cl4[c >> 2], d4 = cd4[c >> 2];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pp[4], ds[4];
+          const float2 nl[2] = {make_float2(-l4.x, -l4.y), make_float2(-l4.z, -l4.w)};
+          const float2 nd[2] = {make_float2(-d4.x, -d4.y), make_float2(-d4.z, -d4.w)};
 #pragma unroll
-          for (int32_t e = 0; e < 4; ++e) {
-            const bool vis = static_cast<uint32_t>(c + e - c_lo) < span;
-            pp[e] = vis ? ex2(__uint_as_float(sv[c + e]) * a.scale_log2 - lv[e]) : 0.f;
-            ds[e] = pp[e] * (__uint_as_float(pv[c + e]) - dv[e]);
+          for (int32_t h2 = 0; h2 < 2; ++h2) {
+            const int32_t cc = c + 2 * h2;  // columns cc, cc + 1 (already read: 0 .. cc - 1)
+            const float2 y =
+                ffma2(make_float2(__uint_as_float(sv[cc]), __uint_as_float(sv[cc + 1])), sc2, nl[h2]);
+            float2 p = make_float2(ex2(y.x), ex2(y.y));
+            if (!whole) {
+              if (!(static_cast<uint32_t>(cc - c_lo) < span)) p.x = 0.f;
+              if (!(static_cast<uint32_t>(cc + 1 - c_lo) < span)) p.y = 0.f;
+            }
+            const float2 ds = fmul2(
+                p, fadd2(make_float2(__uint_as_float(pv[cc]), __uint_as_float(pv[cc + 1])), nd[h2]));
+            sv[cc >> 1] = pack_bf16x2(p.x, p.y);
+            pv[cc >> 1] = pack_bf16x2(ds.x, ds.y);
           }
-          sv[c >> 1] = pack_bf16x2(pp[0], pp[1]);
-          sv[(c >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
-          pv[c >> 1] = pack_bf16x2(ds[0], ds[1]);
-          pv[(c >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
         }
         // dV/dK(g-1) complete: they have read P^T/dS^T(g-1), and every row
         // has read this CTA's other lse / D slot

@@ -6,6 +6,7 @@ an angle or an output row without failing at run time.
 - bwd_dq_kernel, rows: the visible columns of a 32-key half block as one
   unsigned range compare, and the warp-wide shortcut taken when every column is
   visible.
+- bwd_dkdv_kernel, rows: the same shortcut for the query columns of a key.
 - bwd_dq_kernel, epilogue: the lanes of one token share its 32 RoPE angles
   through a shared-memory slot per (warp, token).
 - sinkattn_causal_kernel, epilogue: the output row written by each of the four
@@ -45,6 +46,20 @@ def test_dq_column_range_matches_the_window(window):
         assert vis == want, (ti, kb, window, rvalid)
         # the shortcut is taken exactly when every column is visible
         assert whole == all(want), (ti, kb, window, rvalid)
+
+
+def test_dkdv_whole_shortcut():
+    """bwd_dkdv_kernel, rows: column c is visible iff (unsigned)(c - c_lo) <
+    span (span 0 for a key past the sequence); the shortcut is taken iff the
+    key is valid, c_lo <= 0 and span > 31 - c_lo, which must mean all 32."""
+    rng = random.Random(5)
+    for _ in range(20000):
+        c_lo = rng.randrange(-200, 200)
+        kvalid = rng.random() < 0.9
+        span = rng.randrange(0, 260) if kvalid else 0
+        vis = [((c - c_lo) & 0xFFFFFFFF) < span for c in range(32)]
+        whole = kvalid and c_lo <= 0 and span > 31 - c_lo
+        assert whole == all(vis), (c_lo, span, kvalid)
 
 
 @pytest.mark.parametrize("G", [8, 16, 32, 64])
