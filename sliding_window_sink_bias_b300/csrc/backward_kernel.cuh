@@ -230,7 +230,9 @@ __device__ __forceinline__ void bwd_unrotate(float (&x)[64], int32_t pos, int32_
 }
 
 // The same with the 32 angles of this row's position given, (cos, sin) of
-// pair t at cs[t] (shared memory: the rows of one token share them).
+// pair t at cs[t] (shared memory: the rows of one token share them).  One
+// instance per pairing style, so the index pattern is fixed at compile time
+// and x stays in registers.
 template <int32_t kStyle>
 __device__ __forceinline__ void bwd_unrotate_cs_t(float (&x)[64], const float2 *cs) {
   const float4 *cs4 = reinterpret_cast<const float4 *>(cs);
@@ -249,7 +251,6 @@ __device__ __forceinline__ void bwd_unrotate_cs_t(float (&x)[64], const float2 *
     }
   }
 }
-// (the pairing is a compile-time index pattern in each instance, so x stays in registers)
 __device__ __forceinline__ void bwd_unrotate_cs(float (&x)[64], int32_t style, const float2 *cs) {
   if (style == 0) bwd_unrotate_cs_t<0>(x, cs);
   else bwd_unrotate_cs_t<1>(x, cs);
