@@ -6,7 +6,8 @@ an angle or an output row without failing at run time.
 - bwd_dq_kernel, rows: the visible columns of a 32-key half block as one
   unsigned range compare, and the warp-wide shortcut taken when every column is
   visible.
-- bwd_dkdv_kernel, rows: the same shortcut for the query columns of a key.
+- bwd_dkdv_kernel, rows: the query columns of a key as one range, and the
+  same shortcut.
 - bwd_dq_kernel, epilogue: the lanes of one token share its 32 RoPE angles
   through a shared-memory slot per (warp, token).
 - sinkattn_causal_kernel, epilogue: the output row written by each of the four
@@ -46,6 +47,41 @@ def test_dq_column_range_matches_the_window(window):
         assert vis == want, (ti, kb, window, rvalid)
         # the shortcut is taken exactly when every column is visible
         assert whole == all(want), (ti, kb, window, rvalid)
+
+
+def _dkdv_columns(kj, kvalid, i0, L, window, G, half):
+    """The dk/dv rows' test, as in backward_kernel.cuh: key kj, a sub-tile of
+    64 packed rows starting at query token i0 (column c is token i0 + c // G),
+    this thread's columns 32 half .. 32 half + 31 as c - 32 half."""
+    d0 = kj - i0
+    c_lo = (d0 * G if d0 > 0 else 0) - 32 * half
+    c_hi = min(L - i0, 64) * G
+    if window > 0:
+        c_hi = min(c_hi, max(0, min(d0 + window, 64)) * G)
+    c_hi = min(c_hi, 64) - 32 * half
+    span = c_hi - c_lo if (kvalid and c_hi > c_lo) else 0
+    return [((c - c_lo) & 0xFFFFFFFF) < span for c in range(32)], c_lo, span
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("window", [0, 1, 7, 128, 300])
+def test_dkdv_column_range_matches_the_window(G, window):
+    rng = random.Random(G * 1000 + window)
+    TS = 64 // G
+    for _ in range(1500):
+        L = rng.randrange(1, 1500)
+        kj = rng.randrange(0, L + 130)  # keys past the end too
+        kvalid = kj < L
+        i0 = rng.randrange(0, L) // TS * TS
+        for half in (0, 1):
+            vis, c_lo, span = _dkdv_columns(kj, kvalid, i0, L, window, G, half)
+            for c in range(32):
+                col = c + 32 * half
+                i = i0 + col // G
+                want = kvalid and i < L and _visible(kj, i, window)
+                assert vis[c] == want, (G, window, L, kj, i0, half, c)
+            whole = kvalid and c_lo <= 0 and span > 31 - c_lo
+            assert whole == all(vis)
 
 
 def test_dkdv_whole_shortcut():
