@@ -223,7 +223,11 @@ def dq_roles(nblk, skip=()):
     the dQ that read it (KVE), the Q/dO tile with a commit after the item's last
     S/dP (QE) and hands the finished dQ to the rows with a commit after the
     item's last dQ (ACCF): one phase per item, so neither of the last two waits
-    can find its barrier two phases behind.
+    can find its barrier two phases behind.  Every wait is bounded ("await"):
+    a role whose wait returns False (the CTA is aborting) leaves its loop; the
+    copy thread then waits for the last copy into the Q/dO tile and into each
+    K/V stage and the MMA thread for a commit behind its last MMA, as the
+    kernel does before shared memory and TMEM go back.
     `skip` names waits to leave out (to show that the model notices)."""
     items = list(nblk)
     seq = [(it, j) for it, n in enumerate(items) for j in range(n)]  # loader order
@@ -231,41 +235,65 @@ def dq_roles(nblk, skip=()):
 
     def producer():
         yield ("tma", "QO", ("QO", 0), "QF")
+        n_q, ld_g = 1, 0
         for ld in range(len(seq)):
             st = ld % NS
             if ld >= NS and "producer_kve" not in skip:
-                yield ("wait", f"KVE{st}", ld // NS)  # dQ(ld - NS) read the stage
+                if not (yield ("await", f"KVE{st}", ld // NS)):  # dQ(ld - NS) read the stage
+                    break
             yield ("tma", f"KV{st}", ("KV", ld), f"KV{st}")
+            ld_g += 1
             it, j = seq[ld]
             # once block ld is queued, the next item's Q/dO follows the item's
             # last S/dP (interleaved with the K/V loads as the kernel does)
             if j == items[it] - 1 and it + 1 < len(items):
                 if "producer_qe" not in skip:
-                    yield ("wait", "QE", it + 1)
+                    if not (yield ("await", "QE", it + 1)):
+                        break
                 yield ("tma", "QO", ("QO", it + 1), "QF")
+                n_q += 1
+        # drain: no copy may still be landing when shared memory goes back
+        if "producer_drain" not in skip:
+            yield ("drain", "QF", n_q)
+            for st in range(NS):
+                if ld_g > st:
+                    yield ("drain", f"KV{st}", (ld_g - 1 - st) // NS + 1)
 
     def issuer():
         def issue_sdp(it, g):
-            yield ("wait", f"KV{g % NS}", g // NS + 1)
+            if not (yield ("await", f"KV{g % NS}", g // NS + 1)):
+                return False
             b = g & 1
             yield ("mma", [("QO", ("QO", it)), (f"KV{g % NS}", ("KV", g))],
                    [(f"S{b}h0", ("S", g)), (f"S{b}h1", ("S", g))])
             yield ("commit", f"MM1{b}")
+            return True
+
+        issued = False
+        ok = True
         for it, n in enumerate(items):
             g0 = first[it]
-            yield ("wait", "QF", it + 1)
-            yield from issue_sdp(it, g0)
+            ok = yield ("await", "QF", it + 1)
+            if ok:
+                ok = yield from issue_sdp(it, g0)
+            if not ok:
+                break
+            issued = True
             if n == 1:
                 yield ("commit", "QE")
             for j in range(n):
                 g = g0 + j
                 if j + 1 < n:
-                    yield from issue_sdp(it, g + 1)
+                    ok = yield from issue_sdp(it, g + 1)
+                    if not ok:
+                        break
                     if j + 2 == n:
                         yield ("commit", "QE")  # the item's last S/dP
                 b = g & 1
                 if "issuer_dsr" not in skip:
-                    yield ("wait", f"DSR{b}", (g >> 1) + 1)  # both row halves wrote dS(g)
+                    ok = yield ("await", f"DSR{b}", (g >> 1) + 1)  # both row halves wrote dS(g)
+                    if not ok:
+                        break
                 reads = [(f"S{b}h0", ("dS", g)), (f"S{b}h1", ("dS", g)), (f"KV{g % NS}", ("KV", g))]
                 if j > 0:
                     reads.append(("dQ", ("dQ", it, j - 1)))
@@ -273,6 +301,12 @@ def dq_roles(nblk, skip=()):
                 yield ("commit", f"KVE{g % NS}")
                 if j == n - 1:
                     yield ("commit", "ACCF")
+            if not ok:
+                break
+        # drain: every MMA done before TMEM goes back
+        if issued and "mma_drain" not in skip:
+            yield ("commit", "DRAIN")
+            yield ("drain", "DRAIN", 1)
 
     def rows(h):
         def role():
@@ -281,17 +315,19 @@ def dq_roles(nblk, skip=()):
                 for j in range(n):
                     g = g0 + j
                     b = g & 1
-                    yield ("wait", f"MM1{b}", (g >> 1) + 1)
+                    if not (yield ("await", f"MM1{b}", (g >> 1) + 1)):
+                        return
                     yield ("read", f"S{b}h{h}", ("S", g))
                     yield ("write", f"S{b}h{h}", ("dS", g))  # dS over this half's S columns
                     yield ("arrive", f"DSR{b}")
                 if "rows_accf" not in skip:
-                    yield ("wait", "ACCF", it + 1)  # the item's last dQ
+                    if not (yield ("await", "ACCF", it + 1)):  # the item's last dQ
+                        return
                 yield ("read", "dQ", ("dQ", it, n - 1))
         return role()
 
     roles = {"producer": producer(), "issuer": issuer(), "rows0": rows(0), "rows1": rows(1)}
-    return roles, {"DSR0": 2, "DSR1": 2}
+    return roles, {"DSR0": 2, "DSR1": 2, EXIT_CHECK: True}
 
 
 def dkdv_roles(nsub, skip=()):
@@ -305,7 +341,9 @@ def dkdv_roles(nsub, skip=()):
     every read of that slot's previous contents is done.  The MMA thread
     frees a Q/dO stage after the dV/dK that read it (QSE), the K/V block after
     the item's last S^T/dP^T (KVE) and hands the finished accumulators to the
-    rows after the item's last dV/dK (ACCF).  `skip` names waits to leave out."""
+    rows after the item's last dV/dK (ACCF).  Every wait is bounded, with the
+    copy and MMA threads' drains of the dq kernel.  `skip` names waits to
+    leave out."""
     items = list(nsub)
     seq = [(it, j) for it, n in enumerate(items) for j in range(n)]
     first = [sum(items[:i]) for i in range(len(items))]
@@ -313,38 +351,64 @@ def dkdv_roles(nsub, skip=()):
 
     def producer():
         yield ("tma", "KVB", ("KVB", 0), "KF")
+        n_kv, ld_g = 1, 0
         for ld in range(total):
             it, j = seq[ld]
             if j == 0 and it > 0:
                 if "producer_kve" not in skip:
-                    yield ("wait", "KVE", it)  # the previous item's last S^T/dP^T
+                    if not (yield ("await", "KVE", it)):  # the previous item's last S^T/dP^T
+                        break
                 yield ("tma", "KVB", ("KVB", it), "KF")
+                n_kv += 1
             if ld >= NS and "producer_qse" not in skip:
-                yield ("wait", f"QSE{ld % NS}", ld // NS)  # dV/dK(ld - NS) read the stage
+                # dV/dK(ld - NS) read the stage
+                if not (yield ("await", f"QSE{ld % NS}", ld // NS)):
+                    break
             yield ("tma", f"QO{ld % NS}", ("QO", ld), f"QS{ld % NS}")
+            ld_g += 1
+        if "producer_drain" not in skip:
+            yield ("drain", "KF", n_kv)
+            for st in range(NS):
+                if ld_g > st:
+                    yield ("drain", f"QS{st}", (ld_g - 1 - st) // NS + 1)
 
     def issuer():
         def issue_sdp(it, g):
-            yield ("wait", f"QS{g % NS}", g // NS + 1)
+            if not (yield ("await", f"QS{g % NS}", g // NS + 1)):
+                return False
             yield ("mma", [("KVB", ("KVB", it)), (f"QO{g % NS}", ("QO", g))],
                    [("STh0", ("ST", g)), ("STh1", ("ST", g))])
             yield ("commit", "MM1")
+            return True
+
+        issued = False
+        ok = True
         for it, n in enumerate(items):
             g0 = first[it]
-            yield ("wait", "KF", it + 1)
-            yield from issue_sdp(it, g0)
+            ok = yield ("await", "KF", it + 1)
+            if ok:
+                ok = yield from issue_sdp(it, g0)
+            if not ok:
+                break
+            issued = True
             if n == 1:
                 yield ("commit", "KVE")
             for s in range(n):
                 g = g0 + s
                 if s + 1 < n:
                     if "issuer_sr" not in skip:
-                        yield ("wait", "SR", g + 1)  # S^T/dP^T(g) read by every row
-                    yield from issue_sdp(it, g + 1)
+                        ok = yield ("await", "SR", g + 1)  # S^T/dP^T(g) read by every row
+                        if not ok:
+                            break
+                    ok = yield from issue_sdp(it, g + 1)
+                    if not ok:
+                        break
                     if s + 2 == n:
                         yield ("commit", "KVE")
                 if "issuer_pr" not in skip:
-                    yield ("wait", "PR", g + 1)  # P^T/dS^T(g) written
+                    ok = yield ("await", "PR", g + 1)  # P^T/dS^T(g) written
+                    if not ok:
+                        break
                 reads = [("Ph0", ("P", g)), ("Ph1", ("P", g)), (f"QO{g % NS}", ("QO", g))]
                 if s > 0:
                     reads.append(("acc", ("acc", it, s - 1)))
@@ -353,6 +417,11 @@ def dkdv_roles(nsub, skip=()):
                 yield ("commit", f"QSE{g % NS}")
                 if s + 1 == n:
                     yield ("commit", "ACCF")
+            if not ok:
+                break
+        if issued and "mma_drain" not in skip:
+            yield ("commit", "DRAIN")
+            yield ("drain", "DRAIN", 1)
 
     def rows(h, writer):
         def role():
@@ -363,27 +432,31 @@ def dkdv_roles(nsub, skip=()):
                 g0 = first[it]
                 for s in range(n):
                     g = g0 + s
-                    yield ("wait", "MM1", g + 1)
+                    if not (yield ("await", "MM1", g + 1)):
+                        return
                     yield ("read", f"STh{h}", ("ST", g))
                     yield ("arrive", "SR")
                     if "rows_lf" not in skip:
-                        yield ("wait", f"LF{g & 1}", (g >> 1) + 1)
+                        if not (yield ("await", f"LF{g & 1}", (g >> 1) + 1)):
+                            return
                     yield ("read", f"L{g & 1}", ("L", g))
                     if g > 0 and "rows_mm2" not in skip:
-                        yield ("wait", "MM2", g)  # dV/dK(g-1) read P^T/dS^T
+                        if not (yield ("await", "MM2", g)):  # dV/dK(g-1) read P^T/dS^T
+                            return
                     yield ("write", f"Ph{h}", ("P", g))
                     yield ("arrive", "PR")
                     if writer and g + 1 < total:
                         yield ("write", f"L{(g + 1) & 1}", ("L", g + 1))
                         yield ("arrive", f"LF{(g + 1) & 1}")
-                yield ("wait", "ACCF", it + 1)
+                if not (yield ("await", "ACCF", it + 1)):
+                    return
                 yield ("read", "acc", ("acc", it, n - 1))
         return role()
 
     roles = {"producer": producer(), "issuer": issuer(), "rows0": rows(0, True),
              "rows1": rows(1, False)}
     # PR, SR: both row roles arrive; LF: only the writer
-    return roles, {"PR": 2, "SR": 2}
+    return roles, {"PR": 2, "SR": 2, EXIT_CHECK: True}
 
 
 def run(make_roles, sizes, seed, skip=(), aborts=False):

@@ -158,3 +158,30 @@ def test_band_stalled_mma_thread_drains(lanes):
     for seed in range(200):
         sim = run(lambda s, sk: band_roles(s, sk, stall=True), lanes, seed, aborts=True)
         assert sim.aborted
+
+
+# ------------------------------------------------ abort and drain (backward kernels)
+@pytest.mark.parametrize("make_roles", [dq_roles, dkdv_roles], ids=["dq", "dkdv"])
+@pytest.mark.parametrize("sizes", [[1], [3], [1, 2, 1, 3], [2, 7], [5, 1, 4]])
+def test_backward_abort_drains_everything(make_roles, sizes):
+    """The dq and dk/dv kernels with a bounded wait running out at a random
+    moment: no role waits forever, no read sees the wrong data, and when every
+    role is done no copy is landing and no MMA running."""
+    aborted = 0
+    for seed in range(300):
+        sim = run(make_roles, sizes, seed, aborts=True)
+        aborted += sim.aborted
+    assert aborted > 50
+
+
+@pytest.mark.parametrize("make_roles", [dq_roles, dkdv_roles], ids=["dq", "dkdv"])
+@pytest.mark.parametrize("skip", ["producer_drain", "mma_drain"])
+def test_backward_missing_drain_is_caught(make_roles, skip):
+    caught = False
+    for seed in range(400):
+        try:
+            run(make_roles, [3, 2, 4], seed, skip=(skip,), aborts=True)
+        except ModelError:
+            caught = True
+            break
+    assert caught
