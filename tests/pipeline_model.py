@@ -476,72 +476,111 @@ def decode_roles(nblk, f8=False, skip=()):
     conversion warps rotate each unit's Q tile in shared memory, copy it into
     one of two TMEM buffers (QK^T reads it there) once the last QK^T of the
     unit two back has freed that buffer (QTFREE, a commit), and then free the
-    shared-memory tile."""
+    shared-memory tile.  Every wait is bounded ("await"); after leaving its loop
+    the copy thread waits for the last copy into the Q tile and into each
+    stage or slot, and the MMA thread for a commit behind its last MMA."""
     segs = list(nblk)
     S = 3 if f8 else 4
     S8 = 2
 
     def producer():
-        gk = 0
+        gk = gq = 0
+        ok = True
         for q, n in enumerate(segs):
-            yield ("wait", "QEMPTY", q)  # the rows copied the previous tile to TMEM
+            ok = yield ("await", "QEMPTY", q)  # the rows copied the previous tile to TMEM
+            if not ok:
+                break
             yield ("tma", "Q", ("Qraw", q), "QFULL")
+            gq += 1
             for _ in range(n):
                 if f8:
                     s8 = gk % S8
-                    yield ("wait", f"STGEMPTY{s8}", gk // S8)
+                    ok = yield ("await", f"STGEMPTY{s8}", gk // S8)
+                    if not ok:
+                        break
                     yield ("tma", f"STG{s8}", ("stg", gk), f"STGFULL{s8}")
                 else:
                     st = gk % S
                     if "producer_kvempty" not in skip:
-                        yield ("wait", f"KVEMPTY{st}", gk // S)
+                        ok = yield ("await", f"KVEMPTY{st}", gk // S)
+                        if not ok:
+                            break
                     yield ("tma", [f"K{st}", f"V{st}"], [("Kraw", gk), ("V", gk)], f"KVFULL{st}")
                 gk += 1
+            if not ok:
+                break
+        if "producer_drain" not in skip:
+            if gq > 0:
+                yield ("drain", "QFULL", gq)
+            slots, name = (S8, "STGFULL") if f8 else (S, "KVFULL")
+            for st in range(slots):
+                if gk > st:
+                    yield ("drain", f"{name}{st}", (gk - 1 - st) // slots + 1)
 
     def mma():
         gk = 0
+        issued = False
 
         def issue_pv(q, j, b, first):
-            yield ("wait", f"PFULL{b & 1}", (b >> 1) + 1)
+            if not (yield ("await", f"PFULL{b & 1}", (b >> 1) + 1)):
+                return False
             if first:
-                yield ("wait", "OEMPTY", q)
+                if not (yield ("await", "OEMPTY", q)):
+                    return False
             reads = [(f"P{b & 1}", ("P", b)), (f"V{b % S}", ("V", b))]
             if not first:
                 reads.append(("O", ("Ors", q, j - 1)))
             yield ("mma", reads, [("O", ("O", q, j))])
             yield ("commit", f"KVEMPTY{b % S}")
             yield ("commit", "PVDONE")
+            return True
 
-        for q, n in enumerate(segs):
-            qb = q & 1
-            yield ("wait", f"QTMEM{qb}", q // 2 + 1)
-            for j in range(n):
-                b = gk + j
-                yield ("wait", f"KREADY{b % S}", b // S + 1)
-                yield ("mma", [(f"QT{qb}", ("Q", q)), (f"K{b % S}", ("K", b))], [(f"P{b & 1}", ("S", b))])
-                yield ("commit", f"SFULL{b & 1}")
-                if j == n - 1:
-                    yield ("commit", f"QTFREE{qb}")
-                if j > 0:
-                    yield from issue_pv(q, j - 1, b - 1, j == 1)
-            yield from issue_pv(q, n - 1, gk + n - 1, n == 1)
-            gk += n
+        def body():
+            nonlocal gk, issued
+            for q, n in enumerate(segs):
+                qb = q & 1
+                if not (yield ("await", f"QTMEM{qb}", q // 2 + 1)):
+                    return
+                for j in range(n):
+                    b = gk + j
+                    if not (yield ("await", f"KREADY{b % S}", b // S + 1)):
+                        return
+                    yield ("mma", [(f"QT{qb}", ("Q", q)), (f"K{b % S}", ("K", b))],
+                           [(f"P{b & 1}", ("S", b))])
+                    issued = True
+                    yield ("commit", f"SFULL{b & 1}")
+                    if j == n - 1:
+                        yield ("commit", f"QTFREE{qb}")
+                    if j > 0:
+                        if not (yield from issue_pv(q, j - 1, b - 1, j == 1)):
+                            return
+                if not (yield from issue_pv(q, n - 1, gk + n - 1, n == 1)):
+                    return
+                gk += n
+
+        yield from body()
+        if issued and "mma_drain" not in skip:
+            yield ("commit", "DRAIN")
+            yield ("drain", "DRAIN", 1)
 
     def softmax():
         gs = 0
         for q, n in enumerate(segs):
             for j in range(n):
                 b = gs + j
-                yield ("wait", f"SFULL{b & 1}", (b >> 1) + 1)
+                if not (yield ("await", f"SFULL{b & 1}", (b >> 1) + 1)):
+                    return
                 yield ("read", f"P{b & 1}", ("S", b))
                 yield ("write", f"P{b & 1}", ("P", b))  # P over the S columns
                 if j > 0:
                     if "softmax_pvdone" not in skip:
-                        yield ("wait", "PVDONE", b)  # PV(j-1) complete
+                        if not (yield ("await", "PVDONE", b)):  # PV(j-1) complete
+                            return
                     yield ("read", "O", ("O", q, j - 1))
                     yield ("write", "O", ("Ors", q, j - 1))  # rescale before PV(j)
                 yield ("arrive", f"PFULL{b & 1}")
-            yield ("wait", "PVDONE", gs + n)
+            if not (yield ("await", "PVDONE", gs + n)):
+                return
             yield ("read", "O", ("O", q, n - 1))
             yield ("arrive", "OEMPTY")
             gs += n
@@ -549,12 +588,15 @@ def decode_roles(nblk, f8=False, skip=()):
     def convert():
         gk = 0
         for q, n in enumerate(segs):
-            yield ("wait", "QFULL", q + 1)
+            if not (yield ("await", "QFULL", q + 1)):
+                return
             yield ("read", "Q", ("Qraw", q))
             yield ("write", "Q", ("Q", q))  # RoPE (and fp16) in place
             qb = q & 1
             if q >= 2 and "convert_qtfree" not in skip:
-                yield ("wait", f"QTFREE{qb}", q // 2)  # the unit two back read the buffer
+                # the unit two back read the buffer
+                if not (yield ("await", f"QTFREE{qb}", q // 2)):
+                    return
             yield ("read", "Q", ("Q", q))
             yield ("write", f"QT{qb}", ("Q", q))  # into TMEM buffer qb
             yield ("arrive", f"QTMEM{qb}")
@@ -565,21 +607,25 @@ def decode_roles(nblk, f8=False, skip=()):
                     # the staging slot's bytes go to registers and the slot back
                     # to the copies before the wait for the fp16 stage
                     s8 = gk % S8
-                    yield ("wait", f"STGFULL{s8}", gk // S8 + 1)
+                    if not (yield ("await", f"STGFULL{s8}", gk // S8 + 1)):
+                        return
                     yield ("read", f"STG{s8}", ("stg", gk))
                     yield ("arrive", f"STGEMPTY{s8}")
                     if "convert_kvempty" not in skip:
-                        yield ("wait", f"KVEMPTY{st}", gk // S)  # PV(gk-S) read the stage
+                        if not (yield ("await", f"KVEMPTY{st}", gk // S)):  # PV(gk-S) read the stage
+                            return
                     yield ("write", f"K{st}", ("K", gk))
                     yield ("write", f"V{st}", ("V", gk))
                 else:
-                    yield ("wait", f"KVFULL{st}", gk // S + 1)  # K and V copies landed
+                    if not (yield ("await", f"KVFULL{st}", gk // S + 1)):  # K and V copies landed
+                        return
                     yield ("read", f"K{st}", ("Kraw", gk))
                     yield ("write", f"K{st}", ("K", gk))  # RoPE in place
                 yield ("arrive", f"KREADY{st}")
                 gk += 1
 
-    return {"producer": producer(), "mma": mma(), "softmax": softmax(), "convert": convert()}, {}
+    return ({"producer": producer(), "mma": mma(), "softmax": softmax(), "convert": convert()},
+            {EXIT_CHECK: True})
 
 
 def causal_roles(nblk, skip=()):
@@ -587,43 +633,70 @@ def causal_roles(nblk, skip=()):
     tiles A and B of one KV head) run over nblk[i] 128-key blocks: the Q/K copy
     warp, the V copy warp, the RoPE warps, the MMA thread and the softmax warps
     of each tile.  Per block the MMA thread issues PV_A(j), QK_A(j+1), PV_B(j),
-    QK_B(j+1), so each tile's softmax overlaps the other tile's products."""
+    QK_B(j+1), so each tile's softmax overlaps the other tile's products.
+    Every wait is bounded ("await"); after leaving its loop each copy thread
+    waits for the last copy into each of its buffers and the MMA thread for a
+    commit behind its last MMA, as the kernel does."""
     items = list(nblk)
 
     def producer():
-        gk = 0
+        gk = gi = 0
+        ok = True
         for i, n in enumerate(items):
-            yield ("wait", "QEMPTY", i)  # the previous item's last QK^T read Q
+            ok = yield ("await", "QEMPTY", i)  # the previous item's last QK^T read Q
+            if not ok:
+                break
             for x in range(2):
                 yield ("tma", f"Q{x}", ("Qraw", i, x), f"QFULL{x}")
+            gi += 1
             for _ in range(n):
                 st = gk & 1
                 if "producer_kempty" not in skip:
-                    yield ("wait", f"KEMPTY{st}", gk >> 1)
+                    ok = yield ("await", f"KEMPTY{st}", gk >> 1)
+                    if not ok:
+                        break
                 yield ("tma", f"K{st}", ("Kraw", gk), f"KFULL{st}")
                 gk += 1
+            if not ok:
+                break
+        if "producer_drain" not in skip:
+            for x in range(2):
+                if gi > 0:
+                    yield ("drain", f"QFULL{x}", gi)
+            for st in range(2):
+                if gk > st:
+                    yield ("drain", f"KFULL{st}", (gk - 1 - st) // 2 + 1)
 
     def vloader():
         gv = 0
+        ok = True
         for n in items:
             for _ in range(n):
                 if "vloader_vempty" not in skip:
-                    yield ("wait", "VEMPTY", gv)
+                    ok = yield ("await", "VEMPTY", gv)
+                    if not ok:
+                        break
                 yield ("tma", "V", ("V", gv), "VFULL")
                 gv += 1
+            if not ok:
+                break
+        if gv > 0 and "producer_drain" not in skip:
+            yield ("drain", "VFULL", gv)
 
     def rope():
         gk = 0
         for i, n in enumerate(items):
             for x in range(2):
-                yield ("wait", f"QFULL{x}", i + 1)
+                if not (yield ("await", f"QFULL{x}", i + 1)):
+                    return
                 yield ("read", f"Q{x}", ("Qraw", i, x))
                 yield ("write", f"Q{x}", ("Q", i, x))
                 yield ("arrive", f"QREADY{x}")
             for _ in range(n):
                 st = gk & 1
                 if "rope_kfull" not in skip:
-                    yield ("wait", f"KFULL{st}", (gk >> 1) + 1)
+                    if not (yield ("await", f"KFULL{st}", (gk >> 1) + 1)):
+                        return
                 yield ("read", f"K{st}", ("Kraw", gk))
                 yield ("write", f"K{st}", ("K", gk))
                 yield ("arrive", f"KREADY{st}")
@@ -631,6 +704,7 @@ def causal_roles(nblk, skip=()):
 
     def mma():
         gk = gv = gp = 0
+        issued = False
 
         def qk(i, x, b):
             yield ("mma", [(f"Q{x}", ("Q", i, x)), (f"K{b & 1}", ("K", b))], [(f"S{x}", ("S", x, b))])
@@ -638,68 +712,86 @@ def causal_roles(nblk, skip=()):
 
         def pv(i, x, j, b, first):
             if "mma_pfull" not in skip:
-                yield ("wait", f"PFULL{x}", gp + 1)
+                if not (yield ("await", f"PFULL{x}", gp + 1)):
+                    return False
             # (the O_EMPTY wait is implied by P_FULL: the softmax threads finish
             # the previous item's epilogue before they store this item's P)
             if first:
-                yield ("wait", f"OEMPTY{x}", i)
+                if not (yield ("await", f"OEMPTY{x}", i)):
+                    return False
             reads = [(f"S{x}", ("P", x, b)), ("V", ("V", gv))]
             if not first:
                 reads.append((f"O{x}", ("Ors", x, i, j - 1)))
             yield ("mma", reads, [(f"O{x}", ("O", x, i, j))])
             yield ("commit", f"PVDONE{x}")
+            return True
 
-        for i, n in enumerate(items):
-            yield ("wait", "QREADY0", i + 1)
-            yield ("wait", "QREADY1", i + 1)
-            yield ("wait", f"KREADY{gk & 1}", (gk >> 1) + 1)
-            yield from qk(i, 0, gk)
-            yield from qk(i, 1, gk)
-            yield ("commit", f"KEMPTY{gk & 1}")
-            if n == 1:
-                yield ("commit", "QEMPTY")
-            for j in range(n):
-                more = j + 1 < n
-                yield ("wait", "VFULL", gv + 1)
-                yield from pv(i, 0, j, gk, j == 0)
-                if more:
-                    yield ("wait", f"KREADY{(gk + 1) & 1}", ((gk + 1) >> 1) + 1)
-                    yield from qk(i, 0, gk + 1)
-                yield from pv(i, 1, j, gk, j == 0)
-                yield ("commit", "VEMPTY")
-                gv += 1
-                gp += 1
-                if more:
-                    yield from qk(i, 1, gk + 1)
-                    yield ("commit", f"KEMPTY{(gk + 1) & 1}")
-                    if j + 1 == n - 1:
-                        yield ("commit", "QEMPTY")
-                gk += 1
+        def body():
+            nonlocal gk, gv, gp, issued
+            for i, n in enumerate(items):
+                for w in (("QREADY0", i + 1), ("QREADY1", i + 1), (f"KREADY{gk & 1}", (gk >> 1) + 1)):
+                    if not (yield ("await",) + w):
+                        return
+                yield from qk(i, 0, gk)
+                issued = True
+                yield from qk(i, 1, gk)
+                yield ("commit", f"KEMPTY{gk & 1}")
+                if n == 1:
+                    yield ("commit", "QEMPTY")
+                for j in range(n):
+                    more = j + 1 < n
+                    if not (yield ("await", "VFULL", gv + 1)):
+                        return
+                    if not (yield from pv(i, 0, j, gk, j == 0)):
+                        return
+                    if more:
+                        if not (yield ("await", f"KREADY{(gk + 1) & 1}", ((gk + 1) >> 1) + 1)):
+                            return
+                        yield from qk(i, 0, gk + 1)
+                    if not (yield from pv(i, 1, j, gk, j == 0)):
+                        return
+                    yield ("commit", "VEMPTY")
+                    gv += 1
+                    gp += 1
+                    if more:
+                        yield from qk(i, 1, gk + 1)
+                        yield ("commit", f"KEMPTY{(gk + 1) & 1}")
+                        if j + 1 == n - 1:
+                            yield ("commit", "QEMPTY")
+                    gk += 1
+
+        yield from body()
+        if issued and "mma_drain" not in skip:
+            yield ("commit", "DRAIN")
+            yield ("drain", "DRAIN", 1)
 
     def softmax(x):
         def role():
             gb = 0
             for i, n in enumerate(items):
                 for j in range(n):
-                    yield ("wait", f"SFULL{x}", gb + 1)
+                    if not (yield ("await", f"SFULL{x}", gb + 1)):
+                        return
                     yield ("read", f"S{x}", ("S", x, gb))
                     yield ("write", f"S{x}", ("P", x, gb))  # P over the S columns
                     if j > 0:
                         # (implied by S_FULL(j): QK(j) of this tile was issued
                         # after PV(j-1); the kernel waits all the same)
-                        yield ("wait", f"PVDONE{x}", gb)
+                        if not (yield ("await", f"PVDONE{x}", gb)):
+                            return
                         yield ("read", f"O{x}", ("O", x, i, j - 1))
                         yield ("write", f"O{x}", ("Ors", x, i, j - 1))  # rescale
                     yield ("arrive", f"PFULL{x}")
                     gb += 1
-                yield ("wait", f"PVDONE{x}", gb)
+                if not (yield ("await", f"PVDONE{x}", gb)):
+                    return
                 yield ("read", f"O{x}", ("O", x, i, n - 1))
                 yield ("arrive", f"OEMPTY{x}")
         return role()
 
     roles = {"producer": producer(), "vloader": vloader(), "rope": rope(), "mma": mma(),
              "softmaxA": softmax(0), "softmaxB": softmax(1)}
-    return roles, {}
+    return roles, {EXIT_CHECK: True}
 
 
 def band_roles(lanes, skip=(), nseg=9, R=12, stall=False):

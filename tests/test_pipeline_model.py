@@ -7,7 +7,8 @@ replaced it.  The model transcribes the roles of sinkattn_band_kernel
 (band_kernel.cuh), sinkattn_causal_kernel (causal_kernel.cuh),
 sinkattn_decode_kernel (decode_kernel.cuh), bwd_dq_kernel and bwd_dkdv_kernel
 (backward_kernel.cuh); a wait left out of it must be caught, which the
-*_missing_wait_* tests check."""
+*_missing_wait_* tests check.  Run with random timeouts, every kernel's abort
+path must leave nothing in flight (the *_abort_* and *_missing_drain_* tests)."""
 import random
 
 import pytest
@@ -181,6 +182,40 @@ def test_backward_missing_drain_is_caught(make_roles, skip):
     for seed in range(400):
         try:
             run(make_roles, [3, 2, 4], seed, skip=(skip,), aborts=True)
+        except ModelError:
+            caught = True
+            break
+    assert caught
+
+
+# ------------------------------------------------ abort and drain (causal and decode kernels)
+_ABORT_ROLES = {
+    "causal": causal_roles,
+    "decode": lambda s, sk: decode_roles(s, False, sk),
+    "decode_fp8": lambda s, sk: decode_roles(s, True, sk),
+}
+
+
+@pytest.mark.parametrize("name", sorted(_ABORT_ROLES))
+@pytest.mark.parametrize("sizes", [[1], [3], [1, 2, 1, 3], [2, 7]])
+def test_forward_abort_drains_everything(name, sizes):
+    """The GA prefill and decode kernels with a bounded wait running out at a
+    random moment: every role leaves, nothing is read wrong, and no copy or
+    MMA is in flight when the last role is done."""
+    aborted = 0
+    for seed in range(300):
+        sim = run(_ABORT_ROLES[name], sizes, seed, aborts=True)
+        aborted += sim.aborted
+    assert aborted > 50
+
+
+@pytest.mark.parametrize("name", sorted(_ABORT_ROLES))
+@pytest.mark.parametrize("skip", ["producer_drain", "mma_drain"])
+def test_forward_missing_drain_is_caught(name, skip):
+    caught = False
+    for seed in range(400):
+        try:
+            run(_ABORT_ROLES[name], [3, 2, 4], seed, skip=(skip,), aborts=True)
         except ModelError:
             caught = True
             break
