@@ -1,5 +1,6 @@
 """CPU model of the mbarrier pipelines of the SWA and GA prefill kernels, the
-decode kernel and the backward kernels (dq and dk/dv).
+general prefill kernel, the decode kernel and the backward kernels (dq and
+dk/dv).
 
 Each kernel role (the copy thread, the MMA thread, the row threads of the two
 column halves) is a generator that yields the operations it performs, in the
@@ -626,6 +627,151 @@ def decode_roles(nblk, f8=False, skip=()):
 
     return ({"producer": producer(), "mma": mma(), "softmax": softmax(), "convert": convert()},
             {EXIT_CHECK: True})
+
+
+def general_roles(nblk, skip=(), NQ=1, NKV=2):
+    """sinkattn_fwd_kernel (the general prefill kernel) for one CTA whose items
+    (one query tile each) run over nblk[i] key blocks: the copy thread (Q into
+    NQ stages, K/V into NKV stages), the RoPE warps, the MMA thread and the
+    softmax rows.  With one K/V stage (NQ = 2, NKV = 1: a window that fits one
+    block per tile) PV(j-1) goes out before QK^T(j), which needs the stage back;
+    with two, after it.  S and P share one of two buffers per block.  Every
+    wait is bounded, with the copy and MMA threads' drains."""
+    items = list(nblk)
+
+    def producer():
+        gq = gk = 0
+        ok = True
+        for n in items:
+            qs = gq % NQ
+            ok = yield ("await", f"QEMPTY{qs}", gq // NQ)
+            if not ok:
+                break
+            yield ("tma", f"Q{qs}", ("Qraw", gq), f"QFULL{qs}")
+            gq += 1
+            for _ in range(n):
+                ks = gk % NKV
+                if "producer_kvempty" not in skip:
+                    ok = yield ("await", f"KVEMPTY{ks}", gk // NKV)
+                    if not ok:
+                        break
+                yield ("tma", f"KV{ks}", ("KVraw", gk), f"KVFULL{ks}")
+                gk += 1
+            if not ok:
+                break
+        if "producer_drain" not in skip:
+            for st in range(NQ):
+                if gq > st:
+                    yield ("drain", f"QFULL{st}", (gq - 1 - st) // NQ + 1)
+            for st in range(NKV):
+                if gk > st:
+                    yield ("drain", f"KVFULL{st}", (gk - 1 - st) // NKV + 1)
+
+    def rope():
+        gq = gk = 0
+        for n in items:
+            qs = gq % NQ
+            if not (yield ("await", f"QFULL{qs}", gq // NQ + 1)):
+                return
+            yield ("read", f"Q{qs}", ("Qraw", gq))
+            yield ("write", f"Q{qs}", ("Q", gq))
+            yield ("arrive", f"QREADY{qs}")
+            gq += 1
+            for _ in range(n):
+                ks = gk % NKV
+                if "rope_kvfull" not in skip:
+                    if not (yield ("await", f"KVFULL{ks}", gk // NKV + 1)):
+                        return
+                yield ("read", f"KV{ks}", ("KVraw", gk))
+                yield ("write", f"KV{ks}", ("KV", gk))
+                yield ("arrive", f"KREADY{ks}")
+                gk += 1
+
+    def mma():
+        gq = gk = gs = gt = 0
+        issued = False
+
+        def issue_pv(i, jj):
+            g = gs + jj
+            buf = g & 1
+            if not (yield ("await", f"PFULL{buf}", (g >> 1) + 1)):
+                return False
+            # (the O_EMPTY wait is implied by P_FULL: the softmax rows finish the
+            # previous item's epilogue before they store this item's first P)
+            if jj == 0 and "mma_oempty" not in skip:
+                if not (yield ("await", "OEMPTY", gt)):
+                    return False
+            ks = (gk + jj) % NKV
+            reads = [(f"S{buf}", ("P", g)), (f"KV{ks}", ("KV", gk + jj))]
+            if jj > 0:
+                reads.append(("O", ("Ors", i, jj - 1)))
+            yield ("mma", reads, [("O", ("O", i, jj))])
+            yield ("commit", f"KVEMPTY{ks}")
+            yield ("commit", "PVDONE")
+            return True
+
+        def body():
+            nonlocal gq, gk, gs, gt, issued
+            for i, n in enumerate(items):
+                qs = gq % NQ
+                if not (yield ("await", f"QREADY{qs}", gq // NQ + 1)):
+                    return
+                for j in range(n):
+                    if NKV == 1 and j > 0:
+                        if not (yield from issue_pv(i, j - 1)):
+                            return
+                    gkj = gk + j
+                    ks = gkj % NKV
+                    if not (yield ("await", f"KREADY{ks}", gkj // NKV + 1)):
+                        return
+                    buf = (gs + j) & 1
+                    yield ("mma", [(f"Q{qs}", ("Q", gq)), (f"KV{ks}", ("KV", gkj))],
+                           [(f"S{buf}", ("S", gs + j))])
+                    issued = True
+                    yield ("commit", f"SFULL{buf}")
+                    if j == n - 1:
+                        yield ("commit", f"QEMPTY{qs}")
+                    if NKV > 1 and j > 0:
+                        if not (yield from issue_pv(i, j - 1)):
+                            return
+                if not (yield from issue_pv(i, n - 1)):
+                    return
+                gq += 1
+                gk += n
+                gs += n
+                gt += 1
+
+        yield from body()
+        if issued and "mma_drain" not in skip:
+            yield ("commit", "DRAIN")
+            yield ("drain", "DRAIN", 1)
+
+    def softmax():
+        gs = gp = 0
+        for i, n in enumerate(items):
+            for j in range(n):
+                buf = gs & 1
+                if not (yield ("await", f"SFULL{buf}", (gs >> 1) + 1)):
+                    return
+                yield ("read", f"S{buf}", ("S", gs))
+                yield ("write", f"S{buf}", ("P", gs))  # P over the S columns
+                if j > 0:
+                    if "softmax_pvdone" not in skip:
+                        if not (yield ("await", "PVDONE", gp + 1)):  # PV(j-1) complete
+                            return
+                    yield ("read", "O", ("O", i, j - 1))
+                    yield ("write", "O", ("Ors", i, j - 1))  # lazy rescale before PV(j)
+                    gp += 1
+                yield ("arrive", f"PFULL{buf}")
+                gs += 1
+            if not (yield ("await", "PVDONE", gp + 1)):
+                return
+            yield ("read", "O", ("O", i, n - 1))
+            yield ("arrive", "OEMPTY")
+            gp += 1
+
+    roles = {"producer": producer(), "rope": rope(), "mma": mma(), "softmax": softmax()}
+    return roles, {EXIT_CHECK: True}
 
 
 def causal_roles(nblk, skip=()):

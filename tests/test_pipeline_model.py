@@ -5,6 +5,7 @@ of the awaited one, and no MMA or thread that reads a shared-memory stage or
 TMEM region before the data it expects has landed or after the next write
 replaced it.  The model transcribes the roles of sinkattn_band_kernel
 (band_kernel.cuh), sinkattn_causal_kernel (causal_kernel.cuh),
+sinkattn_fwd_kernel (attn_kernel.cuh, both instances),
 sinkattn_decode_kernel (decode_kernel.cuh), bwd_dq_kernel and bwd_dkdv_kernel
 (backward_kernel.cuh); a wait left out of it must be caught, which the
 *_missing_wait_* tests check.  Run with random timeouts, every kernel's abort
@@ -13,7 +14,8 @@ import random
 
 import pytest
 
-from pipeline_model import ModelError, band_roles, causal_roles, decode_roles, dkdv_roles, dq_roles, run
+from pipeline_model import (ModelError, band_roles, causal_roles, decode_roles, dkdv_roles, dq_roles,
+                            general_roles, run)
 
 SIZES = [[1], [2], [3], [1, 1, 1], [1, 2, 1, 3], [3, 3, 3], [5, 1, 4], [2, 7], [1] * 6]
 
@@ -220,3 +222,34 @@ def test_forward_missing_drain_is_caught(name, skip):
             caught = True
             break
     assert caught
+
+
+# ------------------------------------------------ the general prefill kernel
+_GENERAL = {"one_kv_stage": dict(NQ=2, NKV=1), "two_kv_stages": dict(NQ=1, NKV=2)}
+
+
+@pytest.mark.parametrize("variant", sorted(_GENERAL))
+@pytest.mark.parametrize("sizes", SIZES)
+def test_general_pipeline(variant, sizes):
+    for seed in range(60):
+        run(lambda s, sk: general_roles(s, sk, **_GENERAL[variant]), sizes, seed)
+
+
+@pytest.mark.parametrize("variant,skip", [(v, k) for v in sorted(_GENERAL)
+                                          for k in ("producer_kvempty", "rope_kvfull")]
+                         + [("two_kv_stages", "softmax_pvdone")])
+def test_general_missing_wait_is_caught(variant, skip):
+    # (with one K/V stage PV(j-1) goes out before QK^T(j), so S_FULL(j) implies
+    # PV_DONE(j-1) and the softmax's own wait for it cannot be caught missing;
+    # the MMA thread's O_EMPTY wait is implied by P_FULL in both variants)
+    assert _caught(lambda s, sk: general_roles(s, sk, **_GENERAL[variant]), (skip,))
+
+
+@pytest.mark.parametrize("variant", sorted(_GENERAL))
+def test_general_abort_drains_everything(variant):
+    aborted = 0
+    for seed in range(300):
+        sim = run(lambda s, sk: general_roles(s, sk, **_GENERAL[variant]), [1, 2, 1, 3], seed,
+                  aborts=True)
+        aborted += sim.aborted
+    assert aborted > 50
