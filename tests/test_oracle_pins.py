@@ -222,6 +222,29 @@ def test_shift_invariance(oracle_mod):
     np.testing.assert_allclose(l2, l1 + c, rtol=0, atol=1e-12)
 
 
+# ------------------------------------------- negative logit scale (sign flip)
+@pytest.mark.parametrize("window", [0, 3])
+def test_negative_scale_is_negated_query(oracle_mod, window):
+    """a = scale * (rot(q) . rot(k)) and the rotation is linear, so a scale -s
+    with q is the scale s with -q, bit for bit: the oracle's path for negative
+    scales (the ones the general kernel takes) reduces to its positive one."""
+    rng = np.random.default_rng(11)
+    L, Hq, Hkv = 9, 4, 2
+    q = rng.standard_normal((L, Hq, 192))
+    k = rng.standard_normal((L, Hkv, 192))
+    v = rng.standard_normal((L, Hkv, 128))
+    sink = rng.standard_normal(Hq).astype(np.float32)
+    cu = np.array([0, 5, L], dtype=np.int32)
+    for s in (0.07, 1.0 / math.sqrt(192)):
+        o1, l1 = oracle_mod.prefill(q, k, v, sink, cu, window=window, rope_base=1e4, scale=-s)
+        o2, l2 = oracle_mod.prefill(-q, k, v, sink, cu, window=window, rope_base=1e4, scale=s)
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+        # and it is not the positive-scale result on q itself
+        o3, _ = oracle_mod.prefill(q, k, v, sink, cu, window=window, rope_base=1e4, scale=s)
+        assert np.max(np.abs(o3 - o1)) > 1e-3
+
+
 # ------------------------------------------------------- (vii) large sink
 def test_large_sink_suppresses_output(oracle_mod):
     gen = torch.Generator().manual_seed(1)
